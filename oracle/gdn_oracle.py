@@ -1,0 +1,272 @@
+"""CPU oracle of the slot-indexed Gated DeltaNet layer -- TEST INFRASTRUCTURE.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+import this module.  It shares no code with the CUDA library (it does not
+import the package, and the package never imports it); the two meet only in
+the seeded input generators.  Everything is float64 numpy written the plain
+way, token by token, so that each line can be checked by eye.
+
+Sources (page title and section):
+  [P1] baseRT issue #31, "GDN recurrent state is single-sequence only":
+       "Why this looks tractable" lists the per-layer kernels gdn_conv_silu and
+       gdn_recurrence and a state cache sized by layers, heads, head_dim and
+       conv_k with no slot dimension -- which this pool adds.
+  [P2] b70-optimization-lab, "Plan (research-based)": "What the research
+       found" -- speculative verify without per-draft-token state snapshots,
+       chunked delta rule with the (I+A)^{-1} UT transform.
+  [P3] ai-infra-handbooks, "Project: adding the hybrid model Qwen3.5":
+       "What to do", State row -- one conv cache and one recurrent state per
+       request slot, zero for a new request, carried across chunked-prefill
+       chunks.
+
+The pages name the recurrence but never write it out.  The rule used is the
+gated delta rule of Gated DeltaNet, for each value head:
+    S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+    o_t = scale * S_t q_t
+with S_t of shape [V, K], q_t and k_t L2-normalised (eps inside the sqrt),
+alpha_t = exp(g_t) for the given log-decay g_t <= 0, and value head h reading
+key head h // (H_v / H_k).  Readings of points the pages leave open (output
+after the update, conv orientation, eps, head grouping) are listed in the
+design notes beside this package.
+
+Pins: every function here is checked in tests/test_oracle_pins.py against
+closed forms, exact rational brute force, a library convolution and the
+invariants the pages state (see that file's docstring for the map).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+L2_EPS = 1e-6
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------- conv + SiLU
+
+def silu(u):
+    return u / (1.0 + np.exp(-u))
+
+
+def conv_silu(x, cache, w, bias=None, advance=None):
+    """Causal depthwise short conv followed by SiLU over one sequence [P1].
+
+    x      [L, C]      raw inputs of this call, in time order
+    cache  [C, W-1]    the W-1 raw inputs that precede x, oldest first
+    w      [C, W]      taps; w[:, W-1] multiplies the current token
+    bias   [C] or None
+    advance            how many of the L tokens the cache moves past
+                       (None: all L).  Outputs are produced for all L.
+
+    Returns (y [L, C], new_cache [C, W-1]).
+    """
+    x, cache, w = _f64(x), _f64(cache), _f64(w)
+    L, C = x.shape
+    W = w.shape[1]
+    assert cache.shape == (C, W - 1)
+    # history row j holds the raw input at time j - (W-1) relative to x[0]
+    hist = np.concatenate([cache.T, x], axis=0)
+    y = np.empty((L, C))
+    for t in range(L):
+        window = hist[t:t + W]                      # [W, C], last row is x[t]
+        u = np.sum(w.T * window, axis=0)
+        if bias is not None:
+            u = u + _f64(bias)
+        y[t] = silu(u)
+    a = L if advance is None else int(advance)
+    assert 0 <= a <= L
+    new_cache = hist[a:a + W - 1].T.copy()
+    return y, new_cache
+
+
+# ------------------------------------------------------------ gated delta rule
+
+def l2_normalize(x, eps=L2_EPS):
+    """x / sqrt(sum(x^2) + eps) over the last axis."""
+    x = _f64(x)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def expand_key_heads(a, h_v):
+    """[..., H_k, d] -> [..., H_v, d]: value head h reads key head h // (H_v/H_k)."""
+    a = _f64(a)
+    h_k = a.shape[-2]
+    assert h_v % h_k == 0
+    return np.repeat(a, h_v // h_k, axis=-2)
+
+
+def gdn_step(S, q, k, v, g, beta, scale=1.0, eps=L2_EPS):
+    """One token of the gated delta rule for all value heads of one slot.
+
+    S [H_v, V, K]; q, k [H_k, K]; v [H_v, V]; g, beta [H_v].
+    Returns (S_new [H_v, V, K], o [H_v, V]); o is read from the updated state.
+    """
+    S = _f64(S)
+    h_v = S.shape[0]
+    kh = expand_key_heads(l2_normalize(k, eps), h_v)      # [H_v, K]
+    qh = expand_key_heads(l2_normalize(q, eps), h_v)
+    v, g, beta = _f64(v), _f64(g), _f64(beta)
+    alpha = np.exp(g)
+    a3 = alpha[:, None, None]
+    b3 = beta[:, None, None]
+    # S (I - beta k k^T) = S - beta (S k) k^T
+    Sk = np.einsum("hvk,hk->hv", S, kh)
+    S_new = a3 * (S - b3 * Sk[:, :, None] * kh[:, None, :]) \
+        + b3 * v[:, :, None] * kh[:, None, :]
+    o = scale * np.einsum("hvk,hk->hv", S_new, qh)
+    return S_new, o
+
+
+def gdn_recurrent(S0, q, k, v, g, beta, scale=1.0, eps=L2_EPS):
+    """Token-by-token recurrence over one sequence of T tokens.
+
+    q, k [T, H_k, K]; v [T, H_v, V]; g, beta [T, H_v].
+    Returns (S_T, o [T, H_v, V])."""
+    S = _f64(S0).copy()
+    T = len(q)
+    o = np.empty((T, S.shape[0], S.shape[1]))
+    for t in range(T):
+        S, o[t] = gdn_step(S, q[t], k[t], v[t], g[t], beta[t], scale, eps)
+    return S, o
+
+
+def gdn_chunked(S0, q, k, v, g, beta, scale=1.0, chunk=64, eps=L2_EPS):
+    """The chunked form of the same recurrence [P2, "What the research found":
+    chunked delta rule with the (I+A)^{-1} UT transform], kept as a second,
+    independent oracle path to pin the identity chunked == token by token.
+
+    Within a chunk of n tokens with local cumulative log-decay G_t = sum_{s<=t} g_s
+    and gamma_t = exp(G_t), for each value head:
+        A[t,i] = beta_t exp(G_t - G_i) k_t.k_i           (i < t; 0 elsewhere)
+        Tm     = (I + A)^{-1}
+        W      = Tm diag(beta gamma) K,   U = Tm diag(beta) V
+        Delta  = U - W S0^T                  (the effective values, n x V)
+        O      = diag(gamma) Q S0^T + (mask(i<=t) * exp(G_t - G_i) * Q K^T) Delta
+        S_end  = gamma_n S0 + Delta^T diag(exp(G_n - G)) K
+    """
+    S = _f64(S0).copy()
+    h_v, V, K = S.shape
+    T = len(q)
+    kh = expand_key_heads(l2_normalize(k, eps), h_v)      # [T, H_v, K]
+    qh = expand_key_heads(l2_normalize(q, eps), h_v)
+    v, g, beta = _f64(v), _f64(g), _f64(beta)
+    o = np.empty((T, h_v, V))
+    for h in range(h_v):
+        Sh = S[h]
+        for c0 in range(0, T, chunk):
+            sl = slice(c0, min(c0 + chunk, T))
+            Kc, Qc, Vc = kh[sl, h], qh[sl, h], v[sl, h]
+            b, gc = beta[sl, h], g[sl, h]
+            n = len(gc)
+            G = np.cumsum(gc)
+            gamma = np.exp(G)
+            # exp(G_t - G_i) on and below the diagonal (upper part masked out)
+            decay = np.tril(np.exp(np.tril(G[:, None] - G[None, :])))
+            A = np.tril(b[:, None] * decay * (Kc @ Kc.T), -1)
+            Tm = np.linalg.inv(np.eye(n) + A)
+            Wm = Tm @ ((b * gamma)[:, None] * Kc)
+            Um = Tm @ (b[:, None] * Vc)
+            Delta = Um - Wm @ Sh.T
+            P = decay * (Qc @ Kc.T)
+            O = gamma[:, None] * (Qc @ Sh.T) + P @ Delta
+            Sh = gamma[-1] * Sh + Delta.T @ (np.exp(G[-1] - G)[:, None] * Kc)
+            o[sl, h] = scale * O
+        S[h] = Sh
+    return S, o
+
+
+def spec_verify(S0, q, k, v, g, beta, accept_len=None, scale=1.0, eps=L2_EPS):
+    """Speculative verify over T draft tokens of one slot [P2, "What the
+    research found": outputs for every draft position, no per-position
+    state snapshots].
+
+    o_t is what t decode steps from the committed S0 give; the returned state
+    is the state after `accept_len` steps (S0 itself when None or 0)."""
+    S = _f64(S0).copy()
+    T = len(q)
+    keep = S.copy()
+    a = 0 if accept_len is None else int(accept_len)
+    assert 0 <= a <= T
+    o = np.empty((T, S.shape[0], S.shape[1]))
+    for t in range(T):
+        S, o[t] = gdn_step(S, q[t], k[t], v[t], g[t], beta[t], scale, eps)
+        if t + 1 == a:
+            keep = S.copy()
+    return o, keep
+
+
+# -------------------------------------------------------------------- the pool
+
+class OraclePool:
+    """Slot-indexed pool: per layer and slot a float64 state [H_v, V, K] and a
+    conv cache [C, W-1] [P1 "Why this looks tractable"; P3 "What to do",
+    State row].  Slots are independent; a new request starts from zero."""
+
+    def __init__(self, n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k):
+        self.h_v, self.h_k, self.dk, self.dv = h_v, h_k, dk, dv
+        self.conv_ch, self.conv_k = conv_ch, conv_k
+        self.S = np.zeros((n_layers, n_slots, h_v, dv, dk))
+        self.X = np.zeros((n_layers, n_slots, conv_ch, conv_k - 1))
+
+    def reset(self, slot_ids):
+        for s in slot_ids:
+            self.S[:, s] = 0.0
+            self.X[:, s] = 0.0
+
+    def conv_silu(self, layer, slot_ids, cu_seqlens, x, w, bias=None,
+                  advance=None):
+        """Varlen conv + SiLU: sequence i (tokens cu[i]:cu[i+1] of x) runs on
+        slot slot_ids[i]'s cache; cu_seqlens None means one token per slot."""
+        x = _f64(x)
+        n = len(slot_ids)
+        cu = np.arange(n + 1) if cu_seqlens is None else np.asarray(cu_seqlens)
+        y = np.empty_like(x)
+        for i, s in enumerate(slot_ids):
+            lo, hi = int(cu[i]), int(cu[i + 1])
+            a = None if advance is None else int(advance[i])
+            y[lo:hi], self.X[layer, s] = conv_silu(
+                x[lo:hi], self.X[layer, s], w, bias, a)
+        return y
+
+    def decode_step(self, layer, slot_ids, q, k, v, g, beta, scale=1.0,
+                    eps=L2_EPS):
+        """One token per active slot; q, k [N, H_k, K], v [N, H_v, V]."""
+        o = np.empty((len(slot_ids), self.h_v, self.dv))
+        for i, s in enumerate(slot_ids):
+            self.S[layer, s], o[i] = gdn_step(
+                self.S[layer, s], q[i], k[i], v[i], g[i], beta[i], scale, eps)
+        return o
+
+    def prefill(self, layer, slot_ids, cu_seqlens, q, k, v, g, beta,
+                scale=1.0, chunk=None, eps=L2_EPS):
+        """Varlen prefill of packed sequences, starting from each slot's
+        current state and leaving the final state in the slot [P3, State row].
+        chunk None runs token by token, otherwise the chunked form."""
+        o = np.empty((len(q), self.h_v, self.dv))
+        for i, s in enumerate(slot_ids):
+            lo, hi = int(cu_seqlens[i]), int(cu_seqlens[i + 1])
+            args = (self.S[layer, s], q[lo:hi], k[lo:hi], v[lo:hi],
+                    g[lo:hi], beta[lo:hi])
+            if chunk is None:
+                self.S[layer, s], o[lo:hi] = gdn_recurrent(*args, scale, eps)
+            else:
+                self.S[layer, s], o[lo:hi] = gdn_chunked(*args, scale, chunk, eps)
+        return o
+
+    def spec_verify(self, layer, slot_ids, T, q, k, v, g, beta,
+                    accept_len=None, scale=1.0, eps=L2_EPS):
+        """Draft token t of slot i is token i*T + t of q, k, v, g, beta.
+        Returns o [N, T, H_v, V]; commits each slot at accept_len[i] when
+        accept_len is given, else leaves the pool unchanged."""
+        n = len(slot_ids)
+        o = np.empty((n, T, self.h_v, self.dv))
+        for i, s in enumerate(slot_ids):
+            sl = slice(i * T, (i + 1) * T)
+            a = None if accept_len is None else accept_len[i]
+            o[i], S_keep = spec_verify(self.S[layer, s], q[sl], k[sl], v[sl],
+                                       g[sl], beta[sl], a, scale, eps)
+            if accept_len is not None:
+                self.S[layer, s] = S_keep
+        return o
