@@ -1,0 +1,537 @@
+"""Benchmark of the slot-indexed Gated DeltaNet path on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+
+Headline (one JSON line on stdout): decode slot-steps/s for one GDN layer
+(32 value heads sharing 16 key heads, K = V = 128, fp32 state, conv_k = 4
+over 8192 channels, bf16 activations) on a 256-slot pool with 64 active slot
+ids drawn at random.  One step = gdn_conv_silu over the 64 new tokens, then
+gdn_decode_step reading q, k, v straight out of the conv output.  L2 is
+flushed (a 512 MiB write) between timed steps, outside the timed events.
+
+Also in the line: the same metric end to end through the C ABI with inputs
+copied from pinned host memory and outputs copied back inside the timed
+region (`e2e`), the decode kernel's HBM roofline fraction, the oracle timed
+on the host cores (`cpu_baseline`), SM clocks sampled during timing, and
+`secondary` measurements: the 18-layer slot sweep (N = 1 .. 512),
+speculative verify (128 slots, T = 4) and varlen chunked prefill.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload (the pages publish no runnable implementation of this path).
+Under torchrun each rank runs its own replica (weak scaling, no data-path
+collective); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN decode slot-steps/s"
+UNIT = "slot-steps/s"
+DECODE_WORKLOAD = ("decode step, one GDN layer: 32 value heads / 16 key heads, K=V=128, "
+                   "fp32 state, conv_k=4 over 8192 channels, bf16 activations, pool of 256 "
+                   "slots with 64 active slot ids (random subset), one token per active slot")
+STATE_BYTES_PER_SLOT_LAYER = 2 * 32 * 128 * 128 * 4          # state read + write
+# decode kernel, per slot-step: state r+w, q/k (bf16, 16 heads x 128 each), v (bf16),
+# g and beta (bf16, 32 each), o (fp32, 32 x 128)
+DECODE_KERNEL_BYTES_PER_SLOT = STATE_BYTES_PER_SLOT_LAYER + 2 * 16 * 128 * 2 + 32 * 128 * 2 \
+    + 2 * 32 * 2 + 32 * 128 * 4
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_decode_pool256_active64.md")
+DECODE_SOURCE = os.path.join(ROOT, "gated_deltanet_recurrent_gb300", "csrc", "gdn_decode.cu")
+
+
+def _parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--sweep-steps", type=int, default=128)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--sections", default="sweep,verify,prefill",
+                    help="secondary measurements to run (comma list of sweep, verify, prefill)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- CPU side
+
+def _oracle_decode_sample(n_slots_per_step: int, steps: int, warmup: int):
+    """Time the oracle on conv + decode of `n_slots_per_step` slots per step of
+    the decode workload; returns (seconds, slot-steps)."""
+    import numpy as np
+    from gated_deltanet_recurrent_gb300 import synth
+    from oracle import gdn_oracle as O
+    wl = synth.decode_workload(seed=1)
+    s = wl["shape"]
+    nq = s.h_k * s.dk
+    m = n_slots_per_step
+    S = [wl["states"][i].astype(np.float64) for i in range(m)]
+    X = [wl["conv_cache"][i].astype(np.float64) for i in range(m)]
+
+    def step():
+        for i in range(m):
+            y, X[i] = O.conv_silu(wl["x"][i:i + 1], X[i], wl["conv_w"])
+            y = y[0]
+            S[i], _ = O.gdn_step(S[i], y[:nq].reshape(s.h_k, s.dk),
+                                 y[nq:2 * nq].reshape(s.h_k, s.dk),
+                                 y[2 * nq:].reshape(s.h_v, s.dv),
+                                 wl["tok"]["g"][i], wl["tok"]["beta"][i])
+
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    return time.perf_counter() - t0, steps * m
+
+
+def _cpu_baseline_child(seconds: float):
+    # calibrate one step of 8 slots, then run for about `seconds`
+    dt, _ = _oracle_decode_sample(8, 1, 0)
+    steps = max(1, int(seconds / max(dt, 1e-6)))
+    dt, units = _oracle_decode_sample(8, steps, 1)
+    print(json.dumps({"value": units / dt, "seconds": dt, "units": units, "steps": steps}))
+
+
+def _cpu_env():
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    return env
+
+
+def cpu_baseline(seconds: float):
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
+                        "--cpu-seconds", str(seconds)], capture_output=True, text=True,
+                       env=_cpu_env(), cwd=ROOT, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr[-300:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"float64 numpy oracle, conv+SiLU then gated delta rule, on 8 of the 64 "
+                      f"active slots of the decode workload for {d['steps']} steps "
+                      f"({d['units']} slot-steps, {d['seconds']:.1f} s), single thread"}
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, on: bool):
+        self.windows.append((time.time(), on))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4)
+                          if r[5 + j].strip().lower() == "active"})
+        busy = [x for x in sm if smax and x > 0.3 * max(smax)]
+        return {"sm_mhz": statistics.median(busy or sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------- GPU
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d.get("bf16_tflops"), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def _profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode source."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+        sha = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256_16") != sha:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class DecodeBench:
+    def __init__(self, torch, abi, synth, device):
+        self.torch = torch
+        self.abi = abi
+        wl = synth.decode_workload(seed=1)
+        self.shape = s = wl["shape"]
+        self.n = n = len(wl["slot_ids"])
+        t = lambda a, dt=torch.bfloat16: torch.from_numpy(a).to(device=device, dtype=dt)
+        self.pool = abi.Pool.for_shape(s, 1, wl["n_slots"], conv_dtype=torch.bfloat16,
+                                       host_checks=False, device=device)
+        gen = torch.Generator(device=device).manual_seed(1)
+        self.pool.state.normal_(0.0, 0.1, generator=gen)
+        lid = torch.from_numpy(wl["slot_ids"]).long().to(device)
+        self.pool.state[0, lid] = t(wl["states"], torch.float32)
+        self.pool.conv[0, lid] = t(wl["conv_cache"])
+        self.ids = torch.from_numpy(wl["slot_ids"]).to(device)
+        self.x = t(wl["x"])
+        self.w = t(wl["conv_w"], torch.float32)
+        self.g = t(wl["tok"]["g"])
+        self.beta = t(wl["tok"]["beta"])
+        self.y = torch.empty(n, s.conv_ch, device=device, dtype=torch.bfloat16)
+        nq = s.h_k * s.dk
+        self.q = self.y[:, :nq].view(n, s.h_k, s.dk)
+        self.k = self.y[:, nq:2 * nq].view(n, s.h_k, s.dk)
+        self.v = self.y[:, 2 * nq:].view(n, s.h_v, s.dv)
+        self.o = torch.empty(n, s.h_v, s.dv, device=device)
+        self.flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+        # pinned host buffers for the end-to-end leg
+        self.x_h = self.x.cpu().pin_memory()
+        self.g_h = self.g.cpu().pin_memory()
+        self.b_h = self.beta.cpu().pin_memory()
+        self.o_h = torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
+        self.h2d = sum(a.numel() * a.element_size() for a in (self.x_h, self.g_h, self.b_h))
+        self.d2h = self.o_h.numel() * self.o_h.element_size()
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    def step(self, ev=None):
+        a = self.abi
+        a.gdn_conv_silu(self.pool, 0, self.ids, self.x, self.w, self.y)
+        if ev is not None:
+            ev[0].record()
+        a.gdn_decode_step(self.pool, 0, self.ids, self.q, self.k, self.v, self.g, self.beta,
+                          self.o)
+        if ev is not None:
+            ev[1].record()
+
+    def step_e2e(self):
+        self.x.copy_(self.x_h, non_blocking=True)
+        self.g.copy_(self.g_h, non_blocking=True)
+        self.beta.copy_(self.b_h, non_blocking=True)
+        self.step()
+        self.o_h.copy_(self.o, non_blocking=True)
+
+    def timed(self, fn, steps, kernel_events=False):
+        torch = self.torch
+        E = lambda: torch.cuda.Event(enable_timing=True)
+        evs = [(E(), E()) for _ in range(steps)]
+        kev = [(E(), E()) for _ in range(steps)] if kernel_events else None
+        for i in range(steps):
+            self.flush()
+            evs[i][0].record()
+            if kernel_events:
+                fn(kev[i])
+            else:
+                fn()
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        total = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+        ktime = sum(a.elapsed_time(b) for a, b in kev) / 1e3 if kernel_events else None
+        return total, ktime
+
+
+def sweep_bench(torch, abi, synth, device, steps):
+    """18 stacked layers, N active slots of a 512-slot pool, `steps` decode
+    steps per N; L2 flushed between steps."""
+    s = synth.GDN_LAYER
+    L, P = 18, 512
+    pool = abi.Pool.for_shape(s, L, P, conv_dtype=torch.bfloat16, host_checks=False,
+                              device=device)
+    gen = torch.Generator(device=device).manual_seed(2)
+    pool.state.normal_(0.0, 0.1, generator=gen)
+    order = torch.from_numpy(synth.sweep_slot_order(2, P)).to(device)
+    nq = s.h_k * s.dk
+    sets = 2
+    xs = [torch.randn(P, s.conv_ch, device=device, generator=gen).to(torch.bfloat16)
+          for _ in range(sets)]
+    w = (0.25 * torch.randn(L, s.conv_ch, s.conv_k, device=device, generator=gen))
+    gs = [(-torch.nn.functional.softplus(torch.randn(P, s.h_v, device=device, generator=gen)))
+          .to(torch.bfloat16) for _ in range(sets)]
+    bs = [torch.sigmoid(torch.randn(P, s.h_v, device=device, generator=gen)).to(torch.bfloat16)
+          for _ in range(sets)]
+    y = torch.empty(P, s.conv_ch, device=device, dtype=torch.bfloat16)
+    o = torch.empty(P, s.h_v, s.dv, device=device)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    out = []
+    for N in synth.SWEEP_SLOTS:
+        ids = order[:N].contiguous()
+        q = y[:N, :nq].view(N, s.h_k, s.dk)
+        k = y[:N, nq:2 * nq].view(N, s.h_k, s.dk)
+        v = y[:N, 2 * nq:].view(N, s.h_v, s.dv)
+
+        def one_step(j):
+            for layer in range(L):
+                abi.gdn_conv_silu(pool, layer, ids, xs[j % sets][:N], w[layer], y[:N])
+                abi.gdn_decode_step(pool, layer, ids, q, k, v, gs[j % sets][:N],
+                                    bs[j % sets][:N], o[:N])
+
+        for j in range(3):
+            one_step(j)
+        E = lambda: torch.cuda.Event(enable_timing=True)
+        evs = [(E(), E()) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for j in range(steps):
+            flush.zero_()
+            evs[j][0].record()
+            one_step(j)
+            evs[j][1].record()
+        torch.cuda.synchronize()
+        t = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+        slot_steps = N * steps
+        out.append({"n_active": N, "slot_steps_per_s": slot_steps / t,
+                    "slot_layer_steps_per_s": slot_steps * L / t,
+                    "state_gbs": slot_steps * L * STATE_BYTES_PER_SLOT_LAYER / t / 1e9,
+                    "ms_per_step": t / steps * 1e3})
+    del pool
+    return {"workload": "18 stacked GDN layers (decode-step layer shape), 512-slot pool, "
+                        f"N active, {steps} decode steps per N, conv+decode per layer, "
+                        "L2 flushed between steps", "points": out}
+
+
+def verify_bench(torch, abi, synth, device, steps, peak):
+    wl = synth.verify_workload(seed=4)
+    s, T = wl["shape"], wl["T"]
+    n = len(wl["slot_ids"])
+    pool = abi.Pool.for_shape(s, 1, wl["n_slots"], conv_dtype=torch.bfloat16,
+                              host_checks=False, device=device)
+    lid = torch.from_numpy(wl["slot_ids"]).long().to(device)
+    pool.state[0, lid] = torch.from_numpy(wl["states"]).to(device)
+    ids = torch.from_numpy(wl["slot_ids"]).to(device)
+    draft = [torch.from_numpy(wl["draft"][nm]).to(device=device, dtype=torch.bfloat16)
+             for nm in ("q", "k", "v", "g", "beta")]
+    acc = torch.from_numpy(wl["accept_len"]).to(device)
+    o = torch.empty(n, T, s.h_v, s.dv, device=device, dtype=torch.bfloat16)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    for _ in range(3):
+        abi.gdn_spec_verify(pool, 0, ids, T, *draft, o=o, accept_len=acc)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [(E(), E()) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for j in range(steps):
+        flush.zero_()
+        evs[j][0].record()
+        abi.gdn_spec_verify(pool, 0, ids, T, *draft, o=o, accept_len=acc)
+        evs[j][1].record()
+    torch.cuda.synchronize()
+    t = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    committing = int((wl["accept_len"] > 0).sum())
+    per_call = n * STATE_BYTES_PER_SLOT_LAYER / 2 + committing * STATE_BYTES_PER_SLOT_LAYER / 2 \
+        + n * T * (2 * 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 2 + 32 * 128 * 2)
+    gbs = per_call * steps / t / 1e9
+    return {"workload": "spec verify, decode-step layer shape, 128 active of 256 slots, T=4, "
+                        "bf16 in/out, commit at accepted length U{0..4}, one pass",
+            "slot_verifies_per_s": n * steps / t, "us_per_call": t / steps * 1e6,
+            "algorithmic_gbs": gbs, "hbm_frac": gbs / peak}
+
+
+def prefill_bench(torch, abi, synth, device, steps):
+    wl = synth.prefill_workload(seed=3)
+    s = wl["shape"]
+    lens = wl["lengths"]
+    cu = wl["cu_seqlens"]
+    pool = abi.Pool.for_shape(s, 1, len(lens), conv_dtype=torch.bfloat16, host_checks=False,
+                              device=device)
+    init = torch.from_numpy(wl["states"]).to(device)
+    tok = [torch.from_numpy(wl["tok"][nm]).to(device=device, dtype=torch.bfloat16)
+           for nm in ("q", "k", "v", "g", "beta")]
+    o = torch.empty(int(cu[-1]), s.h_v, s.dv, device=device, dtype=torch.bfloat16)
+    calls = []
+    import numpy as np
+    for idx, starts, ln in synth.prefill_calls(lens, wl["piece"]):
+        # pack the pieces of this call contiguously
+        rows = np.concatenate([np.arange(cu[i] + st, cu[i] + st + l)
+                               for i, st, l in zip(idx, starts, ln)])
+        rows_t = torch.from_numpy(rows).long().to(device)
+        packed = [t[rows_t].contiguous() for t in tok]
+        ccu = torch.from_numpy(synth.cu_seqlens_of(ln)).to(device)
+        ids = torch.tensor(idx, dtype=torch.int32, device=device)
+        ob = torch.empty(len(rows), s.h_v, s.dv, device=device, dtype=torch.bfloat16)
+        calls.append((ids, ccu, packed, ob, max(ln)))
+
+    def run():
+        for ids, ccu, packed, ob, mx in calls:
+            abi.gdn_prefill_chunked(pool, 0, ids, ccu, *packed, ob, max_seqlen=mx)
+
+    try:
+        pool.state[0].copy_(init)
+        run()
+    except abi.GDNError as e:
+        return {"unavailable": str(e)}
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [(E(), E()) for _ in range(steps)]
+    for j in range(steps):
+        pool.state[0].copy_(init)
+        evs[j][0].record()
+        run()
+        evs[j][1].record()
+    torch.cuda.synchronize()
+    t = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    total = int(cu[-1])
+    return {"workload": f"varlen chunked prefill, decode-step layer shape, 8 sequences "
+                        f"(lengths {lens}), pieces of 2048 tokens with the state carried "
+                        f"between calls, bf16 in/out, chunk 64",
+            "tokens_per_s": total * steps / t, "ms_per_pass": t / steps * 1e3,
+            "calls_per_pass": len(calls)}
+
+
+def run_gpu(args, rank, world):
+    import torch
+    from gated_deltanet_recurrent_gb300 import abi, synth
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    abi.load_library()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    peak, _, peak_kind = _peaks()
+
+    b = DecodeBench(torch, abi, synth, device)
+    for _ in range(max(3, args.warmup)):
+        b.step()
+        b.step_e2e()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    t_dev, t_kernel = b.timed(b.step, args.steps, kernel_events=True)
+    barrier()
+    t_e2e, _ = b.timed(b.step_e2e, args.steps)
+    barrier()
+    secondary = {}
+    sections = set() if args.no_secondary else set(args.sections.split(","))
+    if "sweep" in sections:
+        secondary["sweep"] = sweep_bench(torch, abi, synth, device, args.sweep_steps)
+    if "verify" in sections:
+        secondary["verify"] = verify_bench(torch, abi, synth, device, 50, peak)
+    if "prefill" in sections:
+        secondary["prefill"] = prefill_bench(torch, abi, synth, device, 5)
+    time.sleep(0.2)
+    clk = clocks.stop()
+    if dist is not None:
+        tt = torch.tensor([t_dev, t_e2e, t_kernel], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_dev, t_e2e, t_kernel = tt.tolist()
+    if rank != 0:
+        return None
+
+    units = b.n * args.steps * world
+    kernel_avg = t_kernel / args.steps
+    achieved = DECODE_KERNEL_BYTES_PER_SLOT * b.n / kernel_avg / 1e9
+    line = {
+        "metric": METRIC, "value": units / t_dev, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_dev / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; N(0,0.1) states, distributions of the tiny correctness case)",
+        "config": {"workload": DECODE_WORKLOAD, "n_slots": 256, "n_active": b.n,
+                   "layers": 1, "l2": "flushed between timed steps (512 MiB write, untimed)",
+                   "activations": "bf16", "state": "fp32", "parallelism":
+                   f"replicas x{world}" if world > 1 else "single GPU"},
+        "e2e": {"value": units / t_e2e, "unit": UNIT, "h2d_bytes_per_step": b.h2d,
+                "d2h_bytes_per_step": b.d2h,
+                "note": "pinned host x, g, beta -> device, conv + decode, o -> pinned host"},
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "gdn decode_kernel<128, bf16, float>",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": _profiled_traffic(),
+                     "peak_kind": f"{peak_kind} (HBM copy, burst)",
+                     "algorithmic_bytes_per_launch": DECODE_KERNEL_BYTES_PER_SLOT * b.n,
+                     "kernel_us": kernel_avg * 1e6},
+        "clocks": clk,
+    }
+    if secondary:
+        line["secondary"] = secondary
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    slots = 8
+    dt, units = _oracle_decode_sample(slots, args.steps, args.warmup)
+    v = units / dt
+    return {"metric": METRIC, "value": v, "unit": UNIT, "impl": "reference", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DECODE_WORKLOAD, "sample": f"{slots} of the 64 active "
+                       "slots per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "cpu_baseline": {"value": v, "unit": UNIT, "kind": "oracle",
+                             "cores": int(os.environ.get("OMP_NUM_THREADS", "1") or 1),
+                             "sample": f"float64 numpy oracle, conv+SiLU + gated delta rule on "
+                                       f"{slots} slots per step, {args.steps} steps"}}
+
+
+def main():
+    args = _parse()
+    if args.cpu_baseline_child:
+        _cpu_baseline_child(args.cpu_seconds)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ.setdefault(v, "1")
+        line = run_reference(args, rank)
+    else:
+        line = run_gpu(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,391 @@
+// extern "C" entry points of libgdn: argument validation (always), optional
+// host-side validation of the index arrays, and the kernel launches.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <string>
+#include <vector>
+
+#include "gdn_internal.h"
+
+struct gdn_pool {
+  gdn::PoolView view;
+  gdn_pool_desc desc;
+  int device;
+};
+
+namespace {
+
+thread_local std::string g_last_msg;
+
+gdn_status fail(gdn_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_msg = buf;
+  return s;
+}
+
+gdn_status ok() {
+  g_last_msg.clear();
+  return GDN_OK;
+}
+
+gdn_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(GDN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool dtype_ok(gdn_dtype d) { return d == GDN_F32 || d == GDN_BF16; }
+size_t dtype_size(gdn_dtype d) { return d == GDN_F32 ? 4 : 2; }
+bool dk_supported(int dk) { return dk == 16 || dk == 32 || dk == 64 || dk == 128; }
+
+gdn_status check_desc(const gdn_pool_desc *d) {
+  if (!d) return fail(GDN_ERR_ARG, "desc is NULL");
+  if (d->n_layers < 1 || d->n_slots < 1 || d->h_v < 1 || d->h_k < 1 || d->dk < 1 || d->dv < 1 ||
+      d->conv_ch < 1 || d->conv_k < 1)
+    return fail(GDN_ERR_ARG, "pool dimensions must be positive");
+  if (d->h_v % d->h_k != 0) return fail(GDN_ERR_ARG, "h_v (%d) is not a multiple of h_k (%d)",
+                                        d->h_v, d->h_k);
+  if (!dtype_ok(d->conv_dtype)) return fail(GDN_ERR_DTYPE, "conv_dtype must be F32 or BF16");
+  if (!dk_supported(d->dk)) return fail(GDN_ERR_UNSUPPORTED, "dk=%d (supported: 16,32,64,128)",
+                                        d->dk);
+  if (d->dv % 4 != 0 || d->dv > 4096) return fail(GDN_ERR_UNSUPPORTED,
+                                                  "dv=%d must be a multiple of 4, <= 4096", d->dv);
+  if (d->conv_k < 2 || d->conv_k > 8) return fail(GDN_ERR_UNSUPPORTED, "conv_k=%d (2..8)",
+                                                  d->conv_k);
+  if (d->n_slots > 65535) return fail(GDN_ERR_UNSUPPORTED, "n_slots=%d (max 65535)", d->n_slots);
+  return GDN_OK;
+}
+
+gdn_status check_pool(const gdn_pool *p, int layer) {
+  if (!p) return fail(GDN_ERR_ARG, "pool is NULL");
+  if (layer < 0 || layer >= p->desc.n_layers)
+    return fail(GDN_ERR_ARG, "layer %d outside [0, %d)", layer, p->desc.n_layers);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != p->device)
+    return fail(GDN_ERR_ARG, "current device %d is not the pool's device %d", dev, p->device);
+  return GDN_OK;
+}
+
+// Under host checks: is this pointer something the device can dereference?
+gdn_status check_device_ptr(const void *ptr, const char *name) {
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(GDN_ERR_ARG, "%s: cudaPointerGetAttributes failed", name);
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(GDN_ERR_ARG, "%s is not device memory", name);
+  return GDN_OK;
+}
+
+gdn_status fetch(std::vector<int32_t> &dst, const int32_t *src, size_t n, cudaStream_t s,
+                 const char *name) {
+  dst.resize(n);
+  if (n == 0) return GDN_OK;
+  gdn_status st = check_device_ptr(src, name);
+  if (st != GDN_OK) return st;
+  cudaError_t e = cudaMemcpyAsync(dst.data(), src, n * sizeof(int32_t), cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "copying index array to host");
+  return GDN_OK;
+}
+
+gdn_status check_slots(const gdn_pool *p, const int32_t *slot_ids, int n, cudaStream_t s) {
+  std::vector<int32_t> h;
+  gdn_status st = fetch(h, slot_ids, (size_t)n, s, "slot_ids");
+  if (st != GDN_OK) return st;
+  std::vector<unsigned char> seen((size_t)p->desc.n_slots, 0);
+  for (int i = 0; i < n; ++i) {
+    if (h[i] < 0 || h[i] >= p->desc.n_slots)
+      return fail(GDN_ERR_SLOT, "slot_ids[%d] = %d outside [0, %d)", i, h[i], p->desc.n_slots);
+    if (seen[h[i]]) return fail(GDN_ERR_DUP_SLOT, "slot id %d repeated (entry %d)", h[i], i);
+    seen[h[i]] = 1;
+  }
+  return GDN_OK;
+}
+
+gdn_status check_cu(const int32_t *cu, int n_seqs, int total, cudaStream_t s,
+                    std::vector<int32_t> &h) {
+  gdn_status st = fetch(h, cu, (size_t)n_seqs + 1, s, "cu_seqlens");
+  if (st != GDN_OK) return st;
+  if (h[0] != 0) return fail(GDN_ERR_SIZE, "cu_seqlens[0] = %d, expected 0", h[0]);
+  for (int i = 0; i < n_seqs; ++i)
+    if (h[i + 1] < h[i]) return fail(GDN_ERR_SIZE, "cu_seqlens decreases at %d", i);
+  if (h[n_seqs] != total)
+    return fail(GDN_ERR_SIZE, "cu_seqlens[%d] = %d, expected total_tokens %d", n_seqs, h[n_seqs],
+                total);
+  return GDN_OK;
+}
+
+gdn_status check_counts(const int32_t *cnt, int n, const std::vector<int32_t> *cu, int fixed,
+                        cudaStream_t s, const char *name) {
+  std::vector<int32_t> h;
+  gdn_status st = fetch(h, cnt, (size_t)n, s, name);
+  if (st != GDN_OK) return st;
+  for (int i = 0; i < n; ++i) {
+    const int lim = cu ? (*cu)[i + 1] - (*cu)[i] : fixed;
+    if (h[i] < 0 || h[i] > lim)
+      return fail(GDN_ERR_SIZE, "%s[%d] = %d outside [0, %d]", name, i, h[i], lim);
+  }
+  return GDN_OK;
+}
+
+// Validate and resolve a gdn_qkv for `tokens` tokens.
+gdn_status resolve_qkv(const gdn_pool *p, const gdn_qkv *in, int64_t tokens, gdn::QKV &out) {
+  if (!in) return fail(GDN_ERR_ARG, "inputs struct is NULL");
+  if (!dtype_ok(in->dtype)) return fail(GDN_ERR_DTYPE, "input dtype must be F32 or BF16");
+  if (!in->q || !in->k || !in->v || !in->g || !in->beta)
+    return fail(GDN_ERR_ARG, "q, k, v, g and beta must all be non-NULL");
+  const gdn_pool_desc &d = p->desc;
+  const int64_t ld_qk = in->ld_qk ? in->ld_qk : (int64_t)d.h_k * d.dk;
+  const int64_t ld_v = in->ld_v ? in->ld_v : (int64_t)d.h_v * d.dv;
+  if (ld_qk < (int64_t)d.h_k * d.dk || ld_v < (int64_t)d.h_v * d.dv)
+    return fail(GDN_ERR_ARG, "token strides smaller than a token (ld_qk %lld, ld_v %lld)",
+                (long long)ld_qk, (long long)ld_v);
+  const size_t es = dtype_size(in->dtype);
+  const size_t al = in->dtype == GDN_F32 ? 16 : 8;
+  if ((uintptr_t)in->q % al || (uintptr_t)in->k % al || ((size_t)ld_qk * es) % al)
+    return fail(GDN_ERR_ARG, "q/k rows must start %zu-byte aligned", al);
+  if (p->desc.host_checks && tokens > 0) {
+    gdn_status st;
+    if ((st = check_device_ptr(in->q, "q")) || (st = check_device_ptr(in->k, "k")) ||
+        (st = check_device_ptr(in->v, "v")) || (st = check_device_ptr(in->g, "g")) ||
+        (st = check_device_ptr(in->beta, "beta")))
+      return st;
+  }
+  out = gdn::QKV{in->q, in->k, in->v, in->g, in->beta, ld_qk, ld_v, in->dtype};
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_ARG: return "GDN_ERR_ARG";
+    case GDN_ERR_SLOT: return "GDN_ERR_SLOT";
+    case GDN_ERR_DUP_SLOT: return "GDN_ERR_DUP_SLOT";
+    case GDN_ERR_DTYPE: return "GDN_ERR_DTYPE";
+    case GDN_ERR_SIZE: return "GDN_ERR_SIZE";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+  }
+  return "GDN_ERR_<unknown>";
+}
+
+const char *gdn_last_error_message(void) { return g_last_msg.c_str(); }
+
+size_t gdn_pool_state_bytes(const gdn_pool_desc *d) {
+  if (!d || d->n_layers < 0 || d->n_slots < 0) return 0;
+  return (size_t)d->n_layers * d->n_slots * d->h_v * d->dv * d->dk * sizeof(float);
+}
+
+size_t gdn_pool_conv_bytes(const gdn_pool_desc *d) {
+  if (!d || d->n_layers < 0 || d->n_slots < 0 || d->conv_k < 1) return 0;
+  return (size_t)d->n_layers * d->n_slots * d->conv_ch * (d->conv_k - 1) *
+         dtype_size(d->conv_dtype);
+}
+
+gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t state_bytes,
+                           void *conv_mem, size_t conv_bytes, gdn_pool **out) {
+  if (!out) return fail(GDN_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  gdn_status st = check_desc(desc);
+  if (st != GDN_OK) return st;
+  if (!state_mem || !conv_mem) return fail(GDN_ERR_ARG, "state_mem and conv_mem must be non-NULL");
+  if ((uintptr_t)state_mem % 16 || (uintptr_t)conv_mem % 16)
+    return fail(GDN_ERR_ARG, "state_mem and conv_mem must be 16-byte aligned");
+  if (state_bytes < gdn_pool_state_bytes(desc))
+    return fail(GDN_ERR_SIZE, "state_bytes %zu < %zu needed", state_bytes,
+                gdn_pool_state_bytes(desc));
+  if (conv_bytes < gdn_pool_conv_bytes(desc))
+    return fail(GDN_ERR_SIZE, "conv_bytes %zu < %zu needed", conv_bytes, gdn_pool_conv_bytes(desc));
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (desc->host_checks) {
+    if ((st = check_device_ptr(state_mem, "state_mem")) ||
+        (st = check_device_ptr(conv_mem, "conv_mem")))
+      return st;
+  }
+  unsigned int *err = nullptr;
+  e = cudaMalloc(&err, sizeof(unsigned int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+  e = cudaMemset(err, 0, sizeof(unsigned int));
+  if (e != cudaSuccess) {
+    cudaFree(err);
+    return cuda_fail(e, "cudaMemset(error word)");
+  }
+  gdn_pool *p = new gdn_pool;
+  p->desc = *desc;
+  p->device = dev;
+  p->view = gdn::PoolView{static_cast<float *>(state_mem), conv_mem, err,
+                          desc->n_layers, desc->n_slots, desc->h_v, desc->h_k, desc->dk,
+                          desc->dv, desc->conv_ch, desc->conv_k, desc->conv_dtype};
+  *out = p;
+  return ok();
+}
+
+gdn_status gdn_pool_destroy(gdn_pool *p) {
+  if (!p) return ok();
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaError_t e2 = cudaFree(p->view.err);
+  delete p;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree(error word)");
+  return ok();
+}
+
+gdn_status gdn_pool_get_error(gdn_pool *p, uint32_t *dev_err) {
+  if (!p || !dev_err) return fail(GDN_ERR_ARG, "pool and dev_err must be non-NULL");
+  unsigned int h = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&h, p->view.err, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(p->view.err, 0, sizeof(h));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *dev_err = h;
+  return ok();
+}
+
+gdn_status gdn_pool_reset(gdn_pool *p, const int32_t *slot_ids, int32_t n, gdn_stream stream) {
+  gdn_status st = check_pool(p, 0);
+  if (st != GDN_OK) return st;
+  if (n < 0) return fail(GDN_ERR_ARG, "n = %d < 0", n);
+  if (n == 0) return ok();
+  if (!slot_ids) return fail(GDN_ERR_ARG, "slot_ids is NULL");
+  if (n > 65535) return fail(GDN_ERR_SIZE, "n = %d > 65535", n);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks && (st = check_slots(p, slot_ids, n, s))) return st;
+  cudaError_t e = gdn::launch_pool_reset(p->view, slot_ids, n, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pool reset launch");
+  return ok();
+}
+
+gdn_status gdn_conv_silu(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                         const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                         int32_t max_seqlen, const void *x, int64_t ld_x, gdn_dtype x_dtype,
+                         const float *w, const float *bias, void *y, int64_t ld_y,
+                         const int32_t *advance, gdn_stream stream) {
+  gdn_status st = check_pool(p, layer);
+  if (st != GDN_OK) return st;
+  if (n_seqs < 0 || total_tokens < 0) return fail(GDN_ERR_ARG, "negative n_seqs/total_tokens");
+  if (n_seqs > 65535) return fail(GDN_ERR_SIZE, "n_seqs = %d > 65535", n_seqs);
+  if (!cu_seqlens && total_tokens != n_seqs)
+    return fail(GDN_ERR_SIZE, "without cu_seqlens total_tokens must equal n_seqs");
+  if (n_seqs == 0 || total_tokens == 0) return ok();
+  if (x_dtype != p->desc.conv_dtype)
+    return fail(GDN_ERR_DTYPE, "x dtype differs from the pool's conv_dtype");
+  if (!slot_ids || !x || !w) return fail(GDN_ERR_ARG, "slot_ids, x and w must be non-NULL");
+  const int64_t C = p->desc.conv_ch;
+  if (ld_x == 0) ld_x = C;
+  if (ld_y == 0) ld_y = C;
+  if (ld_x < C || ld_y < C) return fail(GDN_ERR_ARG, "row strides smaller than conv_ch");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    if ((st = check_slots(p, slot_ids, n_seqs, s))) return st;
+    std::vector<int32_t> cu;
+    if (cu_seqlens && (st = check_cu(cu_seqlens, n_seqs, total_tokens, s, cu))) return st;
+    if (advance && (st = check_counts(advance, n_seqs, cu_seqlens ? &cu : nullptr, 1, s,
+                                      "advance")))
+      return st;
+    if ((st = check_device_ptr(x, "x")) || (st = check_device_ptr(w, "w")) ||
+        (bias && (st = check_device_ptr(bias, "bias"))) ||
+        (y && (st = check_device_ptr(y, "y"))))
+      return st;
+  }
+  gdn::SeqIndex seq{slot_ids, cu_seqlens, n_seqs, total_tokens};
+  cudaError_t e = gdn::launch_conv_silu(p->view, layer, seq, max_seqlen < 1 ? 1 : max_seqlen, x,
+                                        ld_x, w, bias, y, ld_y, advance, s);
+  if (e != cudaSuccess) return cuda_fail(e, "conv launch");
+  return ok();
+}
+
+gdn_status gdn_decode_step(gdn_pool *p, int32_t layer, const int32_t *slot_ids, int32_t n,
+                           const gdn_qkv *in, void *o, gdn_dtype o_dtype, float scale,
+                           gdn_stream stream) {
+  gdn_status st = check_pool(p, layer);
+  if (st != GDN_OK) return st;
+  if (n < 0) return fail(GDN_ERR_ARG, "n = %d < 0", n);
+  if (n == 0) return ok();
+  if (n > 65535) return fail(GDN_ERR_SIZE, "n = %d > 65535", n);
+  if (!slot_ids || !o) return fail(GDN_ERR_ARG, "slot_ids and o must be non-NULL");
+  if (!dtype_ok(o_dtype)) return fail(GDN_ERR_DTYPE, "o dtype must be F32 or BF16");
+  gdn::QKV q;
+  if ((st = resolve_qkv(p, in, n, q))) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    if ((st = check_slots(p, slot_ids, n, s)) || (st = check_device_ptr(o, "o"))) return st;
+  }
+  cudaError_t e = gdn::launch_decode(p->view, layer, slot_ids, n, q, o, o_dtype, scale, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return ok();
+}
+
+gdn_status gdn_spec_verify(gdn_pool *p, int32_t layer, const int32_t *slot_ids, int32_t n,
+                           int32_t T, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
+                           const int32_t *accept_len, float scale, gdn_stream stream) {
+  gdn_status st = check_pool(p, layer);
+  if (st != GDN_OK) return st;
+  if (n < 0) return fail(GDN_ERR_ARG, "n = %d < 0", n);
+  if (T < 1 || T > gdn::kMaxVerifyT)
+    return fail(GDN_ERR_SIZE, "T = %d outside [1, %d]", T, gdn::kMaxVerifyT);
+  if (!o && !accept_len) return fail(GDN_ERR_ARG, "o and accept_len are both NULL");
+  if (n == 0) return ok();
+  if (n > 65535) return fail(GDN_ERR_SIZE, "n = %d > 65535", n);
+  if (!slot_ids) return fail(GDN_ERR_ARG, "slot_ids is NULL");
+  if (!dtype_ok(o_dtype)) return fail(GDN_ERR_DTYPE, "o dtype must be F32 or BF16");
+  gdn::QKV q;
+  if ((st = resolve_qkv(p, in, (int64_t)n * T, q))) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    if ((st = check_slots(p, slot_ids, n, s))) return st;
+    if (accept_len && (st = check_counts(accept_len, n, nullptr, T, s, "accept_len"))) return st;
+    if (o && (st = check_device_ptr(o, "o"))) return st;
+  }
+  cudaError_t e =
+      gdn::launch_verify(p->view, layer, slot_ids, n, T, q, o, o_dtype, accept_len, scale, s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  return ok();
+}
+
+gdn_status gdn_prefill_chunked(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                               const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                               int32_t max_seqlen, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
+                               float scale, gdn_stream stream) {
+  gdn_status st = check_pool(p, layer);
+  if (st != GDN_OK) return st;
+  if (n_seqs < 0 || total_tokens < 0) return fail(GDN_ERR_ARG, "negative n_seqs/total_tokens");
+  if (n_seqs == 0 || total_tokens == 0) return ok();
+  if (n_seqs > 65535) return fail(GDN_ERR_SIZE, "n_seqs = %d > 65535", n_seqs);
+  if (!slot_ids || !cu_seqlens || !o)
+    return fail(GDN_ERR_ARG, "slot_ids, cu_seqlens and o must be non-NULL");
+  if (!dtype_ok(o_dtype)) return fail(GDN_ERR_DTYPE, "o dtype must be F32 or BF16");
+  gdn::QKV q;
+  if ((st = resolve_qkv(p, in, total_tokens, q))) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    std::vector<int32_t> cu;
+    if ((st = check_slots(p, slot_ids, n_seqs, s)) ||
+        (st = check_cu(cu_seqlens, n_seqs, total_tokens, s, cu)) ||
+        (st = check_device_ptr(o, "o")))
+      return st;
+  }
+  gdn::SeqIndex seq{slot_ids, cu_seqlens, n_seqs, total_tokens};
+  cudaError_t e = gdn::launch_prefill(p->view, layer, seq, total_tokens,
+                                      max_seqlen < 1 ? 1 : max_seqlen, q, o, o_dtype, scale, s);
+  if (e == cudaErrorNotSupported)
+    return fail(GDN_ERR_UNSUPPORTED, "chunked prefill is not available for this shape");
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return ok();
+}
+
+}  // extern "C"

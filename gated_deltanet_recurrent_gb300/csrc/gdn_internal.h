@@ -1,0 +1,67 @@
+// Internal kernel-argument structs and launcher declarations of libgdn.
+// Host code in gdn_api.cu validates arguments and calls these launchers; each
+// launcher lives next to its kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+#if defined(__CUDACC__)
+#define GDN_HD __host__ __device__ __forceinline__
+#else
+#define GDN_HD inline
+#endif
+
+namespace gdn {
+
+constexpr float kL2Eps = 1e-6f;
+constexpr int kChunk = 64;          // prefill chunk length
+constexpr int kMaxVerifyT = 32;     // drafts per slot in one verify call
+
+struct PoolView {
+  float *state;            // [n_layers][n_slots][h_v][dv][dk]
+  void *conv;              // [n_layers][n_slots][conv_ch][conv_k-1]
+  unsigned int *err;       // device error word
+  int n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k;
+  gdn_dtype conv_dtype;
+  GDN_HD int64_t state_slot_elems() const { return (int64_t)h_v * dv * dk; }
+  GDN_HD int64_t conv_slot_elems() const { return (int64_t)conv_ch * (conv_k - 1); }
+};
+
+struct QKV {
+  const void *q, *k, *v, *g, *beta;
+  int64_t ld_qk, ld_v;     // resolved (never 0)
+  gdn_dtype dtype;
+};
+
+// Per-slot token range of a call: sequence i covers tokens [tok0, tok0 + len).
+struct SeqIndex {
+  const int32_t *slot_ids;
+  const int32_t *cu_seqlens;   // NULL: one token per sequence
+  int n_seqs;
+  int total_tokens;            // rows of the packed token arrays
+};
+
+cudaError_t launch_pool_reset(const PoolView &p, const int32_t *slot_ids, int n,
+                              cudaStream_t s);
+
+cudaError_t launch_conv_silu(const PoolView &p, int layer, const SeqIndex &seq,
+                             int max_seqlen, const void *x, int64_t ld_x,
+                             const float *w, const float *bias, void *y, int64_t ld_y,
+                             const int32_t *advance, cudaStream_t s);
+
+cudaError_t launch_decode(const PoolView &p, int layer, const int32_t *slot_ids, int n,
+                          const QKV &in, void *o, gdn_dtype o_dtype, float scale,
+                          cudaStream_t s);
+
+cudaError_t launch_verify(const PoolView &p, int layer, const int32_t *slot_ids, int n,
+                          int T, const QKV &in, void *o, gdn_dtype o_dtype,
+                          const int32_t *accept_len, float scale, cudaStream_t s);
+
+cudaError_t launch_prefill(const PoolView &p, int layer, const SeqIndex &seq,
+                           int total_tokens, int max_seqlen, const QKV &in, void *o,
+                           gdn_dtype o_dtype, float scale, cudaStream_t s);
+
+}  // namespace gdn

@@ -1,0 +1,205 @@
+/*
+ * gdn.h -- C ABI of libgdn: the Gated DeltaNet layer over a slot-indexed pool
+ * of independent per-request recurrent states, for NVIDIA GB300 (sm_103a).
+ *
+ * Why a pool: one recurrent state per layer forces concurrent requests to run
+ * one after another (baseRT issue #31, "Summary" and "Measurement": four
+ * requests take four times as long as one).  The fix that page proposes is an
+ * outer slot dimension on the state cache and a slot index in the GDN kernels
+ * ("Why this looks tractable").  This library is that: a pool of
+ * [n_layers][n_slots] states, and kernels that take a list of slot ids.
+ *
+ * Per value head h of a slot, with key head h' = h / (h_v / h_k), each token
+ * applies the gated delta rule
+ *     S <- alpha * S (I - beta k k^T) + beta v k^T,      o = scale * S q
+ * where S is [dv][dk] float32, q and k are L2-normalised inside the kernels
+ * (x / sqrt(sum x^2 + 1e-6)), alpha = exp(g) with g <= 0 given per token and
+ * value head, and o is read from the updated state.
+ *
+ * Conventions for every call:
+ *  - All array arguments are DEVICE pointers (cudaMalloc / torch memory),
+ *    owned by the caller; the library never frees them.  Index arrays
+ *    (slot_ids, cu_seqlens, advance, accept_len) are int32 device arrays too,
+ *    so a call needs no host round trip and can be recorded into a stream.
+ *  - Every compute call is asynchronous on `stream` (NULL = legacy default
+ *    stream).  The returned status covers argument validation and the launch.
+ *  - With desc.host_checks != 0 the library additionally copies the index
+ *    arrays to the host (synchronising `stream`) and validates them: slot ids
+ *    in range and not repeated, cu_seqlens[0] == 0 and non-decreasing and
+ *    ending at total_tokens, 0 <= advance/accept_len <= the sequence length;
+ *    it also checks that every pointer is device-accessible.  A failed check
+ *    launches nothing.
+ *  - With host checks off, kernels still guard their indexes: an entry with a
+ *    slot id out of range or a malformed length is skipped and a bit is set in
+ *    the pool's device error word (see gdn_pool_get_error).  Kernels never
+ *    trap.  Repeated slot ids in one call are not detected on the device and
+ *    give unspecified results for those slots.
+ *  - n == 0 / empty sequences are valid no-ops.
+ *  - The state layout is [n_layers][n_slots][h_v][dv][dk] float32 and the conv
+ *    cache [n_layers][n_slots][conv_ch][conv_k-1] in conv_dtype, oldest input
+ *    first; both are plain caller memory, so a state can be written, read,
+ *    copied or saved with ordinary memcpy.
+ *  - Not thread-safe per pool: calls on one pool from several host threads
+ *    must be serialised by the caller.  Calls on different streams that touch
+ *    the same slot race.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *gdn_stream; /* identical to cudaStream_t */
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_ARG = 1,         /* null pointer, negative count, bad layer, misaligned pointer */
+  GDN_ERR_SLOT = 2,        /* slot id outside [0, n_slots) (host check) */
+  GDN_ERR_DUP_SLOT = 3,    /* a slot id repeated within one call (host check) */
+  GDN_ERR_DTYPE = 4,       /* dtype not supported for this argument */
+  GDN_ERR_SIZE = 5,        /* buffer too small, malformed cu_seqlens, length/T out of range */
+  GDN_ERR_UNSUPPORTED = 6, /* a shape this build has no kernel for (see gdn_pool_create) */
+  GDN_ERR_CUDA = 7         /* a CUDA runtime call failed (gdn_last_error_message has it) */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Bits of the pool's device error word. */
+#define GDN_DEVERR_SLOT 1u   /* an entry with an out-of-range slot id was skipped */
+#define GDN_DEVERR_SEQ 2u    /* an entry with a malformed cu_seqlens range was skipped */
+#define GDN_DEVERR_COUNT 4u  /* an advance/accept_len outside [0, length] was clamped */
+#define GDN_DEVERR_TIMEOUT 8u /* a bounded wait on an asynchronous copy gave up; outputs of
+                                 that CTA are missing (never expected; reported, not hung) */
+
+/* Shape of every GDN layer in the pool.  Supported: dk in {16, 32, 64, 128},
+ * dv a multiple of 4 (<= 4096), h_v a multiple of h_k, 2 <= conv_k <= 8,
+ * conv_ch >= 1, conv_dtype GDN_F32 or GDN_BF16. */
+typedef struct {
+  int32_t n_layers;
+  int32_t n_slots;
+  int32_t h_v;        /* value heads (one state per value head) */
+  int32_t h_k;        /* key/query heads; value head h uses key head h / (h_v / h_k) */
+  int32_t dk;         /* key head dim = state columns */
+  int32_t dv;         /* value head dim = state rows */
+  int32_t conv_ch;    /* channels of the short conv */
+  int32_t conv_k;     /* conv width; the cache keeps conv_k - 1 inputs */
+  gdn_dtype conv_dtype; /* dtype of conv inputs/outputs and of the cache */
+  int32_t host_checks;  /* nonzero: validate index arrays on the host (syncs) */
+} gdn_pool_desc;
+
+/* Per-token inputs of the recurrence for `tokens` tokens.
+ *   q, k  [tokens][h_k][dk]  token stride ld_qk elements (0: h_k*dk)
+ *   v     [tokens][h_v][dv]  token stride ld_v elements  (0: h_v*dv)
+ *   g     [tokens][h_v]      log of the decay, alpha = exp(g) (g <= 0 expected)
+ *   beta  [tokens][h_v]      delta-rule write strength
+ * All five have type `dtype`.  Each head row must start 16-byte aligned for
+ * GDN_F32 and 8-byte aligned for GDN_BF16 (base pointers and strides). */
+typedef struct {
+  const void *q, *k, *v, *g, *beta;
+  int64_t ld_qk, ld_v;
+  gdn_dtype dtype;
+} gdn_qkv;
+
+typedef struct gdn_pool gdn_pool;
+
+/* Bytes of state / conv-cache memory a pool with this shape needs. */
+size_t gdn_pool_state_bytes(const gdn_pool_desc *desc);
+size_t gdn_pool_conv_bytes(const gdn_pool_desc *desc);
+
+/* State cache create (baseRT issue #31, "Why this looks tractable":
+ * GDNStateCache::create sized by layers, heads, head dim and conv_k, plus the
+ * slot dimension that page asks for).  Wraps caller memory: state_mem and
+ * conv_mem (256-byte aligned device memory of at least the sizes above) are
+ * NOT cleared -- call gdn_pool_reset for new requests, or write states
+ * directly.  The pool allocates only a 4-byte device error word.
+ * On success *out receives the handle. */
+gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t state_bytes,
+                           void *conv_mem, size_t conv_bytes, gdn_pool **out);
+
+/* Zero the state and conv cache of slots slot_ids[0..n) in every layer
+ * (ai-infra-handbooks, "Project: adding the hybrid model Qwen3.5", "What to
+ * do", State row: a new request starts from zero; a reused slot is cleared).
+ * Other slots are not touched. */
+gdn_status gdn_pool_reset(gdn_pool *pool, const int32_t *slot_ids, int32_t n, gdn_stream stream);
+
+/* Release the handle and its error word (caller memory is left alone).
+ * Synchronises the device before freeing. NULL is a no-op. */
+gdn_status gdn_pool_destroy(gdn_pool *pool);
+
+/* Wait for the device, return the device error word (GDN_DEVERR_* bits
+ * accumulated since the last call) in *dev_err and clear it. */
+gdn_status gdn_pool_get_error(gdn_pool *pool, uint32_t *dev_err);
+
+/* Causal depthwise conv of width conv_k followed by SiLU (baseRT issue #31,
+ * "Why this looks tractable": gdn_conv_silu), on each sequence's slot cache.
+ * Sequence i is tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 of x and uses the
+ * cache of slot slot_ids[i]; cu_seqlens == NULL means one token per sequence
+ * (decode).  For each token t and channel c:
+ *     y[t][c] = silu(sum_j w[c][j] * win[j] + bias[c]),
+ *     win = (cache[c][0..conv_k-2], x[t-conv_k+1..t][c]) restricted to the
+ *     conv_k most recent inputs, w[c][conv_k-1] on the current token.
+ * x, y: [total_tokens][conv_ch] in the pool's conv_dtype with row strides
+ * ld_x / ld_y elements (0: conv_ch); w: [conv_ch][conv_k] float32;
+ * bias: [conv_ch] float32 or NULL.  y may be NULL (cache update only).
+ * The cache then holds the conv_k-1 raw inputs preceding token advance[i] of
+ * the sequence (advance == NULL: the whole sequence), so speculative tokens
+ * can be run without moving the cache and committed later.
+ * max_seqlen: an upper bound of the sequence lengths, used only to size the
+ * grid (any value >= 1 is correct; a tight one is fastest). */
+gdn_status gdn_conv_silu(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
+                         const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                         int32_t max_seqlen, const void *x, int64_t ld_x, gdn_dtype x_dtype,
+                         const float *w, const float *bias, void *y, int64_t ld_y,
+                         const int32_t *advance, gdn_stream stream);
+
+/* One decode token for each of n active slots (baseRT issue #31, "Why this
+ * looks tractable": gdn_recurrence, with the slot index that page asks for).
+ * Token i of `in` belongs to slot slot_ids[i]; every head of that slot's
+ * state in `layer` is read once and written once.  o: [n][h_v][dv] in
+ * o_dtype (GDN_F32 or GDN_BF16), read from the updated state. */
+gdn_status gdn_decode_step(gdn_pool *pool, int32_t layer, const int32_t *slot_ids, int32_t n,
+                           const gdn_qkv *in, void *o, gdn_dtype o_dtype, float scale,
+                           gdn_stream stream);
+
+/* Chunked prefill of packed variable-length sequences (b70-optimization-lab
+ * research plan, "What the research found": the chunked delta rule with the
+ * (I+A)^{-1} UT transform; ai-infra-handbooks Qwen3.5 project, "What to do",
+ * State row: the state is carried from chunk to chunk).  Sequence i is tokens
+ * cu_seqlens[i] .. cu_seqlens[i+1]-1 and starts from slot slot_ids[i]'s
+ * current state, which holds the final state afterwards, so a long prompt
+ * can be fed in several calls.  Chunks are 64 tokens; the last one of each
+ * sequence may be partial.  o: [total_tokens][h_v][dv] in o_dtype.
+ * max_seqlen as for gdn_conv_silu. */
+gdn_status gdn_prefill_chunked(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
+                               const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                               int32_t max_seqlen, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
+                               float scale, gdn_stream stream);
+
+/* Speculative verify of T draft tokens per slot without per-position state
+ * snapshots (b70-optimization-lab research plan, "What the research found").
+ * Draft t of slot slot_ids[i] is token i*T + t of `in`.  o_t ([n][T][h_v][dv],
+ * may be NULL) is what t+1 decode steps from the slot's state would output.
+ * accept_len (may be NULL; [n] int32 in [0, T]) commits each slot's state to
+ * the state after accept_len[i] tokens, written once; 0 leaves it untouched.
+ * With accept_len == NULL the pool is only read (verify-then-commit in two
+ * calls, the second recomputing from the same inputs).  o and accept_len
+ * must not both be NULL.  1 <= T <= 32. */
+gdn_status gdn_spec_verify(gdn_pool *pool, int32_t layer, const int32_t *slot_ids, int32_t n,
+                           int32_t T, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
+                           const int32_t *accept_len, float scale, gdn_stream stream);
+
+/* Human-readable name of a status, and the detail of the last failure on
+ * this host thread (empty string if none). */
+const char *gdn_status_string(gdn_status s);
+const char *gdn_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,210 @@
+"""GPU parity of gdn_prefill_chunked (and the tiny end-to-end request flow)
+against the float64 oracle, through the C ABI.
+
+float32 inputs: max|gpu - ref| <= 1e-4 * max|ref| per tensor.  bf16 inputs:
+|gpu - ref| <= 1e-2 + 1e-2 |ref| elementwise.  Full-size cases are checked on
+a sample of value heads (the oracle runs only those heads); untouched slots
+are checked bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_recurrent_gb300 import abi, synth
+from oracle import gdn_oracle as O
+from tests.gpu_util import (assert_close_bf16, assert_maxrel, dev, dev_i32, host, tok_dev,
+                            tok_np)
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 3.25
+
+
+def _pool(shape, n_layers, n_slots, conv_dtype=torch.float32, host_checks=True):
+    p = abi.Pool.for_shape(shape, n_layers, n_slots, conv_dtype=conv_dtype,
+                           host_checks=host_checks)
+    p.state.fill_(SENTINEL)
+    p.conv.fill_(-SENTINEL)
+    return p
+
+
+def _run_tiny_request_gpu(pool, wl, i, slot):
+    seq = wl["seqs"][i]
+    L = wl["lengths"][i]
+    tok, x = seq["tok"], seq["x"]
+    sid = dev_i32([slot])
+    ys, os_ = [], []
+    w = dev(wl["conv_w"])
+    for lo in range(0, L, wl["piece"]):
+        hi = min(lo + wl["piece"], L)
+        cu = dev_i32([0, hi - lo])
+        y = torch.empty(hi - lo, wl["shape"].conv_ch, device="cuda")
+        abi.gdn_conv_silu(pool, 0, sid, dev(x[lo:hi]), w, y, cu_seqlens=cu)
+        o = torch.empty(hi - lo, wl["shape"].h_v, wl["shape"].dv, device="cuda")
+        abi.gdn_prefill_chunked(pool, 0, sid, cu, *[dev(tok[n][lo:hi]) for n in
+                                                    ("q", "k", "v", "g", "beta")], o)
+        ys.append(y)
+        os_.append(o)
+    for t in range(L, L + wl["n_decode"]):
+        y = torch.empty(1, wl["shape"].conv_ch, device="cuda")
+        abi.gdn_conv_silu(pool, 0, sid, dev(x[t:t + 1]), w, y)
+        o = torch.empty(1, wl["shape"].h_v, wl["shape"].dv, device="cuda")
+        abi.gdn_decode_step(pool, 0, sid, *[dev(tok[n][t:t + 1]) for n in
+                                            ("q", "k", "v", "g", "beta")], o)
+        ys.append(y)
+        os_.append(o)
+    return host(torch.cat(ys)), host(torch.cat(os_))
+
+
+def _run_tiny_request_ref(ref, wl, i, slot):
+    seq = wl["seqs"][i]
+    L = wl["lengths"][i]
+    tok, x = seq["tok"], seq["x"]
+    ys, os_ = [], []
+    for lo in range(0, L, wl["piece"]):
+        hi = min(lo + wl["piece"], L)
+        ys.append(ref.conv_silu(0, [slot], [0, hi - lo], x[lo:hi], wl["conv_w"]))
+        os_.append(ref.prefill(0, [slot], [0, hi - lo], *(tok[n][lo:hi] for n in
+                                                           ("q", "k", "v", "g", "beta"))))
+    for t in range(L, L + wl["n_decode"]):
+        ys.append(ref.conv_silu(0, [slot], None, x[t:t + 1], wl["conv_w"]))
+        os_.append(ref.decode_step(0, [slot], *(tok[n][t:t + 1] for n in
+                                                ("q", "k", "v", "g", "beta"))))
+    return np.concatenate(ys), np.concatenate(os_)
+
+
+def test_tiny_request_flow_prefill_decode_reset_rerun():
+    """Pool of 4 slots; sequences of 7 and 13 tokens in slots 1 and 3 fed in
+    4-token prefill pieces, 5 decode steps; reset slot 1 and rerun it."""
+    wl = synth.tiny_workload(0)
+    s = wl["shape"]
+    pool = _pool(s, 1, wl["n_slots"])
+    pool.set_host_checks(True)
+    abi.gdn_pool_reset(pool, dev_i32(wl["slots"]))
+    ref = O.OraclePool(1, wl["n_slots"], s.h_v, s.h_k, s.dk, s.dv, s.conv_ch, s.conv_k)
+    first = []
+    for i, slot in enumerate(wl["slots"]):
+        y, o = _run_tiny_request_gpu(pool, wl, i, slot)
+        y_ref, o_ref = _run_tiny_request_ref(ref, wl, i, slot)
+        assert_maxrel(y, y_ref, 1e-5, f"conv y, seq {i}")
+        assert_maxrel(o, o_ref, 1e-4, f"o, seq {i}")
+        first.append((y, o))
+    for slot in wl["slots"]:
+        assert_maxrel(host(pool.state[0, slot]), ref.S[0, slot], 1e-4, f"S slot {slot}")
+    np.testing.assert_array_equal(host(pool.conv[0, wl["slots"]]), ref.X[0, wl["slots"]])
+    S3 = pool.state[0, 3].clone()
+    abi.gdn_pool_reset(pool, dev_i32([1]))
+    y, o = _run_tiny_request_gpu(pool, wl, 0, 1)
+    np.testing.assert_array_equal(y, first[0][0])       # reset slot == fresh slot, bit for bit
+    np.testing.assert_array_equal(o, first[0][1])
+    assert torch.equal(pool.state[0, 3], S3)
+    assert bool((pool.state[:, [0, 2]] == SENTINEL).all())
+    assert bool((pool.conv[:, [0, 2]] == -SENTINEL).all())
+    assert abi.gdn_pool_get_error(pool) == 0
+
+
+@pytest.mark.parametrize("D", [16, 32, 64, 128])
+def test_prefill_varlen_edge_lengths(D):
+    rng = np.random.default_rng(40 + D)
+    shape = synth.LayerShape(4, 2, D, D, 16, 4)
+    lens = [1, 0, 64, 65, 130, 7]
+    ids = np.array([6, 2, 0, 5, 1, 3], dtype=np.int32)
+    cu = synth.cu_seqlens_of(lens)
+    pool = _pool(shape, 2, 8)
+    S0 = synth.random_states(rng, len(ids), shape)
+    lid = torch.from_numpy(ids).long().cuda()
+    pool.state[1, lid] = dev(S0)
+    tok = synth.token_inputs(rng, int(cu[-1]), shape, "f32")
+    o = torch.empty(int(cu[-1]), shape.h_v, shape.dv, device="cuda")
+    abi.gdn_prefill_chunked(pool, 1, dev_i32(ids), dev_i32(cu), *tok_dev(tok, "f32"), o,
+                            scale=D ** -0.5, max_seqlen=max(lens))
+    ref = O.OraclePool(1, 8, shape.h_v, shape.h_k, shape.dk, shape.dv, 16, 4)
+    ref.S[0, ids] = S0
+    o_ref = ref.prefill(0, ids, cu, *tok_np(tok), scale=D ** -0.5)
+    assert_maxrel(host(o), o_ref, 1e-4, "o")
+    assert_maxrel(host(pool.state[1, lid]), ref.S[0, ids], 1e-4, "S")
+    pool.state[1, lid] = SENTINEL
+    assert bool((pool.state == SENTINEL).all())
+
+
+def test_prefill_split_across_calls_equals_whole_and_token_recurrence():
+    rng = np.random.default_rng(41)
+    shape = synth.LayerShape(2, 1, 128, 128, 16, 4)
+    L = 301
+    S0 = synth.random_states(rng, 1, shape)
+    tok = synth.token_inputs(rng, L, shape, "f32")
+    outs = {}
+    for name, cuts in (("whole", [0, L]), ("pieces", [0, 64, 100, 101, 229, L])):
+        pool = _pool(shape, 1, 2)
+        pool.state[0, 1] = dev(S0[0])
+        parts = []
+        for lo, hi in zip(cuts[:-1], cuts[1:]):
+            o = torch.empty(hi - lo, shape.h_v, shape.dv, device="cuda")
+            abi.gdn_prefill_chunked(pool, 0, dev_i32([1]), dev_i32([0, hi - lo]),
+                                    *[dev(tok[n][lo:hi]) for n in ("q", "k", "v", "g", "beta")],
+                                    o)
+            parts.append(host(o))
+        outs[name] = (np.concatenate(parts), host(pool.state[0, 1]))
+    S_ref, o_ref = O.gdn_recurrent(S0[0], *tok_np(tok))
+    for name, (o, S) in outs.items():
+        assert_maxrel(o, o_ref, 1e-4, f"o {name}")
+        assert_maxrel(S, S_ref, 1e-4, f"S {name}")
+
+
+def _head_sample(tok, heads, group):
+    """Slice value heads `heads` (and the key heads they read) out of a token dict."""
+    kh = [h // group for h in heads]
+    return {"q": tok["q"][:, kh], "k": tok["k"][:, kh], "v": tok["v"][:, heads],
+            "g": tok["g"][:, heads], "beta": tok["beta"][:, heads]}
+
+
+def test_prefill_varlen_pieces_full_size_sampled_heads():
+    """8 sequences with lengths uniform in [512, 8192], fed in 2048-token
+    pieces with the state carried between calls; bf16 in and out; half the
+    slots start from zero, half from N(0, 0.1)."""
+    wl = synth.prefill_workload(seed=3)
+    s = wl["shape"]
+    lens, cu = wl["lengths"], wl["cu_seqlens"]
+    pool = _pool(s, 1, len(lens) + 2, conv_dtype=torch.bfloat16)
+    ids = wl["slot_ids"] + 1                                   # slots 1..8; 0 and 9 untouched
+    lid = torch.from_numpy(ids).long().cuda()
+    pool.state[0, lid] = dev(wl["states"])
+    tok_all = {n: dev(wl["tok"][n], "bf16") for n in ("q", "k", "v", "g", "beta")}
+    o = torch.empty(int(cu[-1]), s.h_v, s.dv, device="cuda", dtype=torch.bfloat16)
+    for idx, starts, ln in synth.prefill_calls(lens, wl["piece"]):
+        rows = np.concatenate([np.arange(cu[i] + st, cu[i] + st + l)
+                               for i, st, l in zip(idx, starts, ln)])
+        rt = torch.from_numpy(rows).long().cuda()
+        packed = [tok_all[n][rt].contiguous() for n in ("q", "k", "v", "g", "beta")]
+        ob = torch.empty(len(rows), s.h_v, s.dv, device="cuda", dtype=torch.bfloat16)
+        abi.gdn_prefill_chunked(pool, 0, dev_i32(ids[idx]), dev_i32(synth.cu_seqlens_of(ln)),
+                                *packed, ob, max_seqlen=max(ln))
+        o[rt] = ob
+    heads = [0, 17, 31]
+    group = s.h_v // s.h_k
+    sub = _head_sample(wl["tok"], heads, group)
+    for i in range(len(lens)):
+        lo, hi = cu[i], cu[i + 1]
+        S_ref, o_ref = O.gdn_recurrent(wl["states"][i][heads],
+                                       *(sub[n][lo:hi] for n in ("q", "k", "v", "g", "beta")))
+        assert_close_bf16(host(o[lo:hi][:, heads]), o_ref, what=f"o seq {i}")
+        assert_close_bf16(host(pool.state[0, ids[i]][heads]), S_ref, what=f"S seq {i}")
+    assert bool((pool.state[0, [0, 9]] == SENTINEL).all())
+
+
+def test_prefill_device_guard_and_host_checks():
+    shape = synth.LayerShape(2, 1, 16, 16, 16, 4)
+    rng = np.random.default_rng(42)
+    tok = tok_dev(synth.token_inputs(rng, 10, shape, "f32"), "f32")
+    o = torch.zeros(10, 2, 16, device="cuda")
+    pool = _pool(shape, 1, 4)
+    with pytest.raises(abi.GDNError) as e:
+        abi.gdn_prefill_chunked(pool, 0, dev_i32([0, 1]), dev_i32([0, 6, 9]), *tok, o)
+    assert e.value.name == "GDN_ERR_SIZE"
+    with pytest.raises(abi.GDNError) as e:
+        abi.gdn_prefill_chunked(pool, 0, dev_i32([0, 0]), dev_i32([0, 6, 10]), *tok, o)
+    assert e.value.name == "GDN_ERR_DUP_SLOT"
+    pool.set_host_checks(False)
+    abi.gdn_prefill_chunked(pool, 0, dev_i32([7, 1]), dev_i32([0, 6, 10]), *tok, o)
+    assert abi.gdn_pool_get_error(pool) == abi.DEVERR_SLOT
+    assert bool((pool.state[0, [0, 2, 3]] == SENTINEL).all())
+    assert bool((o[:6] == 0).all())
