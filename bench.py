@@ -417,6 +417,15 @@ def prefill_bench(torch, abi, synth, device, steps):
             "calls_per_pass": len(calls)}
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise max of per-rank timings (the only cross-rank step: each
+    rank runs its own pool replica, no data moves between ranks)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_gpu(args, rank, world):
     import torch
     from gated_deltanet_recurrent_gb300 import abi, synth
@@ -460,9 +469,7 @@ def run_gpu(args, rank, world):
     time.sleep(0.2)
     clk = clocks.stop()
     if dist is not None:
-        tt = torch.tensor([t_dev, t_e2e, t_kernel], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_dev, t_e2e, t_kernel = tt.tolist()
+        t_dev, t_e2e, t_kernel = max_over_ranks([t_dev, t_e2e, t_kernel], dist, device)
     if rank != 0:
         return None
 

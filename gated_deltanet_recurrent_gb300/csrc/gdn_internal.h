@@ -60,6 +60,9 @@ cudaError_t launch_verify(const PoolView &p, int layer, const int32_t *slot_ids,
                           int T, const QKV &in, void *o, gdn_dtype o_dtype,
                           const int32_t *accept_len, float scale, cudaStream_t s);
 
+cudaError_t launch_prefill_tc(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in,
+                              void *o, gdn_dtype o_dtype, float scale, cudaStream_t s);
+
 cudaError_t launch_prefill(const PoolView &p, int layer, const SeqIndex &seq,
                            int total_tokens, int max_seqlen, const QKV &in, void *o,
                            gdn_dtype o_dtype, float scale, cudaStream_t s);

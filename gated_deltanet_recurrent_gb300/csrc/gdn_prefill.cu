@@ -337,6 +337,13 @@ cudaError_t launch_prefill(const PoolView &p, int layer, const SeqIndex &seq, in
   (void)total_tokens;
   (void)max_seqlen;
   if (p.dk != p.dv) return cudaErrorNotSupported;
+#if !defined(GDN_PREFILL_SIMT_ONLY)
+  // tensor-core path: dk = dv = 128 and 128-bit aligned rows of v
+  const size_t es = in.dtype == GDN_F32 ? 4 : 2;
+  const size_t al = in.dtype == GDN_F32 ? 16 : 8;
+  if (p.dk == 128 && (uintptr_t)in.v % al == 0 && ((size_t)in.ld_v * es) % al == 0)
+    return launch_prefill_tc(p, layer, seq, in, o, o_dtype, scale, s);
+#endif
   switch (p.dk) {
     case 16: return launch_prefill_d<16>(p, layer, seq, in, o, o_dtype, scale, s);
     case 32: return launch_prefill_d<32>(p, layer, seq, in, o, o_dtype, scale, s);

@@ -1,7 +1,8 @@
 """GPU parity of gdn_prefill_chunked (and the tiny end-to-end request flow)
 against the float64 oracle, through the C ABI.
 
-float32 inputs: max|gpu - ref| <= 1e-4 * max|ref| per tensor.  bf16 inputs:
+float32 inputs: max|gpu - ref| <= 1e-4 * max|ref| per tensor (5e-3 on the tf32
+tensor-core path, see _rel_tol).  bf16 inputs:
 |gpu - ref| <= 1e-2 + 1e-2 |ref| elementwise.  Full-size cases are checked on
 a sample of value heads (the oracle runs only those heads); untouched slots
 are checked bit for bit."""
@@ -17,6 +18,16 @@ from tests.gpu_util import (assert_close_bf16, assert_maxrel, dev, dev_i32, host
 pytestmark = pytest.mark.gpu
 
 SENTINEL = 3.25
+
+# Prefill with dk = dv = 128 runs its chunk products on the tensor cores in
+# tf32 (10 explicit mantissa bits, unit roundoff u = 2^-11 ~ 4.9e-4), reading
+# fp32 operands.  Each output is a sum of products of two rounded operands,
+# and the recurrence carries those errors through the state, so a float32
+# input case is held to max|gpu - ref| <= 5e-3 * max|ref| (about 10 u) instead
+# of the 1e-4 of the pure float32 kernels; smaller head dims run the float32
+# CUDA-core kernel and keep 1e-4.
+def _rel_tol(D):
+    return 5e-3 if D == 128 else 1e-4
 
 
 def _pool(shape, n_layers, n_slots, conv_dtype=torch.float32, host_checks=True):
@@ -120,8 +131,8 @@ def test_prefill_varlen_edge_lengths(D):
     ref = O.OraclePool(1, 8, shape.h_v, shape.h_k, shape.dk, shape.dv, 16, 4)
     ref.S[0, ids] = S0
     o_ref = ref.prefill(0, ids, cu, *tok_np(tok), scale=D ** -0.5)
-    assert_maxrel(host(o), o_ref, 1e-4, "o")
-    assert_maxrel(host(pool.state[1, lid]), ref.S[0, ids], 1e-4, "S")
+    assert_maxrel(host(o), o_ref, _rel_tol(D), "o")
+    assert_maxrel(host(pool.state[1, lid]), ref.S[0, ids], _rel_tol(D), "S")
     pool.state[1, lid] = SENTINEL
     assert bool((pool.state == SENTINEL).all())
 
@@ -146,8 +157,8 @@ def test_prefill_split_across_calls_equals_whole_and_token_recurrence():
         outs[name] = (np.concatenate(parts), host(pool.state[0, 1]))
     S_ref, o_ref = O.gdn_recurrent(S0[0], *tok_np(tok))
     for name, (o, S) in outs.items():
-        assert_maxrel(o, o_ref, 1e-4, f"o {name}")
-        assert_maxrel(S, S_ref, 1e-4, f"S {name}")
+        assert_maxrel(o, o_ref, _rel_tol(128), f"o {name}")
+        assert_maxrel(S, S_ref, _rel_tol(128), f"S {name}")
 
 
 def _head_sample(tok, heads, group):
