@@ -311,24 +311,44 @@ def sweep_bench(torch, abi, synth, device, steps):
         for j in range(3):
             one_step(j)
         E = lambda: torch.cuda.Event(enable_timing=True)
-        evs = [(E(), E()) for _ in range(steps)]
-        torch.cuda.synchronize()
-        for j in range(steps):
-            flush.zero_()
-            evs[j][0].record()
-            one_step(j)
-            evs[j][1].record()
-        torch.cuda.synchronize()
-        t = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+
+        def timed(step_fn):
+            evs = [(E(), E()) for _ in range(steps)]
+            torch.cuda.synchronize()
+            for j in range(steps):
+                flush.zero_()
+                evs[j][0].record()
+                step_fn(j)
+                evs[j][1].record()
+            torch.cuda.synchronize()
+            return sum(a.elapsed_time(b) for a, b in evs) / 1e3
+
+        t = timed(one_step)
+        # the same 36 launches captured once into a CUDA graph and replayed
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            one_step(0)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_step(0)
+        graph.replay()
+        t_graph = timed(lambda j: graph.replay())
+        del graph
         slot_steps = N * steps
         out.append({"n_active": N, "slot_steps_per_s": slot_steps / t,
                     "slot_layer_steps_per_s": slot_steps * L / t,
                     "state_gbs": slot_steps * L * STATE_BYTES_PER_SLOT_LAYER / t / 1e9,
-                    "ms_per_step": t / steps * 1e3})
+                    "ms_per_step": t / steps * 1e3,
+                    "graph_slot_steps_per_s": slot_steps / t_graph,
+                    "graph_state_gbs": slot_steps * L * STATE_BYTES_PER_SLOT_LAYER / t_graph / 1e9,
+                    "graph_ms_per_step": t_graph / steps * 1e3})
     del pool
     return {"workload": "18 stacked GDN layers (decode-step layer shape), 512-slot pool, "
                         f"N active, {steps} decode steps per N, conv+decode per layer, "
-                        "L2 flushed between steps", "points": out}
+                        "L2 flushed between steps; graph_* = the step's 36 launches replayed "
+                        "from one CUDA graph (inputs of step 0 each time)", "points": out}
 
 
 def verify_bench(torch, abi, synth, device, steps, peak):
@@ -391,30 +411,36 @@ def prefill_bench(torch, abi, synth, device, steps):
         ob = torch.empty(len(rows), s.h_v, s.dv, device=device, dtype=torch.bfloat16)
         calls.append((ids, ccu, packed, ob, max(ln)))
 
-    def run():
+    def run(fn):
         for ids, ccu, packed, ob, mx in calls:
-            abi.gdn_prefill_chunked(pool, 0, ids, ccu, *packed, ob, max_seqlen=mx)
+            fn(pool, 0, ids, ccu, *packed, ob, max_seqlen=mx)
+
+    def timed(fn):
+        pool.state[0].copy_(init)
+        run(fn)
+        E = lambda: torch.cuda.Event(enable_timing=True)
+        evs = [(E(), E()) for _ in range(steps)]
+        for j in range(steps):
+            pool.state[0].copy_(init)
+            evs[j][0].record()
+            run(fn)
+            evs[j][1].record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / 1e3
 
     try:
-        pool.state[0].copy_(init)
-        run()
+        t = timed(abi.gdn_prefill_chunked)
+        t_rec = timed(abi.gdn_prefill_recurrent)
     except abi.GDNError as e:
         return {"unavailable": str(e)}
-    E = lambda: torch.cuda.Event(enable_timing=True)
-    evs = [(E(), E()) for _ in range(steps)]
-    for j in range(steps):
-        pool.state[0].copy_(init)
-        evs[j][0].record()
-        run()
-        evs[j][1].record()
-    torch.cuda.synchronize()
-    t = sum(a.elapsed_time(b) for a, b in evs) / 1e3
     total = int(cu[-1])
     return {"workload": f"varlen chunked prefill, decode-step layer shape, 8 sequences "
                         f"(lengths {lens}), pieces of 2048 tokens with the state carried "
                         f"between calls, bf16 in/out, chunk 64",
             "tokens_per_s": total * steps / t, "ms_per_pass": t / steps * 1e3,
-            "calls_per_pass": len(calls)}
+            "calls_per_pass": len(calls),
+            "token_by_token_tokens_per_s": total * steps / t_rec,
+            "speedup_over_token_by_token": t_rec / t}
 
 
 def max_over_ranks(values, dist, device):

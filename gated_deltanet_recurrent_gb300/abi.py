@@ -22,8 +22,10 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SLOT", 3: "GDN_ERR_DUP_SLOT
 DEVERR_SLOT, DEVERR_SEQ, DEVERR_COUNT, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "gdn_pool_reset",
+            "gdn_pool_copy",
             "gdn_pool_destroy", "gdn_pool_get_error", "gdn_conv_silu", "gdn_decode_step",
-            "gdn_prefill_chunked", "gdn_spec_verify", "gdn_status_string",
+            "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
+            "gdn_status_string",
             "gdn_last_error_message")
 
 
@@ -68,6 +70,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gdn_pool_create": (st, [P(gdn_pool_desc), vp, ctypes.c_size_t, vp, ctypes.c_size_t,
                                  P(vp)]),
         "gdn_pool_reset": (st, [vp, vp, i32, vp]),
+        "gdn_pool_copy": (st, [vp, vp, vp, i32, vp]),
         "gdn_pool_destroy": (st, [vp]),
         "gdn_pool_get_error": (st, [vp, P(ctypes.c_uint32)]),
         "gdn_conv_silu": (st, [vp, i32, vp, vp, i32, i32, i32, vp, i64, st, vp, vp, vp, i64,
@@ -75,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gdn_decode_step": (st, [vp, i32, vp, i32, P(gdn_qkv), vp, st, ctypes.c_float, vp]),
         "gdn_prefill_chunked": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
                                      ctypes.c_float, vp]),
+        "gdn_prefill_recurrent": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
+                                       ctypes.c_float, vp]),
         "gdn_spec_verify": (st, [vp, i32, vp, i32, i32, P(gdn_qkv), vp, st, vp,
                                  ctypes.c_float, vp]),
         "gdn_status_string": (ctypes.c_char_p, [st]),
@@ -214,6 +219,14 @@ def gdn_pool_reset(pool: Pool, slot_ids: torch.Tensor, stream=None):
                                          slot_ids.numel(), _stream(stream)))
 
 
+def gdn_pool_copy(pool: Pool, src_slots: torch.Tensor, dst_slots: torch.Tensor, stream=None):
+    if src_slots.numel() != dst_slots.numel():
+        raise GDNError(5, "src_slots and dst_slots differ in length")
+    _check(load_library().gdn_pool_copy(pool.handle, _idx(src_slots, "src_slots"),
+                                        _idx(dst_slots, "dst_slots"), src_slots.numel(),
+                                        _stream(stream)))
+
+
 def gdn_pool_get_error(pool: Pool) -> int:
     err = ctypes.c_uint32(0)
     _check(load_library().gdn_pool_get_error(pool.handle, ctypes.byref(err)))
@@ -257,6 +270,20 @@ def gdn_prefill_chunked(pool: Pool, layer: int, slot_ids: torch.Tensor,
     if max_seqlen <= 0:
         max_seqlen = q.shape[0]
     _check(load_library().gdn_prefill_chunked(
+        pool.handle, layer, _idx(slot_ids, "slot_ids"), _idx(cu_seqlens, "cu_seqlens"),
+        slot_ids.numel(), q.shape[0], max_seqlen, ctypes.byref(inp), _ptr(o), _dt(o), scale,
+        _stream(stream)))
+    return o
+
+
+def gdn_prefill_recurrent(pool: Pool, layer: int, slot_ids: torch.Tensor,
+                          cu_seqlens: torch.Tensor, q, k, v, g, beta, o: torch.Tensor,
+                          scale: float = 1.0, max_seqlen: int = 0, stream=None):
+    """Token-by-token prefill; same arguments and results as gdn_prefill_chunked."""
+    inp = _qkv(pool, q, k, v, g, beta)
+    if max_seqlen <= 0:
+        max_seqlen = q.shape[0]
+    _check(load_library().gdn_prefill_recurrent(
         pool.handle, layer, _idx(slot_ids, "slot_ids"), _idx(cu_seqlens, "cu_seqlens"),
         slot_ids.numel(), q.shape[0], max_seqlen, ctypes.byref(inp), _ptr(o), _dt(o), scale,
         _stream(stream)))

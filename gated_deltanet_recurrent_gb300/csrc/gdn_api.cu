@@ -270,6 +270,35 @@ gdn_status gdn_pool_reset(gdn_pool *p, const int32_t *slot_ids, int32_t n, gdn_s
   return ok();
 }
 
+gdn_status gdn_pool_copy(gdn_pool *p, const int32_t *src_slots, const int32_t *dst_slots,
+                         int32_t n, gdn_stream stream) {
+  gdn_status st = check_pool(p, 0);
+  if (st != GDN_OK) return st;
+  if (n < 0) return fail(GDN_ERR_ARG, "n = %d < 0", n);
+  if (n == 0) return ok();
+  if (!src_slots || !dst_slots) return fail(GDN_ERR_ARG, "src_slots and dst_slots must be non-NULL");
+  if (n > 65535) return fail(GDN_ERR_SIZE, "n = %d > 65535", n);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    if ((st = check_slots(p, dst_slots, n, s))) return st;
+    std::vector<int32_t> hs, hd;
+    if ((st = fetch(hs, src_slots, (size_t)n, s, "src_slots")) ||
+        (st = fetch(hd, dst_slots, (size_t)n, s, "dst_slots")))
+      return st;
+    std::vector<unsigned char> is_dst((size_t)p->desc.n_slots, 0);
+    for (int i = 0; i < n; ++i) is_dst[hd[i]] = 1;
+    for (int i = 0; i < n; ++i) {
+      if (hs[i] < 0 || hs[i] >= p->desc.n_slots)
+        return fail(GDN_ERR_SLOT, "src_slots[%d] = %d outside [0, %d)", i, hs[i], p->desc.n_slots);
+      if (is_dst[hs[i]])
+        return fail(GDN_ERR_DUP_SLOT, "slot %d is both a source and a destination", hs[i]);
+    }
+  }
+  cudaError_t e = gdn::launch_pool_copy(p->view, src_slots, dst_slots, n, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pool copy launch");
+  return ok();
+}
+
 gdn_status gdn_conv_silu(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
                          const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
                          int32_t max_seqlen, const void *x, int64_t ld_x, gdn_dtype x_dtype,
@@ -357,10 +386,12 @@ gdn_status gdn_spec_verify(gdn_pool *p, int32_t layer, const int32_t *slot_ids, 
   return ok();
 }
 
-gdn_status gdn_prefill_chunked(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
-                               const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
-                               int32_t max_seqlen, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
-                               float scale, gdn_stream stream) {
+namespace {
+
+gdn_status prefill_common(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                          const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                          int32_t max_seqlen, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
+                          float scale, gdn_stream stream, bool chunked) {
   gdn_status st = check_pool(p, layer);
   if (st != GDN_OK) return st;
   if (n_seqs < 0 || total_tokens < 0) return fail(GDN_ERR_ARG, "negative n_seqs/total_tokens");
@@ -380,12 +411,32 @@ gdn_status gdn_prefill_chunked(gdn_pool *p, int32_t layer, const int32_t *slot_i
       return st;
   }
   gdn::SeqIndex seq{slot_ids, cu_seqlens, n_seqs, total_tokens};
-  cudaError_t e = gdn::launch_prefill(p->view, layer, seq, total_tokens,
-                                      max_seqlen < 1 ? 1 : max_seqlen, q, o, o_dtype, scale, s);
+  cudaError_t e =
+      chunked ? gdn::launch_prefill(p->view, layer, seq, total_tokens,
+                                    max_seqlen < 1 ? 1 : max_seqlen, q, o, o_dtype, scale, s)
+              : gdn::launch_prefill_recurrent(p->view, layer, seq, q, o, o_dtype, scale, s);
   if (e == cudaErrorNotSupported)
-    return fail(GDN_ERR_UNSUPPORTED, "chunked prefill is not available for this shape");
+    return fail(GDN_ERR_UNSUPPORTED, "prefill is not available for this shape");
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return ok();
+}
+
+}  // namespace
+
+gdn_status gdn_prefill_chunked(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                               const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                               int32_t max_seqlen, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
+                               float scale, gdn_stream stream) {
+  return prefill_common(p, layer, slot_ids, cu_seqlens, n_seqs, total_tokens, max_seqlen, in, o,
+                        o_dtype, scale, stream, true);
+}
+
+gdn_status gdn_prefill_recurrent(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                                 const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                                 int32_t max_seqlen, const gdn_qkv *in, void *o,
+                                 gdn_dtype o_dtype, float scale, gdn_stream stream) {
+  return prefill_common(p, layer, slot_ids, cu_seqlens, n_seqs, total_tokens, max_seqlen, in, o,
+                        o_dtype, scale, stream, false);
 }
 
 }  // extern "C"

@@ -287,6 +287,34 @@ __global__ void reset_kernel(PoolView p, const int32_t *__restrict__ slot_ids) {
     zero_elems(static_cast<bf16 *>(p.conv) + coff, nc, start, stride);
 }
 
+// grid (blocks, n_layers, n); copy state and conv cache of src[i] to dst[i].
+__global__ void copy_kernel(PoolView p, const int32_t *__restrict__ src,
+                            const int32_t *__restrict__ dst) {
+  const int i = blockIdx.z;
+  const int layer = blockIdx.y;
+  const int a = src[i], b = dst[i];
+  if (a < 0 || a >= p.n_slots || b < 0 || b >= p.n_slots) {
+    if (blockIdx.x == 0 && layer == 0 && threadIdx.x == 0) raise_error(p.err, GDN_DEVERR_SLOT);
+    return;
+  }
+  const int64_t start = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t per = p.state_slot_elems();
+  const float4 *sa = reinterpret_cast<const float4 *>(p.state + ((int64_t)layer * p.n_slots + a) * per);
+  float4 *sb = reinterpret_cast<float4 *>(p.state + ((int64_t)layer * p.n_slots + b) * per);
+  for (int64_t e = start; e < per / 4; e += stride) sb[e] = sa[e];
+  const int64_t nc = p.conv_slot_elems();
+  if (p.conv_dtype == GDN_F32) {
+    const float *ca = static_cast<const float *>(p.conv) + ((int64_t)layer * p.n_slots + a) * nc;
+    float *cb = static_cast<float *>(p.conv) + ((int64_t)layer * p.n_slots + b) * nc;
+    for (int64_t e = start; e < nc; e += stride) cb[e] = ca[e];
+  } else {
+    const bf16 *ca = static_cast<const bf16 *>(p.conv) + ((int64_t)layer * p.n_slots + a) * nc;
+    bf16 *cb = static_cast<bf16 *>(p.conv) + ((int64_t)layer * p.n_slots + b) * nc;
+    for (int64_t e = start; e < nc; e += stride) cb[e] = ca[e];
+  }
+}
+
 template <typename T, int W>
 cudaError_t launch_conv_t(const PoolView &p, int layer, const SeqIndex &seq, int max_seqlen,
                           const void *x, int64_t ld_x, const float *w, const float *bias,
@@ -327,6 +355,17 @@ cudaError_t launch_conv_w(const PoolView &p, int layer, const SeqIndex &seq, int
 }
 
 }  // namespace
+
+cudaError_t launch_pool_copy(const PoolView &p, const int32_t *src, const int32_t *dst, int n,
+                             cudaStream_t s) {
+  const int64_t per_slot = p.state_slot_elems() / 4;
+  const int threads = 256;
+  int64_t blocks = (per_slot + threads * 8 - 1) / (threads * 8);
+  blocks = blocks < 1 ? 1 : (blocks > 64 ? 64 : blocks);
+  dim3 grid((unsigned)blocks, p.n_layers, n);
+  copy_kernel<<<grid, threads, 0, s>>>(p, src, dst);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_conv_silu(const PoolView &p, int layer, const SeqIndex &seq, int max_seqlen,
                              const void *x, int64_t ld_x, const float *w, const float *bias,

@@ -47,6 +47,9 @@ struct SeqIndex {
 cudaError_t launch_pool_reset(const PoolView &p, const int32_t *slot_ids, int n,
                               cudaStream_t s);
 
+cudaError_t launch_pool_copy(const PoolView &p, const int32_t *src, const int32_t *dst, int n,
+                             cudaStream_t s);
+
 cudaError_t launch_conv_silu(const PoolView &p, int layer, const SeqIndex &seq,
                              int max_seqlen, const void *x, int64_t ld_x,
                              const float *w, const float *bias, void *y, int64_t ld_y,
@@ -59,6 +62,10 @@ cudaError_t launch_decode(const PoolView &p, int layer, const int32_t *slot_ids,
 cudaError_t launch_verify(const PoolView &p, int layer, const int32_t *slot_ids, int n,
                           int T, const QKV &in, void *o, gdn_dtype o_dtype,
                           const int32_t *accept_len, float scale, cudaStream_t s);
+
+cudaError_t launch_prefill_recurrent(const PoolView &p, int layer, const SeqIndex &seq,
+                                     const QKV &in, void *o, gdn_dtype o_dtype, float scale,
+                                     cudaStream_t s);
 
 cudaError_t launch_prefill_tc(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in,
                               void *o, gdn_dtype o_dtype, float scale, cudaStream_t s);

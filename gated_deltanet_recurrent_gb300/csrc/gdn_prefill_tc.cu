@@ -1,7 +1,7 @@
 // Chunked prefill on the 5th-generation tensor cores (tcgen05, kind::tf32),
 // for dk = dv = 128.
 //
-// One CTA (128 threads) per (sequence, value head) walks the sequence in
+// One CTA (256 threads) per (sequence, value head) walks the sequence in
 // 64-token chunks.  The float32 state S [dv][dk] lives in tensor memory for
 // the whole call (TMEM columns 0..127, row v in lane v) and is the A operand
 // of the state-dependent products, so it never leaves the SM between chunks.
@@ -10,12 +10,12 @@
 //   MMA1  D1 = [Q;K] K^T                     -> A = beta e^{dG} KK^T (strict),
 //                                              P = e^{dG} QK^T (lower, incl. diag)
 //   solve (I + A) [W | U] = [diag(beta gamma) K | diag(beta) V]   (CUDA cores)
-//   MMA2  D2 = S W^T,  MMA3  D3 = S Q^T      -> Delta^T = U^T - D2
+//   MMA2  D2 = S W^T,  MMA3  D3 = S Q^T      -> Delta^T = U^T - D2;  S <- gamma_n S
 //   MMA4  D4 = Delta^T P^T                    -> O^T = diag(gamma) D3 + D4
-//   MMA5  D5 = Delta^T Ktil, Ktil = diag(e^{G_n - G}) K  -> S <- gamma_n S + D5
-// Everything that is not S-dependent (the stage, MMA1, the solve) is on the
-// chunk's critical path too in this version.  Operands are K-major,
-// no-swizzle core-matrix tiles in shared memory (see gdn_tc.cuh).
+//   MMA5  S += Delta^T Ktil,  Ktil = diag(e^{G_n - G}) K
+// TMEM lanes are split over warps w and w+4 (same lane quadrant, column
+// halves).  Operands are K-major, no-swizzle core-matrix tiles in shared
+// memory (see gdn_tc.cuh).
 #include "gdn_tc.cuh"
 
 namespace gdn {
@@ -23,7 +23,7 @@ namespace {
 
 constexpr int C = kChunk;   // 64
 constexpr int D = 128;      // dk = dv
-constexpr int NT = 128;     // threads
+constexpr int NT = 256;     // threads
 constexpr int XS = D + 4;   // plain row stride (floats) of the solve buffers
 constexpr int AS = C + 4;   // plain row stride of the A matrix
 
@@ -40,7 +40,7 @@ static_assert(128 * C * 4 <= C * XS * 4, "Delta^T tile fits the W solve buffer")
 static_assert(C * C * 4 <= C * AS * 4, "P tile fits the A buffer");
 
 // TMEM columns
-constexpr uint32_t T_S = 0, T_D1 = 128, T_D2 = 192, T_D3 = 256, T_D4 = 320, T_D5 = 384;
+constexpr uint32_t T_S = 0, T_D1 = 128, T_D2 = 192, T_D3 = 256, T_D4 = 320;
 constexpr uint32_t TMEM_COLS = 512;
 
 template <typename TI, typename TO>
@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(NT, 1)
   const int si = blockIdx.y;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  const int quad = warp & 3;                    // TMEM lane quadrant of this warp
+  const int half = warp >> 2;                   // which half of the columns it takes
+  const int row = 32 * quad + lane;             // TMEM lane = accumulator row
   const int slot = seq.slot_ids[si];
   const bool first = h == 0 && tid == 0;
   if (slot < 0 || slot >= p.n_slots) {
@@ -91,20 +94,20 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tm = tmem_slot;
-  const uint32_t lrow = tm + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
+  const uint32_t lrow = tm + ((uint32_t)(32 * quad) << 16);  // this warp's TMEM lanes
 
-  // state row tid -> TMEM (lane tid, columns 0..127)
+  // state row `row`, column half `half` -> TMEM
   {
-    const float4 *src = reinterpret_cast<const float4 *>(Sg + (int64_t)tid * D);
+    const float4 *src = reinterpret_cast<const float4 *>(Sg + (int64_t)row * D + 64 * half);
 #pragma unroll 1
-    for (int c = 0; c < D / 16; ++c) {
+    for (int c = 0; c < 4; ++c) {
       float v[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float4 x = src[c * 4 + j];
         v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
       }
-      tc::tmem_st16(lrow + T_S + c * 16, v);
+      tc::tmem_st16(lrow + T_S + 64 * half + c * 16, v);
     }
     tc::tmem_st_wait();
   }
@@ -128,27 +131,47 @@ __global__ void __launch_bounds__(NT, 1)
   for (int c0 = 0; c0 < len && alive; c0 += C) {
     const int n = min(C, len - c0);
 
-    // ---- S0: stage normalised q, k (core tiles), beta v (plain), g, beta
-    for (int t = warp; t < C; t += NT / 32) {
-      const bool real = t < n;
+    // ---- S0: stage normalised q, k (core tiles), beta v (plain), g, beta.
+    // Warp w takes tokens 8w .. 8w+7; lane = token (3 bits) + 8 * chunk group, so a
+    // quarter-warp writes the 8 rows of one core matrix (contiguous 128 bytes).
+    {
+      const int tl = lane & 7, cg = lane >> 3;      // token in group, chunk group 0..3
+      const int t = 8 * warp + tl;
       const int64_t tok = lo + c0 + t;
-      float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4, v4 = q4;
-      float gt = 0.f, bt = 0.f;
-      if (real) {
-        q4 = Elem<TI>::load4(qg + tok * in.ld_qk + (int64_t)hk * D + 4 * lane);
-        k4 = Elem<TI>::load4(kg + tok * in.ld_qk + (int64_t)hk * D + 4 * lane);
-        v4 = Elem<TI>::load4(vg + tok * in.ld_v + (int64_t)h * D + 4 * lane);
-        gt = Elem<TI>::load1(gg + tok * p.h_v + h);
-        bt = Elem<TI>::load1(bg + tok * p.h_v + h);
+      const bool real = t < n;
+      float4 q4[D / 16], k4[D / 16], v4[D / 16];   // chunks c = cg + 4 j
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const int c = cg + 4 * j;
+        q4[j] = k4[j] = v4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (real) {
+          q4[j] = Elem<TI>::load4(qg + tok * in.ld_qk + (int64_t)hk * D + 4 * c);
+          k4[j] = Elem<TI>::load4(kg + tok * in.ld_qk + (int64_t)hk * D + 4 * c);
+          v4[j] = Elem<TI>::load4(vg + tok * in.ld_v + (int64_t)h * D + 4 * c);
+        }
       }
-      const float qq = group_sum<32>(dot4(q4, q4));
-      const float kk = group_sum<32>(dot4(k4, k4));
-      *reinterpret_cast<float4 *>(QK + tc::core_off(t, 4 * lane, D)) =
-          scale4(rsqrtf(qq + kL2Eps), q4);
-      *reinterpret_cast<float4 *>(QK + tc::core_off(64 + t, 4 * lane, D)) =
-          scale4(rsqrtf(kk + kL2Eps), k4);
-      *reinterpret_cast<float4 *>(XU + t * XS + 4 * lane) = scale4(bt, v4);
-      if (lane == 0) {
+      const float gt = real ? Elem<TI>::load1(gg + tok * p.h_v + h) : 0.f;
+      const float bt = real ? Elem<TI>::load1(bg + tok * p.h_v + h) : 0.f;
+      float qq = 0.f, kk = 0.f;
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        qq += dot4(q4[j], q4[j]);
+        kk += dot4(k4[j], k4[j]);
+      }
+      // reduce over the four chunk groups of this token (lane bits 3 and 4)
+      qq += __shfl_xor_sync(0xffffffffu, qq, 8);
+      qq += __shfl_xor_sync(0xffffffffu, qq, 16);
+      kk += __shfl_xor_sync(0xffffffffu, kk, 8);
+      kk += __shfl_xor_sync(0xffffffffu, kk, 16);
+      const float qs = rsqrtf(qq + kL2Eps), ks = rsqrtf(kk + kL2Eps);
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const int c = cg + 4 * j;
+        *reinterpret_cast<float4 *>(QK + tc::core_off(t, 4 * c, D)) = scale4(qs, q4[j]);
+        *reinterpret_cast<float4 *>(QK + tc::core_off(64 + t, 4 * c, D)) = scale4(ks, k4[j]);
+        *reinterpret_cast<float4 *>(XU + t * XS + 4 * c) = scale4(bt, v4[j]);
+      }
+      if (cg == 0) {
         sG[t] = gt;
         sBeta[t] = bt;
       }
@@ -185,16 +208,18 @@ __global__ void __launch_bounds__(NT, 1)
                    tc::smem_desc(k_s + j * KSTEP, tc::kLBO, SBO_D), id, j > 0);
       tc::mma_commit(&bar);
     }
-    // meanwhile: W right-hand side (beta gamma k, plain) and Ktil^T tile
+    // meanwhile: W right-hand side (beta gamma k, plain) and the Ktil^T tile
     for (int e = tid; e < C * (D / 4); e += NT) {
       const int t = e % C, c4 = e / C;
       const float4 k4 = *reinterpret_cast<const float4 *>(QK + tc::core_off(64 + t, 4 * c4, D));
       *reinterpret_cast<float4 *>(XW + t * XS + 4 * c4) = scale4(sBeta[t] * sGam[t], k4);
     }
     {
-      const int kc = tid;  // row k of Ktil^T
-#pragma unroll 4
-      for (int i4 = 0; i4 < C / 4; ++i4) {
+      const int kc = tid & 127;            // row k of Ktil^T
+      const int ib = (tid >> 7) * (C / 8); // which half of the i chunks
+#pragma unroll 2
+      for (int q = 0; q < C / 8; ++q) {
+        const int i4 = ib + ((q + (kc >> 2)) & (C / 8 - 1));   // rotated: spreads banks
         float4 x;
         x.x = sDte[4 * i4 + 0] * QK[tc::core_off(64 + 4 * i4 + 0, kc, D)];
         x.y = sDte[4 * i4 + 1] * QK[tc::core_off(64 + 4 * i4 + 1, kc, D)];
@@ -209,17 +234,18 @@ __global__ void __launch_bounds__(NT, 1)
     tc::fence_after_sync();
 
     // ---- S2: A[t][i] = beta_t e^{G_t - G_i} (k_t . k_i), i < t   (rows 64..127 of D1)
-    if (warp >= 2) {
-      const int t = tid - 64;
+    if (quad >= 2) {
+      const int t = row - 64;
       const float bt = sBeta[t], gt = sG[t];
 #pragma unroll 1
-      for (int cb = 0; cb < C / 16; ++cb) {
+      for (int cb = 0; cb < 2; ++cb) {
         float v[16];
-        tc::tmem_ld16(lrow + T_D1 + cb * 16, v);
+        const int i0 = 32 * half + 16 * cb;
+        tc::tmem_ld16(lrow + T_D1 + i0, v);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
           float4 a;
-          const int i = cb * 16 + j;
+          const int i = i0 + j;
           a.x = i + 0 < t ? bt * expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
           a.y = i + 1 < t ? bt * expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
           a.z = i + 2 < t ? bt * expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
@@ -230,10 +256,9 @@ __global__ void __launch_bounds__(NT, 1)
     }
     __syncthreads();
 
-    // ---- S3: forward substitution (I + A) X = RHS; thread = one W and one U column
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      float *Xc = (pass == 0 ? XW : XU) + tid;
+    // ---- S3: forward substitution (I + A) X = RHS; thread = one column of [W | U]
+    {
+      float *Xc = (tid < D ? XW + tid : XU + (tid - D));
       float x[C];
 #pragma unroll
       for (int t = 0; t < C; ++t) x[t] = Xc[t * XS];
@@ -264,17 +289,18 @@ __global__ void __launch_bounds__(NT, 1)
       *reinterpret_cast<float4 *>(QK + tc::core_off(64 + t, 4 * c4, D)) =
           *reinterpret_cast<const float4 *>(XW + t * XS + 4 * c4);
     }
-    if (warp < 2) {
-      const int t = tid;
+    if (quad < 2) {
+      const int t = row;
       const float gt = sG[t];
 #pragma unroll 1
-      for (int cb = 0; cb < C / 16; ++cb) {
+      for (int cb = 0; cb < 2; ++cb) {
         float v[16];
-        tc::tmem_ld16(lrow + T_D1 + cb * 16, v);
+        const int i0 = 32 * half + 16 * cb;
+        tc::tmem_ld16(lrow + T_D1 + i0, v);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
           float4 pv;
-          const int i = cb * 16 + j;
+          const int i = i0 + j;
           pv.x = i + 0 <= t ? expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
           pv.y = i + 1 <= t ? expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
           pv.z = i + 2 <= t ? expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
@@ -293,12 +319,12 @@ __global__ void __launch_bounds__(NT, 1)
       constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll
       for (int j = 0; j < D / 8; ++j)
-        tc::mma_ts(tm + T_D2, tm + T_S + j * 8, tc::smem_desc(k_s + j * KSTEP, tc::kLBO, SBO_D), id,
-                   j > 0);
+        tc::mma_ts(tm + T_D2, tm + T_S + j * 8,
+                   tc::smem_desc(k_s + j * KSTEP, tc::kLBO, SBO_D), id, j > 0);
 #pragma unroll
       for (int j = 0; j < D / 8; ++j)
-        tc::mma_ts(tm + T_D3, tm + T_S + j * 8, tc::smem_desc(qk_s + j * KSTEP, tc::kLBO, SBO_D),
-                   id, j > 0);
+        tc::mma_ts(tm + T_D3, tm + T_S + j * 8,
+                   tc::smem_desc(qk_s + j * KSTEP, tc::kLBO, SBO_D), id, j > 0);
       tc::mma_commit(&bar);
     }
     alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));
@@ -306,18 +332,20 @@ __global__ void __launch_bounds__(NT, 1)
     phase ^= 1;
     tc::fence_after_sync();
 
-    // ---- S6: Delta^T[v][t] = U[t][v] - D2[v][t]  (tile, K = t);  o part = gamma_t D3[v][t]
-    float op[C];
+    // ---- S6: Delta^T[v][t] = U[t][v] - D2[v][t] (tile, K = t); o part = gamma_t D3[v][t];
+    //          S <- gamma_n S (MMA5 then accumulates Delta^T Ktil into it)
+    float op[C / 2];
     {
-      const int v = tid;
+      const int v = row;
 #pragma unroll
-      for (int cb = 0; cb < C / 16; ++cb) {
+      for (int cb = 0; cb < 2; ++cb) {
+        const int t0 = 32 * half + 16 * cb;
         float d2[16], d3[16];
-        tc::tmem_ld16(lrow + T_D2 + cb * 16, d2);
-        tc::tmem_ld16(lrow + T_D3 + cb * 16, d3);
+        tc::tmem_ld16(lrow + T_D2 + t0, d2);
+        tc::tmem_ld16(lrow + T_D3 + t0, d3);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
-          const int t = cb * 16 + j;
+          const int t = t0 + j;
           float4 dd;
           dd.x = XU[(t + 0) * XS + v] - d2[j + 0];
           dd.y = XU[(t + 1) * XS + v] - d2[j + 1];
@@ -325,26 +353,37 @@ __global__ void __launch_bounds__(NT, 1)
           dd.w = XU[(t + 3) * XS + v] - d2[j + 3];
           *reinterpret_cast<float4 *>(XW + tc::core_off(v, t, C)) = dd;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) op[t + q] = sGam[t + q] * d3[j + q];
+          for (int q = 0; q < 4; ++q) op[16 * cb + j + q] = sGam[t + q] * d3[j + q];
         }
       }
+      const float gn = sGam[C - 1];
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float s[16];
+        tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, s);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) s[j] *= gn;
+        tc::tmem_st16(lrow + T_S + 64 * half + 16 * cb, s);
+      }
+      tc::tmem_st_wait();
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
 
-    // ---- S7: MMA4  D4 = Delta^T P^T (N 64),  MMA5  D5 = Delta^T Ktil (N 128); K = 64
+    // ---- S7: MMA4  D4 = Delta^T P^T (N 64),  MMA5  S += Delta^T Ktil (N 128); K = 64
     if (tid == 0) {
 #pragma unroll
       for (int j = 0; j < C / 8; ++j)
         tc::mma_ss(tm + T_D4, tc::smem_desc(dt_s + j * KSTEP, tc::kLBO, SBO_C),
-                   tc::smem_desc(p_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 64), j > 0);
+                   tc::smem_desc(p_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 64),
+                   j > 0);
 #pragma unroll
       for (int j = 0; j < C / 8; ++j)
-        tc::mma_ss(tm + T_D5, tc::smem_desc(dt_s + j * KSTEP, tc::kLBO, SBO_C),
+        tc::mma_ss(tm + T_S, tc::smem_desc(dt_s + j * KSTEP, tc::kLBO, SBO_C),
                    tc::smem_desc(kt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 128),
-                   j > 0);
+                   1);
       tc::mma_commit(&bar);
     }
     alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));
@@ -352,31 +391,22 @@ __global__ void __launch_bounds__(NT, 1)
     phase ^= 1;
     tc::fence_after_sync();
 
-    // ---- S8: outputs and the state update
+    // ---- S8: outputs o[t][v] = scale (gamma_t D3 + D4), this warp's half of t
     {
-      const int v = tid;
+      const int v = row;
       TO *ob = o + (lo + c0) * p.h_v * D + (int64_t)h * D + v;
 #pragma unroll
-      for (int cb = 0; cb < C / 16; ++cb) {
+      for (int cb = 0; cb < 2; ++cb) {
+        const int t0 = 32 * half + 16 * cb;
         float d4[16];
-        tc::tmem_ld16(lrow + T_D4 + cb * 16, d4);
+        tc::tmem_ld16(lrow + T_D4 + t0, d4);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int t = cb * 16 + j;
-          if (t < n) Elem<TO>::store1(ob + (int64_t)t * p.h_v * D, scale * (op[t] + d4[j]));
+          const int t = t0 + j;
+          if (t < n)
+            Elem<TO>::store1(ob + (int64_t)t * p.h_v * D, scale * (op[16 * cb + j] + d4[j]));
         }
       }
-      const float gn = sGam[C - 1];
-#pragma unroll 1
-      for (int cb = 0; cb < D / 16; ++cb) {
-        float s[16], d5[16];
-        tc::tmem_ld16(lrow + T_S + cb * 16, s);
-        tc::tmem_ld16(lrow + T_D5 + cb * 16, d5);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) s[j] = gn * s[j] + d5[j];
-        tc::tmem_st16(lrow + T_S + cb * 16, s);
-      }
-      tc::tmem_st_wait();
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -384,11 +414,11 @@ __global__ void __launch_bounds__(NT, 1)
   }
 
   if (alive) {
-    float4 *dst = reinterpret_cast<float4 *>(Sg + (int64_t)tid * D);
+    float4 *dst = reinterpret_cast<float4 *>(Sg + (int64_t)row * D + 64 * half);
 #pragma unroll 1
-    for (int c = 0; c < D / 16; ++c) {
+    for (int c = 0; c < 4; ++c) {
       float v[16];
-      tc::tmem_ld16(lrow + T_S + c * 16, v);
+      tc::tmem_ld16(lrow + T_S + 64 * half + c * 16, v);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         dst[c * 4 + j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);

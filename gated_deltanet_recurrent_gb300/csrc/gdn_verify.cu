@@ -8,9 +8,10 @@ namespace gdn {
 namespace {
 
 using rows::kThreads;
-using rows::kBulkBytes;
 using rows::state_head;
 using rows::dispatch;
+
+constexpr int kTileBytes = 32768;  // state tile per CTA (one bulk copy)
 
 // Row-level WY form for T tokens (speculative verify; decode is T = 1).
 //
@@ -33,16 +34,17 @@ __global__ void __launch_bounds__(kThreads)
     rows_kernel(PoolView p, int layer, const int32_t *__restrict__ slot_ids, int T, QKV in,
                 TO *__restrict__ o, const int32_t *__restrict__ accept_len, int commit_all,
                 float scale) {
-  constexpr int R = kBulkBytes / (DK * 4);   // rows per CTA
+  constexpr int R = kTileBytes / (DK * 4);   // rows per CTA
   constexpr int LPR = 4;                     // lanes per row
   constexpr int C4 = DK / 16;                // float4 chunks per lane per row
   constexpr int RPP = 32 / LPR;              // rows per warp pass
   constexpr int RPW = R / (kThreads / 32);   // rows per warp
   constexpr int PASSES = RPW / RPP;
   static_assert(PASSES >= 1 && RPW % RPP == 0, "row mapping");
-  __shared__ __align__(128) float4 tile[kBulkBytes / 16];
+  __shared__ __align__(128) float4 tile[kTileBytes / 16];
   __shared__ __align__(8) uint64_t bar;
-  // dynamic: k, q [T][DK]; v [T][R]; Gram KK, KQ [T][T]; D [(T+1)][(T+1)]; alpha, beta [T]
+  // dynamic: k, q [T][DK]; v [T][R]; Gram KK, KQ [T][T]; D [(T+1)][(T+1)]; alpha, beta [T];
+  // G [T+1]
   extern __shared__ float4 dsm[];
   float4 *sk4 = dsm;
   float4 *sq4 = sk4 + T * (DK / 4);
@@ -52,8 +54,9 @@ __global__ void __launch_bounds__(kThreads)
   float *Dm = KQ + T * T;
   float *sal = Dm + (T + 1) * (T + 1);
   float *sbe = sal + T;
+  float *sG = sbe + T;  // cumulative log-decay after t tokens, t = 0..T
   // looped variant only (TMAX > 8): per-row dot products and deltas, [32 rows][T] each
-  float *rdk = sbe + T;
+  float *rdk = sG + T + 1;
   float *rdq = rdk + 32 * T;
   float *rdl = rdq + 32 * T;
 
@@ -108,38 +111,42 @@ __global__ void __launch_bounds__(kThreads)
     const int t = e / R, rl = e % R;
     sv[e] = rl < nrows ? Elem<TI>::load1(vg + ((int64_t)i * T + t) * in.ld_v + rl) : 0.f;
   }
+  const TI *gg = static_cast<const TI *>(in.g) + (int64_t)i * T * p.h_v + h;
   if (tid < T) {
-    const int64_t gb = ((int64_t)i * T + tid) * p.h_v + h;
-    sal[tid] = Elem<TI>::load1(static_cast<const TI *>(in.g) + gb);  // g for now
-    sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(in.beta) + gb);
+    const int64_t gb = (int64_t)tid * p.h_v;
+    sal[tid] = expf(Elem<TI>::load1(gg + gb));  // alpha_t
+    sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(in.beta) + (int64_t)i * T * p.h_v + h + gb);
   }
-  __syncthreads();
-  // Gram scalars (one warp per pair) and the decay table
-  const float *skf = reinterpret_cast<const float *>(sk4);
-  const float *sqf = reinterpret_cast<const float *>(sq4);
-  for (int e = warp; e < 2 * T * T; e += kThreads / 32) {
-    const int which = e / (T * T), ii = (e / T) % T, tt = e % T;
-    const float *x = skf + ii * DK;
-    const float *y = (which ? sqf : skf) + tt * DK;
+  if (tid <= T) {  // G_t = g_0 + ... + g_{t-1}
     float acc = 0.f;
-    for (int c = lane; c < DK; c += 32) acc += x[c] * y[c];
-    acc = group_sum<32>(acc);
-    if (lane == 0) (which ? KQ : KK)[ii * T + tt] = acc;
-  }
-  if (tid == 0) {
-    float G[TMAX + 1];
-    G[0] = 0.f;
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t)
-      if (t < T) G[t + 1] = G[t] + sal[t];
-#pragma unroll
-    for (int aa = 0; aa <= TMAX; ++aa)
-#pragma unroll
-      for (int bb = 0; bb <= TMAX; ++bb)
-        if (aa <= T && bb <= aa) Dm[aa * (T + 1) + bb] = expf(G[aa] - G[bb]);
+    for (int t = 0; t < tid; ++t) acc += Elem<TI>::load1(gg + (int64_t)t * p.h_v);
+    sG[tid] = acc;
   }
   __syncthreads();
-  if (tid < T) sal[tid] = Dm[(tid + 1) * (T + 1) + tid];  // alpha_t = exp(g_t)
+  // Gram scalars k_i.k_t and k_i.q_t (four lanes per pair) and the decay table
+  for (int e0 = 0; e0 < 2 * T * T; e0 += kThreads / 4) {
+    const int e = e0 + tid / 4, sub4 = tid % 4;
+    float acc = 0.f;
+    if (e < 2 * T * T) {
+      const int which = e / (T * T), ii = (e / T) % T, tt = e % T;
+      const float4 *x = sk4 + ii * (DK / 4);
+      const float4 *y = (which ? sq4 : sk4) + tt * (DK / 4);
+#pragma unroll
+      for (int j = 0; j < DK / 16; ++j) {
+        const int c = ((j + e) % (DK / 16)) * 4 + sub4;
+        acc += dot4(x[c], y[c]);
+      }
+    }
+    acc = group_sum<4>(acc);
+    if (e < 2 * T * T && sub4 == 0) {
+      const int which = e / (T * T), ii = (e / T) % T, tt = e % T;
+      (which ? KQ : KK)[ii * T + tt] = acc;
+    }
+  }
+  for (int e = tid; e < (T + 1) * (T + 1); e += kThreads) {
+    const int aa = e / (T + 1), bb = e % (T + 1);
+    Dm[e] = bb <= aa ? expf(sG[aa] - sG[bb]) : 0.f;
+  }
   __syncthreads();
 
   if (!mbar_wait_bounded(&bar, 0)) {
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(kThreads)
 
 inline size_t rows_smem_bytes(int DK, int R, int T, bool looped) {
   return (size_t)T * (DK / 4) * sizeof(float4) * 2 +
-         ((size_t)T * R + 2 * (size_t)T * T + (size_t)(T + 1) * (T + 1) + 2 * (size_t)T +
+         ((size_t)T * R + 2 * (size_t)T * T + (size_t)(T + 1) * (T + 1) + 3 * (size_t)T + 1 +
           (looped ? 3 * 32 * (size_t)T : 0)) *
              sizeof(float);
 }
@@ -278,11 +285,11 @@ template <int DK, int TMAX, typename TI, typename TO>
 cudaError_t launch_rows_t(const PoolView &p, int layer, const int32_t *slot_ids, int n, int T,
                           const QKV &in, void *o, const int32_t *accept_len, int commit_all,
                           float scale, cudaStream_t s) {
-  constexpr int R = kBulkBytes / (DK * 4);
+  constexpr int R = kTileBytes / (DK * 4);
   const size_t smem = rows_smem_bytes(DK, R, T, TMAX > 8);
   auto kern = rows_kernel<DK, TMAX, TI, TO>;
-  // the static 16 KiB tile counts against the default 48 KiB per-block limit
-  if (smem + kBulkBytes + 64 > 48 * 1024) {
+  // the static tile counts against the default 48 KiB per-block limit
+  if (smem + kTileBytes + 64 > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

@@ -127,6 +127,15 @@ gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t st
  * Other slots are not touched. */
 gdn_status gdn_pool_reset(gdn_pool *pool, const int32_t *slot_ids, int32_t n, gdn_stream stream);
 
+/* Copy the state and conv cache of slot src_slots[i] into slot dst_slots[i],
+ * in every layer (state checkpoints for prefix caching: a recurrent state can
+ * only be saved and copied whole -- ai-infra-handbooks, "Project: adding the
+ * hybrid model Qwen3.5", "What to do", Prefix cache row, and "Why it is worth
+ * doing").  Destinations must be distinct and must not also be sources (host
+ * checks reject it; without them the result is unspecified). */
+gdn_status gdn_pool_copy(gdn_pool *pool, const int32_t *src_slots, const int32_t *dst_slots,
+                         int32_t n, gdn_stream stream);
+
 /* Release the handle and its error word (caller memory is left alone).
  * Synchronises the device before freeing. NULL is a no-op. */
 gdn_status gdn_pool_destroy(gdn_pool *pool);
@@ -179,6 +188,16 @@ gdn_status gdn_prefill_chunked(gdn_pool *pool, int32_t layer, const int32_t *slo
                                const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
                                int32_t max_seqlen, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
                                float scale, gdn_stream stream);
+
+/* Token-by-token prefill: the same contract, arguments and results as
+ * gdn_prefill_chunked, computed by applying the recurrence to each token in
+ * order (baseRT issue #31, "Why this looks tractable": the per-token
+ * gdn_recurrence kernel).  It is the reference point the chunked form is
+ * measured against and accepts every supported head dim. */
+gdn_status gdn_prefill_recurrent(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
+                                 const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                                 int32_t max_seqlen, const gdn_qkv *in, void *o,
+                                 gdn_dtype o_dtype, float scale, gdn_stream stream);
 
 /* Speculative verify of T draft tokens per slot without per-position state
  * snapshots (b70-optimization-lab research plan, "What the research found").

@@ -306,3 +306,44 @@ def test_device_guard_skips_bad_slot_and_sets_error_word():
     abi.gdn_spec_verify(pool, 0, dev_i32([0]), 1, *[tt[:1] for tt in tok_dev(t, "f32")],
                         accept_len=dev_i32([5]))
     assert abi.gdn_pool_get_error(pool) == abi.DEVERR_COUNT
+
+
+def test_pool_copy_checkpoints_slots_bit_exact():
+    shape = synth.LayerShape(4, 2, 32, 32, 24, 4)
+    pool = _pool(shape, 3, 8)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    pool.state.normal_(generator=gen)
+    pool.conv.copy_(torch.randn(pool.conv.shape, device="cuda", generator=gen))
+    before = (pool.state.clone(), pool.conv.clone())
+    src, dst = [3, 5], [0, 6]
+    abi.gdn_pool_copy(pool, dev_i32(src), dev_i32(dst))
+    torch.cuda.synchronize()
+    for a, b in zip(src, dst):
+        assert torch.equal(pool.state[:, b], before[0][:, a])
+        assert torch.equal(pool.conv[:, b], before[1][:, a])
+    others = [s for s in range(8) if s not in dst]
+    assert torch.equal(pool.state[:, others], before[0][:, others])
+    assert torch.equal(pool.conv[:, others], before[1][:, others])
+    for s_, d_, status in (([1, 2], [4, 4], "GDN_ERR_DUP_SLOT"), ([1, 4], [4, 2], "GDN_ERR_DUP_SLOT"),
+                           ([9], [1], "GDN_ERR_SLOT")):
+        with pytest.raises(abi.GDNError) as e:
+            abi.gdn_pool_copy(pool, dev_i32(s_), dev_i32(d_))
+        assert e.value.name == status
+
+
+def test_pool_copy_then_continue_matches_uninterrupted_request():
+    """A checkpoint copied mid-request continues exactly like the original slot."""
+    rng = np.random.default_rng(12)
+    shape = synth.LayerShape(2, 1, 64, 64, 16, 4)
+    pool = _pool(shape, 1, 4, conv_dtype=torch.float32)
+    abi.gdn_pool_reset(pool, dev_i32([0, 2]))
+    tok = synth.token_inputs(rng, 150, shape, "f32")
+    d = tok_dev(tok, "f32")
+    o = torch.empty(150, 2, 64, device="cuda")
+    abi.gdn_prefill_chunked(pool, 0, dev_i32([0]), dev_i32([0, 100]), *[t[:100] for t in d], o[:100])
+    abi.gdn_pool_copy(pool, dev_i32([0]), dev_i32([2]))
+    o2 = torch.empty(50, 2, 64, device="cuda")
+    abi.gdn_prefill_chunked(pool, 0, dev_i32([0]), dev_i32([0, 50]), *[t[100:] for t in d], o[100:])
+    abi.gdn_prefill_chunked(pool, 0, dev_i32([2]), dev_i32([0, 50]), *[t[100:] for t in d], o2)
+    assert torch.equal(o[100:], o2)
+    assert torch.equal(pool.state[0, 0], pool.state[0, 2])
