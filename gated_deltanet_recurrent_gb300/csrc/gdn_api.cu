@@ -1,5 +1,7 @@
 // extern "C" entry points of libgdn: argument validation (always), optional
 // host-side validation of the index arrays, and the kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <stdarg.h>
 #include <stdio.h>
 
@@ -12,6 +14,8 @@ struct gdn_pool {
   gdn::PoolView view;
   gdn_pool_desc desc;
   int device;
+  bool has_tmap;
+  alignas(64) CUtensorMap tmap;  // the state as a [rows][dk] float32 tensor (TMA)
 };
 
 namespace {
@@ -163,6 +167,34 @@ gdn_status resolve_qkv(const gdn_pool *p, const gdn_qkv *in, int64_t tokens, gdn
   return GDN_OK;
 }
 
+// Tensor map over the whole state viewed as [n_layers*n_slots*h_v*dv][dk]
+// float32, box 128 rows x 32 columns, 128-byte swizzle (one value head of
+// 128 x 128 is four boxes).  Encoded through the runtime's driver entry
+// point, so the library does not link libcuda.  Returns false if unavailable.
+bool encode_state_map(gdn_pool *p) {
+  const gdn_pool_desc &d = p->desc;
+  if (d.dk != 128 || d.dv != 128) return false;
+  const uint64_t rows = (uint64_t)d.n_layers * d.n_slots * d.h_v * d.dv;
+  if (rows > 0x7fffffffull) return false;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      fn == nullptr || q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  cuuint64_t dims[2] = {(cuuint64_t)d.dk, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d.dk * sizeof(float)};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t elem[2] = {1, 1};
+  return encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p->view.state, dims, strides, box,
+                elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -230,6 +262,7 @@ gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t st
   p->view = gdn::PoolView{static_cast<float *>(state_mem), conv_mem, err,
                           desc->n_layers, desc->n_slots, desc->h_v, desc->h_k, desc->dk,
                           desc->dv, desc->conv_ch, desc->conv_k, desc->conv_dtype};
+  p->has_tmap = encode_state_map(p);
   *out = p;
   return ok();
 }
@@ -354,7 +387,8 @@ gdn_status gdn_decode_step(gdn_pool *p, int32_t layer, const int32_t *slot_ids, 
   if (p->desc.host_checks) {
     if ((st = check_slots(p, slot_ids, n, s)) || (st = check_device_ptr(o, "o"))) return st;
   }
-  cudaError_t e = gdn::launch_decode(p->view, layer, slot_ids, n, q, o, o_dtype, scale, s);
+  cudaError_t e = gdn::launch_decode(p->view, p->has_tmap ? &p->tmap : nullptr, layer, slot_ids,
+                                     n, q, o, o_dtype, scale, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return ok();
 }
@@ -380,8 +414,8 @@ gdn_status gdn_spec_verify(gdn_pool *p, int32_t layer, const int32_t *slot_ids, 
     if (accept_len && (st = check_counts(accept_len, n, nullptr, T, s, "accept_len"))) return st;
     if (o && (st = check_device_ptr(o, "o"))) return st;
   }
-  cudaError_t e =
-      gdn::launch_verify(p->view, layer, slot_ids, n, T, q, o, o_dtype, accept_len, scale, s);
+  cudaError_t e = gdn::launch_verify(p->view, p->has_tmap ? &p->tmap : nullptr, layer, slot_ids,
+                                     n, T, q, o, o_dtype, accept_len, scale, s);
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   return ok();
 }

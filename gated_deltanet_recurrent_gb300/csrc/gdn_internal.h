@@ -55,13 +55,19 @@ cudaError_t launch_conv_silu(const PoolView &p, int layer, const SeqIndex &seq,
                              const float *w, const float *bias, void *y, int64_t ld_y,
                              const int32_t *advance, cudaStream_t s);
 
-cudaError_t launch_decode(const PoolView &p, int layer, const int32_t *slot_ids, int n,
-                          const QKV &in, void *o, gdn_dtype o_dtype, float scale,
-                          cudaStream_t s);
+cudaError_t launch_decode(const PoolView &p, const void *tmap, int layer,
+                          const int32_t *slot_ids, int n, const QKV &in, void *o,
+                          gdn_dtype o_dtype, float scale, cudaStream_t s);
 
-cudaError_t launch_verify(const PoolView &p, int layer, const int32_t *slot_ids, int n,
-                          int T, const QKV &in, void *o, gdn_dtype o_dtype,
+// tmap: the pool's state tensor map (CUtensorMap), or NULL
+cudaError_t launch_verify(const PoolView &p, const void *tmap, int layer, const int32_t *slot_ids,
+                          int n, int T, const QKV &in, void *o, gdn_dtype o_dtype,
                           const int32_t *accept_len, float scale, cudaStream_t s);
+
+cudaError_t launch_verify_tma(const PoolView &p, const void *tmap, int layer,
+                              const int32_t *slot_ids, int n, int T, const QKV &in, void *o,
+                              gdn_dtype o_dtype, const int32_t *accept_len, int commit_all,
+                              float scale, cudaStream_t s);
 
 cudaError_t launch_prefill_recurrent(const PoolView &p, int layer, const SeqIndex &seq,
                                      const QKV &in, void *o, gdn_dtype o_dtype, float scale,

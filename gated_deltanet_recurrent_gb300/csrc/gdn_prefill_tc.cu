@@ -4,18 +4,22 @@
 // One CTA (256 threads) per (sequence, value head) walks the sequence in
 // 64-token chunks.  The float32 state S [dv][dk] lives in tensor memory for
 // the whole call (TMEM columns 0..127, row v in lane v) and is the A operand
-// of the state-dependent products, so it never leaves the SM between chunks.
-// Per chunk (notation of the chunked delta rule, b70-optimization-lab research
-// plan, "What the research found": the (I+A)^{-1} UT transform):
-//   MMA1  D1 = [Q;K] K^T                     -> A = beta e^{dG} KK^T (strict),
-//                                              P = e^{dG} QK^T (lower, incl. diag)
-//   solve (I + A) [W | U] = [diag(beta gamma) K | diag(beta) V]   (CUDA cores)
-//   MMA2  D2 = S W^T,  MMA3  D3 = S Q^T      -> Delta^T = U^T - D2;  S <- gamma_n S
-//   MMA4  D4 = Delta^T P^T                    -> O^T = diag(gamma) D3 + D4
+// of the state products, so it never leaves the SM between chunks.
+// The chunked delta rule (b70-optimization-lab research plan, "What the
+// research found": the (I+A)^{-1} UT transform) gives, with T = (I + A)^{-1},
+//   W = T diag(beta gamma) K,  U = T diag(beta) V,  Delta = U - W S^T.
+// Re-associating, Delta^T = F T^T with F = diag(beta) (V^T - E diag(gamma))
+// and E = S K^T, so W and U are never formed and the only triangular work is
+// the 64 x 64 inverse T.  Per chunk:
+//   MMA1  D1 = [Q;K] K^T,  MMAE  E = S K^T,  MMA3  D3 = S Q^T     (one batch)
+//         -> A = beta e^{dG} KK^T (strict), P = e^{dG} QK^T (lower, incl. diag),
+//            F into TMEM, S <- gamma_n S;  T = (I + A)^{-1} by 16 x 16 blocks
+//   MMAD  Dd = F T^T                 (= Delta^T, stays in TMEM)
+//   MMA4  D4 = Delta^T P^T  -> O^T = diag(gamma) D3 + D4
 //   MMA5  S += Delta^T Ktil,  Ktil = diag(e^{G_n - G}) K
 // TMEM lanes are split over warps w and w+4 (same lane quadrant, column
 // halves).  Operands are K-major, no-swizzle core-matrix tiles in shared
-// memory (see gdn_tc.cuh).
+// memory (see gdn_tc.cuh); F and Delta^T are A operands read from TMEM.
 #include "gdn_tc.cuh"
 
 namespace gdn {
@@ -24,23 +28,26 @@ namespace {
 constexpr int C = kChunk;   // 64
 constexpr int D = 128;      // dk = dv
 constexpr int NT = 256;     // threads
-constexpr int XS = D + 4;   // plain row stride (floats) of the solve buffers
-constexpr int AS = C + 4;   // plain row stride of the A matrix
+constexpr int XS = D + 4;   // plain row stride (floats) of the staged values
+constexpr int AS = C + 4;   // plain row stride of A and of T
 
 // shared-memory map (bytes)
-constexpr int OFF_QK = 0;                          // [Q;K] then [Q;W], 128 x 128 core tile
-constexpr int OFF_XW = OFF_QK + 128 * D * 4;       // W solve (plain 64 x XS), then Delta^T tile
-constexpr int OFF_XU = OFF_XW + C * XS * 4;        // U solve (plain 64 x XS)
-constexpr int OFF_AP = OFF_XU + C * XS * 4;        // A (plain 64 x AS), then P tile 64 x 64
-constexpr int OFF_KT = OFF_AP + C * AS * 4;        // Ktil^T tile 128 x 64
-constexpr int OFF_SC = OFF_KT + D * C * 4;         // scalars
+constexpr int OFF_QK = 0;                          // [Q;K] core tile, 128 x 128
+constexpr int OFF_XU = OFF_QK + 128 * D * 4;       // beta v (plain 64 x XS)
+constexpr int OFF_AP = OFF_XU + C * XS * 4;        // A (plain 64 x AS)
+constexpr int OFF_TP = OFF_AP + C * AS * 4;        // T (plain 64 x AS)
+constexpr int OFF_PT = OFF_TP + C * AS * 4;        // P tile [t][i], 64 x 64
+constexpr int OFF_TT = OFF_PT + C * C * 4;         // T tile [t][i], 64 x 64
+constexpr int OFF_KT = OFF_TT + C * C * 4;         // Ktil^T tile [k][i], 128 x 64
+constexpr int OFF_MS = OFF_KT + D * C * 4;         // block-inverse scratch, 3 x 16 x 16
+constexpr int OFF_SC = OFF_MS + 3 * 256 * 4;       // scalars
 constexpr int SMEM_BYTES = OFF_SC + 4 * C * 4 + 64;
-static_assert(OFF_XW % 1024 == 0 && OFF_KT % 16 == 0 && OFF_AP % 16 == 0, "alignment");
-static_assert(128 * C * 4 <= C * XS * 4, "Delta^T tile fits the W solve buffer");
-static_assert(C * C * 4 <= C * AS * 4, "P tile fits the A buffer");
+static_assert(OFF_PT % 16 == 0 && OFF_TT % 16 == 0 && OFF_KT % 16 == 0, "tile alignment");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 // TMEM columns
-constexpr uint32_t T_S = 0, T_D1 = 128, T_D2 = 192, T_D3 = 256, T_D4 = 320;
+constexpr uint32_t T_S = 0, T_D1 = 128, T_E = 192, T_D3 = 256, T_F = 320, T_DD = 384,
+                   T_D4 = 448;
 constexpr uint32_t TMEM_COLS = 512;
 
 template <typename TI, typename TO>
@@ -49,10 +56,13 @@ __global__ void __launch_bounds__(NT, 1)
                       float scale) {
   extern __shared__ __align__(1024) unsigned char smem[];
   float *QK = reinterpret_cast<float *>(smem + OFF_QK);
-  float *XW = reinterpret_cast<float *>(smem + OFF_XW);
   float *XU = reinterpret_cast<float *>(smem + OFF_XU);
   float *AP = reinterpret_cast<float *>(smem + OFF_AP);
+  float *TP = reinterpret_cast<float *>(smem + OFF_TP);
+  float *PT = reinterpret_cast<float *>(smem + OFF_PT);
+  float *TT = reinterpret_cast<float *>(smem + OFF_TT);
   float *KT = reinterpret_cast<float *>(smem + OFF_KT);
+  float *MS = reinterpret_cast<float *>(smem + OFF_MS);
   float *sG = reinterpret_cast<float *>(smem + OFF_SC);
   float *sGam = sG + C;
   float *sBeta = sGam + C;
@@ -90,6 +100,11 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_init(&bar, 1);
     mbar_fence_init();
   }
+  // T is lower triangular: its strictly-upper 16 x 16 blocks stay zero
+  for (int e = tid; e < C * C; e += NT) {
+    const int r = e / C, c = e % C;
+    if ((c >> 4) > (r >> 4)) TP[r * AS + c] = 0.f;
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -119,8 +134,8 @@ __global__ void __launch_bounds__(NT, 1)
   const TI *bg = static_cast<const TI *>(in.beta);
   const uint32_t qk_s = smem_addr(QK);
   const uint32_t k_s = qk_s + 64 * D * 4;  // rows 64..127 of the [Q;K] tile
-  const uint32_t dt_s = smem_addr(XW);
-  const uint32_t p_s = smem_addr(AP);
+  const uint32_t pt_s = smem_addr(PT);
+  const uint32_t tt_s = smem_addr(TT);
   const uint32_t kt_s = smem_addr(KT);
   constexpr uint32_t SBO_D = tc::sbo_bytes(D);  // 4096
   constexpr uint32_t SBO_C = tc::sbo_bytes(C);  // 2048
@@ -131,7 +146,7 @@ __global__ void __launch_bounds__(NT, 1)
   for (int c0 = 0; c0 < len && alive; c0 += C) {
     const int n = min(C, len - c0);
 
-    // ---- S0: stage normalised q, k (core tiles), beta v (plain), g, beta.
+    // ---- P0: stage normalised q, k (core tiles), beta v (plain), g, beta.
     // Warp w takes tokens 8w .. 8w+7; lane = token (3 bits) + 8 * chunk group, so a
     // quarter-warp writes the 8 rows of one core matrix (contiguous 128 bytes).
     {
@@ -199,7 +214,7 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     tc::fence_after_sync();
 
-    // ---- S1: MMA1  D1 = [Q;K] K^T  (M 128, N 64, K 128)
+    // ---- P1: MMA1 D1 = [Q;K] K^T  (M 128, N 64, K 128)
     if (tid == 0) {
       constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll
@@ -208,12 +223,7 @@ __global__ void __launch_bounds__(NT, 1)
                    tc::smem_desc(k_s + j * KSTEP, tc::kLBO, SBO_D), id, j > 0);
       tc::mma_commit(&bar);
     }
-    // meanwhile: W right-hand side (beta gamma k, plain) and the Ktil^T tile
-    for (int e = tid; e < C * (D / 4); e += NT) {
-      const int t = e % C, c4 = e / C;
-      const float4 k4 = *reinterpret_cast<const float4 *>(QK + tc::core_off(64 + t, 4 * c4, D));
-      *reinterpret_cast<float4 *>(XW + t * XS + 4 * c4) = scale4(sBeta[t] * sGam[t], k4);
-    }
+    // meanwhile: the Ktil^T tile, Ktil = diag(e^{G_n - G}) K
     {
       const int kc = tid & 127;            // row k of Ktil^T
       const int ib = (tid >> 7) * (C / 8); // which half of the i chunks
@@ -233,157 +243,172 @@ __global__ void __launch_bounds__(NT, 1)
     phase ^= 1;
     tc::fence_after_sync();
 
-    // ---- S2: A[t][i] = beta_t e^{G_t - G_i} (k_t . k_i), i < t   (rows 64..127 of D1)
-    if (quad >= 2) {
+    // ---- P2: A (plain) and P (tile) from D1; o part and F from D3 and E; S <- gamma_n S
+    const int i0 = 32 * half;  // this warp's half of the 64 chunk columns
+    if (quad >= 2) {           // rows 64..127 of D1: A[t][i] = beta_t e^{G_t - G_i} k_t.k_i, i < t
       const int t = row - 64;
       const float bt = sBeta[t], gt = sG[t];
-#pragma unroll 1
+#pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         float v[16];
-        const int i0 = 32 * half + 16 * cb;
-        tc::tmem_ld16(lrow + T_D1 + i0, v);
+        tc::tmem_ld16(lrow + T_D1 + i0 + 16 * cb, v);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
+          const int i = i0 + 16 * cb + j;
           float4 a;
-          const int i = i0 + j;
-          a.x = i + 0 < t ? bt * expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
-          a.y = i + 1 < t ? bt * expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
-          a.z = i + 2 < t ? bt * expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
-          a.w = i + 3 < t ? bt * expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
+          a.x = i + 0 < t ? bt * __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
+          a.y = i + 1 < t ? bt * __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
+          a.z = i + 2 < t ? bt * __expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
+          a.w = i + 3 < t ? bt * __expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
           *reinterpret_cast<float4 *>(AP + t * AS + i) = a;
         }
       }
-    }
-    __syncthreads();
-
-    // ---- S3: forward substitution (I + A) X = RHS; thread = one column of [W | U]
-    {
-      float *Xc = (tid < D ? XW + tid : XU + (tid - D));
-      float x[C];
-#pragma unroll
-      for (int t = 0; t < C; ++t) x[t] = Xc[t * XS];
-#pragma unroll
-      for (int t = 1; t < C; ++t) {
-        const float *ar = AP + t * AS;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int i = 0; i + 3 < t; i += 4) {
-          const float4 av = *reinterpret_cast<const float4 *>(ar + i);
-          a0 += av.x * x[i];
-          a1 += av.y * x[i + 1];
-          a2 += av.z * x[i + 2];
-          a3 += av.w * x[i + 3];
-        }
-#pragma unroll
-        for (int i = (t / 4) * 4; i < t; ++i) a0 += ar[i] * x[i];
-        x[t] -= (a0 + a1) + (a2 + a3);
-      }
-#pragma unroll
-      for (int t = 0; t < C; ++t) Xc[t * XS] = x[t];
-    }
-    __syncthreads();
-
-    // ---- S4: W -> rows 64..127 of the [Q;K] tile; P tile (rows 0..63 of D1)
-    for (int e = tid; e < C * (D / 4); e += NT) {
-      const int t = e % C, c4 = e / C;
-      *reinterpret_cast<float4 *>(QK + tc::core_off(64 + t, 4 * c4, D)) =
-          *reinterpret_cast<const float4 *>(XW + t * XS + 4 * c4);
-    }
-    if (quad < 2) {
+    } else {                   // rows 0..63 of D1: P[t][i] = e^{G_t - G_i} q_t.k_i, i <= t
       const int t = row;
       const float gt = sG[t];
-#pragma unroll 1
+#pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         float v[16];
-        const int i0 = 32 * half + 16 * cb;
-        tc::tmem_ld16(lrow + T_D1 + i0, v);
+        tc::tmem_ld16(lrow + T_D1 + i0 + 16 * cb, v);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
+          const int i = i0 + 16 * cb + j;
           float4 pv;
-          const int i = i0 + j;
-          pv.x = i + 0 <= t ? expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
-          pv.y = i + 1 <= t ? expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
-          pv.z = i + 2 <= t ? expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
-          pv.w = i + 3 <= t ? expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
-          *reinterpret_cast<float4 *>(AP + tc::core_off(t, i, C)) = pv;
+          pv.x = i + 0 <= t ? __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
+          pv.y = i + 1 <= t ? __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
+          pv.z = i + 2 <= t ? __expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
+          pv.w = i + 3 <= t ? __expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
+          *reinterpret_cast<float4 *>(PT + tc::core_off(t, i, C)) = pv;
         }
       }
     }
-    tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-
-    // ---- S5: MMA2  D2 = S W^T,  MMA3  D3 = S Q^T   (M 128, N 64, K 128; A from TMEM)
+    // MMAE  E = S K^T, MMA3  D3 = S Q^T (A = S from TMEM): run while the CUDA cores invert
     if (tid == 0) {
       constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll
       for (int j = 0; j < D / 8; ++j)
-        tc::mma_ts(tm + T_D2, tm + T_S + j * 8,
-                   tc::smem_desc(k_s + j * KSTEP, tc::kLBO, SBO_D), id, j > 0);
+        tc::mma_ts(tm + T_E, tm + T_S + j * 8, tc::smem_desc(k_s + j * KSTEP, tc::kLBO, SBO_D),
+                   id, j > 0);
 #pragma unroll
       for (int j = 0; j < D / 8; ++j)
         tc::mma_ts(tm + T_D3, tm + T_S + j * 8,
                    tc::smem_desc(qk_s + j * KSTEP, tc::kLBO, SBO_D), id, j > 0);
       tc::mma_commit(&bar);
     }
+
+    // ---- P3: T = (I + A)^{-1} by 16 x 16 blocks.  First pull the next chunk's
+    // q, k, v rows towards L2 so its staging loads do not wait on HBM.
+    {
+      const int t = tid & (C - 1);
+      const int64_t tok = lo + c0 + C + t;
+      if (tok < hi) {
+        constexpr int LINES = (D * (int)sizeof(TI) + 127) / 128;  // 128-byte lines per row
+        const char *qr = reinterpret_cast<const char *>(qg + tok * in.ld_qk + (int64_t)hk * D);
+        const char *kr = reinterpret_cast<const char *>(kg + tok * in.ld_qk + (int64_t)hk * D);
+        const char *vr = reinterpret_cast<const char *>(vg + tok * in.ld_v + (int64_t)h * D);
+        for (int l = tid >> 6; l < 3 * LINES; l += NT / C) {
+          const char *base = l < LINES ? qr : (l < 2 * LINES ? kr : vr);
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 128 * (l % LINES)));
+        }
+      }
+    }
+    if (tid < C) {  // diagonal blocks: column j of (I + A_bb)^{-1} by forward substitution
+      const int bb = tid >> 4, j = tid & 15;
+      const float *Ab = AP + (16 * bb) * AS + 16 * bb;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = r == j ? 1.f : 0.f;
+#pragma unroll
+        for (int c = 0; c < r; ++c) acc -= Ab[r * AS + c] * x[c];
+        x[r] = acc;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) TP[(16 * bb + r) * AS + 16 * bb + j] = x[r];
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int d = 1; d < 4; ++d) {
+      // M_ij = sum_{k=j}^{i-1} A_ik T_kj for the blocks (i, j) = (b + d, b)
+      for (int e = tid; e < (4 - d) * 256; e += NT) {
+        const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+        const int bi = b + d;
+        float acc = 0.f;
+        for (int kb = b; kb < bi; ++kb) {
+          const float *ar = AP + (16 * bi + r) * AS + 16 * kb;
+          const float *tcol = TP + (16 * kb) * AS + 16 * b + c;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) acc += ar[m] * tcol[m * AS];
+        }
+        MS[e] = acc;
+      }
+      __syncthreads();
+      // T_ij = -T_ii M_ij
+      for (int e = tid; e < (4 - d) * 256; e += NT) {
+        const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+        const int bi = b + d;
+        const float *tr = TP + (16 * bi + r) * AS + 16 * bi;
+        const float *mc = MS + (b << 8) + c;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc += tr[m] * mc[m * 16];
+        TP[(16 * bi + r) * AS + 16 * b + c] = -acc;
+      }
+      __syncthreads();
+    }
+    for (int e = tid; e < C * (C / 4); e += NT) {  // T tile [t][i]
+      const int t = e % C, c4 = e / C;
+      *reinterpret_cast<float4 *>(TT + tc::core_off(t, 4 * c4, C)) =
+          *reinterpret_cast<const float4 *>(TP + t * AS + 4 * c4);
+    }
     alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));
     if (!alive) break;
     phase ^= 1;
     tc::fence_after_sync();
-
-    // ---- S6: Delta^T[v][t] = U[t][v] - D2[v][t] (tile, K = t); o part = gamma_t D3[v][t];
-    //          S <- gamma_n S (MMA5 then accumulates Delta^T Ktil into it)
-    float op[C / 2];
+    // F[v][t] = beta_t v_t[v] - beta_t gamma_t E[v][t] into TMEM; o part; S <- gamma_n S
+    float op[C / 2];  // gamma_t (S Q^T)[v][t] for this warp's half of t
     {
       const int v = row;
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
-        const int t0 = 32 * half + 16 * cb;
-        float d2[16], d3[16];
-        tc::tmem_ld16(lrow + T_D2 + t0, d2);
+        const int t0 = i0 + 16 * cb;
+        float e[16], d3[16], f[16];
+        tc::tmem_ld16(lrow + T_E + t0, e);
         tc::tmem_ld16(lrow + T_D3 + t0, d3);
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
+        for (int j = 0; j < 16; ++j) {
           const int t = t0 + j;
-          float4 dd;
-          dd.x = XU[(t + 0) * XS + v] - d2[j + 0];
-          dd.y = XU[(t + 1) * XS + v] - d2[j + 1];
-          dd.z = XU[(t + 2) * XS + v] - d2[j + 2];
-          dd.w = XU[(t + 3) * XS + v] - d2[j + 3];
-          *reinterpret_cast<float4 *>(XW + tc::core_off(v, t, C)) = dd;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) op[16 * cb + j + q] = sGam[t + q] * d3[j + q];
+          op[16 * cb + j] = sGam[t] * d3[j];
+          f[j] = XU[t * XS + v] - sBeta[t] * sGam[t] * e[j];   // F[v][t]
         }
+        tc::tmem_st16(lrow + T_F + t0, f);
       }
       const float gn = sGam[C - 1];
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
-        float s[16];
-        tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, s);
+        float sv[16];
+        tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, sv);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) s[j] *= gn;
-        tc::tmem_st16(lrow + T_S + 64 * half + 16 * cb, s);
+        for (int j = 0; j < 16; ++j) sv[j] *= gn;
+        tc::tmem_st16(lrow + T_S + 64 * half + 16 * cb, sv);
       }
       tc::tmem_st_wait();
     }
+
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
 
-    // ---- S7: MMA4  D4 = Delta^T P^T (N 64),  MMA5  S += Delta^T Ktil (N 128); K = 64
+    // ---- P4: MMAD  Delta^T = F T^T  (A = F from TMEM, M 128, N 64, K 64)
     if (tid == 0) {
 #pragma unroll
       for (int j = 0; j < C / 8; ++j)
-        tc::mma_ss(tm + T_D4, tc::smem_desc(dt_s + j * KSTEP, tc::kLBO, SBO_C),
-                   tc::smem_desc(p_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 64),
-                   j > 0);
-#pragma unroll
-      for (int j = 0; j < C / 8; ++j)
-        tc::mma_ss(tm + T_S, tc::smem_desc(dt_s + j * KSTEP, tc::kLBO, SBO_C),
-                   tc::smem_desc(kt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 128),
-                   1);
+        tc::mma_ts(tm + T_DD, tm + T_F + j * 8, tc::smem_desc(tt_s + j * KSTEP, tc::kLBO, SBO_C),
+                   tc::idesc_tf32(128, 64), j > 0);
       tc::mma_commit(&bar);
     }
     alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));
@@ -391,13 +416,30 @@ __global__ void __launch_bounds__(NT, 1)
     phase ^= 1;
     tc::fence_after_sync();
 
-    // ---- S8: outputs o[t][v] = scale (gamma_t D3 + D4), this warp's half of t
+    // ---- P5: MMA4  D4 = Delta^T P^T (N 64),  MMA5  S += Delta^T Ktil (N 128); K = 64
+    if (tid == 0) {
+#pragma unroll
+      for (int j = 0; j < C / 8; ++j)
+        tc::mma_ts(tm + T_D4, tm + T_DD + j * 8, tc::smem_desc(pt_s + j * KSTEP, tc::kLBO, SBO_C),
+                   tc::idesc_tf32(128, 64), j > 0);
+#pragma unroll
+      for (int j = 0; j < C / 8; ++j)
+        tc::mma_ts(tm + T_S, tm + T_DD + j * 8, tc::smem_desc(kt_s + j * KSTEP, tc::kLBO, SBO_C),
+                   tc::idesc_tf32(128, 128), 1);
+      tc::mma_commit(&bar);
+    }
+    alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));
+    if (!alive) break;
+    phase ^= 1;
+    tc::fence_after_sync();
+
+    // ---- P6: outputs o[t][v] = scale (gamma_t D3 + D4), this warp's half of t
     {
       const int v = row;
       TO *ob = o + (lo + c0) * p.h_v * D + (int64_t)h * D + v;
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
-        const int t0 = 32 * half + 16 * cb;
+        const int t0 = i0 + 16 * cb;
         float d4[16];
         tc::tmem_ld16(lrow + T_D4 + t0, d4);
 #pragma unroll

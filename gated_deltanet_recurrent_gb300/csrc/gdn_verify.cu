@@ -320,9 +320,14 @@ struct VerifyF {
 
 }  // namespace
 
-cudaError_t launch_verify(const PoolView &p, int layer, const int32_t *slot_ids, int n, int T,
-                          const QKV &in, void *o, gdn_dtype o_dtype, const int32_t *accept_len,
-                          float scale, cudaStream_t s) {
+cudaError_t launch_verify(const PoolView &p, const void *tmap, int layer, const int32_t *slot_ids,
+                          int n, int T, const QKV &in, void *o, gdn_dtype o_dtype,
+                          const int32_t *accept_len, float scale, cudaStream_t s) {
+#if !defined(GDN_VERIFY_ROWS_ONLY)
+  const cudaError_t e =
+      launch_verify_tma(p, tmap, layer, slot_ids, n, T, in, o, o_dtype, accept_len, 0, scale, s);
+  if (e != cudaErrorNotSupported) return e;
+#endif
   return dispatch<VerifyF>(p.dk, in.dtype, o_dtype, p, layer, slot_ids, n, T, in, o, accept_len,
                            scale, s);
 }

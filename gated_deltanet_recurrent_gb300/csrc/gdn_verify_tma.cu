@@ -1,0 +1,269 @@
+// Speculative verify for dk = dv = 128 and T <= 8, with the state head moved
+// by the TMA engine and the row dot products on the tensor cores.
+//
+// One CTA (128 threads) per (slot, value head).  Four tensor-map loads bring
+// the head's 128 x 128 float32 state into shared memory in the 128-byte
+// swizzled layout, which tcgen05 reads directly as a K-major A operand.  One
+// MMA batch computes every row's 2T dot products with the staged, normalised
+// keys and queries (D = S [K;Q]^T, M 128, N 16, into TMEM).  Thread v then
+// owns state row v: the row-level WY recurrences of the verify (see
+// gdn_verify.cu) give its o_t and delta_t, and when the slot commits it
+// rebuilds its row in place (the swizzle makes these row-per-thread accesses
+// conflict-free) before four tensor-map stores write the head back.
+#include <cuda.h>
+
+#include "gdn_rows.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int D = 128;
+constexpr int NT = 128;
+constexpr int TMX = 8;            // drafts handled here (2T <= 16 MMA columns)
+constexpr int NX = 16;            // rows of the [K; Q] operand
+constexpr int TILE = D * D * 4;   // 64 KiB
+constexpr int SLAB = 128 * 32 * 4;  // 16 KiB: 128 rows x 32 floats (one swizzle column)
+
+// shared-memory map after the 1024-byte alignment pad (bytes)
+constexpr int O_X = TILE;                    // [K;Q] core tile 16 x 128
+constexpr int O_KK = O_X + NX * D * 4;       // Gram k.k [8][8]
+constexpr int O_KQ = O_KK + TMX * TMX * 4;   // Gram k.q [8][8]
+constexpr int O_DM = O_KQ + TMX * TMX * 4;   // decay table [9][9]
+constexpr int O_SC = O_DM + 96 * 4;          // alpha, beta, G
+constexpr int SMEM = 1024 + O_SC + 32 * 4;
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(NT)
+    verify_tma_kernel(PoolView p, const __grid_constant__ CUtensorMap tmap, int layer,
+                      const int32_t *__restrict__ slot_ids, int T, QKV in, TO *__restrict__ o,
+                      const int32_t *__restrict__ accept_len, int commit_all, float scale) {
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  unsigned char *base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
+  unsigned char *tile = base;
+  float *X = reinterpret_cast<float *>(base + O_X);
+  float *KK = reinterpret_cast<float *>(base + O_KK);
+  float *KQ = reinterpret_cast<float *>(base + O_KQ);
+  float *Dm = reinterpret_cast<float *>(base + O_DM);
+  float *sal = reinterpret_cast<float *>(base + O_SC);
+  float *sbe = sal + TMX;
+  float *sG = sbe + TMX;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_slot;
+
+  const int h = blockIdx.x, i = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = slot_ids[i];
+  if (slot < 0 || slot >= p.n_slots) {
+    if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
+    return;
+  }
+  int a = commit_all ? T : (accept_len ? accept_len[i] : 0);
+  if (a < 0 || a > T) {
+    if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
+    a = a < 0 ? 0 : T;
+  }
+  const int row0 = ((layer * p.n_slots + slot) * p.h_v + h) * D;  // tensor-map row
+  const int hk = h / (p.h_v / p.h_k);
+
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 32);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  for (int e = tid; e < (NX - 2 * T) * (D / 4); e += NT) {  // zero the unused X rows
+    const int r = 2 * T + e / (D / 4), c4 = e % (D / 4);
+    *reinterpret_cast<float4 *>(X + tc::core_off(r, 4 * c4, D)) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = tmem_slot;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, TILE);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+          "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(tile + s * SLAB)),
+          "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(32 * s), "r"(row0), "r"(smem_addr(&bar))
+          : "memory");
+  }
+
+  // ---- stage the drafts while the head is in flight
+  for (int t = warp; t < T; t += NT / 32) {
+    const int64_t tok = (int64_t)i * T + t;
+    float4 q4 = Elem<TI>::load4(static_cast<const TI *>(in.q) + tok * in.ld_qk + (int64_t)hk * D + 4 * lane);
+    float4 k4 = Elem<TI>::load4(static_cast<const TI *>(in.k) + tok * in.ld_qk + (int64_t)hk * D + 4 * lane);
+    const float qq = group_sum<32>(dot4(q4, q4));
+    const float kk = group_sum<32>(dot4(k4, k4));
+    *reinterpret_cast<float4 *>(X + tc::core_off(t, 4 * lane, D)) = scale4(rsqrtf(kk + kL2Eps), k4);
+    *reinterpret_cast<float4 *>(X + tc::core_off(T + t, 4 * lane, D)) =
+        scale4(rsqrtf(qq + kL2Eps), q4);
+  }
+  const int v = tid;  // this thread's state row
+  float vr[TMX];
+#pragma unroll
+  for (int t = 0; t < TMX; ++t)
+    vr[t] = t < T ? Elem<TI>::load1(static_cast<const TI *>(in.v) +
+                                    ((int64_t)i * T + t) * in.ld_v + (int64_t)h * D + v)
+                  : 0.f;
+  const TI *gg = static_cast<const TI *>(in.g) + (int64_t)i * T * p.h_v + h;
+  if (tid < T) {
+    sal[tid] = expf(Elem<TI>::load1(gg + (int64_t)tid * p.h_v));
+    sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(in.beta) + (int64_t)i * T * p.h_v + h +
+                               (int64_t)tid * p.h_v);
+  }
+  if (tid <= T) {
+    float acc = 0.f;
+    for (int t = 0; t < tid; ++t) acc += Elem<TI>::load1(gg + (int64_t)t * p.h_v);
+    sG[tid] = acc;
+  }
+  __syncthreads();
+  // Gram scalars (four lanes per pair) and the decay table
+  for (int e0 = 0; e0 < 2 * T * T; e0 += NT / 4) {
+    const int e = e0 + tid / 4, sub4 = tid % 4;
+    float acc = 0.f;
+    const int which = e / (T * T), ii = (e / T) % T, tt = e % T;
+    if (e < 2 * T * T) {
+      const int ry = which ? T + tt : tt;
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const int c = 4 * (4 * j + sub4);
+        acc += dot4(*reinterpret_cast<const float4 *>(X + tc::core_off(ii, c, D)),
+                    *reinterpret_cast<const float4 *>(X + tc::core_off(ry, c, D)));
+      }
+    }
+    acc = group_sum<4>(acc);
+    if (e < 2 * T * T && sub4 == 0) (which ? KQ : KK)[ii * TMX + tt] = acc;
+  }
+  for (int e = tid; e < (T + 1) * (T + 1); e += NT) {
+    const int aa = e / (T + 1), bb = e % (T + 1);
+    Dm[aa * (TMX + 1) + bb] = bb <= aa ? expf(sG[aa] - sG[bb]) : 0.f;
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  bool alive = __syncthreads_and(mbar_wait_bounded(&bar, 0));
+  tc::fence_after_sync();
+
+  // ---- D[v][t'] = S[v][:] . X[t'][:]  (M 128, N 16, K 128)
+  if (alive && tid == 0) {
+    const uint32_t t_s = smem_addr(tile), x_s = smem_addr(X);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        tc::mma_ss(tm, desc_sw128(t_s + s * SLAB + j * 32),
+                   tc::smem_desc(x_s + (4 * s + j) * 2 * tc::kLBO, tc::kLBO, tc::sbo_bytes(D)),
+                   tc::idesc_tf32(128, NX), (s | j) != 0);
+    tc::mma_commit(&bar);
+  }
+  if (alive) alive = __syncthreads_and(mbar_wait_bounded(&bar, 1));
+  tc::fence_after_sync();
+
+  if (alive) {
+    float dots[16];
+    tc::tmem_ld16(tm + ((uint32_t)(32 * warp) << 16), dots);
+    float dl[TMX];
+    TO *ob = o == nullptr ? nullptr : o + ((int64_t)i * T * p.h_v + h) * D + v;
+#pragma unroll
+    for (int t = 0; t < TMX; ++t) {
+      dl[t] = 0.f;
+      if (t < T) {
+        float pt = Dm[t * (TMX + 1)] * dots[t];
+#pragma unroll
+        for (int ii = 0; ii < TMX; ++ii)
+          if (ii < t) pt += Dm[t * (TMX + 1) + ii + 1] * dl[ii] * KK[ii * TMX + t];
+        dl[t] = sbe[t] * (vr[t] - sal[t] * pt);
+        if (ob != nullptr) {
+          float dq = 0.f;  // dots[T + t] without a runtime register index
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (u == T + t) dq = dots[u];
+          float ot = Dm[(t + 1) * (TMX + 1)] * dq;
+#pragma unroll
+          for (int ii = 0; ii < TMX; ++ii)
+            if (ii <= t) ot += Dm[(t + 1) * (TMX + 1) + ii + 1] * dl[ii] * KQ[ii * TMX + t];
+          Elem<TO>::store1(ob + (int64_t)t * p.h_v * D, scale * ot);
+        }
+      }
+    }
+    if (a > 0) {  // rebuild row v at the accepted length, in place (swizzled)
+      const float c0 = Dm[a * (TMX + 1)];
+      float cf[TMX];
+#pragma unroll
+      for (int ii = 0; ii < TMX; ++ii) cf[ii] = ii < a ? Dm[a * (TMX + 1) + ii + 1] * dl[ii] : 0.f;
+      unsigned char *rowp = tile + (v >> 3) * 1024 + (v & 7) * 128;
+#pragma unroll 4
+      for (int c = 0; c < D / 4; ++c) {
+        float4 *sp = reinterpret_cast<float4 *>(rowp + (c >> 3) * SLAB + (((c & 7) ^ (v & 7)) << 4));
+        float4 acc = scale4(c0, *sp);
+#pragma unroll
+        for (int ii = 0; ii < TMX; ++ii)
+          if (ii < a)
+            acc = axpby4(1.f, acc, cf[ii],
+                         *reinterpret_cast<const float4 *>(X + tc::core_off(ii, 4 * c, D)));
+        *sp = acc;
+      }
+      tc::fence_async_smem();
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (alive && a > 0 && tid == 0) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+              reinterpret_cast<uint64_t>(&tmap)),
+          "r"(32 * s), "r"(row0), "r"(smem_addr(tile + s * SLAB))
+          : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  }
+  if (!alive) {
+    if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
+    mbar_wait_bounded(&bar, 0);
+    mbar_wait_bounded(&bar, 1);
+  }
+  tc::fence_after_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tm, 32);
+}
+
+template <typename TI, typename TO>
+cudaError_t launch_t(const PoolView &p, const CUtensorMap &tmap, int layer,
+                     const int32_t *slot_ids, int n, int T, const QKV &in, void *o,
+                     const int32_t *accept_len, int commit_all, float scale, cudaStream_t s) {
+  auto kern = verify_tma_kernel<TI, TO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.h_v, n);
+  kern<<<grid, NT, SMEM, s>>>(p, tmap, layer, slot_ids, T, in, static_cast<TO *>(o), accept_len,
+                              commit_all, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_verify_tma(const PoolView &p, const void *tmap, int layer,
+                              const int32_t *slot_ids, int n, int T, const QKV &in, void *o,
+                              gdn_dtype o_dtype, const int32_t *accept_len, int commit_all,
+                              float scale, cudaStream_t s) {
+  if (tmap == nullptr || p.dk != D || p.dv != D || T > TMX) return cudaErrorNotSupported;
+  const CUtensorMap &m = *static_cast<const CUtensorMap *>(tmap);
+#define GDN_GO(TI, TO) \
+  return launch_t<TI, TO>(p, m, layer, slot_ids, n, T, in, o, accept_len, commit_all, scale, s)
+  if (in.dtype == GDN_F32 && o_dtype == GDN_F32) GDN_GO(float, float);
+  if (in.dtype == GDN_F32 && o_dtype == GDN_BF16) GDN_GO(float, bf16);
+  if (in.dtype == GDN_BF16 && o_dtype == GDN_F32) GDN_GO(bf16, float);
+  GDN_GO(bf16, bf16);
+#undef GDN_GO
+}
+
+}  // namespace gdn
