@@ -365,26 +365,45 @@ def verify_bench(torch, abi, synth, device, steps, peak):
     acc = torch.from_numpy(wl["accept_len"]).to(device)
     o = torch.empty(n, T, s.h_v, s.dv, device=device, dtype=torch.bfloat16)
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
-    for _ in range(3):
-        abi.gdn_spec_verify(pool, 0, ids, T, *draft, o=o, accept_len=acc)
     E = lambda: torch.cuda.Event(enable_timing=True)
-    evs = [(E(), E()) for _ in range(steps)]
-    torch.cuda.synchronize()
-    for j in range(steps):
-        flush.zero_()
-        evs[j][0].record()
-        abi.gdn_spec_verify(pool, 0, ids, T, *draft, o=o, accept_len=acc)
-        evs[j][1].record()
-    torch.cuda.synchronize()
-    t = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+
+    def timed(round_fn):
+        for _ in range(3):
+            round_fn()
+        evs = [(E(), E()) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for j in range(steps):
+            flush.zero_()
+            evs[j][0].record()
+            round_fn()
+            evs[j][1].record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / 1e3 / steps
+
+    # one pass with the accepted lengths known: outputs + commit
+    t = timed(lambda: abi.gdn_spec_verify(pool, 0, ids, T, *draft, o=o, accept_len=acc))
     committing = int((wl["accept_len"] > 0).sum())
+    tok_bytes = T * (2 * 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 2 + 32 * 128 * 2)
     per_call = n * STATE_BYTES_PER_SLOT_LAYER / 2 + committing * STATE_BYTES_PER_SLOT_LAYER / 2 \
-        + n * T * (2 * 16 * 128 * 2 + 32 * 128 * 2 + 2 * 32 * 2 + 32 * 128 * 2)
-    gbs = per_call * steps / t / 1e9
+        + n * tok_bytes
+    gbs = per_call / t / 1e9
+    # a speculative round when the acceptance is known only after the outputs:
+    # two-phase (verify, then commit recomputing the drafts) against deferred
+    # (the previous round's accepted drafts committed inside this round's call)
+    t_two = timed(lambda: (abi.gdn_spec_verify(pool, 0, ids, T, *draft, o=o),
+                           abi.gdn_spec_verify(pool, 0, ids, T, *draft, accept_len=acc)))
+    t_def = timed(lambda: abi.gdn_spec_verify_deferred(pool, 0, ids, T, *draft, o, prev=draft,
+                                                       prev_accept=acc))
+    per_def = per_call + n * tok_bytes
+    del pool
     return {"workload": "spec verify, decode-step layer shape, 128 active of 256 slots, T=4, "
                         "bf16 in/out, commit at accepted length U{0..4}, one pass",
-            "slot_verifies_per_s": n * steps / t, "us_per_call": t / steps * 1e6,
-            "algorithmic_gbs": gbs, "hbm_frac": gbs / peak}
+            "slot_verifies_per_s": n / t, "us_per_call": t * 1e6,
+            "algorithmic_gbs": gbs, "hbm_frac": gbs / peak,
+            "round_two_phase_us": t_two * 1e6, "round_deferred_us": t_def * 1e6,
+            "round_deferred_speedup": t_two / t_def,
+            "deferred_algorithmic_gbs": per_def / t_def / 1e9,
+            "deferred_hbm_frac": per_def / t_def / 1e9 / peak}
 
 
 def prefill_bench(torch, abi, synth, device, steps):

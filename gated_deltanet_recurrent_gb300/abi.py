@@ -25,7 +25,7 @@ EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "g
             "gdn_pool_copy",
             "gdn_pool_destroy", "gdn_pool_get_error", "gdn_conv_silu", "gdn_decode_step",
             "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
-            "gdn_status_string",
+            "gdn_spec_verify_deferred", "gdn_status_string",
             "gdn_last_error_message")
 
 
@@ -82,6 +82,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                        ctypes.c_float, vp]),
         "gdn_spec_verify": (st, [vp, i32, vp, i32, i32, P(gdn_qkv), vp, st, vp,
                                  ctypes.c_float, vp]),
+        "gdn_spec_verify_deferred": (st, [vp, i32, vp, i32, i32, P(gdn_qkv), vp, st, i32,
+                                          P(gdn_qkv), vp, ctypes.c_float, vp]),
         "gdn_status_string": (ctypes.c_char_p, [st]),
         "gdn_last_error_message": (ctypes.c_char_p, []),
     }
@@ -301,4 +303,26 @@ def gdn_spec_verify(pool: Pool, layer: int, slot_ids: torch.Tensor, T: int, q, k
         pool.handle, layer, _idx(slot_ids, "slot_ids"), slot_ids.numel(), T,
         ctypes.byref(inp), _ptr(o), o_dt, _idx(accept_len, "accept_len"), scale,
         _stream(stream)))
+    return o
+
+
+def gdn_spec_verify_deferred(pool: Pool, layer: int, slot_ids: torch.Tensor, T: int, q, k, v, g,
+                             beta, o: torch.Tensor, prev=None,
+                             prev_accept: Optional[torch.Tensor] = None, scale: float = 1.0,
+                             stream=None):
+    """Commit the first prev_accept[i] of last round's drafts, then output this
+    round's T drafts without committing them.  prev = (q, k, v, g, beta) of
+    last round ([n*T_prev, ...] each) or None; o [n, T, h_v, dv]."""
+    inp = _qkv(pool, q, k, v, g, beta)
+    n = slot_ids.numel()
+    T_prev, pin = 0, None
+    if prev is not None:
+        pin = _qkv(pool, *prev)
+        if n == 0 or prev[0].shape[0] % n:
+            raise GDNError(5, "prev holds no whole number of drafts per slot")
+        T_prev = prev[0].shape[0] // n
+    _check(load_library().gdn_spec_verify_deferred(
+        pool.handle, layer, _idx(slot_ids, "slot_ids"), n, T, ctypes.byref(inp), _ptr(o),
+        _dt(o), T_prev, None if pin is None else ctypes.byref(pin),
+        _idx(prev_accept, "prev_accept"), scale, _stream(stream)))
     return o

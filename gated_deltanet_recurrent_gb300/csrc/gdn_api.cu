@@ -414,9 +414,48 @@ gdn_status gdn_spec_verify(gdn_pool *p, int32_t layer, const int32_t *slot_ids, 
     if (accept_len && (st = check_counts(accept_len, n, nullptr, T, s, "accept_len"))) return st;
     if (o && (st = check_device_ptr(o, "o"))) return st;
   }
-  cudaError_t e = gdn::launch_verify(p->view, p->has_tmap ? &p->tmap : nullptr, layer, slot_ids,
-                                     n, T, q, o, o_dtype, accept_len, scale, s);
+  gdn::VerifyArgs va{slot_ids, n, T, q, accept_len, 0, gdn::QKV{}, 0, nullptr, scale};
+  cudaError_t e =
+      gdn::launch_verify(p->view, p->has_tmap ? &p->tmap : nullptr, layer, va, o, o_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  return ok();
+}
+
+gdn_status gdn_spec_verify_deferred(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                                    int32_t n, int32_t T, const gdn_qkv *in, void *o,
+                                    gdn_dtype o_dtype, int32_t T_prev, const gdn_qkv *prev,
+                                    const int32_t *prev_accept, float scale, gdn_stream stream) {
+  gdn_status st = check_pool(p, layer);
+  if (st != GDN_OK) return st;
+  if (n < 0) return fail(GDN_ERR_ARG, "n = %d < 0", n);
+  if (T < 1 || T_prev < 0 || T + T_prev > gdn::kMaxVerifyT)
+    return fail(GDN_ERR_SIZE, "T = %d, T_prev = %d: need T >= 1, T_prev >= 0, T + T_prev <= %d",
+                T, T_prev, gdn::kMaxVerifyT);
+  if (!o) return fail(GDN_ERR_ARG, "o is NULL");
+  if (n == 0) return ok();
+  if (n > 65535) return fail(GDN_ERR_SIZE, "n = %d > 65535", n);
+  if (!slot_ids) return fail(GDN_ERR_ARG, "slot_ids is NULL");
+  if (!dtype_ok(o_dtype)) return fail(GDN_ERR_DTYPE, "o dtype must be F32 or BF16");
+  const bool pending = prev != nullptr && prev_accept != nullptr && T_prev > 0;
+  if ((prev != nullptr) != (prev_accept != nullptr))
+    return fail(GDN_ERR_ARG, "prev and prev_accept must both be set or both be NULL");
+  gdn::QKV q, qp{};
+  if ((st = resolve_qkv(p, in, (int64_t)n * T, q))) return st;
+  if (pending) {
+    if ((st = resolve_qkv(p, prev, (int64_t)n * T_prev, qp))) return st;
+    if (qp.dtype != q.dtype) return fail(GDN_ERR_DTYPE, "prev and in must share one dtype");
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    if ((st = check_slots(p, slot_ids, n, s)) || (st = check_device_ptr(o, "o"))) return st;
+    if (pending && (st = check_counts(prev_accept, n, nullptr, T_prev, s, "prev_accept")))
+      return st;
+  }
+  gdn::VerifyArgs va{slot_ids, n, T, q, nullptr, 0, pending ? qp : gdn::QKV{},
+                     pending ? T_prev : 0, pending ? prev_accept : nullptr, scale};
+  cudaError_t e =
+      gdn::launch_verify(p->view, p->has_tmap ? &p->tmap : nullptr, layer, va, o, o_dtype, s);
+  if (e != cudaSuccess) return cuda_fail(e, "deferred verify launch");
   return ok();
 }
 

@@ -59,15 +59,30 @@ cudaError_t launch_decode(const PoolView &p, const void *tmap, int layer,
                           const int32_t *slot_ids, int n, const QKV &in, void *o,
                           gdn_dtype o_dtype, float scale, cudaStream_t s);
 
+// Speculative verify of T new drafts per slot.  Normal mode: commit at
+// accept_len[i] (or after all T with commit_all).  Deferred mode (prev.q set):
+// slot i first replays the first prev_accept[i] drafts of the previous round
+// (token i*T_prev + t of prev), commits the state right after them, and then
+// runs the new drafts for their outputs only.
+struct VerifyArgs {
+  const int32_t *slot_ids;
+  int n;
+  int T;
+  QKV in;
+  const int32_t *accept_len;
+  int commit_all;
+  QKV prev;                    // prev.q == NULL: no pending drafts
+  int T_prev;
+  const int32_t *prev_accept;
+  float scale;
+};
+
 // tmap: the pool's state tensor map (CUtensorMap), or NULL
-cudaError_t launch_verify(const PoolView &p, const void *tmap, int layer, const int32_t *slot_ids,
-                          int n, int T, const QKV &in, void *o, gdn_dtype o_dtype,
-                          const int32_t *accept_len, float scale, cudaStream_t s);
+cudaError_t launch_verify(const PoolView &p, const void *tmap, int layer, const VerifyArgs &va,
+                          void *o, gdn_dtype o_dtype, cudaStream_t s);
 
 cudaError_t launch_verify_tma(const PoolView &p, const void *tmap, int layer,
-                              const int32_t *slot_ids, int n, int T, const QKV &in, void *o,
-                              gdn_dtype o_dtype, const int32_t *accept_len, int commit_all,
-                              float scale, cudaStream_t s);
+                              const VerifyArgs &va, void *o, gdn_dtype o_dtype, cudaStream_t s);
 
 cudaError_t launch_prefill_recurrent(const PoolView &p, int layer, const SeqIndex &seq,
                                      const QKV &in, void *o, gdn_dtype o_dtype, float scale,

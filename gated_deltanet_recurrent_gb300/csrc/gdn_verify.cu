@@ -31,9 +31,7 @@ constexpr int kTileBytes = 32768;  // state tile per CTA (one bulk copy)
 // copy while the tokens are staged.  grid (ceil(dv / R), h_v, n).
 template <int DK, int TMAX, typename TI, typename TO>
 __global__ void __launch_bounds__(kThreads)
-    rows_kernel(PoolView p, int layer, const int32_t *__restrict__ slot_ids, int T, QKV in,
-                TO *__restrict__ o, const int32_t *__restrict__ accept_len, int commit_all,
-                float scale) {
+    rows_kernel(PoolView p, int layer, VerifyArgs va, TO *__restrict__ o) {
   constexpr int R = kTileBytes / (DK * 4);   // rows per CTA
   constexpr int LPR = 4;                     // lanes per row
   constexpr int C4 = DK / 16;                // float4 chunks per lane per row
@@ -45,34 +43,52 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ __align__(8) uint64_t bar;
   // dynamic: k, q [T][DK]; v [T][R]; Gram KK, KQ [T][T]; D [(T+1)][(T+1)]; alpha, beta [T];
   // G [T+1]
+  // (sized for Tb = T_prev + T tokens; this CTA runs T = ap + T_new <= Tb)
   extern __shared__ float4 dsm[];
+  const int Tb = va.T + va.T_prev;
   float4 *sk4 = dsm;
-  float4 *sq4 = sk4 + T * (DK / 4);
-  float *sv = reinterpret_cast<float *>(sq4 + T * (DK / 4));
-  float *KK = sv + T * R;
-  float *KQ = KK + T * T;
-  float *Dm = KQ + T * T;
-  float *sal = Dm + (T + 1) * (T + 1);
-  float *sbe = sal + T;
-  float *sG = sbe + T;  // cumulative log-decay after t tokens, t = 0..T
+  float4 *sq4 = sk4 + Tb * (DK / 4);
+  float *sv = reinterpret_cast<float *>(sq4 + Tb * (DK / 4));
+  float *KK = sv + Tb * R;
+  float *KQ = KK + Tb * Tb;
+  float *Dm = KQ + Tb * Tb;
+  float *sal = Dm + (Tb + 1) * (Tb + 1);
+  float *sbe = sal + Tb;
+  float *sG = sbe + Tb;  // cumulative log-decay after t tokens, t = 0..T
   // looped variant only (TMAX > 8): per-row dot products and deltas, [32 rows][T] each
-  float *rdk = sG + T + 1;
-  float *rdq = rdk + 32 * T;
-  float *rdl = rdq + 32 * T;
+  float *rdk = sG + Tb + 1;
+  float *rdq = rdk + 32 * Tb;
+  float *rdl = rdq + 32 * Tb;
 
   const int i = blockIdx.z;
   const int h = blockIdx.y;
   const int tid = threadIdx.x;
-  const int slot = slot_ids[i];
+  const int slot = va.slot_ids[i];
   if (slot < 0 || slot >= p.n_slots) {
     if (blockIdx.x == 0 && h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
     return;
   }
-  int a = commit_all ? T : (accept_len ? accept_len[i] : 0);
+  const bool deferred = va.prev.q != nullptr && va.prev_accept != nullptr;
+  int ap = deferred ? va.prev_accept[i] : 0;  // pending drafts replayed first
+  if (ap < 0 || ap > va.T_prev) {
+    if (blockIdx.x == 0 && h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
+    ap = ap < 0 ? 0 : va.T_prev;
+  }
+  const int T = ap + va.T;
+  int a = deferred ? ap : (va.commit_all ? T : (va.accept_len ? va.accept_len[i] : 0));
   if (a < 0 || a > T) {
     if (blockIdx.x == 0 && h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
     a = a < 0 ? 0 : T;
   }
+  // token t of this CTA's sequence: pending draft t, or new draft t - ap
+  auto src_of = [&](int t, int64_t &row) -> const QKV & {
+    if (t < ap) {
+      row = (int64_t)i * va.T_prev + t;
+      return va.prev;
+    }
+    row = (int64_t)i * va.T + (t - ap);
+    return va.in;
+  };
   const int r0 = blockIdx.x * R;
   const int nrows = min(R, p.dv - r0);
   float *S = state_head(p, layer, slot, h) + (int64_t)r0 * DK;
@@ -90,14 +106,13 @@ __global__ void __launch_bounds__(kThreads)
   // ---- stage the T tokens (overlaps the bulk copy)
   const int lane = tid & 31, warp = tid >> 5;
   const int hk = h / (p.h_v / p.h_k);
-  const TI *qg = static_cast<const TI *>(in.q);
-  const TI *kg = static_cast<const TI *>(in.k);
   for (int t = warp; t < T; t += kThreads / 32) {
-    const int64_t tok = (int64_t)i * T + t;
+    int64_t tok;
+    const QKV &src = src_of(t, tok);
     float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4;
     if (lane < DK / 4) {
-      q4 = Elem<TI>::load4(qg + tok * in.ld_qk + (int64_t)hk * DK + 4 * lane);
-      k4 = Elem<TI>::load4(kg + tok * in.ld_qk + (int64_t)hk * DK + 4 * lane);
+      q4 = Elem<TI>::load4(static_cast<const TI *>(src.q) + tok * src.ld_qk + (int64_t)hk * DK + 4 * lane);
+      k4 = Elem<TI>::load4(static_cast<const TI *>(src.k) + tok * src.ld_qk + (int64_t)hk * DK + 4 * lane);
     }
     const float qq = group_sum<32>(dot4(q4, q4));
     const float kk = group_sum<32>(dot4(k4, k4));
@@ -106,20 +121,27 @@ __global__ void __launch_bounds__(kThreads)
       sk4[t * (DK / 4) + lane] = scale4(rsqrtf(kk + kL2Eps), k4);
     }
   }
-  const TI *vg = static_cast<const TI *>(in.v) + (int64_t)h * p.dv + r0;
   for (int e = tid; e < T * R; e += kThreads) {
     const int t = e / R, rl = e % R;
-    sv[e] = rl < nrows ? Elem<TI>::load1(vg + ((int64_t)i * T + t) * in.ld_v + rl) : 0.f;
+    int64_t tok;
+    const QKV &src = src_of(t, tok);
+    sv[e] = rl < nrows ? Elem<TI>::load1(static_cast<const TI *>(src.v) + tok * src.ld_v +
+                                        (int64_t)h * p.dv + r0 + rl)
+                       : 0.f;
   }
-  const TI *gg = static_cast<const TI *>(in.g) + (int64_t)i * T * p.h_v + h;
   if (tid < T) {
-    const int64_t gb = (int64_t)tid * p.h_v;
-    sal[tid] = expf(Elem<TI>::load1(gg + gb));  // alpha_t
-    sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(in.beta) + (int64_t)i * T * p.h_v + h + gb);
+    int64_t tok;
+    const QKV &src = src_of(tid, tok);
+    sal[tid] = expf(Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h));  // alpha_t
+    sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * p.h_v + h);
   }
   if (tid <= T) {  // G_t = g_0 + ... + g_{t-1}
     float acc = 0.f;
-    for (int t = 0; t < tid; ++t) acc += Elem<TI>::load1(gg + (int64_t)t * p.h_v);
+    for (int t = 0; t < tid; ++t) {
+      int64_t tok;
+      const QKV &src = src_of(t, tok);
+      acc += Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
+    }
     sG[tid] = acc;
   }
   __syncthreads();
@@ -159,7 +181,9 @@ __global__ void __launch_bounds__(kThreads)
   const int rho = lane / LPR;
   const int rot = rho % C4;  // per-row rotation of the chunk order (bank spread)
   const int64_t o_tok = (int64_t)p.h_v * p.dv;
-  TO *obase = o == nullptr ? nullptr : o + ((int64_t)i * T * p.h_v + h) * p.dv + r0;
+  // output of token t >= ap: new draft t - ap of slot i
+  TO *obase = o == nullptr ? nullptr : o + ((int64_t)i * va.T * p.h_v + h) * p.dv + r0;
+  const float scale = va.scale;
 #pragma unroll
   for (int ps = 0; ps < PASSES; ++ps) {
     const int rl = warp * RPW + ps * RPP + rho;
@@ -201,7 +225,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int ii = 0; ii < TMAX; ++ii)
               if (ii <= t) ot += Dm[(t + 1) * (T + 1) + ii + 1] * dl[ii] * KQ[ii * T + t];
-            if (live && (t % LPR) == sub) Elem<TO>::store1(obase + t * o_tok + rl, scale * ot);
+            if (live && t >= ap && (t % LPR) == sub)
+              Elem<TO>::store1(obase + (t - ap) * o_tok + rl, scale * ot);
           }
         } else {
           dl[t] = 0.f;
@@ -251,7 +276,7 @@ __global__ void __launch_bounds__(kThreads)
             float ot = Dm[(t + 1) * (T + 1)] * rdq[rs + t];
             for (int ii = 0; ii <= t; ++ii)
               ot += Dm[(t + 1) * (T + 1) + ii + 1] * rdl[rs + ii] * KQ[ii * T + t];
-            if (live) Elem<TO>::store1(obase + t * o_tok + rl, scale * ot);
+            if (live && t >= ap) Elem<TO>::store1(obase + (t - ap) * o_tok + rl, scale * ot);
           }
         }
       }
@@ -282,11 +307,10 @@ inline size_t rows_smem_bytes(int DK, int R, int T, bool looped) {
 }
 
 template <int DK, int TMAX, typename TI, typename TO>
-cudaError_t launch_rows_t(const PoolView &p, int layer, const int32_t *slot_ids, int n, int T,
-                          const QKV &in, void *o, const int32_t *accept_len, int commit_all,
-                          float scale, cudaStream_t s) {
+cudaError_t launch_rows_t(const PoolView &p, int layer, const VerifyArgs &va, void *o,
+                          cudaStream_t s) {
   constexpr int R = kTileBytes / (DK * 4);
-  const size_t smem = rows_smem_bytes(DK, R, T, TMAX > 8);
+  const size_t smem = rows_smem_bytes(DK, R, va.T + va.T_prev, TMAX > 8);
   auto kern = rows_kernel<DK, TMAX, TI, TO>;
   // the static tile counts against the default 48 KiB per-block limit
   if (smem + kTileBytes + 64 > 48 * 1024) {
@@ -294,42 +318,27 @@ cudaError_t launch_rows_t(const PoolView &p, int layer, const int32_t *slot_ids,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid((p.dv + R - 1) / R, p.h_v, n);
-  kern<<<grid, kThreads, smem, s>>>(p, layer, slot_ids, T, in, static_cast<TO *>(o), accept_len,
-                                     commit_all, scale);
+  dim3 grid((p.dv + R - 1) / R, p.h_v, va.n);
+  kern<<<grid, kThreads, smem, s>>>(p, layer, va, static_cast<TO *>(o));
   return cudaGetLastError();
 }
 
 template <int DK, typename TI, typename TO>
-cudaError_t launch_verify_t(const PoolView &p, int layer, const int32_t *slot_ids, int n, int T,
-                            const QKV &in, void *o, const int32_t *accept_len, float scale,
-                            cudaStream_t s) {
-  if (T <= 4)
-    return launch_rows_t<DK, 4, TI, TO>(p, layer, slot_ids, n, T, in, o, accept_len, 0, scale, s);
-  return launch_rows_t<DK, 32, TI, TO>(p, layer, slot_ids, n, T, in, o, accept_len, 0, scale, s);
-}
-
-template <int DK, typename TI, typename TO>
 struct VerifyF {
-  static cudaError_t run(const PoolView &p, int layer, const int32_t *slot_ids, int n, int T,
-                         const QKV &in, void *o, const int32_t *accept_len, float scale,
+  static cudaError_t run(const PoolView &p, int layer, const VerifyArgs &va, void *o,
                          cudaStream_t s) {
-    return launch_verify_t<DK, TI, TO>(p, layer, slot_ids, n, T, in, o, accept_len, scale, s);
+    if (va.T + va.T_prev <= 4) return launch_rows_t<DK, 4, TI, TO>(p, layer, va, o, s);
+    return launch_rows_t<DK, 32, TI, TO>(p, layer, va, o, s);
   }
 };
 
 }  // namespace
 
-cudaError_t launch_verify(const PoolView &p, const void *tmap, int layer, const int32_t *slot_ids,
-                          int n, int T, const QKV &in, void *o, gdn_dtype o_dtype,
-                          const int32_t *accept_len, float scale, cudaStream_t s) {
-#if !defined(GDN_VERIFY_ROWS_ONLY)
-  const cudaError_t e =
-      launch_verify_tma(p, tmap, layer, slot_ids, n, T, in, o, o_dtype, accept_len, 0, scale, s);
+cudaError_t launch_verify(const PoolView &p, const void *tmap, int layer, const VerifyArgs &va,
+                          void *o, gdn_dtype o_dtype, cudaStream_t s) {
+  const cudaError_t e = launch_verify_tma(p, tmap, layer, va, o, o_dtype, s);
   if (e != cudaErrorNotSupported) return e;
-#endif
-  return dispatch<VerifyF>(p.dk, in.dtype, o_dtype, p, layer, slot_ids, n, T, in, o, accept_len,
-                           scale, s);
+  return dispatch<VerifyF>(p.dk, va.in.dtype, o_dtype, p, layer, va, o, s);
 }
 
 }  // namespace gdn

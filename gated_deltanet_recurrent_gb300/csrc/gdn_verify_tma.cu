@@ -41,8 +41,7 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(NT)
     verify_tma_kernel(PoolView p, const __grid_constant__ CUtensorMap tmap, int layer,
-                      const int32_t *__restrict__ slot_ids, int T, QKV in, TO *__restrict__ o,
-                      const int32_t *__restrict__ accept_len, int commit_all, float scale) {
+                      VerifyArgs va, TO *__restrict__ o) {
   extern __shared__ __align__(1024) unsigned char dsm[];
   unsigned char *base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
   unsigned char *tile = base;
@@ -58,16 +57,31 @@ __global__ void __launch_bounds__(NT)
 
   const int h = blockIdx.x, i = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slot = slot_ids[i];
+  const int slot = va.slot_ids[i];
   if (slot < 0 || slot >= p.n_slots) {
     if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
     return;
   }
-  int a = commit_all ? T : (accept_len ? accept_len[i] : 0);
+  const bool deferred = va.prev.q != nullptr && va.prev_accept != nullptr;
+  int ap = deferred ? va.prev_accept[i] : 0;  // pending drafts replayed first
+  if (ap < 0 || ap > va.T_prev) {
+    if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
+    ap = ap < 0 ? 0 : va.T_prev;
+  }
+  const int T = ap + va.T;  // <= TMX (checked by the launcher)
+  int a = deferred ? ap : (va.commit_all ? T : (va.accept_len ? va.accept_len[i] : 0));
   if (a < 0 || a > T) {
     if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
     a = a < 0 ? 0 : T;
   }
+  auto src_of = [&](int t, int64_t &row) -> const QKV & {
+    if (t < ap) {
+      row = (int64_t)i * va.T_prev + t;
+      return va.prev;
+    }
+    row = (int64_t)i * va.T + (t - ap);
+    return va.in;
+  };
   const int row0 = ((layer * p.n_slots + slot) * p.h_v + h) * D;  // tensor-map row
   const int hk = h / (p.h_v / p.h_k);
 
@@ -97,9 +111,10 @@ __global__ void __launch_bounds__(NT)
 
   // ---- stage the drafts while the head is in flight
   for (int t = warp; t < T; t += NT / 32) {
-    const int64_t tok = (int64_t)i * T + t;
-    float4 q4 = Elem<TI>::load4(static_cast<const TI *>(in.q) + tok * in.ld_qk + (int64_t)hk * D + 4 * lane);
-    float4 k4 = Elem<TI>::load4(static_cast<const TI *>(in.k) + tok * in.ld_qk + (int64_t)hk * D + 4 * lane);
+    int64_t tok;
+    const QKV &src = src_of(t, tok);
+    float4 q4 = Elem<TI>::load4(static_cast<const TI *>(src.q) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
+    float4 k4 = Elem<TI>::load4(static_cast<const TI *>(src.k) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
     const float qq = group_sum<32>(dot4(q4, q4));
     const float kk = group_sum<32>(dot4(k4, k4));
     *reinterpret_cast<float4 *>(X + tc::core_off(t, 4 * lane, D)) = scale4(rsqrtf(kk + kL2Eps), k4);
@@ -109,19 +124,27 @@ __global__ void __launch_bounds__(NT)
   const int v = tid;  // this thread's state row
   float vr[TMX];
 #pragma unroll
-  for (int t = 0; t < TMX; ++t)
-    vr[t] = t < T ? Elem<TI>::load1(static_cast<const TI *>(in.v) +
-                                    ((int64_t)i * T + t) * in.ld_v + (int64_t)h * D + v)
-                  : 0.f;
-  const TI *gg = static_cast<const TI *>(in.g) + (int64_t)i * T * p.h_v + h;
+  for (int t = 0; t < TMX; ++t) {
+    vr[t] = 0.f;
+    if (t < T) {
+      int64_t tok;
+      const QKV &src = src_of(t, tok);
+      vr[t] = Elem<TI>::load1(static_cast<const TI *>(src.v) + tok * src.ld_v + (int64_t)h * D + v);
+    }
+  }
   if (tid < T) {
-    sal[tid] = expf(Elem<TI>::load1(gg + (int64_t)tid * p.h_v));
-    sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(in.beta) + (int64_t)i * T * p.h_v + h +
-                               (int64_t)tid * p.h_v);
+    int64_t tok;
+    const QKV &src = src_of(tid, tok);
+    sal[tid] = expf(Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h));
+    sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * p.h_v + h);
   }
   if (tid <= T) {
     float acc = 0.f;
-    for (int t = 0; t < tid; ++t) acc += Elem<TI>::load1(gg + (int64_t)t * p.h_v);
+    for (int t = 0; t < tid; ++t) {
+      int64_t tok;
+      const QKV &src = src_of(t, tok);
+      acc += Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
+    }
     sG[tid] = acc;
   }
   __syncthreads();
@@ -170,7 +193,8 @@ __global__ void __launch_bounds__(NT)
     float dots[16];
     tc::tmem_ld16(tm + ((uint32_t)(32 * warp) << 16), dots);
     float dl[TMX];
-    TO *ob = o == nullptr ? nullptr : o + ((int64_t)i * T * p.h_v + h) * D + v;
+    // output of token t >= ap: new draft t - ap of slot i
+    TO *ob = o == nullptr ? nullptr : o + ((int64_t)i * va.T * p.h_v + h) * D + v;
 #pragma unroll
     for (int t = 0; t < TMX; ++t) {
       dl[t] = 0.f;
@@ -180,7 +204,7 @@ __global__ void __launch_bounds__(NT)
         for (int ii = 0; ii < TMX; ++ii)
           if (ii < t) pt += Dm[t * (TMX + 1) + ii + 1] * dl[ii] * KK[ii * TMX + t];
         dl[t] = sbe[t] * (vr[t] - sal[t] * pt);
-        if (ob != nullptr) {
+        if (ob != nullptr && t >= ap) {
           float dq = 0.f;  // dots[T + t] without a runtime register index
 #pragma unroll
           for (int u = 0; u < 16; ++u)
@@ -189,7 +213,7 @@ __global__ void __launch_bounds__(NT)
 #pragma unroll
           for (int ii = 0; ii < TMX; ++ii)
             if (ii <= t) ot += Dm[(t + 1) * (TMX + 1) + ii + 1] * dl[ii] * KQ[ii * TMX + t];
-          Elem<TO>::store1(ob + (int64_t)t * p.h_v * D, scale * ot);
+          Elem<TO>::store1(ob + (int64_t)(t - ap) * p.h_v * D, va.scale * ot);
         }
       }
     }
@@ -237,33 +261,27 @@ __global__ void __launch_bounds__(NT)
 }
 
 template <typename TI, typename TO>
-cudaError_t launch_t(const PoolView &p, const CUtensorMap &tmap, int layer,
-                     const int32_t *slot_ids, int n, int T, const QKV &in, void *o,
-                     const int32_t *accept_len, int commit_all, float scale, cudaStream_t s) {
+cudaError_t launch_t(const PoolView &p, const CUtensorMap &tmap, int layer, const VerifyArgs &va,
+                     void *o, cudaStream_t s) {
   auto kern = verify_tma_kernel<TI, TO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.h_v, n);
-  kern<<<grid, NT, SMEM, s>>>(p, tmap, layer, slot_ids, T, in, static_cast<TO *>(o), accept_len,
-                              commit_all, scale);
+  dim3 grid(p.h_v, va.n);
+  kern<<<grid, NT, SMEM, s>>>(p, tmap, layer, va, static_cast<TO *>(o));
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_verify_tma(const PoolView &p, const void *tmap, int layer,
-                              const int32_t *slot_ids, int n, int T, const QKV &in, void *o,
-                              gdn_dtype o_dtype, const int32_t *accept_len, int commit_all,
-                              float scale, cudaStream_t s) {
-  if (tmap == nullptr || p.dk != D || p.dv != D || T > TMX) return cudaErrorNotSupported;
+                              const VerifyArgs &va, void *o, gdn_dtype o_dtype, cudaStream_t s) {
+  if (tmap == nullptr || p.dk != D || p.dv != D || va.T + va.T_prev > TMX)
+    return cudaErrorNotSupported;
   const CUtensorMap &m = *static_cast<const CUtensorMap *>(tmap);
-#define GDN_GO(TI, TO) \
-  return launch_t<TI, TO>(p, m, layer, slot_ids, n, T, in, o, accept_len, commit_all, scale, s)
-  if (in.dtype == GDN_F32 && o_dtype == GDN_F32) GDN_GO(float, float);
-  if (in.dtype == GDN_F32 && o_dtype == GDN_BF16) GDN_GO(float, bf16);
-  if (in.dtype == GDN_BF16 && o_dtype == GDN_F32) GDN_GO(bf16, float);
-  GDN_GO(bf16, bf16);
-#undef GDN_GO
+  if (va.in.dtype == GDN_F32 && o_dtype == GDN_F32) return launch_t<float, float>(p, m, layer, va, o, s);
+  if (va.in.dtype == GDN_F32 && o_dtype == GDN_BF16) return launch_t<float, bf16>(p, m, layer, va, o, s);
+  if (va.in.dtype == GDN_BF16 && o_dtype == GDN_F32) return launch_t<bf16, float>(p, m, layer, va, o, s);
+  return launch_t<bf16, bf16>(p, m, layer, va, o, s);
 }
 
 }  // namespace gdn

@@ -212,6 +212,27 @@ gdn_status gdn_spec_verify(gdn_pool *pool, int32_t layer, const int32_t *slot_id
                            int32_t T, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
                            const int32_t *accept_len, float scale, gdn_stream stream);
 
+/* Speculative verify with the commit deferred to the next round
+ * (b70-optimization-lab research plan, "What the research found": the
+ * drafts' inputs are kept and the full state is written back only later).
+ * Each slot first replays the first prev_accept[i] of last round's T_prev
+ * drafts (`prev`, draft t of slot i at token i*T_prev + t) and commits the
+ * state after them; on that committed state it computes the outputs of this
+ * round's T drafts (`in`, draft t at token i*T + t) without committing them.
+ * o: [n][T][h_v][dv] in o_dtype, required.  One call reads each state once
+ * and writes it at most once; a two-phase round (gdn_spec_verify without,
+ * then with, accept_len) reads it twice and writes it once.  The caller
+ * keeps this round's inputs until the next call, which passes them as
+ * `prev` with the accepted counts; gdn_spec_verify with accept_len flushes
+ * them without new drafts.  prev and prev_accept are both NULL (no pending
+ * drafts: outputs only) or both set; prev_accept: [n] int32 in [0, T_prev];
+ * prev and in share one dtype.  T >= 1, T_prev >= 0, T + T_prev <= 32: the
+ * pending drafts plus this round's fit one 32-token window. */
+gdn_status gdn_spec_verify_deferred(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
+                                    int32_t n, int32_t T, const gdn_qkv *in, void *o,
+                                    gdn_dtype o_dtype, int32_t T_prev, const gdn_qkv *prev,
+                                    const int32_t *prev_accept, float scale, gdn_stream stream);
+
 /* Human-readable name of a status, and the detail of the last failure on
  * this host thread (empty string if none). */
 const char *gdn_status_string(gdn_status s);

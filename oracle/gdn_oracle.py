@@ -270,3 +270,25 @@ class OraclePool:
             if accept_len is not None:
                 self.S[layer, s] = S_keep
         return o
+
+    def spec_verify_deferred(self, layer, slot_ids, T, q, k, v, g, beta,
+                             T_prev=0, prev=None, prev_accept=None, scale=1.0, eps=L2_EPS):
+        """Deferred commit [P2, "What the research found": keep the drafts'
+        inputs and write the full state back later].  Slot i first advances
+        its committed state by the first prev_accept[i] of last round's
+        drafts (prev = (q, k, v, g, beta), draft t at token i*T_prev + t) and
+        commits it; then its T new drafts (token i*T + t) are verified on that
+        state, outputs only.  Returns o [N, T, H_v, V]."""
+        n = len(slot_ids)
+        o = np.empty((n, T, self.h_v, self.dv))
+        for i, s in enumerate(slot_ids):
+            if prev is not None:
+                pq, pk, pv, pg, pb = prev
+                for t in range(int(prev_accept[i])):
+                    r = i * T_prev + t
+                    self.S[layer, s], _ = gdn_step(self.S[layer, s], pq[r], pk[r], pv[r],
+                                                   pg[r], pb[r], scale, eps)
+            sl = slice(i * T, (i + 1) * T)
+            o[i], _ = spec_verify(self.S[layer, s], q[sl], k[sl], v[sl], g[sl], beta[sl],
+                                  None, scale, eps)
+        return o

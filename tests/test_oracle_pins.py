@@ -15,6 +15,8 @@ Map (oracle function -> pins):
                   planted mistakes are caught by the brute force
   gdn_chunked     equals token by token for several chunk sizes; golden example
   spec_verify     equals decode steps; commit at a == a steps; a = 0 unchanged
+  spec_verify_deferred  rounds equal the two-phase rounds; the state after
+                  the flush equals decoding only the accepted drafts
   OraclePool      N slots == each alone; reset == fresh; prefill split
                   invariance across pieces (chunked-prefill state carry)
 """
@@ -503,3 +505,43 @@ def test_pool_spec_verify_commit_then_decode():
             ref.decode_step(0, [s], *(a[j:j + 1] for a in args))
         np.testing.assert_array_equal(p.S[0, s], ref.S[0, s])
     np.testing.assert_array_equal(p.S[0, 1], before[0, 1])
+
+
+def test_pool_deferred_rounds_equal_two_phase_rounds():
+    """Three speculative rounds with pending commits folded into the next
+    round give the outputs of verify-then-commit rounds, and after a final
+    flush the states equal decoding only the accepted drafts one by one."""
+    rng = np.random.default_rng(34)
+    shape = synth.LayerShape(2, 1, 8, 8, 16, 4)
+    n, slots = 3, [1, 3, 0]
+    Ts = [3, 2, 4]
+    accepts = [[2, 0, 3], [1, 2, 0], [4, 1, 2]]
+    mk = lambda: O.OraclePool(1, 4, shape.h_v, shape.h_k, shape.dk, shape.dv,
+                              shape.conv_ch, shape.conv_k)
+    S0 = rng.standard_normal((1, 4, shape.h_v, shape.dv, shape.dk))
+    rounds = []
+    for T in Ts:
+        d = synth.token_inputs(rng, n * T, shape)
+        rounds.append([d[nm] for nm in ("q", "k", "v", "g", "beta")])
+    two, dfr, dec = mk(), mk(), mk()
+    for p in (two, dfr, dec):
+        p.S[:] = S0
+    prev, T_prev, prev_acc = None, 0, None
+    for T, args, acc in zip(Ts, rounds, accepts):
+        o_two = two.spec_verify(0, slots, T, *args)
+        two.spec_verify(0, slots, T, *args, accept_len=acc)
+        o_dfr = dfr.spec_verify_deferred(0, slots, T, *args, T_prev=T_prev, prev=prev,
+                                         prev_accept=prev_acc)
+        np.testing.assert_allclose(o_dfr, o_two, rtol=1e-12, atol=1e-12)
+        for i, s in enumerate(slots):
+            for t in range(acc[i]):
+                j = i * T + t
+                dec.decode_step(0, [s], *(a[j:j + 1] for a in args))
+        prev, T_prev, prev_acc = args, T, acc
+    # pending drafts are still outstanding: the deferred pool lags until flushed
+    assert not np.allclose(dfr.S, two.S)
+    dfr.spec_verify(0, slots, T_prev, *prev, accept_len=prev_acc)
+    np.testing.assert_allclose(dfr.S, two.S, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dfr.S, dec.S, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(dfr.S[0, 2], S0[0, 2])
+
