@@ -430,25 +430,30 @@ def prefill_bench(torch, abi, synth, device, steps):
         ob = torch.empty(len(rows), s.h_v, s.dv, device=device, dtype=torch.bfloat16)
         calls.append((ids, ccu, packed, ob, max(ln)))
 
-    def run(fn):
-        for ids, ccu, packed, ob, mx in calls:
-            fn(pool, 0, ids, ccu, *packed, ob, max_seqlen=mx)
+    # the same pool memory under a 1-byte workspace limit: the single-launch kernel
+    single = abi.Pool.for_shape(s, 1, len(lens), conv_dtype=torch.bfloat16, host_checks=False,
+                                device=device, prefill_workspace_max=1)
 
-    def timed(fn):
-        pool.state[0].copy_(init)
-        run(fn)
+    def run(fn, pl):
+        for ids, ccu, packed, ob, mx in calls:
+            fn(pl, 0, ids, ccu, *packed, ob, max_seqlen=mx)
+
+    def timed(fn, pl=pool):
+        pl.state[0].copy_(init)
+        run(fn, pl)
         E = lambda: torch.cuda.Event(enable_timing=True)
         evs = [(E(), E()) for _ in range(steps)]
         for j in range(steps):
-            pool.state[0].copy_(init)
+            pl.state[0].copy_(init)
             evs[j][0].record()
-            run(fn)
+            run(fn, pl)
             evs[j][1].record()
         torch.cuda.synchronize()
         return sum(a.elapsed_time(b) for a, b in evs) / 1e3
 
     try:
         t = timed(abi.gdn_prefill_chunked)
+        t_single = timed(abi.gdn_prefill_chunked, single)
         t_rec = timed(abi.gdn_prefill_recurrent)
     except abi.GDNError as e:
         return {"unavailable": str(e)}
@@ -458,6 +463,7 @@ def prefill_bench(torch, abi, synth, device, steps):
                         f"between calls, bf16 in/out, chunk 64",
             "tokens_per_s": total * steps / t, "ms_per_pass": t / steps * 1e3,
             "calls_per_pass": len(calls),
+            "single_launch_tokens_per_s": total * steps / t_single,
             "token_by_token_tokens_per_s": total * steps / t_rec,
             "speedup_over_token_by_token": t_rec / t}
 

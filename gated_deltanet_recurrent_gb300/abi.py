@@ -41,7 +41,8 @@ class gdn_pool_desc(ctypes.Structure):
                 ("h_v", ctypes.c_int32), ("h_k", ctypes.c_int32),
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
                 ("conv_ch", ctypes.c_int32), ("conv_k", ctypes.c_int32),
-                ("conv_dtype", ctypes.c_int), ("host_checks", ctypes.c_int32)]
+                ("conv_dtype", ctypes.c_int), ("host_checks", ctypes.c_int32),
+                ("prefill_workspace_max", ctypes.c_uint64)]
 
 
 class gdn_qkv(ctypes.Structure):
@@ -159,10 +160,11 @@ class Pool:
     conv_ch, conv_k-1] in conv_dtype.  Both start at zero."""
 
     def __init__(self, n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k,
-                 conv_dtype=torch.bfloat16, host_checks=True, device="cuda"):
+                 conv_dtype=torch.bfloat16, host_checks=True, device="cuda",
+                 prefill_workspace_max=0):
         self.desc = gdn_pool_desc(n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k,
                                   GDN_F32 if conv_dtype == torch.float32 else GDN_BF16,
-                                  1 if host_checks else 0)
+                                  1 if host_checks else 0, prefill_workspace_max)
         self.state = torch.zeros((n_layers, n_slots, h_v, dv, dk), dtype=torch.float32,
                                  device=device)
         self.conv = torch.zeros((n_layers, n_slots, conv_ch, conv_k - 1), dtype=conv_dtype,
@@ -171,9 +173,10 @@ class Pool:
 
     @classmethod
     def for_shape(cls, shape, n_layers, n_slots, conv_dtype=torch.bfloat16, host_checks=True,
-                  device="cuda"):
+                  device="cuda", prefill_workspace_max=0):
         return cls(n_layers, n_slots, shape.h_v, shape.h_k, shape.dk, shape.dv,
-                   shape.conv_ch, shape.conv_k, conv_dtype, host_checks, device)
+                   shape.conv_ch, shape.conv_k, conv_dtype, host_checks, device,
+                   prefill_workspace_max)
 
     def set_host_checks(self, on: bool):
         """Recreate the handle with host checks switched on or off (same memory)."""

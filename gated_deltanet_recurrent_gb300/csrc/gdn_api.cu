@@ -16,6 +16,7 @@ struct gdn_pool {
   int device;
   bool has_tmap;
   alignas(64) CUtensorMap tmap;  // the state as a [rows][dk] float32 tensor (TMA)
+  cudaMemPool_t work_pool;       // stream-ordered prefill workspaces (kept until destroy)
 };
 
 namespace {
@@ -263,6 +264,21 @@ gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t st
                           desc->n_layers, desc->n_slots, desc->h_v, desc->h_k, desc->dk,
                           desc->dv, desc->conv_ch, desc->conv_k, desc->conv_dtype};
   p->has_tmap = encode_state_map(p);
+  cudaMemPoolProps props = {};
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  e = cudaMemPoolCreate(&p->work_pool, &props);
+  if (e == cudaSuccess) {
+    uint64_t keep = UINT64_MAX;  // keep freed workspace for the next call
+    e = cudaMemPoolSetAttribute(p->work_pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) cudaMemPoolDestroy(p->work_pool);
+  }
+  if (e != cudaSuccess) {
+    cudaFree(err);
+    delete p;
+    return cuda_fail(e, "creating the workspace memory pool");
+  }
   *out = p;
   return ok();
 }
@@ -271,6 +287,8 @@ gdn_status gdn_pool_destroy(gdn_pool *p) {
   if (!p) return ok();
   cudaError_t e = cudaDeviceSynchronize();
   cudaError_t e2 = cudaFree(p->view.err);
+  cudaError_t e3 = cudaMemPoolDestroy(p->work_pool);
+  if (e2 == cudaSuccess) e2 = e3;
   delete p;
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree(error word)");
@@ -484,10 +502,26 @@ gdn_status prefill_common(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
       return st;
   }
   gdn::SeqIndex seq{slot_ids, cu_seqlens, n_seqs, total_tokens};
-  cudaError_t e =
-      chunked ? gdn::launch_prefill(p->view, layer, seq, total_tokens,
-                                    max_seqlen < 1 ? 1 : max_seqlen, q, o, o_dtype, scale, s)
-              : gdn::launch_prefill_recurrent(p->view, layer, seq, q, o, o_dtype, scale, s);
+  cudaError_t e;
+  if (chunked) {
+    // the two-launch path keeps per-chunk tiles in a stream-ordered workspace;
+    // without one (allocation refused) the single-launch kernel runs instead
+    void *work = nullptr;
+    const uint64_t lim = p->desc.prefill_workspace_max ? p->desc.prefill_workspace_max
+                                                       : (uint64_t)8 << 30;
+    const size_t wb = gdn::prefill_workspace_bytes(p->view, seq, q, (size_t)lim);
+    if (wb > 0 && cudaMallocFromPoolAsync(&work, wb, p->work_pool, s) != cudaSuccess) {
+      cudaGetLastError();
+      work = nullptr;
+    }
+    e = gdn::launch_prefill(p->view, layer, seq, q, o, o_dtype, scale, work, s);
+    if (work != nullptr) {
+      const cudaError_t ef = cudaFreeAsync(work, s);
+      if (e == cudaSuccess) e = ef;
+    }
+  } else {
+    e = gdn::launch_prefill_recurrent(p->view, layer, seq, q, o, o_dtype, scale, s);
+  }
   if (e == cudaErrorNotSupported)
     return fail(GDN_ERR_UNSUPPORTED, "prefill is not available for this shape");
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

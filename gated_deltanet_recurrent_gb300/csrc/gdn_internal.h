@@ -91,8 +91,22 @@ cudaError_t launch_prefill_recurrent(const PoolView &p, int layer, const SeqInde
 cudaError_t launch_prefill_tc(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in,
                               void *o, gdn_dtype o_dtype, float scale, cudaStream_t s);
 
-cudaError_t launch_prefill(const PoolView &p, int layer, const SeqIndex &seq,
-                           int total_tokens, int max_seqlen, const QKV &in, void *o,
-                           gdn_dtype o_dtype, float scale, cudaStream_t s);
+// Two-launch chunked prefill (dk = dv = 128): key-side tiles of every chunk
+// in parallel into `work`, then the state side sequence by sequence.
+size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v);
+cudaError_t launch_prefill_split(const PoolView &p, int layer, const SeqIndex &seq,
+                                 const QKV &in, void *o, gdn_dtype o_dtype, float scale,
+                                 void *work, cudaStream_t s);
+
+// Workspace bytes the chunked prefill of this call would use, or 0 when it
+// runs without one (not the tensor-core shape, or more than `limit` bytes).
+size_t prefill_workspace_bytes(const PoolView &p, const SeqIndex &seq, const QKV &in,
+                               size_t limit);
+
+// Chunked prefill; `work` is a device workspace of prefill_workspace_bytes()
+// bytes, or NULL (the single-launch kernels, which need none).
+cudaError_t launch_prefill(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in,
+                           void *o, gdn_dtype o_dtype, float scale, void *work,
+                           cudaStream_t s);
 
 }  // namespace gdn

@@ -331,19 +331,33 @@ cudaError_t launch_prefill_d(const PoolView &p, int layer, const SeqIndex &seq, 
 
 }  // namespace
 
-cudaError_t launch_prefill(const PoolView &p, int layer, const SeqIndex &seq, int total_tokens,
-                           int max_seqlen, const QKV &in, void *o, gdn_dtype o_dtype, float scale,
-                           cudaStream_t s) {
-  (void)total_tokens;
-  (void)max_seqlen;
-  if (p.dk != p.dv) return cudaErrorNotSupported;
-#if !defined(GDN_PREFILL_SIMT_ONLY)
-  // tensor-core path: dk = dv = 128 and 128-bit aligned rows of v
+namespace {
+
+// tensor-core paths: dk = dv = 128 and 128-bit aligned rows of v
+bool tc_shape(const PoolView &p, const QKV &in) {
   const size_t es = in.dtype == GDN_F32 ? 4 : 2;
   const size_t al = in.dtype == GDN_F32 ? 16 : 8;
-  if (p.dk == 128 && (uintptr_t)in.v % al == 0 && ((size_t)in.ld_v * es) % al == 0)
+  return p.dk == 128 && p.dv == 128 && (uintptr_t)in.v % al == 0 &&
+         ((size_t)in.ld_v * es) % al == 0;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(const PoolView &p, const SeqIndex &seq, const QKV &in,
+                               size_t limit) {
+  if (!tc_shape(p, in)) return 0;
+  const size_t b = prefill_split_workspace_bytes(seq.n_seqs, seq.total_tokens, p.h_v);
+  return b <= limit ? b : 0;
+}
+
+cudaError_t launch_prefill(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in,
+                           void *o, gdn_dtype o_dtype, float scale, void *work,
+                           cudaStream_t s) {
+  if (p.dk != p.dv) return cudaErrorNotSupported;
+  if (tc_shape(p, in)) {
+    if (work != nullptr) return launch_prefill_split(p, layer, seq, in, o, o_dtype, scale, work, s);
     return launch_prefill_tc(p, layer, seq, in, o, o_dtype, scale, s);
-#endif
+  }
   switch (p.dk) {
     case 16: return launch_prefill_d<16>(p, layer, seq, in, o, o_dtype, scale, s);
     case 32: return launch_prefill_d<32>(p, layer, seq, in, o, o_dtype, scale, s);

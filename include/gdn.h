@@ -90,6 +90,11 @@ typedef struct {
   int32_t conv_k;     /* conv width; the cache keeps conv_k - 1 inputs */
   gdn_dtype conv_dtype; /* dtype of conv inputs/outputs and of the cache */
   int32_t host_checks;  /* nonzero: validate index arrays on the host (syncs) */
+  /* Upper bound (bytes) on the workspace one gdn_prefill_chunked call may take
+   * for its two-launch tensor-core path (about 32 KiB per 64-token chunk per
+   * value head); 0 means 8 GiB.  Calls that would need more, or whose
+   * workspace cannot be allocated, run the single-launch kernel instead. */
+  uint64_t prefill_workspace_max;
 } gdn_pool_desc;
 
 /* Per-token inputs of the recurrence for `tokens` tokens.
@@ -116,8 +121,10 @@ size_t gdn_pool_conv_bytes(const gdn_pool_desc *desc);
  * slot dimension that page asks for).  Wraps caller memory: state_mem and
  * conv_mem (256-byte aligned device memory of at least the sizes above) are
  * NOT cleared -- call gdn_pool_reset for new requests, or write states
- * directly.  The pool allocates only a 4-byte device error word.
- * On success *out receives the handle. */
+ * directly.  The pool allocates a 4-byte device error word and owns a
+ * stream-ordered memory pool from which chunked prefill takes its workspace
+ * (kept for reuse until gdn_pool_destroy).  On success *out receives the
+ * handle. */
 gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t state_bytes,
                            void *conv_mem, size_t conv_bytes, gdn_pool **out);
 
@@ -136,7 +143,8 @@ gdn_status gdn_pool_reset(gdn_pool *pool, const int32_t *slot_ids, int32_t n, gd
 gdn_status gdn_pool_copy(gdn_pool *pool, const int32_t *src_slots, const int32_t *dst_slots,
                          int32_t n, gdn_stream stream);
 
-/* Release the handle and its error word (caller memory is left alone).
+/* Release the handle, its error word and its workspace memory pool (caller
+ * memory is left alone).
  * Synchronises the device before freeing. NULL is a no-op. */
 gdn_status gdn_pool_destroy(gdn_pool *pool);
 

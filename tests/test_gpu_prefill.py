@@ -167,6 +167,39 @@ def test_prefill_split_across_calls_equals_whole_and_token_recurrence(entry):
         assert_maxrel(S, S_ref, tol, f"S {name}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prefill_two_launch_path_equals_single_launch_kernel(dtype):
+    """dk = dv = 128: the two-launch path (per-chunk key-side tiles in a
+    workspace) and the single-launch kernel (no workspace: forced by a 1-byte
+    workspace limit) run the same arithmetic, so they agree to float32
+    rounding; both also match the oracle."""
+    rng = np.random.default_rng(44)
+    shape = synth.LayerShape(4, 2, 128, 128, 16, 4)
+    lens = [200, 0, 1, 64, 129, 77]
+    ids = np.array([5, 0, 2, 7, 1, 4], dtype=np.int32)
+    cu = synth.cu_seqlens_of(lens)
+    S0 = synth.random_states(rng, len(ids), shape)
+    tok = synth.token_inputs(rng, int(cu[-1]), shape, dtype)
+    lid = torch.from_numpy(ids).long().cuda()
+    res = {}
+    for name, limit in (("two-launch", 0), ("single", 1)):
+        pool = abi.Pool.for_shape(shape, 1, 8, conv_dtype=torch.float32,
+                                  prefill_workspace_max=limit)
+        pool.state[0, lid] = dev(S0)
+        o = torch.empty(int(cu[-1]), shape.h_v, shape.dv, device="cuda")
+        abi.gdn_prefill_chunked(pool, 0, dev_i32(ids), dev_i32(cu), *tok_dev(tok, dtype), o,
+                                max_seqlen=max(lens))
+        res[name] = (host(o), host(pool.state[0, lid]))
+        assert abi.gdn_pool_get_error(pool) == 0
+    assert_maxrel(res["two-launch"][0], res["single"][0], 1e-5, "o two-launch vs single")
+    assert_maxrel(res["two-launch"][1], res["single"][1], 1e-5, "S two-launch vs single")
+    ref = O.OraclePool(1, 8, shape.h_v, shape.h_k, shape.dk, shape.dv, 16, 4)
+    ref.S[0, ids] = S0
+    o_ref = ref.prefill(0, ids, cu, *tok_np(tok))
+    assert_maxrel(res["two-launch"][0], o_ref, _rel_tol(128), "o")
+    assert_maxrel(res["two-launch"][1], ref.S[0, ids], _rel_tol(128), "S")
+
+
 def _head_sample(tok, heads, group):
     """Slice value heads `heads` (and the key heads they read) out of a token dict."""
     kh = [h // group for h in heads]
