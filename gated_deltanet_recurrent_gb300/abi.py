@@ -25,7 +25,7 @@ EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "g
             "gdn_pool_copy",
             "gdn_pool_destroy", "gdn_pool_get_error", "gdn_conv_silu", "gdn_decode_step",
             "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
-            "gdn_spec_verify_deferred", "gdn_status_string",
+            "gdn_spec_verify_deferred", "gdn_prefill_chunked_noalloc", "gdn_status_string",
             "gdn_last_error_message")
 
 
@@ -85,6 +85,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                  ctypes.c_float, vp]),
         "gdn_spec_verify_deferred": (st, [vp, i32, vp, i32, i32, P(gdn_qkv), vp, st, i32,
                                           P(gdn_qkv), vp, ctypes.c_float, vp]),
+        "gdn_prefill_chunked_noalloc": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
+                                             ctypes.c_float, vp]),
         "gdn_status_string": (ctypes.c_char_p, [st]),
         "gdn_last_error_message": (ctypes.c_char_p, []),
     }
@@ -328,4 +330,19 @@ def gdn_spec_verify_deferred(pool: Pool, layer: int, slot_ids: torch.Tensor, T: 
         pool.handle, layer, _idx(slot_ids, "slot_ids"), n, T, ctypes.byref(inp), _ptr(o),
         _dt(o), T_prev, None if pin is None else ctypes.byref(pin),
         _idx(prev_accept, "prev_accept"), scale, _stream(stream)))
+    return o
+
+
+def gdn_prefill_chunked_noalloc(pool: Pool, layer: int, slot_ids: torch.Tensor,
+                                cu_seqlens: torch.Tensor, q, k, v, g, beta, o: torch.Tensor,
+                                scale: float = 1.0, max_seqlen: int = 0, stream=None):
+    """gdn_prefill_chunked without any device allocation: its workspace is a
+    fixed 64 MiB array inside the library, shared by all calls."""
+    inp = _qkv(pool, q, k, v, g, beta)
+    if max_seqlen <= 0:
+        max_seqlen = q.shape[0]
+    _check(load_library().gdn_prefill_chunked_noalloc(
+        pool.handle, layer, _idx(slot_ids, "slot_ids"), _idx(cu_seqlens, "cu_seqlens"),
+        slot_ids.numel(), q.shape[0], max_seqlen, ctypes.byref(inp), _ptr(o), _dt(o), scale,
+        _stream(stream)))
     return o

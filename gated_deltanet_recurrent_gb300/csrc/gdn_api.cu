@@ -5,6 +5,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -544,6 +545,85 @@ gdn_status gdn_prefill_recurrent(gdn_pool *p, int32_t layer, const int32_t *slot
                                  gdn_dtype o_dtype, float scale, gdn_stream stream) {
   return prefill_common(p, layer, slot_ids, cu_seqlens, n_seqs, total_tokens, max_seqlen, in, o,
                         o_dtype, scale, stream, false);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------
+// Chunked prefill that allocates no device memory: the two-launch path's
+// workspace lives in one file-scope device array, shared by every call.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_prefill_scratch[kNoAllocScratchBytes];
+
+// The array's device address on `dev` (which must be current), looked up once
+// per device.  In host code the array's name is only a stand-in, never a
+// pointer a kernel may be given.
+cudaError_t noalloc_scratch(int dev, void **out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void *addr[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_prefill_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_prefill_chunked_noalloc(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                                       const int32_t *cu_seqlens, int32_t n_seqs,
+                                       int32_t total_tokens, int32_t max_seqlen,
+                                       const gdn_qkv *in, void *o, gdn_dtype o_dtype, float scale,
+                                       gdn_stream stream) {
+  (void)max_seqlen;
+  gdn_status st = check_pool(p, layer);
+  if (st != GDN_OK) return st;
+  if (n_seqs < 0 || total_tokens < 0) return fail(GDN_ERR_ARG, "negative n_seqs/total_tokens");
+  if (n_seqs == 0 || total_tokens == 0) return ok();
+  if (n_seqs > 65535) return fail(GDN_ERR_SIZE, "n_seqs = %d > 65535", n_seqs);
+  if (!slot_ids || !cu_seqlens || !o)
+    return fail(GDN_ERR_ARG, "slot_ids, cu_seqlens and o must be non-NULL");
+  if (!dtype_ok(o_dtype)) return fail(GDN_ERR_DTYPE, "o dtype must be F32 or BF16");
+  gdn::QKV q;
+  if ((st = resolve_qkv(p, in, total_tokens, q))) return st;
+  gdn::SeqIndex seq{slot_ids, cu_seqlens, n_seqs, total_tokens};
+  // no workspace limit here: the check below is against the fixed array
+  const size_t wb = gdn::prefill_workspace_bytes(p->view, seq, q, (size_t)-1);
+  if (wb > kNoAllocScratchBytes)
+    return fail(GDN_ERR_SIZE,
+                "prefill needs %zu bytes of scratch, more than the %zu-byte array of "
+                "gdn_prefill_chunked_noalloc (%d value heads, %d tokens, %d sequences); split "
+                "the call into fewer tokens",
+                wb, kNoAllocScratchBytes, p->desc.h_v, total_tokens, n_seqs);
+  void *work = nullptr;
+  if (wb > 0) {
+    const cudaError_t e = noalloc_scratch(p->device, &work);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(prefill scratch)");
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    std::vector<int32_t> cu;
+    if ((st = check_slots(p, slot_ids, n_seqs, s)) ||
+        (st = check_cu(cu_seqlens, n_seqs, total_tokens, s, cu)) ||
+        (st = check_device_ptr(o, "o")))
+      return st;
+  }
+  const cudaError_t e = gdn::launch_prefill(p->view, layer, seq, q, o, o_dtype, scale, work, s);
+  if (e == cudaErrorNotSupported)
+    return fail(GDN_ERR_UNSUPPORTED, "prefill is not available for this shape");
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return ok();
 }
 
 }  // extern "C"

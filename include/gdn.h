@@ -241,6 +241,28 @@ gdn_status gdn_spec_verify_deferred(gdn_pool *pool, int32_t layer, const int32_t
                                     gdn_dtype o_dtype, int32_t T_prev, const gdn_qkv *prev,
                                     const int32_t *prev_accept, float scale, gdn_stream stream);
 
+/* gdn_prefill_chunked for callers that must not allocate device memory:
+ * code running under an allocator that owns the whole GPU (a serving engine
+ * that reserves its memory up front), or with a fixed memory budget where an
+ * allocation in the middle of a step is not allowed to fail or wait.  The
+ * source pages have no counterpart to this entry point.
+ * Arguments, results and errors are those of gdn_prefill_chunked.  Where that
+ * function would take its workspace from the pool's memory pool (dk = dv =
+ * 128), this one uses a 64 MiB array compiled into the library, which every
+ * GPU that loads the library holds until the process exits; it calls no
+ * allocator.  A call needing more than 64 MiB -- about 32 KiB per 64-token
+ * chunk per value head, counting (tokens / 64 + sequences) chunks -- returns
+ * GDN_ERR_SIZE and launches nothing.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  Every call shares the one array: calls whose work
+ * overlaps on the GPU (other streams, other threads, other pools of the same
+ * device) race on it and must be serialised by the caller. */
+gdn_status gdn_prefill_chunked_noalloc(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
+                                       const int32_t *cu_seqlens, int32_t n_seqs,
+                                       int32_t total_tokens, int32_t max_seqlen,
+                                       const gdn_qkv *in, void *o, gdn_dtype o_dtype, float scale,
+                                       gdn_stream stream);
+
 /* Human-readable name of a status, and the detail of the last failure on
  * this host thread (empty string if none). */
 const char *gdn_status_string(gdn_status s);
