@@ -23,6 +23,8 @@
 // (chunk, value head) 32 KiB: the P tile, then the T tile, each 64 x 64 float32
 // in the K-major core-matrix layout of gdn_tc.cuh.  Chunks are numbered
 // sequence by sequence; offsets[i] is the first chunk of sequence i.
+#include <type_traits>
+
 #include "gdn_tc.cuh"
 
 namespace gdn {
@@ -76,35 +78,46 @@ __global__ void __launch_bounds__(1024)
   if (tid == 1023) off[n] = (int32_t)min(part[1023], cap + 1);
 }
 
+// This thread's token in the staging map below (warp w: tokens 8w .. 8w+7).
+__device__ __forceinline__ int stage_token() { return 8 * (threadIdx.x >> 5) + (threadIdx.x & 7); }
+
+// g and beta of this thread's token of the chunk starting at tok0 (0 if padded).
+template <typename TI>
+__device__ __forceinline__ void load_gb(const QKV &in, const PoolView &p, int h, int64_t tok0,
+                                        int n, float &gt, float &bt) {
+  const int t = stage_token();
+  gt = bt = 0.f;
+  if (t < n) {
+    gt = Elem<TI>::load1(static_cast<const TI *>(in.g) + (tok0 + t) * p.h_v + h);
+    bt = Elem<TI>::load1(static_cast<const TI *>(in.beta) + (tok0 + t) * p.h_v + h);
+  }
+}
+
 // Stage normalised q and k of one chunk as the [Q;K] core tile (rows 0..63 Q,
-// 64..127 K; padded tokens zero) and g, beta into shared memory.  Warp w takes
-// tokens 8w .. 8w+7; lane = token (3 bits) + 8 * chunk group, so a quarter-warp
-// writes the 8 rows of one core matrix (contiguous 128 bytes).
+// 64..127 K; padded tokens zero), beta v (plain rows) and g, beta.  Row t of
+// q, k, v starts at q0 + t ldq (k0 + t ldq, v0 + t ldv): global memory, or the
+// raw copy of the chunk in shared memory.  Warp w takes tokens 8w .. 8w+7;
+// lane = token (3 bits) + 8 * chunk group, so a quarter-warp writes the 8 rows
+// of one core matrix (contiguous 128 bytes).
 template <typename TI, bool WITH_V>
-__device__ __forceinline__ void stage_chunk(const QKV &in, const PoolView &p, int h, int hk,
-                                            int64_t tok0, int n, float *QK, float *XU,
-                                            float *sG, float *sBeta) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int tl = lane & 7, cg = lane >> 3;
-  const int t = 8 * warp + tl;
-  const int64_t tok = tok0 + t;
+__device__ __forceinline__ void stage_rows(const TI *q0, const TI *k0, const TI *v0, int64_t ldq,
+                                           int64_t ldv, int n, float gt, float bt, float *QK,
+                                           float *XU, float *sG, float *sBeta) {
+  const int lane = threadIdx.x & 31;
+  const int cg = lane >> 3;
+  const int t = stage_token();
   const bool real = t < n;
-  const TI *qg = static_cast<const TI *>(in.q);
-  const TI *kg = static_cast<const TI *>(in.k);
-  const TI *vg = static_cast<const TI *>(in.v);
   float4 q4[D / 16], k4[D / 16], v4[D / 16];
 #pragma unroll
   for (int j = 0; j < D / 16; ++j) {
     const int c = cg + 4 * j;
     q4[j] = k4[j] = v4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (real) {
-      q4[j] = Elem<TI>::load4(qg + tok * in.ld_qk + (int64_t)hk * D + 4 * c);
-      k4[j] = Elem<TI>::load4(kg + tok * in.ld_qk + (int64_t)hk * D + 4 * c);
-      if (WITH_V) v4[j] = Elem<TI>::load4(vg + tok * in.ld_v + (int64_t)h * D + 4 * c);
+      q4[j] = Elem<TI>::load4(q0 + t * ldq + 4 * c);
+      k4[j] = Elem<TI>::load4(k0 + t * ldq + 4 * c);
+      if (WITH_V) v4[j] = Elem<TI>::load4(v0 + t * ldv + 4 * c);
     }
   }
-  const float gt = real ? Elem<TI>::load1(static_cast<const TI *>(in.g) + tok * p.h_v + h) : 0.f;
-  const float bt = real ? Elem<TI>::load1(static_cast<const TI *>(in.beta) + tok * p.h_v + h) : 0.f;
   float qq = 0.f, kk = 0.f;
 #pragma unroll
   for (int j = 0; j < D / 16; ++j) {
@@ -129,31 +142,196 @@ __device__ __forceinline__ void stage_chunk(const QKV &in, const PoolView &p, in
   }
 }
 
-// ----------------------------------------------------------------- key side
-// shared-memory map of prep_kernel (bytes)
-constexpr int P_QK = 0;                        // [Q;K] core tile 128 x 128
-constexpr int P_AP = P_QK + 128 * D * 4;       // A (plain 64 x AS)
-constexpr int P_TP = P_AP + C * AS * 4;        // T (plain 64 x AS)
-constexpr int P_MS = P_TP + C * AS * 4;        // block-inverse scratch 3 x 16 x 16
-constexpr int P_SC = P_MS + 3 * 256 * 4;       // G, beta
-constexpr int PREP_SMEM = P_SC + 2 * C * 4;
-static_assert(2 * (PREP_SMEM + 1024) <= 228 * 1024, "two prep CTAs per SM");
+// The same from global memory, for the chunk starting at token tok0.
+template <typename TI, bool WITH_V>
+__device__ __forceinline__ void stage_chunk(const QKV &in, const PoolView &p, int h, int hk,
+                                            int64_t tok0, int n, float *QK, float *XU,
+                                            float *sG, float *sBeta) {
+  float gt, bt;
+  load_gb<TI>(in, p, h, tok0, n, gt, bt);
+  stage_rows<TI, WITH_V>(static_cast<const TI *>(in.q) + tok0 * in.ld_qk + (int64_t)hk * D,
+                         static_cast<const TI *>(in.k) + tok0 * in.ld_qk + (int64_t)hk * D,
+                         static_cast<const TI *>(in.v) + tok0 * in.ld_v + (int64_t)h * D,
+                         in.ld_qk, in.ld_v, n, gt, bt, QK, XU, sG, sBeta);
+}
 
+// Raw bf16 copy of one chunk's q, k and v rows in shared memory, filled by
+// bulk copies (one 256-byte row each) while the previous chunk computes:
+// [3][64 tokens][kRawLd] bf16, rows padded to 272 bytes so the staging reads
+// spread over the banks.  Used when the rows are 16-byte aligned.
+constexpr int kRawLd = D + 8;
+constexpr int kRawBytes = 3 * C * kRawLd * 2;
+
+__device__ __forceinline__ void prefetch_raw(const QKV &in, int h, int hk, int64_t tok0, int n,
+                                             bf16 *raw, uint64_t *rbar) {
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(rbar, (uint32_t)n * 3 * D * 2);
+  const int e = threadIdx.x;  // 3 tensors x 64 tokens, one row per thread
+  if (e < 3 * C) {
+    const int which = e / C, t = e % C;
+    if (t < n) {
+      const int64_t tok = tok0 + t;
+      const bf16 *src =
+          which == 0 ? static_cast<const bf16 *>(in.q) + tok * in.ld_qk + (int64_t)hk * D
+          : which == 1 ? static_cast<const bf16 *>(in.k) + tok * in.ld_qk + (int64_t)hk * D
+                       : static_cast<const bf16 *>(in.v) + tok * in.ld_v + (int64_t)h * D;
+      bulk_g2s(raw + (which * C + t) * kRawLd, src, D * 2, rbar);
+    }
+  }
+}
+
+// ----------------------------------------------------------------- key side
+// Raw bf16 q and k rows of one chunk as the [Q;K] 16-bit core tile (rows 0..63
+// Q, 64..127 K; padded tokens zero), with rq[t], rk[t] = 1 / |q_t|, 1 / |k_t|
+// (epsilon as everywhere).  The tile feeds a kind::f16 MMA on the exact input
+// values; the norms are applied to its products.  Warp w takes tokens
+// 8w .. 8w+7; lane = token (3 bits) + 8 * part, part p holding the 4-element
+// pieces p, p+4, ..., so one store instruction fills two whole core matrices.
+__device__ __forceinline__ void stage_qk_bf16(const bf16 *q0, const bf16 *k0, int64_t ld, int n,
+                                              unsigned char *tile, float *rq, float *rk) {
+  const int lane = threadIdx.x & 31;
+  const int part = lane >> 3;
+  const int t = stage_token();
+  const bool real = t < n;
+  uint2 qv[8], kv[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int c = part + 4 * m;
+    qv[m] = kv[m] = make_uint2(0u, 0u);
+    if (real) {
+      qv[m] = *reinterpret_cast<const uint2 *>(q0 + t * ld + 4 * c);
+      kv[m] = *reinterpret_cast<const uint2 *>(k0 + t * ld + 4 * c);
+    }
+  }
+  float qq = 0.f, kk = 0.f;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const float a0 = __uint_as_float(qv[m].x << 16), a1 = __uint_as_float(qv[m].x & 0xffff0000u);
+    const float a2 = __uint_as_float(qv[m].y << 16), a3 = __uint_as_float(qv[m].y & 0xffff0000u);
+    const float b0 = __uint_as_float(kv[m].x << 16), b1 = __uint_as_float(kv[m].x & 0xffff0000u);
+    const float b2 = __uint_as_float(kv[m].y << 16), b3 = __uint_as_float(kv[m].y & 0xffff0000u);
+    qq += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+    kk += b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
+  }
+  qq += __shfl_xor_sync(0xffffffffu, qq, 8);
+  qq += __shfl_xor_sync(0xffffffffu, qq, 16);
+  kk += __shfl_xor_sync(0xffffffffu, kk, 8);
+  kk += __shfl_xor_sync(0xffffffffu, kk, 16);
+  constexpr uint32_t SBO = tc::sbo_bytes16(D);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int c = part + 4 * m;  // elements 4c .. 4c+3
+    const uint32_t off = (uint32_t)(c >> 1) * tc::kLBO + (uint32_t)(t & 7) * 16 + (c & 1) * 8;
+    *reinterpret_cast<uint2 *>(tile + (t >> 3) * SBO + off) = qv[m];
+    *reinterpret_cast<uint2 *>(tile + (8 + (t >> 3)) * SBO + off) = kv[m];
+  }
+  if (part == 0) {
+    rq[t] = rsqrtf(qq + kL2Eps);
+    rk[t] = rsqrtf(kk + kL2Eps);
+  }
+}
+
+__device__ __forceinline__ void group_sync(int id) {  // one 128-thread warpgroup
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+
+// T = (I + A)^{-1} for a strictly lower 64 x 64 A (plain rows, stride AS), by
+// one warpgroup (thread tt of 128, named barrier `bar`).  T's strictly-upper
+// 16 x 16 blocks must be zero on entry; X is 1024 floats of scratch.  With
+// T_b the inverse of diagonal block b and lower-triangular blocks throughout,
+//   T_{b+1,b} = -T_{b+1,b+1} A_{b+1,b} T_{b,b}            (16 x 16, b = 0, 2)
+//   T_L       = -T_hi A_L T_lo                             (32 x 32 lower left)
+// where T_lo, T_hi are the finished upper-left and lower-right 32 x 32 halves.
+__device__ __forceinline__ void invert_unit_lower(const float *A, float *T, float *X, int tt,
+                                                  int bar) {
+  if (tt < C) {  // diagonal blocks: column j of (I + A_bb)^{-1} by forward substitution
+    const int bb = tt >> 4, j = tt & 15;
+    const float *Ab = A + (16 * bb) * AS + 16 * bb;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = r == j ? 1.f : 0.f;
+#pragma unroll
+      for (int c = 0; c < r; ++c) acc -= Ab[r * AS + c] * x[c];
+      x[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) T[(16 * bb + r) * AS + 16 * bb + j] = x[r];
+  }
+  group_sync(bar);
+  const int which = tt >> 6, r = (tt >> 2) & 15, q0 = 4 * (tt & 3);
+  const int b = 2 * which;
+  {  // X_b = A_{b+1,b} T_{b,b}   (T_{b,b}[k][c] = 0 for k < c)
+    const float *ar = A + (16 * (b + 1) + r) * AS + 16 * b;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = q0; k < 16; ++k)
+      x = axpby4(1.f, x, ar[k], *reinterpret_cast<const float4 *>(T + (16 * b + k) * AS + 16 * b + q0));
+    *reinterpret_cast<float4 *>(X + which * 256 + r * 16 + q0) = x;
+  }
+  group_sync(bar);
+  {  // T_{b+1,b} = -T_{b+1,b+1} X_b
+    const float *tr = T + (16 * (b + 1) + r) * AS + 16 * (b + 1);
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k <= r; ++k)
+      y = axpby4(1.f, y, tr[k], *reinterpret_cast<const float4 *>(X + which * 256 + k * 16 + q0));
+    *reinterpret_cast<float4 *>(T + (16 * (b + 1) + r) * AS + 16 * b + q0) = scale4(-1.f, y);
+  }
+  group_sync(bar);
+  const int r0 = 2 * (tt >> 3), c0 = 4 * (tt & 7);
+  {  // Y = A_L T_lo  (rows 32 + r0, 33 + r0; T_lo[k][c] = 0 for k < c)
+    const float *a0 = A + (32 + r0) * AS, *a1 = a0 + AS;
+    float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+    for (int k = c0; k < 32; ++k) {
+      const float4 tv = *reinterpret_cast<const float4 *>(T + k * AS + c0);
+      y0 = axpby4(1.f, y0, a0[k], tv);
+      y1 = axpby4(1.f, y1, a1[k], tv);
+    }
+    *reinterpret_cast<float4 *>(X + r0 * 32 + c0) = y0;
+    *reinterpret_cast<float4 *>(X + (r0 + 1) * 32 + c0) = y1;
+  }
+  group_sync(bar);
+  {  // T_L = -T_hi Y   (T_hi[r0][r0 + 1] = 0)
+    const float *t0 = T + (32 + r0) * AS + 32, *t1 = t0 + AS;
+    float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+    for (int k = 0; k <= r0 + 1; ++k) {
+      const float4 xv = *reinterpret_cast<const float4 *>(X + k * 32 + c0);
+      y0 = axpby4(1.f, y0, t0[k], xv);
+      y1 = axpby4(1.f, y1, t1[k], xv);
+    }
+    *reinterpret_cast<float4 *>(T + (32 + r0) * AS + c0) = scale4(-1.f, y0);
+    *reinterpret_cast<float4 *>(T + (33 + r0) * AS + c0) = scale4(-1.f, y1);
+  }
+  group_sync(bar);
+}
+
+// shared-memory map of prep_kernel: the [Q;K] tile, then per value head of
+// the CTA's pair: A and T (plain 64 x AS), 1024 floats of inverse scratch,
+// G and beta; then rq, rk.
+constexpr int kHeadFloats = 2 * C * AS + 1024 + 2 * C;
+template <typename TI>
+constexpr int prep_tile_bytes() { return std::is_same<TI, bf16>::value ? 128 * D * 2 : 128 * D * 4; }
+template <typename TI>
+constexpr int prep_smem() { return prep_tile_bytes<TI>() + (2 * kHeadFloats + 2 * C) * 4; }
+static_assert(2 * (prep_smem<bf16>() + 1024 + 64) <= 228 * 1024, "two bf16 prep CTAs per SM");
+static_assert(prep_smem<float>() <= 227 * 1024, "shared memory");
+
+// One CTA per (chunk, key head, pair of the value heads that read that key
+// head).  Both warpgroups share the staged [Q;K] tile and the Gram product
+// D1 = [Q;K] K^T; warpgroup wg then forms P and A for value head 2 pair + wg
+// of the group and inverts I + A.
 template <typename TI>
 __global__ void __launch_bounds__(NT, 2)
     prep_kernel(PoolView p, SeqIndex seq, QKV in, const int32_t *__restrict__ off,
                 float *__restrict__ work) {
+  constexpr bool B16 = std::is_same<TI, bf16>::value;  // raw bf16 tile, kind::f16
   extern __shared__ __align__(1024) unsigned char smem[];
-  float *QK = reinterpret_cast<float *>(smem + P_QK);
-  float *AP = reinterpret_cast<float *>(smem + P_AP);
-  float *TP = reinterpret_cast<float *>(smem + P_TP);
-  float *MS = reinterpret_cast<float *>(smem + P_MS);
-  float *sG = reinterpret_cast<float *>(smem + P_SC);
-  float *sBeta = sG + C;
+  unsigned char *tile = smem;
+  float *heads = reinterpret_cast<float *>(smem + prep_tile_bytes<TI>());
+  float *rq = heads + 2 * kHeadFloats;
+  float *rk = rq + C;
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tmem_slot;
 
-  const int cidx = blockIdx.x, h = blockIdx.y;
+  const int cidx = blockIdx.x;
   if (cidx >= off[seq.n_seqs]) return;
   int si = 0;  // the sequence holding chunk cidx: the last i with off[i] <= cidx
   for (int b = seq.n_seqs - 1; si < b;) {
@@ -164,23 +342,48 @@ __global__ void __launch_bounds__(NT, 2)
   const int c0 = (cidx - off[si]) * C;
   const int64_t rest = hi - lo - c0;
   const int n = rest < C ? (int)rest : C;
-  const int hk = h / (p.h_v / p.h_k);
+  const int64_t tok0 = lo + c0;
+  const int G = p.h_v / p.h_k, npair = (G + 1) / 2;
+  const int kh = blockIdx.y / npair, pair = blockIdx.y % npair;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int quad = warp & 3, half = warp >> 2;
-  const int row = 32 * quad + lane;
+  const int wg = warp >> 2, quad = warp & 3, tt = tid & 127;
+  const bool live = 2 * pair + wg < G;  // this warpgroup has a value head
+  const int h = kh * G + (live ? 2 * pair + wg : 0);
+  float *AP = heads + wg * kHeadFloats;
+  float *TP = AP + C * AS;
+  float *XS_ = TP + C * AS;
+  float *sG = XS_ + 1024;
+  float *sBeta = sG + C;
 
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 64);
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_fence_init();
   }
-  for (int e = tid; e < C * C; e += NT) {  // T's strictly-upper 16 x 16 blocks stay zero
+  for (int e = tt; e < C * C; e += 128) {  // T's strictly-upper 16 x 16 blocks stay zero
     const int r = e / C, c = e % C;
     if ((c >> 4) > (r >> 4)) TP[r * AS + c] = 0.f;
   }
-  stage_chunk<TI, false>(in, p, h, hk, lo + c0, n, QK, nullptr, sG, sBeta);
+  if (tt < C) {  // this head's g and beta (padded tokens 0)
+    float gt = 0.f, bt = 0.f;
+    if (live && tt < n) {
+      gt = Elem<TI>::load1(static_cast<const TI *>(in.g) + (tok0 + tt) * p.h_v + h);
+      bt = Elem<TI>::load1(static_cast<const TI *>(in.beta) + (tok0 + tt) * p.h_v + h);
+    }
+    sG[tt] = gt;
+    sBeta[tt] = bt;
+  }
+  const TI *q0 = static_cast<const TI *>(in.q) + tok0 * in.ld_qk + (int64_t)kh * D;
+  const TI *k0 = static_cast<const TI *>(in.k) + tok0 * in.ld_qk + (int64_t)kh * D;
+  if constexpr (B16) {
+    stage_qk_bf16(q0, k0, in.ld_qk, n, tile, rq, rk);
+  } else {
+    // normalised float32 rows; rq = rk = 1 (written through the g / beta slots)
+    stage_rows<TI, false>(q0, k0, nullptr, in.ld_qk, 0, n, 1.f, 1.f,
+                          reinterpret_cast<float *>(tile), nullptr, rq, rk);
+  }
   __syncthreads();
-  if (warp == 0) {  // cumulative log-decay over the chunk (padded tokens carry g = 0)
+  if (quad == 0 && tt < 32) {  // warp 4 wg: cumulative log-decay of this head
     const float a = sG[2 * lane], b = sG[2 * lane + 1];
     float incl = a + b;
 #pragma unroll
@@ -200,58 +403,70 @@ __global__ void __launch_bounds__(NT, 2)
 
   // D1 = [Q;K] K^T  (M 128, N 64, K 128)
   if (tid == 0) {
-    const uint32_t qk_s = smem_addr(QK), k_s = qk_s + 64 * D * 4;
-    constexpr uint32_t SBO_D = tc::sbo_bytes(D), KSTEP = 2 * tc::kLBO;
+    const uint32_t a_s = smem_addr(tile);
+    constexpr uint32_t KSTEP = 2 * tc::kLBO;
+    if constexpr (B16) {
+      constexpr uint32_t SBO = tc::sbo_bytes16(D);
+      const uint32_t b_s = a_s + 8 * SBO;
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j)
-      tc::mma_ss(tm, tc::smem_desc(qk_s + j * KSTEP, tc::kLBO, SBO_D),
-                 tc::smem_desc(k_s + j * KSTEP, tc::kLBO, SBO_D), tc::idesc_tf32(128, 64), j > 0);
+      for (int j = 0; j < D / 16; ++j)
+        tc::mma_ss_f16(tm, tc::smem_desc(a_s + j * KSTEP, tc::kLBO, SBO),
+                       tc::smem_desc(b_s + j * KSTEP, tc::kLBO, SBO), tc::idesc_bf16(128, 64),
+                       j > 0);
+    } else {
+      constexpr uint32_t SBO = tc::sbo_bytes(D);
+      const uint32_t b_s = a_s + 8 * SBO;
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j)
+        tc::mma_ss(tm, tc::smem_desc(a_s + j * KSTEP, tc::kLBO, SBO),
+                   tc::smem_desc(b_s + j * KSTEP, tc::kLBO, SBO), tc::idesc_tf32(128, 64), j > 0);
+    }
     tc::mma_commit(&bar);
   }
   const bool alive = __syncthreads_and(mbar_wait_bounded(&bar, 0));
   tc::fence_after_sync();
   float *Pg = work + ((int64_t)cidx * p.h_v + h) * (2 * TILE);
   float *Tg = Pg + TILE;
-  if (alive) {
-    const int i0 = 32 * half;
-    if (quad >= 2) {  // rows 64..127: A[t][i] = beta_t e^{G_t - G_i} k_t.k_i, i < t
+  if (alive && live) {
+    const int row = 32 * quad + lane;
+    if (quad >= 2) {  // rows 64..127: A[t][i] = beta_t e^{G_t - G_i} k~_t.k~_i, i < t
       const int t = row - 64;
-      const float bt = sBeta[t], gt = sG[t];
+      const float bt = sBeta[t] * rk[t], gt = sG[t];
 #pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
+      for (int cb = 0; cb < 4; ++cb) {
         float v[16];
-        tc::tmem_ld16(lrow + i0 + 16 * cb, v);
+        tc::tmem_ld16(lrow + 16 * cb, v);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
-          const int i = i0 + 16 * cb + j;
+          const int i = 16 * cb + j;
           float4 a;
-          a.x = i + 0 < t ? bt * __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
-          a.y = i + 1 < t ? bt * __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
-          a.z = i + 2 < t ? bt * __expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
-          a.w = i + 3 < t ? bt * __expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
+          a.x = i + 0 < t ? bt * rk[i + 0] * __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
+          a.y = i + 1 < t ? bt * rk[i + 1] * __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
+          a.z = i + 2 < t ? bt * rk[i + 2] * __expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
+          a.w = i + 3 < t ? bt * rk[i + 3] * __expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
           *reinterpret_cast<float4 *>(AP + t * AS + i) = a;
         }
       }
-    } else {  // rows 0..63: P[t][i] = e^{G_t - G_i} q_t.k_i, i <= t, straight to the workspace
+    } else {  // rows 0..63: P[t][i] = e^{G_t - G_i} q~_t.k~_i, i <= t, to the workspace
       const int t = row;
-      const float gt = sG[t];
+      const float qt = rq[t], gt = sG[t];
 #pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
+      for (int cb = 0; cb < 4; ++cb) {
         float v[16];
-        tc::tmem_ld16(lrow + i0 + 16 * cb, v);
+        tc::tmem_ld16(lrow + 16 * cb, v);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
-          const int i = i0 + 16 * cb + j;
+          const int i = 16 * cb + j;
           float4 pv;
-          pv.x = i + 0 <= t ? __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
-          pv.y = i + 1 <= t ? __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
-          pv.z = i + 2 <= t ? __expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
-          pv.w = i + 3 <= t ? __expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
+          pv.x = i + 0 <= t ? qt * rk[i + 0] * __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
+          pv.y = i + 1 <= t ? qt * rk[i + 1] * __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
+          pv.z = i + 2 <= t ? qt * rk[i + 2] * __expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
+          pv.w = i + 3 <= t ? qt * rk[i + 3] * __expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
           *reinterpret_cast<float4 *>(Pg + tc::core_off(t, i, C)) = pv;
         }
       }
     }
-  } else {
+  } else if (!alive) {
     if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
     mbar_wait_bounded(&bar, 0);  // a second bounded chance before TMEM is released
   }
@@ -259,55 +474,10 @@ __global__ void __launch_bounds__(NT, 2)
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tm, 64);
-  if (!alive) return;
+  if (!alive || !live) return;
 
-  // T = (I + A)^{-1} by 16 x 16 blocks: diagonal blocks by forward substitution
-  // (one column per thread), then block row d below the diagonal from the rows above.
-  if (tid < C) {
-    const int bb = tid >> 4, j = tid & 15;
-    const float *Ab = AP + (16 * bb) * AS + 16 * bb;
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float acc = r == j ? 1.f : 0.f;
-#pragma unroll
-      for (int c = 0; c < r; ++c) acc -= Ab[r * AS + c] * x[c];
-      x[r] = acc;
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) TP[(16 * bb + r) * AS + 16 * bb + j] = x[r];
-  }
-  __syncthreads();
-#pragma unroll 1
-  for (int d = 1; d < 4; ++d) {
-    // M_ij = sum_{k=j}^{i-1} A_ik T_kj for the blocks (i, j) = (b + d, b)
-    for (int e = tid; e < (4 - d) * 256; e += NT) {
-      const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      const int bi = b + d;
-      float acc = 0.f;
-      for (int kb = b; kb < bi; ++kb) {
-        const float *ar = AP + (16 * bi + r) * AS + 16 * kb;
-        const float *tcol = TP + (16 * kb) * AS + 16 * b + c;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) acc += ar[m] * tcol[m * AS];
-      }
-      MS[e] = acc;
-    }
-    __syncthreads();
-    // T_ij = -T_ii M_ij
-    for (int e = tid; e < (4 - d) * 256; e += NT) {
-      const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      const int bi = b + d;
-      const float *tr = TP + (16 * bi + r) * AS + 16 * bi;
-      const float *mc = MS + (b << 8) + c;
-      float acc = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; ++m) acc += tr[m] * mc[m * 16];
-      TP[(16 * bi + r) * AS + 16 * b + c] = -acc;
-    }
-    __syncthreads();
-  }
-  for (int e = tid; e < C * (C / 4); e += NT) {  // T tile [t][i] -> workspace
+  invert_unit_lower(AP, TP, XS_, tt, 1 + wg);
+  for (int e = tt; e < C * (C / 4); e += 128) {  // T tile [t][i] -> workspace
     const int t = e % C, c4 = e / C;
     *reinterpret_cast<float4 *>(Tg + tc::core_off(t, 4 * c4, C)) =
         *reinterpret_cast<const float4 *>(TP + t * AS + 4 * c4);
@@ -322,21 +492,28 @@ constexpr int S_PT = S_XU + C * XS * 4;        // P tile (from the workspace)
 constexpr int S_TT = S_PT + TILE * 4;          // T tile (same bulk copy)
 constexpr int S_KT = S_TT + TILE * 4;          // Ktil^T tile [k][i], 128 x 64
 constexpr int S_SC = S_KT + D * C * 4;         // G, gamma, beta, e^{G_n - G}
-constexpr int SEQ_SMEM = S_SC + 4 * C * 4;
-static_assert(S_PT % 16 == 0 && S_KT % 16 == 0, "tile alignment");
-static_assert(SEQ_SMEM <= 227 * 1024, "shared memory");
+constexpr int S_RAW = S_SC + 4 * C * 4;        // raw bf16 q, k, v of the next chunk
+template <typename TI>
+constexpr int seq_smem() { return S_RAW + (std::is_same<TI, bf16>::value ? kRawBytes : 0); }
+static_assert(S_PT % 16 == 0 && S_KT % 16 == 0 && S_RAW % 16 == 0, "tile alignment");
+static_assert(S_RAW + kRawBytes <= 227 * 1024, "shared memory");
 
 // TMEM columns
-constexpr uint32_t T_S = 0, T_E = 128, T_D3 = 192, T_F = 256, T_DD = 320, T_D4 = 384;
+// [S Q^T | S K^T] is one N = 128 product over the [Q;K] tile: D3 then E
+constexpr uint32_t T_S = 0, T_D3 = 128, T_E = 192, T_F = 256, T_DD = 320, T_D4 = 384;
 constexpr uint32_t SEQ_TMEM = 512;
 
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(NT, 1)
     seq_kernel(PoolView p, int layer, SeqIndex seq, QKV in, TO *__restrict__ o, float scale,
-               const int32_t *__restrict__ off, int64_t cap, const float *__restrict__ work) {
+               const int32_t *__restrict__ off, int64_t cap, const float *__restrict__ work,
+               int raw_rows) {
+  // bf16 rows that are 16-byte aligned: stage from a bulk copy made a chunk ahead
+  const bool RAW = std::is_same<TI, bf16>::value && raw_rows != 0;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *QK = reinterpret_cast<float *>(smem + S_QK);
   float *XU = reinterpret_cast<float *>(smem + S_XU);
+  bf16 *RW = reinterpret_cast<bf16 *>(smem + S_RAW);
   float *PT = reinterpret_cast<float *>(smem + S_PT);
   float *KT = reinterpret_cast<float *>(smem + S_KT);
   float *sG = reinterpret_cast<float *>(smem + S_SC);
@@ -345,6 +522,7 @@ __global__ void __launch_bounds__(NT, 1)
   float *sDte = sBeta + C;
   __shared__ __align__(8) uint64_t bar;    // MMA completion
   __shared__ __align__(8) uint64_t tbar;   // P / T tiles landed
+  __shared__ __align__(8) uint64_t rbar;   // raw q, k, v rows landed
   __shared__ uint32_t tmem_slot;
 
   const int h = blockIdx.x, si = blockIdx.y;
@@ -378,6 +556,7 @@ __global__ void __launch_bounds__(NT, 1)
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_init(&tbar, 1);
+    mbar_init(&rbar, 1);
     mbar_fence_init();
   }
   tc::fence_before_sync();
@@ -408,27 +587,44 @@ __global__ void __launch_bounds__(NT, 1)
   const TI *kg = static_cast<const TI *>(in.k);
   const TI *vg = static_cast<const TI *>(in.v);
   const uint32_t qk_s = smem_addr(QK);
-  const uint32_t k_s = qk_s + 64 * D * 4;
   const uint32_t pt_s = smem_addr(PT);
   const uint32_t tt_s = pt_s + kTileBytes;
   const uint32_t kt_s = smem_addr(KT);
   constexpr uint32_t SBO_D = tc::sbo_bytes(D);
   constexpr uint32_t SBO_C = tc::sbo_bytes(C);
   constexpr uint32_t KSTEP = 2 * tc::kLBO;
-  uint32_t phase = 0, tphase = 0;
+  uint32_t phase = 0, tphase = 0, rphase = 0;
   bool alive = true;
+  float g_next = 0.f, b_next = 0.f;  // this thread's g, beta of the next chunk to stage (RAW)
 
-  for (int c0 = 0; c0 < len && alive; c0 += C) {
-    const int n = min(C, len - c0);
-    stage_chunk<TI, true>(in, p, h, hk, lo + c0, n, QK, XU, sG, sBeta);
+  // Stage chunk c0s into QK, XU and the scalars (then start fetching the one
+  // after it), and form its cumulative decays.  Ends with the tile writes
+  // fenced for the tensor core; the caller's next barrier publishes them.
+  auto stage_next = [&](int c0s) {
+    const int ns = min(C, len - c0s);
+    if (RAW) {
+      alive = __syncthreads_and(alive && mbar_wait_bounded(&rbar, rphase));
+      rphase ^= 1;
+      stage_rows<TI, true>(reinterpret_cast<const TI *>(RW),
+                           reinterpret_cast<const TI *>(RW + C * kRawLd),
+                           reinterpret_cast<const TI *>(RW + 2 * C * kRawLd), kRawLd, kRawLd, ns,
+                           g_next, b_next, QK, XU, sG, sBeta);
+    } else {
+      stage_chunk<TI, true>(in, p, h, hk, lo + c0s, ns, QK, XU, sG, sBeta);
+    }
     __syncthreads();
+    if (RAW && c0s + C < len) {  // the raw copy is consumed: fetch the next chunk's
+      const int nn = min(C, len - c0s - C);
+      prefetch_raw(in, h, hk, lo + c0s + C, nn, RW, &rbar);
+      load_gb<TI>(in, p, h, lo + c0s + C, nn, g_next, b_next);
+    }
     if (warp == 0) {  // cumulative log-decay (padded tokens carry g = 0)
       const float a = sG[2 * lane], b = sG[2 * lane + 1];
       float incl = a + b;
 #pragma unroll
-      for (int s = 1; s < 32; s <<= 1) {
-        const float up = __shfl_up_sync(0xffffffffu, incl, s);
-        if (lane >= s) incl += up;
+      for (int sh = 1; sh < 32; sh <<= 1) {
+        const float up = __shfl_up_sync(0xffffffffu, incl, sh);
+        if (lane >= sh) incl += up;
       }
       const float g0 = incl - b;
       const float gl = __shfl_sync(0xffffffffu, incl, 31);
@@ -440,51 +636,84 @@ __global__ void __launch_bounds__(NT, 1)
       sDte[2 * lane + 1] = expf(gl - incl);
     }
     tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    // E = S K^T, D3 = S Q^T (A = S from TMEM; M 128, N 64, K 128)
+  };
+  // [D3 | E] = S [Q;K]^T (A = S from TMEM; M 128, N 128, K 128), one commit
+  auto issue_ed3 = [&]() {
     if (tid == 0) {
-      constexpr uint32_t id = tc::idesc_tf32(128, 64);
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j)
-        tc::mma_ts(tm + T_E, tm + T_S + j * 8, tc::smem_desc(k_s + j * KSTEP, tc::kLBO, SBO_D),
-                   id, j > 0);
+      constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll
       for (int j = 0; j < D / 8; ++j)
         tc::mma_ts(tm + T_D3, tm + T_S + j * 8,
                    tc::smem_desc(qk_s + j * KSTEP, tc::kLBO, SBO_D), id, j > 0);
       tc::mma_commit(&bar);
     }
-    // meanwhile: the Ktil^T tile, and the next chunk's rows pulled towards L2
-    {
-      const int kc = tid & 127;
-      const int ib = (tid >> 7) * (C / 8);
+  };
+  // The Ktil^T tile of the staged chunk (needs its sDte), and rows `ahead`
+  // chunks further on pulled towards L2.
+  // Each thread reads 4 consecutive k of one token (a 16-byte piece of the K
+  // core tile), the 4 lanes of a quad transpose their 4 x 4 block with two
+  // xor-shuffle rounds, and each stores 4 consecutive tokens of one k.
+  auto build_kt = [&](int c0s) {
+    const int l4 = lane & 3;
 #pragma unroll 2
-      for (int q = 0; q < C / 8; ++q) {
-        const int i4 = ib + ((q + (kc >> 2)) & (C / 8 - 1));
-        float4 x;
-        x.x = sDte[4 * i4 + 0] * QK[tc::core_off(64 + 4 * i4 + 0, kc, D)];
-        x.y = sDte[4 * i4 + 1] * QK[tc::core_off(64 + 4 * i4 + 1, kc, D)];
-        x.z = sDte[4 * i4 + 2] * QK[tc::core_off(64 + 4 * i4 + 2, kc, D)];
-        x.w = sDte[4 * i4 + 3] * QK[tc::core_off(64 + 4 * i4 + 3, kc, D)];
-        *reinterpret_cast<float4 *>(KT + tc::core_off(kc, 4 * i4, C)) = x;
-      }
-      const int t = tid & (C - 1);
-      const int64_t tok = lo + c0 + C + t;
-      if (tok < hi) {
-        constexpr int LINES = (D * (int)sizeof(TI) + 127) / 128;
-        const char *qr = reinterpret_cast<const char *>(qg + tok * in.ld_qk + (int64_t)hk * D);
-        const char *kr = reinterpret_cast<const char *>(kg + tok * in.ld_qk + (int64_t)hk * D);
-        const char *vr = reinterpret_cast<const char *>(vg + tok * in.ld_v + (int64_t)h * D);
-        for (int l = tid >> 6; l < 3 * LINES; l += NT / C) {
-          const char *base = l < LINES ? qr : (l < 2 * LINES ? kr : vr);
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 128 * (l % LINES)));
-        }
+    for (int it = 0; it < 8; ++it) {
+      const int blk = it * 8 + warp;                 // 8 token groups x 8 k-quad groups
+      const int i = 8 * (blk & 7) + (lane & 7);
+      const int k4 = 4 * (blk >> 3) + (lane >> 3);   // columns 4 k4 .. 4 k4 + 3
+      const float4 x = *reinterpret_cast<const float4 *>(QK + tc::core_off(64 + i, 4 * k4, D));
+      const float d = sDte[i];
+      const float v0 = d * x.x, v1 = d * x.y, v2 = d * x.z, v3 = d * x.w;
+      // round 1 (xor 2): lanes 0,1 keep columns 0,1 and take rows 2,3's; lanes 2,3 the rest
+      const bool hi2 = (l4 & 2) != 0;
+      const float r0 = __shfl_xor_sync(0xffffffffu, hi2 ? v0 : v2, 2);
+      const float r1 = __shfl_xor_sync(0xffffffffu, hi2 ? v1 : v3, 2);
+      const float a0 = hi2 ? r0 : v0, a1 = hi2 ? r1 : v1;
+      const float a2 = hi2 ? v2 : r0, a3 = hi2 ? v3 : r1;
+      // round 2 (xor 1): 2 x 2 transposes
+      const bool hi1 = (l4 & 1) != 0;
+      const float s0 = __shfl_xor_sync(0xffffffffu, hi1 ? a0 : a1, 1);
+      const float s1 = __shfl_xor_sync(0xffffffffu, hi1 ? a2 : a3, 1);
+      const float4 w = hi1 ? make_float4(s0, a1, s1, a3) : make_float4(a0, s0, a2, s1);
+      // lane l4 now holds column k = 4 k4 + l4 of tokens ib .. ib + 3
+      const int ib = 8 * (blk & 7) + (lane & 4);
+      *reinterpret_cast<float4 *>(KT + tc::core_off(4 * k4 + l4, ib, C)) = w;
+    }
+    const int t = tid & (C - 1);
+    const int64_t tok = lo + c0s + (RAW ? 3 * C : 2 * C) + t;
+    if (tok < hi) {
+      constexpr int LINES = (D * (int)sizeof(TI) + 127) / 128;
+      const char *qr = reinterpret_cast<const char *>(qg + tok * in.ld_qk + (int64_t)hk * D);
+      const char *kr = reinterpret_cast<const char *>(kg + tok * in.ld_qk + (int64_t)hk * D);
+      const char *vr = reinterpret_cast<const char *>(vg + tok * in.ld_v + (int64_t)h * D);
+      for (int l = tid >> 6; l < 3 * LINES; l += NT / C) {
+        const char *base = l < LINES ? qr : (l < 2 * LINES ? kr : vr);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 128 * (l % LINES)));
       }
     }
-    alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));
+    tc::fence_async_smem();
+  };
+
+  // chunk 0: stage, start E and D3, build its Ktil^T while they run
+  if (RAW) {
+    prefetch_raw(in, h, hk, lo, min(C, len), RW, &rbar);
+    load_gb<TI>(in, p, h, lo, min(C, len), g_next, b_next);
+  }
+  stage_next(0);
+  tc::fence_before_sync();
+  alive = __syncthreads_and(alive);
+  tc::fence_after_sync();
+  if (alive) {
+    issue_ed3();
+    build_kt(0);
+  }
+
+  // Per chunk the state chain is E/D3 -> F -> Delta -> state update -> next
+  // E/D3; the next chunk's staging runs under the state update, and this
+  // chunk's outputs and the next chunk's Ktil^T under the next E/D3.
+  for (int c0 = 0; c0 < len && alive; c0 += C) {
+    const int n = min(C, len - c0);
+    const bool last = c0 + C >= len;
+    alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));  // E, D3 done
     if (!alive) break;
     phase ^= 1;
     tc::fence_after_sync();
@@ -519,10 +748,8 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc::tmem_st_wait();
     }
-    tc::fence_async_smem();
     tc::fence_before_sync();
-    // this chunk's P and T tiles must have landed
-    alive = __syncthreads_and(mbar_wait_bounded(&tbar, tphase));
+    alive = __syncthreads_and(mbar_wait_bounded(&tbar, tphase));  // P, T tiles landed
     if (!alive) break;
     tphase ^= 1;
     tc::fence_after_sync();
@@ -552,13 +779,18 @@ __global__ void __launch_bounds__(NT, 1)
                    tc::idesc_tf32(128, 128), 1);
       tc::mma_commit(&bar);
     }
-    alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));
+    if (!last) stage_next(c0 + C);  // QK, XU and the scalars are free; the MMAs do not read them
+    tc::fence_before_sync();
+    alive = __syncthreads_and(alive && mbar_wait_bounded(&bar, phase));  // D4, new state ready
     if (!alive) break;
     phase ^= 1;
     tc::fence_after_sync();
-    if (tid == 0 && c0 + C < len) {  // the tiles are free again: fetch the next chunk's
-      mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
-      bulk_g2s(PT, wsq + (int64_t)(c0 / C + 1) * wstep, 2 * kTileBytes, &tbar);
+    if (!last) {
+      if (tid == 0) {  // the tiles are free again: fetch the next chunk's
+        mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
+        bulk_g2s(PT, wsq + (int64_t)(c0 / C + 1) * wstep, 2 * kTileBytes, &tbar);
+      }
+      issue_ed3();
     }
 
     // outputs o[t][v] = scale (gamma_t D3 + D4), this warp's half of t
@@ -578,9 +810,8 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
     }
+    if (!last) build_kt(c0 + C);
     tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
   }
 
   if (alive) {
@@ -598,6 +829,7 @@ __global__ void __launch_bounds__(NT, 1)
     // give outstanding MMA groups and tile copies a second bounded chance to finish
     mbar_wait_bounded(&bar, phase);
     mbar_wait_bounded(&tbar, tphase);
+    if (RAW) mbar_wait_bounded(&rbar, rphase);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -615,15 +847,21 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto prep = prep_kernel<TI>;
-  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+  constexpr int prep_bytes = prep_smem<TI>();
+  e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_bytes);
   if (e != cudaSuccess) return e;
-  prep<<<dim3((unsigned)nc, p.h_v), NT, PREP_SMEM, s>>>(p, seq, in, off, tiles);
+  const int npair = (p.h_v / p.h_k + 1) / 2;
+  prep<<<dim3((unsigned)nc, p.h_k * npair), NT, prep_bytes, s>>>(p, seq, in, off, tiles);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto kern = seq_kernel<TI, TO>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SEQ_SMEM);
+  constexpr int smem = seq_smem<TI>();
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(p.h_v, seq.n_seqs), NT, SEQ_SMEM, s>>>(p, layer, seq, in, static_cast<TO *>(o),
-                                                     scale, off, nc, tiles);
+  const bool aligned16 = (uintptr_t)in.q % 16 == 0 && (uintptr_t)in.k % 16 == 0 &&
+                         (uintptr_t)in.v % 16 == 0 && (in.ld_qk * sizeof(TI)) % 16 == 0 &&
+                         (in.ld_v * sizeof(TI)) % 16 == 0;
+  kern<<<dim3(p.h_v, seq.n_seqs), NT, smem, s>>>(p, layer, seq, in, static_cast<TO *>(o),
+                                                     scale, off, nc, tiles, aligned16 ? 1 : 0);
   return cudaGetLastError();
 }
 

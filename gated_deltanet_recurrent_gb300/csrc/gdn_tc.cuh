@@ -1,6 +1,6 @@
 // tcgen05 (5th-generation tensor core) helpers in inline PTX for sm_100+:
 // TMEM allocation, shared-memory matrix descriptors (K-major, no swizzle),
-// the kind::tf32 instruction descriptor, MMA issue/commit and TMEM loads and
+// the kind::tf32 and kind::f16 (bf16) instruction descriptors, MMA issue/commit and TMEM loads and
 // stores.  Operand layout used throughout ("core-matrix" layout): an
 // R x K float32 operand is stored as 8-row x 16-byte core matrices; element
 // (r, k) lives at float offset
@@ -42,6 +42,19 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16 with bf16 A and B: D float32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// 16-bit operands use the same core-matrix scheme with 8 elements per 16-byte
+// core-matrix row: element (r, k) at byte offset
+//     (r / 8) * SBO + (k / 8) * LBO + (r % 8) * 16 + (k % 8) * 2,
+// LBO = 128 bytes, SBO = K/8 * 128 bytes; one MMA step (K = 16) spans two core
+// matrices, like one tf32 step (K = 8).
+__host__ __device__ constexpr uint32_t sbo_bytes16(int kdim) { return (uint32_t)(kdim / 8) * 128u; }
+
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_addr(slot)),
@@ -72,6 +85,16 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, 
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 operands (kind::f16)
+__device__ __forceinline__ void mma_ss_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
