@@ -80,14 +80,14 @@ __global__ void __launch_bounds__(kThreads)
     if (blockIdx.x == 0 && h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
     a = a < 0 ? 0 : T;
   }
-  // token t of this CTA's sequence: pending draft t, or new draft t - ap
-  auto src_of = [&](int t, int64_t &row) -> const QKV & {
-    if (t < ap) {
-      row = (int64_t)i * va.T_prev + t;
-      return va.prev;
-    }
-    row = (int64_t)i * va.T + (t - ap);
-    return va.in;
+  // token t of this slot's sequence: pending draft t, or new draft t - ap
+  // (register copies: no address of the parameter block is taken)
+  const QKV cur = va.in, prv = va.prev;
+  const int T_new = va.T, T_old = va.T_prev;
+  auto src_of = [&](int t, int64_t &row) -> QKV {
+    const bool pend = t < ap;
+    row = pend ? (int64_t)i * T_old + t : (int64_t)i * T_new + (t - ap);
+    return pend ? prv : cur;
   };
   const int r0 = blockIdx.x * R;
   const int nrows = min(R, p.dv - r0);
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads)
   const int hk = h / (p.h_v / p.h_k);
   for (int t = warp; t < T; t += kThreads / 32) {
     int64_t tok;
-    const QKV &src = src_of(t, tok);
+    const QKV src = src_of(t, tok);
     float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4;
     if (lane < DK / 4) {
       q4 = Elem<TI>::load4(static_cast<const TI *>(src.q) + tok * src.ld_qk + (int64_t)hk * DK + 4 * lane);
@@ -124,14 +124,14 @@ __global__ void __launch_bounds__(kThreads)
   for (int e = tid; e < T * R; e += kThreads) {
     const int t = e / R, rl = e % R;
     int64_t tok;
-    const QKV &src = src_of(t, tok);
+    const QKV src = src_of(t, tok);
     sv[e] = rl < nrows ? Elem<TI>::load1(static_cast<const TI *>(src.v) + tok * src.ld_v +
                                         (int64_t)h * p.dv + r0 + rl)
                        : 0.f;
   }
   if (tid < T) {
     int64_t tok;
-    const QKV &src = src_of(tid, tok);
+    const QKV src = src_of(tid, tok);
     sal[tid] = expf(Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h));  // alpha_t
     sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * p.h_v + h);
   }
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads)
     float acc = 0.f;
     for (int t = 0; t < tid; ++t) {
       int64_t tok;
-      const QKV &src = src_of(t, tok);
+      const QKV src = src_of(t, tok);
       acc += Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
     }
     sG[tid] = acc;

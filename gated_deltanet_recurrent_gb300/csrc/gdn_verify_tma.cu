@@ -38,7 +38,7 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-template <typename TI, typename TO>
+template <typename TI, typename TO, bool DEFERRED>
 __global__ void __launch_bounds__(NT)
     verify_tma_kernel(PoolView p, const __grid_constant__ CUtensorMap tmap, int layer,
                       VerifyArgs va, TO *__restrict__ o) {
@@ -62,25 +62,28 @@ __global__ void __launch_bounds__(NT)
     if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
     return;
   }
-  const bool deferred = va.prev.q != nullptr && va.prev_accept != nullptr;
-  int ap = deferred ? va.prev_accept[i] : 0;  // pending drafts replayed first
-  if (ap < 0 || ap > va.T_prev) {
-    if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
-    ap = ap < 0 ? 0 : va.T_prev;
+  int ap = 0;  // pending drafts replayed first (deferred commit only)
+  if constexpr (DEFERRED) {
+    ap = va.prev_accept[i];
+    if (ap < 0 || ap > va.T_prev) {
+      if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
+      ap = ap < 0 ? 0 : va.T_prev;
+    }
   }
   const int T = ap + va.T;  // <= TMX (checked by the launcher)
-  int a = deferred ? ap : (va.commit_all ? T : (va.accept_len ? va.accept_len[i] : 0));
+  int a = DEFERRED ? ap : (va.commit_all ? T : (va.accept_len ? va.accept_len[i] : 0));
   if (a < 0 || a > T) {
     if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_COUNT);
     a = a < 0 ? 0 : T;
   }
-  auto src_of = [&](int t, int64_t &row) -> const QKV & {
-    if (t < ap) {
-      row = (int64_t)i * va.T_prev + t;
-      return va.prev;
-    }
-    row = (int64_t)i * va.T + (t - ap);
-    return va.in;
+  // token t of this slot's sequence: pending draft t, or new draft t - ap
+  // (register copies: no address of the parameter block is taken)
+  const QKV cur = va.in, prv = va.prev;
+  const int T_new = va.T, T_old = va.T_prev;
+  auto src_of = [&](int t, int64_t &row) -> QKV {
+    const bool pend = DEFERRED && t < ap;
+    row = pend ? (int64_t)i * T_old + t : (int64_t)i * T_new + (t - ap);
+    return pend ? prv : cur;
   };
   const int row0 = ((layer * p.n_slots + slot) * p.h_v + h) * D;  // tensor-map row
   const int hk = h / (p.h_v / p.h_k);
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(NT)
   // ---- stage the drafts while the head is in flight
   for (int t = warp; t < T; t += NT / 32) {
     int64_t tok;
-    const QKV &src = src_of(t, tok);
+    const QKV src = src_of(t, tok);
     float4 q4 = Elem<TI>::load4(static_cast<const TI *>(src.q) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
     float4 k4 = Elem<TI>::load4(static_cast<const TI *>(src.k) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
     const float qq = group_sum<32>(dot4(q4, q4));
@@ -128,13 +131,13 @@ __global__ void __launch_bounds__(NT)
     vr[t] = 0.f;
     if (t < T) {
       int64_t tok;
-      const QKV &src = src_of(t, tok);
+      const QKV src = src_of(t, tok);
       vr[t] = Elem<TI>::load1(static_cast<const TI *>(src.v) + tok * src.ld_v + (int64_t)h * D + v);
     }
   }
   if (tid < T) {
     int64_t tok;
-    const QKV &src = src_of(tid, tok);
+    const QKV src = src_of(tid, tok);
     sal[tid] = expf(Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h));
     sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * p.h_v + h);
   }
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(NT)
     float acc = 0.f;
     for (int t = 0; t < tid; ++t) {
       int64_t tok;
-      const QKV &src = src_of(t, tok);
+      const QKV src = src_of(t, tok);
       acc += Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
     }
     sG[tid] = acc;
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(NT)
         for (int ii = 0; ii < TMX; ++ii)
           if (ii < t) pt += Dm[t * (TMX + 1) + ii + 1] * dl[ii] * KK[ii * TMX + t];
         dl[t] = sbe[t] * (vr[t] - sal[t] * pt);
-        if (ob != nullptr && t >= ap) {
+        if (ob != nullptr && (!DEFERRED || t >= ap)) {
           float dq = 0.f;  // dots[T + t] without a runtime register index
 #pragma unroll
           for (int u = 0; u < 16; ++u)
@@ -263,7 +266,8 @@ __global__ void __launch_bounds__(NT)
 template <typename TI, typename TO>
 cudaError_t launch_t(const PoolView &p, const CUtensorMap &tmap, int layer, const VerifyArgs &va,
                      void *o, cudaStream_t s) {
-  auto kern = verify_tma_kernel<TI, TO>;
+  const bool deferred = va.prev.q != nullptr && va.prev_accept != nullptr;
+  auto kern = deferred ? verify_tma_kernel<TI, TO, true> : verify_tma_kernel<TI, TO, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.h_v, va.n);
