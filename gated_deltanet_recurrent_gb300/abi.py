@@ -25,7 +25,8 @@ EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "g
             "gdn_pool_copy",
             "gdn_pool_destroy", "gdn_pool_get_error", "gdn_conv_silu", "gdn_decode_step",
             "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
-            "gdn_spec_verify_deferred", "gdn_prefill_chunked_noalloc", "gdn_status_string",
+            "gdn_spec_verify_deferred", "gdn_prefill_chunked_noalloc", "gdn_prefill_chunked_ckpt",
+            "gdn_status_string",
             "gdn_last_error_message")
 
 
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                           P(gdn_qkv), vp, ctypes.c_float, vp]),
         "gdn_prefill_chunked_noalloc": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
                                              ctypes.c_float, vp]),
+        "gdn_prefill_chunked_ckpt": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
+                                          ctypes.c_float, vp, i32, i32, vp]),
         "gdn_status_string": (ctypes.c_char_p, [st]),
         "gdn_last_error_message": (ctypes.c_char_p, []),
     }
@@ -344,5 +347,24 @@ def gdn_prefill_chunked_noalloc(pool: Pool, layer: int, slot_ids: torch.Tensor,
     _check(load_library().gdn_prefill_chunked_noalloc(
         pool.handle, layer, _idx(slot_ids, "slot_ids"), _idx(cu_seqlens, "cu_seqlens"),
         slot_ids.numel(), q.shape[0], max_seqlen, ctypes.byref(inp), _ptr(o), _dt(o), scale,
+        _stream(stream)))
+    return o
+
+
+def gdn_prefill_chunked_ckpt(pool: Pool, layer: int, slot_ids: torch.Tensor,
+                             cu_seqlens: torch.Tensor, q, k, v, g, beta, o: torch.Tensor,
+                             ckpt_slots: torch.Tensor, ckpt_every: int, scale: float = 1.0,
+                             max_seqlen: int = 0, stream=None):
+    """gdn_prefill_chunked that also writes the state after every ckpt_every
+    tokens of sequence i into slot ckpt_slots[i, j] (int32 [n_seqs, m], -1: none)."""
+    inp = _qkv(pool, q, k, v, g, beta)
+    if max_seqlen <= 0:
+        max_seqlen = q.shape[0]
+    if ckpt_slots.dim() != 2 or ckpt_slots.shape[0] != slot_ids.numel():
+        raise GDNError(5, "ckpt_slots must be [n_seqs, m]")
+    _check(load_library().gdn_prefill_chunked_ckpt(
+        pool.handle, layer, _idx(slot_ids, "slot_ids"), _idx(cu_seqlens, "cu_seqlens"),
+        slot_ids.numel(), q.shape[0], max_seqlen, ctypes.byref(inp), _ptr(o), _dt(o), scale,
+        _idx(ckpt_slots.contiguous(), "ckpt_slots"), ckpt_slots.shape[1], ckpt_every,
         _stream(stream)))
     return o

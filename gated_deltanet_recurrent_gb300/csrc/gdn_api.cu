@@ -539,6 +539,68 @@ gdn_status gdn_prefill_chunked(gdn_pool *p, int32_t layer, const int32_t *slot_i
                         o_dtype, scale, stream, true);
 }
 
+gdn_status gdn_prefill_chunked_ckpt(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                                    const int32_t *cu_seqlens, int32_t n_seqs,
+                                    int32_t total_tokens, int32_t max_seqlen, const gdn_qkv *in,
+                                    void *o, gdn_dtype o_dtype, float scale,
+                                    const int32_t *ckpt_slots, int32_t ckpt_per_seq,
+                                    int32_t ckpt_every, gdn_stream stream) {
+  (void)max_seqlen;
+  gdn_status st = check_pool(p, layer);
+  if (st != GDN_OK) return st;
+  if (n_seqs < 0 || total_tokens < 0) return fail(GDN_ERR_ARG, "negative n_seqs/total_tokens");
+  if (n_seqs == 0 || total_tokens == 0) return ok();
+  if (n_seqs > 65535) return fail(GDN_ERR_SIZE, "n_seqs = %d > 65535", n_seqs);
+  if (!slot_ids || !cu_seqlens || !o || !ckpt_slots)
+    return fail(GDN_ERR_ARG, "slot_ids, cu_seqlens, o and ckpt_slots must be non-NULL");
+  if (ckpt_every < gdn::kChunk || ckpt_every % gdn::kChunk != 0 || ckpt_per_seq < 1)
+    return fail(GDN_ERR_ARG, "ckpt_every = %d must be a positive multiple of %d, ckpt_per_seq = %d >= 1",
+                ckpt_every, gdn::kChunk, ckpt_per_seq);
+  if (!dtype_ok(o_dtype)) return fail(GDN_ERR_DTYPE, "o dtype must be F32 or BF16");
+  gdn::QKV q;
+  if ((st = resolve_qkv(p, in, total_tokens, q))) return st;
+  gdn::SeqIndex seq{slot_ids, cu_seqlens, n_seqs, total_tokens};
+  const uint64_t lim = p->desc.prefill_workspace_max ? p->desc.prefill_workspace_max
+                                                     : (uint64_t)8 << 30;
+  const size_t wb = gdn::prefill_workspace_bytes(p->view, seq, q, (size_t)lim);
+  if (wb == 0)
+    return fail(GDN_ERR_UNSUPPORTED,
+                "checkpoints need the two-launch path: dk = dv = 128, 16-byte aligned v rows "
+                "and a workspace within prefill_workspace_max");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    std::vector<int32_t> cu, act, ck;
+    if ((st = check_slots(p, slot_ids, n_seqs, s)) ||
+        (st = check_cu(cu_seqlens, n_seqs, total_tokens, s, cu)) ||
+        (st = check_device_ptr(o, "o")) || (st = fetch(act, slot_ids, (size_t)n_seqs, s, "slot_ids")) ||
+        (st = fetch(ck, ckpt_slots, (size_t)n_seqs * ckpt_per_seq, s, "ckpt_slots")))
+      return st;
+    std::vector<char> used((size_t)p->desc.n_slots, 0);
+    for (int32_t a : act) used[(size_t)a] = 1;
+    for (size_t e = 0; e < ck.size(); ++e) {
+      const int32_t d = ck[e];
+      if (d < 0) continue;
+      if (d >= p->desc.n_slots)
+        return fail(GDN_ERR_SLOT, "ckpt_slots[%zu] = %d outside [0, %d)", e, d, p->desc.n_slots);
+      if (used[(size_t)d])
+        return fail(GDN_ERR_DUP_SLOT, "ckpt_slots[%zu] = %d is an active or repeated slot", e, d);
+      used[(size_t)d] = 1;
+    }
+  }
+  void *work = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&work, wb, p->work_pool, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "prefill workspace");
+  }
+  gdn::Checkpoints ck{ckpt_slots, ckpt_per_seq, ckpt_every};
+  e = gdn::launch_prefill_split(p->view, layer, seq, q, o, o_dtype, scale, work, s, ck);
+  const cudaError_t ef = cudaFreeAsync(work, s);
+  if (e == cudaSuccess) e = ef;
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return ok();
+}
+
 gdn_status gdn_prefill_recurrent(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
                                  const int32_t *cu_seqlens, int32_t n_seqs, int32_t total_tokens,
                                  int32_t max_seqlen, const gdn_qkv *in, void *o,

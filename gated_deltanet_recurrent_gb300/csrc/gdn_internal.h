@@ -44,6 +44,15 @@ struct SeqIndex {
   int total_tokens;            // rows of the packed token arrays
 };
 
+// State checkpoints during a chunked prefill: after (j + 1) * every tokens of
+// sequence i in the call, the state goes to slot slots[i * per_seq + j] (if
+// that entry is >= 0).  every == 0: none.
+struct Checkpoints {
+  const int32_t *slots;
+  int per_seq;
+  int every;                   // a multiple of the chunk (64)
+};
+
 cudaError_t launch_pool_reset(const PoolView &p, const int32_t *slot_ids, int n,
                               cudaStream_t s);
 
@@ -96,7 +105,7 @@ cudaError_t launch_prefill_tc(const PoolView &p, int layer, const SeqIndex &seq,
 size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v);
 cudaError_t launch_prefill_split(const PoolView &p, int layer, const SeqIndex &seq,
                                  const QKV &in, void *o, gdn_dtype o_dtype, float scale,
-                                 void *work, cudaStream_t s);
+                                 void *work, cudaStream_t s, const Checkpoints &ck = {});
 
 // Workspace bytes the chunked prefill of this call would use, or 0 when it
 // runs without one (not the tensor-core shape, or more than `limit` bytes).

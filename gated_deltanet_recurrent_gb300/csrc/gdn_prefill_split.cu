@@ -507,7 +507,7 @@ template <typename TI, typename TO>
 __global__ void __launch_bounds__(NT, 1)
     seq_kernel(PoolView p, int layer, SeqIndex seq, QKV in, TO *__restrict__ o, float scale,
                const int32_t *__restrict__ off, int64_t cap, const float *__restrict__ work,
-               int raw_rows) {
+               int raw_rows, Checkpoints ck) {
   // bf16 rows that are 16-byte aligned: stage from a bulk copy made a chunk ahead
   const bool RAW = std::is_same<TI, bf16>::value && raw_rows != 0;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -785,6 +785,25 @@ __global__ void __launch_bounds__(NT, 1)
     if (!alive) break;
     phase ^= 1;
     tc::fence_after_sync();
+    if (ck.every > 0 && c0 + C <= len && (c0 + C) % ck.every == 0) {  // checkpoint: copy S out
+      const int j = (c0 + C) / ck.every - 1;
+      const int ds = j < ck.per_seq ? ck.slots[(int64_t)si * ck.per_seq + j] : -1;
+      if (ds >= p.n_slots) {
+        if (tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
+      } else if (ds >= 0) {
+        float4 *dst = reinterpret_cast<float4 *>(
+            p.state + ((int64_t)layer * p.n_slots + ds) * p.state_slot_elems() +
+            ((int64_t)h * D + row) * D + 64 * half);
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          float v[16];
+          tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, v);
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4)
+            dst[cb * 4 + j4] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+        }
+      }
+    }
     if (!last) {
       if (tid == 0) {  // the tiles are free again: fetch the next chunk's
         mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
@@ -839,7 +858,7 @@ __global__ void __launch_bounds__(NT, 1)
 
 template <typename TI, typename TO>
 cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in, void *o,
-                     float scale, void *work, cudaStream_t s) {
+                     float scale, void *work, cudaStream_t s, const Checkpoints &ck) {
   int32_t *off = static_cast<int32_t *>(work);
   float *tiles = reinterpret_cast<float *>(static_cast<char *>(work) + offsets_bytes(seq.n_seqs));
   const int64_t nc = max_chunks(seq.n_seqs, seq.total_tokens);
@@ -861,7 +880,8 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
                          (uintptr_t)in.v % 16 == 0 && (in.ld_qk * sizeof(TI)) % 16 == 0 &&
                          (in.ld_v * sizeof(TI)) % 16 == 0;
   kern<<<dim3(p.h_v, seq.n_seqs), NT, smem, s>>>(p, layer, seq, in, static_cast<TO *>(o),
-                                                     scale, off, nc, tiles, aligned16 ? 1 : 0);
+                                                     scale, off, nc, tiles, aligned16 ? 1 : 0,
+                                                     ck);
   return cudaGetLastError();
 }
 
@@ -874,15 +894,15 @@ size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v) {
 
 cudaError_t launch_prefill_split(const PoolView &p, int layer, const SeqIndex &seq,
                                  const QKV &in, void *o, gdn_dtype o_dtype, float scale,
-                                 void *work, cudaStream_t s) {
+                                 void *work, cudaStream_t s, const Checkpoints &ck) {
   if (p.dk != D || p.dv != D) return cudaErrorNotSupported;
   if (in.dtype == GDN_F32 && o_dtype == GDN_F32)
-    return launch_t<float, float>(p, layer, seq, in, o, scale, work, s);
+    return launch_t<float, float>(p, layer, seq, in, o, scale, work, s, ck);
   if (in.dtype == GDN_F32 && o_dtype == GDN_BF16)
-    return launch_t<float, bf16>(p, layer, seq, in, o, scale, work, s);
+    return launch_t<float, bf16>(p, layer, seq, in, o, scale, work, s, ck);
   if (in.dtype == GDN_BF16 && o_dtype == GDN_F32)
-    return launch_t<bf16, float>(p, layer, seq, in, o, scale, work, s);
-  return launch_t<bf16, bf16>(p, layer, seq, in, o, scale, work, s);
+    return launch_t<bf16, float>(p, layer, seq, in, o, scale, work, s, ck);
+  return launch_t<bf16, bf16>(p, layer, seq, in, o, scale, work, s, ck);
 }
 
 }  // namespace gdn

@@ -197,6 +197,28 @@ gdn_status gdn_prefill_chunked(gdn_pool *pool, int32_t layer, const int32_t *slo
                                int32_t max_seqlen, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
                                float scale, gdn_stream stream);
 
+/* gdn_prefill_chunked that also stores state checkpoints for prefix caching
+ * (ai-infra-handbooks, "Project: adding the hybrid model Qwen3.5", "What to
+ * do", Prefix cache row: a cached prefix can resume only where a state
+ * checkpoint was stored; "Why it is worth doing": a recurrent state is saved
+ * and copied whole).  After (j + 1) * ckpt_every tokens of sequence i in this
+ * call, the recurrent state of every value head is written into slot
+ * ckpt_slots[i * ckpt_per_seq + j] of the same layer (entries < 0: none;
+ * ckpt_every a positive multiple of 64, so checkpoints fall on chunk
+ * boundaries).  Only the recurrent state is written: the conv window at a
+ * boundary is the last conv_k - 1 conv inputs before it, which the caller
+ * holds.  Checkpoint slots must differ from the active slots and from each
+ * other (host checks reject it; without them an out-of-range slot sets
+ * GDN_DEVERR_SLOT and is skipped).  Needs the two-launch path (dk = dv = 128,
+ * 16-byte aligned v rows, workspace within prefill_workspace_max):
+ * GDN_ERR_UNSUPPORTED otherwise. */
+gdn_status gdn_prefill_chunked_ckpt(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
+                                    const int32_t *cu_seqlens, int32_t n_seqs,
+                                    int32_t total_tokens, int32_t max_seqlen, const gdn_qkv *in,
+                                    void *o, gdn_dtype o_dtype, float scale,
+                                    const int32_t *ckpt_slots, int32_t ckpt_per_seq,
+                                    int32_t ckpt_every, gdn_stream stream);
+
 /* Token-by-token prefill: the same contract, arguments and results as
  * gdn_prefill_chunked, computed by applying the recurrence to each token in
  * order (baseRT issue #31, "Why this looks tractable": the per-token

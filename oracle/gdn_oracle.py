@@ -255,6 +255,28 @@ class OraclePool:
                 self.S[layer, s], o[lo:hi] = gdn_chunked(*args, scale, chunk, eps)
         return o
 
+    def prefill_checkpointed(self, layer, slot_ids, cu_seqlens, q, k, v, g, beta,
+                             ckpt_slots, ckpt_every, scale=1.0, eps=L2_EPS):
+        """Prefill token by token that also saves state checkpoints [P3,
+        "What to do", Prefix cache row: the prefix cache hits only where a
+        state checkpoint was stored; "Why it is worth doing": a state is saved
+        and copied whole].  ckpt_slots [n_seqs][m]: after (j + 1) * ckpt_every
+        tokens of sequence i in this call, its state is copied into slot
+        ckpt_slots[i][j] (skipped when negative)."""
+        o = np.empty((len(q), self.h_v, self.dv))
+        for i, s in enumerate(slot_ids):
+            lo, hi = int(cu_seqlens[i]), int(cu_seqlens[i + 1])
+            S = self.S[layer, s].copy()
+            for t in range(lo, hi):
+                S, o[t] = gdn_step(S, q[t], k[t], v[t], g[t], beta[t], scale, eps)
+                n_done = t + 1 - lo
+                if n_done % ckpt_every == 0:
+                    j = n_done // ckpt_every - 1
+                    if j < len(ckpt_slots[i]) and ckpt_slots[i][j] >= 0:
+                        self.S[layer, ckpt_slots[i][j]] = S
+            self.S[layer, s] = S
+        return o
+
     def spec_verify(self, layer, slot_ids, T, q, k, v, g, beta,
                     accept_len=None, scale=1.0, eps=L2_EPS):
         """Draft token t of slot i is token i*T + t of q, k, v, g, beta.

@@ -238,6 +238,71 @@ def test_prefill_two_launch_rows_not_16_byte_aligned():
     assert torch.equal(res[0][1], res[1][1])
 
 
+def test_prefill_checkpoints_match_oracle_and_resume():
+    """gdn_prefill_chunked_ckpt: the state after every 64 tokens goes to the
+    requested slots (prefix-cache checkpoints).  Each checkpoint matches the
+    oracle's state after that prefix, and a request resumed from a checkpoint
+    slot with the rest of its tokens ends where the uninterrupted one does."""
+    rng = np.random.default_rng(46)
+    shape = synth.LayerShape(4, 2, 128, 128, 16, 4)
+    lens = [300, 64, 130]
+    ids = np.array([0, 1, 2], dtype=np.int32)
+    cu = synth.cu_seqlens_of(lens)
+    T = int(cu[-1])
+    S0 = synth.random_states(rng, 3, shape)
+    tok = synth.token_inputs(rng, T, shape, "bf16")
+    ck = np.array([[3, -1, 4, 5], [6, -1, -1, -1], [7, 8, -1, -1]], dtype=np.int32)
+    pool = abi.Pool.for_shape(shape, 1, 12, conv_dtype=torch.float32)
+    pool.state.fill_(SENTINEL)
+    lid = torch.from_numpy(ids).long().cuda()
+    pool.state[0, lid] = dev(S0)
+    o = torch.empty(T, shape.h_v, shape.dv, device="cuda")
+    abi.gdn_prefill_chunked_ckpt(pool, 0, dev_i32(ids), dev_i32(cu), *tok_dev(tok, "bf16"), o,
+                                 dev_i32(ck), 64)
+    assert abi.gdn_pool_get_error(pool) == 0
+    ref = O.OraclePool(1, 12, shape.h_v, shape.h_k, shape.dk, shape.dv, 16, 4)
+    ref.S[0, ids] = S0
+    o_ref = ref.prefill_checkpointed(0, ids, cu, *tok_np(tok), ckpt_slots=ck, ckpt_every=64)
+    assert_close_bf16(host(o), o_ref, what="o")
+    assert_maxrel(host(o), o_ref, _rel_tol(128), "o")
+    used = sorted(int(d) for d in ck.ravel() if d >= 0)
+    for d in used:
+        assert_maxrel(host(pool.state[0, d]), ref.S[0, d], _rel_tol(128), f"checkpoint slot {d}")
+    assert_maxrel(host(pool.state[0, lid]), ref.S[0, ids], _rel_tol(128), "final S")
+    rest = [s for s in range(12) if s not in used and s not in ids]
+    assert bool((pool.state[0, rest] == SENTINEL).all())
+    # resume sequence 0 from its checkpoint after 192 tokens (slot 4): prefill tokens 192..299
+    q, k, v, g, beta = tok_dev(tok, "bf16")
+    lo, hi = 192, 300
+    o2 = torch.empty(hi - lo, shape.h_v, shape.dv, device="cuda")
+    abi.gdn_prefill_chunked(pool, 0, dev_i32([4]), dev_i32([0, hi - lo]),
+                            q[lo:hi], k[lo:hi], v[lo:hi], g[lo:hi], beta[lo:hi], o2)
+    assert_maxrel(host(pool.state[0, 4]), host(pool.state[0, 0]), _rel_tol(128), "resumed S")
+    assert_maxrel(host(o2), host(o[lo:hi]), _rel_tol(128), "resumed o")
+
+
+def test_prefill_checkpoint_argument_checks():
+    shape = synth.LayerShape(2, 1, 128, 128, 16, 4)
+    pool = abi.Pool.for_shape(shape, 1, 4, conv_dtype=torch.float32)
+    rng = np.random.default_rng(47)
+    tok = tok_dev(synth.token_inputs(rng, 70, shape, "bf16"), "bf16")
+    o = torch.zeros(70, 2, 128, device="cuda")
+    for ck, every, status in (([[0]], 64, "GDN_ERR_DUP_SLOT"), ([[2, 2]], 64, "GDN_ERR_DUP_SLOT"),
+                              ([[4]], 64, "GDN_ERR_SLOT"), ([[2]], 32, "GDN_ERR_ARG")):
+        with pytest.raises(abi.GDNError) as e:
+            abi.gdn_prefill_chunked_ckpt(pool, 0, dev_i32([0]), dev_i32([0, 70]), *tok, o,
+                                         dev_i32(ck), every)
+        assert e.value.name == status
+    small = abi.Pool.for_shape(synth.LayerShape(2, 1, 16, 16, 16, 4), 1, 4,
+                               conv_dtype=torch.float32)
+    t16 = tok_dev(synth.token_inputs(rng, 70, synth.LayerShape(2, 1, 16, 16, 16, 4), "bf16"),
+                  "bf16")
+    with pytest.raises(abi.GDNError) as e:
+        abi.gdn_prefill_chunked_ckpt(small, 0, dev_i32([0]), dev_i32([0, 70]), *t16,
+                                     torch.zeros(70, 2, 16, device="cuda"), dev_i32([[2]]), 64)
+    assert e.value.name == "GDN_ERR_UNSUPPORTED"
+
+
 def _head_sample(tok, heads, group):
     """Slice value heads `heads` (and the key heads they read) out of a token dict."""
     kh = [h // group for h in heads]

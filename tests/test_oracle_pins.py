@@ -17,6 +17,8 @@ Map (oracle function -> pins):
   spec_verify     equals decode steps; commit at a == a steps; a = 0 unchanged
   spec_verify_deferred  rounds equal the two-phase rounds; the state after
                   the flush equals decoding only the accepted drafts
+  prefill_checkpointed  each checkpoint equals the recurrence over the
+                  prefix it closes; outputs and final state equal prefill
   OraclePool      N slots == each alone; reset == fresh; prefill split
                   invariance across pieces (chunked-prefill state carry)
 """
@@ -544,4 +546,37 @@ def test_pool_deferred_rounds_equal_two_phase_rounds():
     np.testing.assert_allclose(dfr.S, two.S, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(dfr.S, dec.S, rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(dfr.S[0, 2], S0[0, 2])
+
+
+def test_pool_prefill_checkpoints_are_prefix_states():
+    rng = np.random.default_rng(35)
+    shape = synth.LayerShape(2, 1, 8, 8, 16, 4)
+    lens = [13, 4, 9]
+    cu = synth.cu_seqlens_of(lens)
+    tok = synth.token_inputs(rng, int(cu[-1]), shape)
+    args = [tok[nm] for nm in ("q", "k", "v", "g", "beta")]
+    mk = lambda: O.OraclePool(1, 12, shape.h_v, shape.h_k, shape.dk, shape.dv,
+                              shape.conv_ch, shape.conv_k)
+    S0 = rng.standard_normal((1, 12, shape.h_v, shape.dv, shape.dk))
+    slots = [0, 1, 2]
+    ck = [[5, -1, 6], [7, 8, 9], [10, 11, -1]]
+    a, b = mk(), mk()
+    a.S[:] = S0
+    b.S[:] = S0
+    o_a = a.prefill_checkpointed(0, slots, cu, *args, ckpt_slots=ck, ckpt_every=4)
+    o_b = b.prefill(0, slots, cu, *args)
+    np.testing.assert_allclose(o_a, o_b, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a.S[0, slots], b.S[0, slots], rtol=1e-12, atol=1e-12)
+    for i, s in enumerate(slots):
+        lo = cu[i]
+        for j, d in enumerate(ck[i]):
+            n = 4 * (j + 1)
+            if d < 0:
+                continue
+            if n > lens[i]:
+                np.testing.assert_array_equal(a.S[0, d], S0[0, d])   # never reached
+                continue
+            S_ref, _ = O.gdn_recurrent(S0[0, s], *(x[lo:lo + n] for x in args))
+            np.testing.assert_allclose(a.S[0, d], S_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(a.S[0, [3, 4]], S0[0, [3, 4]])
 
