@@ -23,6 +23,9 @@
 // (chunk, value head) 32 KiB: the P tile, then the T tile, each 64 x 64 float32
 // in the K-major core-matrix layout of gdn_tc.cuh.  Chunks are numbered
 // sequence by sequence; offsets[i] is the first chunk of sequence i.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <type_traits>
 
 #include "gdn_tc.cuh"
@@ -107,34 +110,32 @@ __device__ __forceinline__ void stage_rows(const TI *q0, const TI *k0, const TI 
   const int cg = lane >> 3;
   const int t = stage_token();
   const bool real = t < n;
-  float4 q4[D / 16], k4[D / 16], v4[D / 16];
+  // q, then k (normalised rows of the core tile), then beta v: one row in registers at a time
 #pragma unroll
-  for (int j = 0; j < D / 16; ++j) {
-    const int c = cg + 4 * j;
-    q4[j] = k4[j] = v4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (real) {
-      q4[j] = Elem<TI>::load4(q0 + t * ldq + 4 * c);
-      k4[j] = Elem<TI>::load4(k0 + t * ldq + 4 * c);
-      if (WITH_V) v4[j] = Elem<TI>::load4(v0 + t * ldv + 4 * c);
+  for (int which = 0; which < 2; ++which) {
+    const TI *src = (which == 0 ? q0 : k0) + t * ldq;
+    float4 x4[D / 16];
+    float xx = 0.f;
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      x4[j] = real ? Elem<TI>::load4(src + 4 * (cg + 4 * j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      xx += dot4(x4[j], x4[j]);
     }
-  }
-  float qq = 0.f, kk = 0.f;
+    xx += __shfl_xor_sync(0xffffffffu, xx, 8);
+    xx += __shfl_xor_sync(0xffffffffu, xx, 16);
+    const float xs = rsqrtf(xx + kL2Eps);
 #pragma unroll
-  for (int j = 0; j < D / 16; ++j) {
-    qq += dot4(q4[j], q4[j]);
-    kk += dot4(k4[j], k4[j]);
+    for (int j = 0; j < D / 16; ++j)
+      *reinterpret_cast<float4 *>(QK + tc::core_off(64 * which + t, 4 * (cg + 4 * j), D)) =
+          scale4(xs, x4[j]);
   }
-  qq += __shfl_xor_sync(0xffffffffu, qq, 8);
-  qq += __shfl_xor_sync(0xffffffffu, qq, 16);
-  kk += __shfl_xor_sync(0xffffffffu, kk, 8);
-  kk += __shfl_xor_sync(0xffffffffu, kk, 16);
-  const float qs = rsqrtf(qq + kL2Eps), ks = rsqrtf(kk + kL2Eps);
+  if (WITH_V) {
 #pragma unroll
-  for (int j = 0; j < D / 16; ++j) {
-    const int c = cg + 4 * j;
-    *reinterpret_cast<float4 *>(QK + tc::core_off(t, 4 * c, D)) = scale4(qs, q4[j]);
-    *reinterpret_cast<float4 *>(QK + tc::core_off(64 + t, 4 * c, D)) = scale4(ks, k4[j]);
-    if (WITH_V) *reinterpret_cast<float4 *>(XU + t * XS + 4 * c) = scale4(bt, v4[j]);
+    for (int j = 0; j < D / 16; ++j) {
+      const int c = cg + 4 * j;
+      const float4 v4 = real ? Elem<TI>::load4(v0 + t * ldv + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4 *>(XU + t * XS + 4 * c) = scale4(bt, v4);
+    }
   }
   if (cg == 0) {
     sG[t] = gt;
@@ -155,27 +156,97 @@ __device__ __forceinline__ void stage_chunk(const QKV &in, const PoolView &p, in
                          in.ld_qk, in.ld_v, n, gt, bt, QK, XU, sG, sBeta);
 }
 
-// Raw bf16 copy of one chunk's q, k and v rows in shared memory, filled by
-// bulk copies (one 256-byte row each) while the previous chunk computes:
-// [3][64 tokens][kRawLd] bf16, rows padded to 272 bytes so the staging reads
-// spread over the banks.  Used when the rows are 16-byte aligned.
-constexpr int kRawLd = D + 8;
-constexpr int kRawBytes = 3 * C * kRawLd * 2;
+// Raw bf16 copy of one chunk's q, k and v (and optionally g, beta) in shared
+// memory, loaded by tensor-map copies a chunk ahead (16-byte aligned rows):
+// q, k, v each as two 64-column halves of [64 tokens][64] bf16 in the 128-byte
+// swizzled layout (8 KiB each, 1024-byte aligned), then g and beta as
+// [64 tokens][8 heads] bf16 (the 8-head group holding this head).
+struct InMaps {
+  CUtensorMap q, k, v, g, b;   // q, k, v: {128, heads, tokens}; g, b: {h_v, tokens}
+};
+constexpr int kRawHalf = C * 64 * 2;            // 8 KiB
+constexpr int kRawGB = C * 8 * 2;               // 1 KiB
+constexpr int kRawQKV = 6 * kRawHalf;
+constexpr int kRawBytes = kRawQKV + 2 * kRawGB + 1024;  // + alignment slack
 
-__device__ __forceinline__ void prefetch_raw(const QKV &in, int h, int hk, int64_t tok0, int n,
-                                             bf16 *raw, uint64_t *rbar) {
-  if (threadIdx.x == 0) mbar_arrive_expect_tx(rbar, (uint32_t)n * 3 * D * 2);
-  const int e = threadIdx.x;  // 3 tensors x 64 tokens, one row per thread
-  if (e < 3 * C) {
-    const int which = e / C, t = e % C;
-    if (t < n) {
-      const int64_t tok = tok0 + t;
-      const bf16 *src =
-          which == 0 ? static_cast<const bf16 *>(in.q) + tok * in.ld_qk + (int64_t)hk * D
-          : which == 1 ? static_cast<const bf16 *>(in.k) + tok * in.ld_qk + (int64_t)hk * D
-                       : static_cast<const bf16 *>(in.v) + tok * in.ld_v + (int64_t)h * D;
-      bulk_g2s(raw + (which * C + t) * kRawLd, src, D * 2, rbar);
+__device__ __forceinline__ void tma3(void *dst, const CUtensorMap *m, int x, int y, int z,
+                                     uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma2(void *dst, const CUtensorMap *m, int x, int y,
+                                     uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// One thread: the chunk's q, k, v halves (and g, beta) onto rbar.
+__device__ __forceinline__ void prefetch_raw(const InMaps &m, bool gb, int h, int hk,
+                                             int64_t tok0, unsigned char *raw, uint64_t *rbar) {
+  mbar_arrive_expect_tx(rbar, kRawQKV + (gb ? 2 * kRawGB : 0));
+  const int z = (int)tok0;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    tma3(raw + (0 + hf) * kRawHalf, &m.q, 64 * hf, hk, z, rbar);
+    tma3(raw + (2 + hf) * kRawHalf, &m.k, 64 * hf, hk, z, rbar);
+    tma3(raw + (4 + hf) * kRawHalf, &m.v, 64 * hf, h, z, rbar);
+  }
+  if (gb) {
+    tma2(raw + kRawQKV, &m.g, h & ~7, z, rbar);
+    tma2(raw + kRawQKV + kRawGB, &m.b, h & ~7, z, rbar);
+  }
+}
+
+// Elements 4c .. 4c+3 of token t of a [64][128] bf16 tile stored as two swizzled halves.
+__device__ __forceinline__ float4 raw_load4(const unsigned char *tile, int t, int c) {
+  const int col = (4 * c) & 63;
+  const int chunk = (col >> 3) ^ (t & 7);
+  const uint2 r = *reinterpret_cast<const uint2 *>(tile + ((4 * c) >> 6) * kRawHalf + t * 128 +
+                                                   chunk * 16 + (col & 7) * 2);
+  return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u),
+                     __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+}
+
+// stage_rows from the raw tiles (same mapping and arithmetic).
+__device__ __forceinline__ void stage_rows_raw(const unsigned char *raw, int n, float gt, float bt,
+                                               float *QK, float *XU, float *sG, float *sBeta) {
+  const int lane = threadIdx.x & 31;
+  const int cg = lane >> 3;
+  const int t = stage_token();
+  const bool real = t < n;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const unsigned char *tile = raw + 2 * which * kRawHalf;
+    float4 x4[D / 16];
+    float xx = 0.f;
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      x4[j] = real ? raw_load4(tile, t, cg + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      xx += dot4(x4[j], x4[j]);
     }
+    xx += __shfl_xor_sync(0xffffffffu, xx, 8);
+    xx += __shfl_xor_sync(0xffffffffu, xx, 16);
+    const float xs = rsqrtf(xx + kL2Eps);
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j)
+      *reinterpret_cast<float4 *>(QK + tc::core_off(64 * which + t, 4 * (cg + 4 * j), D)) =
+          scale4(xs, x4[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < D / 16; ++j) {
+    const int c = cg + 4 * j;
+    const float4 v4 = real ? raw_load4(raw + 4 * kRawHalf, t, c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4 *>(XU + t * XS + 4 * c) = scale4(bt, v4);
+  }
+  if (cg == 0) {
+    sG[t] = gt;
+    sBeta[t] = bt;
   }
 }
 
@@ -507,13 +578,14 @@ template <typename TI, typename TO>
 __global__ void __launch_bounds__(NT, 1)
     seq_kernel(PoolView p, int layer, SeqIndex seq, QKV in, TO *__restrict__ o, float scale,
                const int32_t *__restrict__ off, int64_t cap, const float *__restrict__ work,
-               int raw_rows, Checkpoints ck) {
+               const __grid_constant__ InMaps maps, int raw_rows, int raw_gb, Checkpoints ck) {
   // bf16 rows that are 16-byte aligned: stage from a bulk copy made a chunk ahead
   const bool RAW = std::is_same<TI, bf16>::value && raw_rows != 0;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *QK = reinterpret_cast<float *>(smem + S_QK);
   float *XU = reinterpret_cast<float *>(smem + S_XU);
-  bf16 *RW = reinterpret_cast<bf16 *>(smem + S_RAW);
+  unsigned char *RW = smem + S_RAW + ((1024u - (smem_addr(smem + S_RAW) & 1023u)) & 1023u);
+  const bool GB = RAW && raw_gb != 0;  // g, beta come with the tensor-map copies too
   float *PT = reinterpret_cast<float *>(smem + S_PT);
   float *KT = reinterpret_cast<float *>(smem + S_KT);
   float *sG = reinterpret_cast<float *>(smem + S_SC);
@@ -605,18 +677,21 @@ __global__ void __launch_bounds__(NT, 1)
     if (RAW) {
       alive = __syncthreads_and(alive && mbar_wait_bounded(&rbar, rphase));
       rphase ^= 1;
-      stage_rows<TI, true>(reinterpret_cast<const TI *>(RW),
-                           reinterpret_cast<const TI *>(RW + C * kRawLd),
-                           reinterpret_cast<const TI *>(RW + 2 * C * kRawLd), kRawLd, kRawLd, ns,
-                           g_next, b_next, QK, XU, sG, sBeta);
+      if (GB) {  // this head's column of the [64][8] g and beta tiles (padded tokens 0)
+        const int t = stage_token();
+        const bf16 *gt8 = reinterpret_cast<const bf16 *>(RW + kRawQKV);
+        g_next = t < ns ? __bfloat162float(gt8[t * 8 + (h & 7)]) : 0.f;
+        b_next = t < ns ? __bfloat162float(gt8[C * 8 + t * 8 + (h & 7)]) : 0.f;
+      }
+      stage_rows_raw(RW, ns, g_next, b_next, QK, XU, sG, sBeta);
     } else {
       stage_chunk<TI, true>(in, p, h, hk, lo + c0s, ns, QK, XU, sG, sBeta);
     }
     __syncthreads();
     if (RAW && c0s + C < len) {  // the raw copy is consumed: fetch the next chunk's
       const int nn = min(C, len - c0s - C);
-      prefetch_raw(in, h, hk, lo + c0s + C, nn, RW, &rbar);
-      load_gb<TI>(in, p, h, lo + c0s + C, nn, g_next, b_next);
+      if (tid == 0) prefetch_raw(maps, GB, h, hk, lo + c0s + C, RW, &rbar);
+      if (!GB) load_gb<TI>(in, p, h, lo + c0s + C, nn, g_next, b_next);
     }
     if (warp == 0) {  // cumulative log-decay (padded tokens carry g = 0)
       const float a = sG[2 * lane], b = sG[2 * lane + 1];
@@ -695,8 +770,8 @@ __global__ void __launch_bounds__(NT, 1)
 
   // chunk 0: stage, start E and D3, build its Ktil^T while they run
   if (RAW) {
-    prefetch_raw(in, h, hk, lo, min(C, len), RW, &rbar);
-    load_gb<TI>(in, p, h, lo, min(C, len), g_next, b_next);
+    if (tid == 0) prefetch_raw(maps, GB, h, hk, lo, RW, &rbar);
+    if (!GB) load_gb<TI>(in, p, h, lo, min(C, len), g_next, b_next);
   }
   stage_next(0);
   tc::fence_before_sync();
@@ -720,7 +795,6 @@ __global__ void __launch_bounds__(NT, 1)
 
     // F[v][t] = beta_t v_t[v] - beta_t gamma_t E[v][t] into TMEM; o part; S <- gamma_n S
     const int i0 = 32 * half;
-    float op[C / 2];
     {
       const int v = row;
 #pragma unroll
@@ -732,10 +806,11 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int t = t0 + j;
-          op[16 * cb + j] = sGam[t] * d3[j];
+          d3[j] *= sGam[t];
           f[j] = XU[t * XS + v] - sBeta[t] * sGam[t] * e[j];
         }
         tc::tmem_st16(lrow + T_F + t0, f);
+        tc::tmem_st16(lrow + T_D4 + t0, d3);
       }
       const float gn = sGam[C - 1];
 #pragma unroll 1
@@ -772,7 +847,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int j = 0; j < C / 8; ++j)
         tc::mma_ts(tm + T_D4, tm + T_DD + j * 8, tc::smem_desc(pt_s + j * KSTEP, tc::kLBO, SBO_C),
-                   tc::idesc_tf32(128, 64), j > 0);
+                   tc::idesc_tf32(128, 64), 1);
 #pragma unroll
       for (int j = 0; j < C / 8; ++j)
         tc::mma_ts(tm + T_S, tm + T_DD + j * 8, tc::smem_desc(kt_s + j * KSTEP, tc::kLBO, SBO_C),
@@ -824,8 +899,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int t = t0 + j;
-          if (t < n)
-            Elem<TO>::store1(ob + (int64_t)t * p.h_v * D, scale * (op[16 * cb + j] + d4[j]));
+          if (t < n) Elem<TO>::store1(ob + (int64_t)t * p.h_v * D, scale * d4[j]);
         }
       }
     }
@@ -856,6 +930,56 @@ __global__ void __launch_bounds__(NT, 1)
   if (warp == 0) tc::tmem_dealloc(tm, SEQ_TMEM);
 }
 
+// Tensor maps for the bf16 inputs of a call: q, k {128, h_k, tokens} and v
+// {128, h_v, tokens} with boxes {64, 1, 64} in the 128-byte swizzle (rows and
+// strides 16-byte aligned), and g, beta {h_v, tokens} with boxes {8, 64} when
+// their rows are 16-byte aligned too (gb).  False: stage from global memory.
+bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMaps &m, bool &gb) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      fn = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  gb = false;
+  if (encode == nullptr) return false;
+  const size_t es = 2;
+  auto a16 = [](const void *x) { return (uintptr_t)x % 16 == 0; };
+  if (!a16(in.q) || !a16(in.k) || !a16(in.v) || (in.ld_qk * es) % 16 || (in.ld_v * es) % 16)
+    return false;
+  const cuuint64_t tokens = (cuuint64_t)seq.total_tokens;
+  cuuint32_t box[3] = {64, 1, C}, elem[3] = {1, 1, 1};
+  auto map3 = [&](CUtensorMap *dst, const void *base, int heads, int64_t ld) {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)ld * es};
+    return encode(dst, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                  strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+  };
+  if (!map3(&m.q, in.q, p.h_k, in.ld_qk) || !map3(&m.k, in.k, p.h_k, in.ld_qk) ||
+      !map3(&m.v, in.v, p.h_v, in.ld_v))
+    return false;
+  if (a16(in.g) && a16(in.beta) && ((size_t)p.h_v * es) % 16 == 0) {
+    cuuint64_t dims[2] = {(cuuint64_t)p.h_v, tokens};
+    cuuint64_t strides[1] = {(cuuint64_t)p.h_v * es};
+    cuuint32_t box2[2] = {8, C};
+    auto map2 = [&](CUtensorMap *dst, const void *base) {
+      return encode(dst, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box2, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+             CUDA_SUCCESS;
+    };
+    gb = map2(&m.g, in.g) && map2(&m.b, in.beta);
+  }
+  return true;
+}
+
 template <typename TI, typename TO>
 cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in, void *o,
                      float scale, void *work, cudaStream_t s, const Checkpoints &ck) {
@@ -876,12 +1000,12 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   constexpr int smem = seq_smem<TI>();
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const bool aligned16 = (uintptr_t)in.q % 16 == 0 && (uintptr_t)in.k % 16 == 0 &&
-                         (uintptr_t)in.v % 16 == 0 && (in.ld_qk * sizeof(TI)) % 16 == 0 &&
-                         (in.ld_v * sizeof(TI)) % 16 == 0;
+  InMaps maps;
+  bool gb = false;
+  const bool raw = std::is_same<TI, bf16>::value && encode_in_maps(p, seq, in, maps, gb);
   kern<<<dim3(p.h_v, seq.n_seqs), NT, smem, s>>>(p, layer, seq, in, static_cast<TO *>(o),
-                                                     scale, off, nc, tiles, aligned16 ? 1 : 0,
-                                                     ck);
+                                                     scale, off, nc, tiles, maps, raw ? 1 : 0,
+                                                     gb ? 1 : 0, ck);
   return cudaGetLastError();
 }
 
