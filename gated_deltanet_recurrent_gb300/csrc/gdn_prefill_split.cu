@@ -560,18 +560,25 @@ __global__ void __launch_bounds__(NT, 2)
 constexpr int S_QK = 0;                        // [Q;K] core tile 128 x 128
 constexpr int S_XU = S_QK + 128 * D * 4;       // beta v (plain 64 x XS)
 constexpr int S_PT = S_XU + C * XS * 4;        // P tile (from the workspace)
-constexpr int S_TT = S_PT + TILE * 4;          // T tile (same bulk copy)
-constexpr int S_KT = S_TT + TILE * 4;          // Ktil^T tile [k][i], 128 x 64
-constexpr int S_SC = S_KT + D * C * 4;         // G, gamma, beta, e^{G_n - G}
+constexpr int S_KT = S_PT + TILE * 4;          // Ktil^T tile [k][i], 128 x 64, right after P:
+                                               // [P; Ktil^T] is one 192-row B operand
+constexpr int S_TT = S_KT + D * C * 4;         // T tile (from the workspace)
+constexpr int S_SC = S_TT + TILE * 4;          // G, gamma, beta, e^{G_n - G}
 constexpr int S_RAW = S_SC + 4 * C * 4;        // raw bf16 q, k, v of the next chunk
 template <typename TI>
 constexpr int seq_smem() { return S_RAW + (std::is_same<TI, bf16>::value ? kRawBytes : 0); }
-static_assert(S_PT % 16 == 0 && S_KT % 16 == 0 && S_RAW % 16 == 0, "tile alignment");
+static_assert(S_PT % 16 == 0 && S_KT == S_PT + TILE * 4 && S_TT % 16 == 0 && S_RAW % 16 == 0,
+              "tile alignment");
 static_assert(S_RAW + kRawBytes <= 227 * 1024, "shared memory");
+
+// Thread that issues the bulk and tensor-map copies (warp 6), away from the
+// MMA-issuing thread 0 and the scan warp 7, so no warp carries two serial jobs.
+constexpr int kCopier = 192;
 
 // TMEM columns
 // [S Q^T | S K^T] is one N = 128 product over the [Q;K] tile: D3 then E
-constexpr uint32_t T_S = 0, T_D3 = 128, T_E = 192, T_F = 256, T_DD = 320, T_D4 = 384;
+// [D4 | S] is one N = 192 accumulator over [P; Ktil^T]: output part then state
+constexpr uint32_t T_D4 = 0, T_S = 64, T_D3 = 192, T_E = 256, T_F = 320, T_DD = 384;
 constexpr uint32_t SEQ_TMEM = 512;
 
 template <typename TI, typename TO>
@@ -588,6 +595,7 @@ __global__ void __launch_bounds__(NT, 1)
   const bool GB = RAW && raw_gb != 0;  // g, beta come with the tensor-map copies too
   float *PT = reinterpret_cast<float *>(smem + S_PT);
   float *KT = reinterpret_cast<float *>(smem + S_KT);
+  float *TT = reinterpret_cast<float *>(smem + S_TT);
   float *sG = reinterpret_cast<float *>(smem + S_SC);
   float *sGam = sG + C;
   float *sBeta = sGam + C;
@@ -634,9 +642,10 @@ __global__ void __launch_bounds__(NT, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (tid == 0) {  // chunk 0's P and T tiles
+  if (tid == kCopier) {  // chunk 0's P and T tiles
     mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
-    bulk_g2s(PT, wsq, 2 * kTileBytes, &tbar);
+    bulk_g2s(PT, wsq, kTileBytes, &tbar);
+    bulk_g2s(TT, wsq + TILE, kTileBytes, &tbar);
   }
   const uint32_t tm = tmem_slot;
   const uint32_t lrow = tm + ((uint32_t)(32 * quad) << 16);
@@ -660,8 +669,7 @@ __global__ void __launch_bounds__(NT, 1)
   const TI *vg = static_cast<const TI *>(in.v);
   const uint32_t qk_s = smem_addr(QK);
   const uint32_t pt_s = smem_addr(PT);
-  const uint32_t tt_s = pt_s + kTileBytes;
-  const uint32_t kt_s = smem_addr(KT);
+  const uint32_t tt_s = smem_addr(TT);
   constexpr uint32_t SBO_D = tc::sbo_bytes(D);
   constexpr uint32_t SBO_C = tc::sbo_bytes(C);
   constexpr uint32_t KSTEP = 2 * tc::kLBO;
@@ -690,10 +698,10 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     if (RAW && c0s + C < len) {  // the raw copy is consumed: fetch the next chunk's
       const int nn = min(C, len - c0s - C);
-      if (tid == 0) prefetch_raw(maps, GB, h, hk, lo + c0s + C, RW, &rbar);
+      if (tid == kCopier) prefetch_raw(maps, GB, h, hk, lo + c0s + C, RW, &rbar);
       if (!GB) load_gb<TI>(in, p, h, lo + c0s + C, nn, g_next, b_next);
     }
-    if (warp == 0) {  // cumulative log-decay (padded tokens carry g = 0)
+    if (warp == 7) {  // cumulative log-decay (padded tokens carry g = 0)
       const float a = sG[2 * lane], b = sG[2 * lane + 1];
       float incl = a + b;
 #pragma unroll
@@ -770,7 +778,7 @@ __global__ void __launch_bounds__(NT, 1)
 
   // chunk 0: stage, start E and D3, build its Ktil^T while they run
   if (RAW) {
-    if (tid == 0) prefetch_raw(maps, GB, h, hk, lo, RW, &rbar);
+    if (tid == kCopier) prefetch_raw(maps, GB, h, hk, lo, RW, &rbar);
     if (!GB) load_gb<TI>(in, p, h, lo, min(C, len), g_next, b_next);
   }
   stage_next(0);
@@ -793,7 +801,9 @@ __global__ void __launch_bounds__(NT, 1)
     phase ^= 1;
     tc::fence_after_sync();
 
-    // F[v][t] = beta_t v_t[v] - beta_t gamma_t E[v][t] into TMEM; o part; S <- gamma_n S
+    // F[v][t] = beta_t v_t[v] - beta_t gamma_t E[v][t] into TMEM; the output's state
+    // part gamma_t (S Q^T)[v][t] into the D4 columns (the Delta^T P^T MMA adds to it);
+    // S <- gamma_n S
     const int i0 = 32 * half;
     {
       const int v = row;
@@ -842,16 +852,13 @@ __global__ void __launch_bounds__(NT, 1)
     phase ^= 1;
     tc::fence_after_sync();
 
-    // D4 = Delta^T P^T (N 64),  S += Delta^T Ktil (N 128); K = 64
+    // [D4 | S] += Delta^T [P; Ktil^T]^T: D4 (onto gamma S Q^T) and the state update in one
+    // N = 192 chain; K = 64
     if (tid == 0) {
 #pragma unroll
       for (int j = 0; j < C / 8; ++j)
         tc::mma_ts(tm + T_D4, tm + T_DD + j * 8, tc::smem_desc(pt_s + j * KSTEP, tc::kLBO, SBO_C),
-                   tc::idesc_tf32(128, 64), 1);
-#pragma unroll
-      for (int j = 0; j < C / 8; ++j)
-        tc::mma_ts(tm + T_S, tm + T_DD + j * 8, tc::smem_desc(kt_s + j * KSTEP, tc::kLBO, SBO_C),
-                   tc::idesc_tf32(128, 128), 1);
+                   tc::idesc_tf32(128, 192), 1);
       tc::mma_commit(&bar);
     }
     if (!last) stage_next(c0 + C);  // QK, XU and the scalars are free; the MMAs do not read them
@@ -880,14 +887,16 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
     if (!last) {
-      if (tid == 0) {  // the tiles are free again: fetch the next chunk's
+      if (tid == kCopier) {  // the tiles are free again: fetch the next chunk's
+        const float *src = wsq + (int64_t)(c0 / C + 1) * wstep;
         mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
-        bulk_g2s(PT, wsq + (int64_t)(c0 / C + 1) * wstep, 2 * kTileBytes, &tbar);
+        bulk_g2s(PT, src, kTileBytes, &tbar);
+        bulk_g2s(TT, src + TILE, kTileBytes, &tbar);
       }
       issue_ed3();
     }
 
-    // outputs o[t][v] = scale (gamma_t D3 + D4), this warp's half of t
+    // outputs o[t][v] = scale D4[v][t] (gamma_t S Q^T + Delta^T P^T), this warp's half of t
     {
       const int v = row;
       TO *ob = o + (lo + c0) * p.h_v * D + (int64_t)h * D + v;
