@@ -381,7 +381,9 @@ constexpr int kHeadFloats = 2 * C * AS + 1024 + 2 * C;
 template <typename TI>
 constexpr int prep_tile_bytes() { return std::is_same<TI, bf16>::value ? 128 * D * 2 : 128 * D * 4; }
 template <typename TI>
-constexpr int prep_smem() { return prep_tile_bytes<TI>() + (2 * kHeadFloats + 2 * C) * 4; }
+constexpr int prep_smem() {  // + 1024: the tile is aligned to 1024 bytes inside the allocation
+  return prep_tile_bytes<TI>() + (2 * kHeadFloats + 2 * C) * 4 + 1024;
+}
 static_assert(2 * (prep_smem<bf16>() + 1024 + 64) <= 228 * 1024, "two bf16 prep CTAs per SM");
 static_assert(prep_smem<float>() <= 227 * 1024, "shared memory");
 
@@ -392,14 +394,18 @@ static_assert(prep_smem<float>() <= 227 * 1024, "shared memory");
 template <typename TI>
 __global__ void __launch_bounds__(NT, 2)
     prep_kernel(PoolView p, SeqIndex seq, QKV in, const int32_t *__restrict__ off,
-                float *__restrict__ work) {
+                float *__restrict__ work, const __grid_constant__ InMaps maps, int raw_rows) {
   constexpr bool B16 = std::is_same<TI, bf16>::value;  // raw bf16 tile, kind::f16
+  // 16-byte aligned bf16 rows: the tile arrives by tensor-map copies in the 128-byte
+  // swizzle, two K halves [Q;K] x 64 columns (16 KiB each), read by swizzled descriptors
+  const bool TMAQK = B16 && raw_rows != 0;
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char *tile = smem;
-  float *heads = reinterpret_cast<float *>(smem + prep_tile_bytes<TI>());
+  unsigned char *tile = smem + ((1024u - (smem_addr(smem) & 1023u)) & 1023u);
+  float *heads = reinterpret_cast<float *>(tile + prep_tile_bytes<TI>());
   float *rq = heads + 2 * kHeadFloats;
   float *rk = rq + C;
   __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t lbar;   // tensor-map copies of q, k
   __shared__ uint32_t tmem_slot;
 
   const int cidx = blockIdx.x;
@@ -429,7 +435,19 @@ __global__ void __launch_bounds__(NT, 2)
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 64);
   if (tid == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&lbar, 1);
     mbar_fence_init();
+  }
+  if (TMAQK) {
+    __syncthreads();
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&lbar, 4 * kRawHalf);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        tma3(tile + hf * 2 * kRawHalf, &maps.q, 64 * hf, kh, (int)tok0, &lbar);
+        tma3(tile + hf * 2 * kRawHalf + kRawHalf, &maps.k, 64 * hf, kh, (int)tok0, &lbar);
+      }
+    }
   }
   for (int e = tt; e < C * C; e += 128) {  // T's strictly-upper 16 x 16 blocks stay zero
     const int r = e / C, c = e % C;
@@ -446,7 +464,36 @@ __global__ void __launch_bounds__(NT, 2)
   }
   const TI *q0 = static_cast<const TI *>(in.q) + tok0 * in.ld_qk + (int64_t)kh * D;
   const TI *k0 = static_cast<const TI *>(in.k) + tok0 * in.ld_qk + (int64_t)kh * D;
-  if constexpr (B16) {
+  bool loaded = true;
+  if (TMAQK) {  // norms of the tensor-map rows, summed in stage_qk_bf16's order
+    loaded = mbar_wait_bounded(&lbar, 0);
+    const int t = stage_token(), part = lane >> 3;
+    float qq = 0.f, kk = 0.f;
+    if (loaded) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int c = part + 4 * m;                  // elements 4c .. 4c+3
+        const int col = (4 * c) & 63, hf = (4 * c) >> 6;
+        const int off8 = t * 128 + ((((col >> 3) ^ (t & 7))) << 4) + (col & 7) * 2;
+        const uint2 qv = *reinterpret_cast<const uint2 *>(tile + hf * 2 * kRawHalf + off8);
+        const uint2 kv = *reinterpret_cast<const uint2 *>(tile + hf * 2 * kRawHalf + kRawHalf + off8);
+        const float a0 = __uint_as_float(qv.x << 16), a1 = __uint_as_float(qv.x & 0xffff0000u);
+        const float a2 = __uint_as_float(qv.y << 16), a3 = __uint_as_float(qv.y & 0xffff0000u);
+        const float b0 = __uint_as_float(kv.x << 16), b1 = __uint_as_float(kv.x & 0xffff0000u);
+        const float b2 = __uint_as_float(kv.y << 16), b3 = __uint_as_float(kv.y & 0xffff0000u);
+        qq += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+        kk += b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
+      }
+    }
+    qq += __shfl_xor_sync(0xffffffffu, qq, 8);
+    qq += __shfl_xor_sync(0xffffffffu, qq, 16);
+    kk += __shfl_xor_sync(0xffffffffu, kk, 8);
+    kk += __shfl_xor_sync(0xffffffffu, kk, 16);
+    if (part == 0) {
+      rq[t] = rsqrtf(qq + kL2Eps);
+      rk[t] = rsqrtf(kk + kL2Eps);
+    }
+  } else if constexpr (B16) {
     stage_qk_bf16(q0, k0, in.ld_qk, n, tile, rq, rk);
   } else {
     // normalised float32 rows; rq = rk = 1 (written through the g / beta slots)
@@ -473,10 +520,24 @@ __global__ void __launch_bounds__(NT, 2)
   const uint32_t lrow = tm + ((uint32_t)(32 * quad) << 16);
 
   // D1 = [Q;K] K^T  (M 128, N 64, K 128)
+  if (!__syncthreads_and(loaded)) {  // the q, k copies never landed
+    if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
+    mbar_wait_bounded(&lbar, 0);
+    if (warp == 0) tc::tmem_dealloc(tmem_slot, 64);
+    return;
+  }
   if (tid == 0) {
     const uint32_t a_s = smem_addr(tile);
     constexpr uint32_t KSTEP = 2 * tc::kLBO;
-    if constexpr (B16) {
+    if (TMAQK) {  // K halves of 64: 4 steps of 16 (32 bytes) inside each 128-byte row
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tc::mma_ss_f16(tm, tc::smem_desc_sw128(a_s + hf * 2 * kRawHalf + 32 * j),
+                         tc::smem_desc_sw128(a_s + hf * 2 * kRawHalf + kRawHalf + 32 * j),
+                         tc::idesc_bf16(128, 64), (hf | j) != 0);
+    } else if constexpr (B16) {
       constexpr uint32_t SBO = tc::sbo_bytes16(D);
       const uint32_t b_s = a_s + 8 * SBO;
 #pragma unroll
@@ -504,12 +565,13 @@ __global__ void __launch_bounds__(NT, 2)
       const int t = row - 64;
       const float bt = sBeta[t] * rk[t], gt = sG[t];
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        float v[16];
-        tc::tmem_ld16(lrow + 16 * cb, v);
+      for (int cp = 0; cp < 2; ++cp) {
+        float v2[32];
+        tc::tmem_ld32(lrow + 32 * cp, lrow + 32 * cp + 16, v2);
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-          const int i = 16 * cb + j;
+        for (int j2 = 0; j2 < 32; j2 += 4) {
+          const int i = 32 * cp + j2, j = j2;
+          const float *v = v2;
           float4 a;
           a.x = i + 0 < t ? bt * rk[i + 0] * __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
           a.y = i + 1 < t ? bt * rk[i + 1] * __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
@@ -522,12 +584,13 @@ __global__ void __launch_bounds__(NT, 2)
       const int t = row;
       const float qt = rq[t], gt = sG[t];
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        float v[16];
-        tc::tmem_ld16(lrow + 16 * cb, v);
+      for (int cp = 0; cp < 2; ++cp) {
+        float v2[32];
+        tc::tmem_ld32(lrow + 32 * cp, lrow + 32 * cp + 16, v2);
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-          const int i = 16 * cb + j;
+        for (int j2 = 0; j2 < 32; j2 += 4) {
+          const int i = 32 * cp + j2, j = j2;
+          const float *v = v2;
           float4 pv;
           pv.x = i + 0 <= t ? qt * rk[i + 0] * __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
           pv.y = i + 1 <= t ? qt * rk[i + 1] * __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
@@ -998,20 +1061,21 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   chunk_offsets_kernel<<<1, 1024, 0, s>>>(seq, off, nc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  InMaps maps;
+  bool gb = false;
+  const bool raw = std::is_same<TI, bf16>::value && encode_in_maps(p, seq, in, maps, gb);
   auto prep = prep_kernel<TI>;
   constexpr int prep_bytes = prep_smem<TI>();
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_bytes);
   if (e != cudaSuccess) return e;
   const int npair = (p.h_v / p.h_k + 1) / 2;
-  prep<<<dim3((unsigned)nc, p.h_k * npair), NT, prep_bytes, s>>>(p, seq, in, off, tiles);
+  prep<<<dim3((unsigned)nc, p.h_k * npair), NT, prep_bytes, s>>>(p, seq, in, off, tiles, maps,
+                                                                  raw ? 1 : 0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto kern = seq_kernel<TI, TO>;
   constexpr int smem = seq_smem<TI>();
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  InMaps maps;
-  bool gb = false;
-  const bool raw = std::is_same<TI, bf16>::value && encode_in_maps(p, seq, in, maps, gb);
   kern<<<dim3(p.h_v, seq.n_seqs), NT, smem, s>>>(p, layer, seq, in, static_cast<TO *>(o),
                                                      scale, off, nc, tiles, maps, raw ? 1 : 0,
                                                      gb ? 1 : 0, ck);
