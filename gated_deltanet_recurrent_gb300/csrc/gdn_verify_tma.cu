@@ -33,11 +33,6 @@ constexpr int O_DM = O_KQ + TMX * TMX * 4;   // decay table [9][9]
 constexpr int O_SC = O_DM + 96 * 4;          // alpha, beta, G
 constexpr int SMEM = 1024 + O_SC + 32 * 4;
 
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
 template <typename TI, typename TO, bool DEFERRED>
 __global__ void __launch_bounds__(NT)
     verify_tma_kernel(PoolView p, const __grid_constant__ CUtensorMap tmap, int layer,
@@ -184,7 +179,7 @@ __global__ void __launch_bounds__(NT)
     for (int s = 0; s < 4; ++s)
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        tc::mma_ss(tm, desc_sw128(t_s + s * SLAB + j * 32),
+        tc::mma_ss(tm, tc::smem_desc_sw128(t_s + s * SLAB + j * 32),
                    tc::smem_desc(x_s + (4 * s + j) * 2 * tc::kLBO, tc::kLBO, tc::sbo_bytes(D)),
                    tc::idesc_tf32(128, NX), (s | j) != 0);
     tc::mma_commit(&bar);
