@@ -57,6 +57,29 @@ __global__ void __launch_bounds__(NT)
     if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
     return;
   }
+  // the head's load goes out first: it does not depend on the draft counts
+  const int row0 = ((layer * p.n_slots + slot) * p.h_v + h) * D;  // tensor-map row
+  const int hk = h / (p.h_v / p.h_k);
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 32);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = tmem_slot;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, TILE);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+          "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(tile + s * SLAB)),
+          "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(32 * s), "r"(row0), "r"(smem_addr(&bar))
+          : "memory");
+  }
+
   int ap = 0;  // pending drafts replayed first (deferred commit only)
   if constexpr (DEFERRED) {
     ap = va.prev_accept[i];
@@ -80,31 +103,9 @@ __global__ void __launch_bounds__(NT)
     row = pend ? (int64_t)i * T_old + t : (int64_t)i * T_new + (t - ap);
     return pend ? prv : cur;
   };
-  const int row0 = ((layer * p.n_slots + slot) * p.h_v + h) * D;  // tensor-map row
-  const int hk = h / (p.h_v / p.h_k);
-
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 32);
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    mbar_fence_init();
-  }
   for (int e = tid; e < (NX - 2 * T) * (D / 4); e += NT) {  // zero the unused X rows
     const int r = 2 * T + e / (D / 4), c4 = e % (D / 4);
     *reinterpret_cast<float4 *>(X + tc::core_off(r, 4 * c4, D)) = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tm = tmem_slot;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar, TILE);
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-      asm volatile(
-          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-          "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(tile + s * SLAB)),
-          "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(32 * s), "r"(row0), "r"(smem_addr(&bar))
-          : "memory");
   }
 
   // ---- stage the drafts while the head is in flight
