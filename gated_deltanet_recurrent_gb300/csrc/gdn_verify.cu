@@ -129,20 +129,19 @@ __global__ void __launch_bounds__(kThreads)
                                         (int64_t)h * p.dv + r0 + rl)
                        : 0.f;
   }
-  if (tid < T) {
+  if (tid < T) {  // g_t into sG[t + 1] (summed below), alpha_t, beta_t
     int64_t tok;
     const QKV src = src_of(tid, tok);
-    sal[tid] = expf(Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h));  // alpha_t
+    const float gt = Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
+    sG[tid + 1] = gt;
+    sal[tid] = expf(gt);
     sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * p.h_v + h);
   }
-  if (tid <= T) {  // G_t = g_0 + ... + g_{t-1}
+  __syncthreads();
+  if (tid == 0) {  // G_t = g_0 + ... + g_{t-1}
     float acc = 0.f;
-    for (int t = 0; t < tid; ++t) {
-      int64_t tok;
-      const QKV src = src_of(t, tok);
-      acc += Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
-    }
-    sG[tid] = acc;
+    sG[0] = 0.f;
+    for (int t = 1; t <= T; ++t) sG[t] = (acc += sG[t]);
   }
   __syncthreads();
   // Gram scalars k_i.k_t and k_i.q_t (four lanes per pair) and the decay table

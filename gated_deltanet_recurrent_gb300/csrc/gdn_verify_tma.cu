@@ -131,20 +131,21 @@ __global__ void __launch_bounds__(NT)
       vr[t] = Elem<TI>::load1(static_cast<const TI *>(src.v) + tok * src.ld_v + (int64_t)h * D + v);
     }
   }
-  if (tid < T) {
+  if (tid < T) {  // g_t into sG[t + 1] (summed below), alpha_t, beta_t
     int64_t tok;
     const QKV src = src_of(tid, tok);
-    sal[tid] = expf(Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h));
+    const float gt = Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
+    sG[tid + 1] = gt;
+    sal[tid] = expf(gt);
     sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * p.h_v + h);
   }
-  if (tid <= T) {
+  __syncthreads();
+  if (tid == 0) {  // G_t = g_0 + ... + g_{t-1}, T <= 8 terms
     float acc = 0.f;
-    for (int t = 0; t < tid; ++t) {
-      int64_t tok;
-      const QKV src = src_of(t, tok);
-      acc += Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
-    }
-    sG[tid] = acc;
+    sG[0] = 0.f;
+#pragma unroll
+    for (int t = 1; t <= TMX; ++t)
+      if (t <= T) sG[t] = (acc += sG[t]);
   }
   __syncthreads();
   // Gram scalars (four lanes per pair) and the decay table
