@@ -223,16 +223,24 @@ __global__ void __launch_bounds__(NT)
 #pragma unroll
       for (int ii = 0; ii < TMX; ++ii) cf[ii] = ii < a ? Dm[a * (TMX + 1) + ii + 1] * dl[ii] : 0.f;
       unsigned char *rowp = tile + (v >> 3) * 1024 + (v & 7) * 128;
-#pragma unroll 4
-      for (int c = 0; c < D / 4; ++c) {
-        float4 *sp = reinterpret_cast<float4 *>(rowp + (c >> 3) * SLAB + (((c & 7) ^ (v & 7)) << 4));
-        float4 acc = scale4(c0, *sp);
+      // One 128-byte segment (8 float4, one slab) at a time: all of its loads
+      // are issued before any of its stores, since the row and X share memory.
+#pragma unroll 1
+      for (int s = 0; s < D / 32; ++s) {
+        float4 *sp = reinterpret_cast<float4 *>(rowp + s * SLAB);
+        float4 acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = scale4(c0, sp[j ^ (v & 7)]);
 #pragma unroll
         for (int ii = 0; ii < TMX; ++ii)
-          if (ii < a)
-            acc = axpby4(1.f, acc, cf[ii],
-                         *reinterpret_cast<const float4 *>(X + tc::core_off(ii, 4 * c, D)));
-        *sp = acc;
+          if (ii < a) {
+            const float *xr = X + tc::core_off(ii, 32 * s, D);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              acc[j] = axpby4(1.f, acc[j], cf[ii], *reinterpret_cast<const float4 *>(xr + 32 * j));
+          }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sp[j ^ (v & 7)] = acc[j];
       }
       tc::fence_async_smem();
     }
