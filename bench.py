@@ -5,13 +5,16 @@
 Headline (one JSON line on stdout): decode slot-steps/s for one GDN layer
 (32 value heads sharing 16 key heads, K = V = 128, fp32 state, conv_k = 4
 over 8192 channels, bf16 activations) on a 256-slot pool with 64 active slot
-ids drawn at random.  One step = gdn_conv_silu over the 64 new tokens, then
-gdn_decode_step reading q, k, v straight out of the conv output.  L2 is
-flushed (a 512 MiB write) between timed steps, outside the timed events.
+ids drawn at random.  One step = one gdn_decode_step_conv call: the conv +
+SiLU over the 64 new tokens, then the decode step reading q, k, v straight
+out of the conv output (its launch overlapping the conv).  L2 is flushed (a
+512 MiB write) between timed steps, outside the timed events.
 
 Also in the line: the same metric end to end through the C ABI with inputs
 copied from pinned host memory and outputs copied back inside the timed
-region (`e2e`), the decode kernel's HBM roofline fraction, the oracle timed
+region (`e2e`), the same step as two calls (`two_calls`: gdn_conv_silu, then
+gdn_decode_step), the decode kernel's HBM roofline fraction (timed on the
+decode launch of the two-call step), the oracle timed
 on the host cores (`cpu_baseline`), SM clocks sampled during timing, and
 `secondary` measurements: the 18-layer slot sweep (N = 1 .. 512),
 speculative verify (128 slots, T = 4) and varlen chunked prefill.
@@ -237,7 +240,14 @@ class DecodeBench:
     def flush(self):
         self.flush_buf.zero_()
 
-    def step(self, ev=None):
+    def step(self):
+        """The decode step of the layer as one call (conv + SiLU, then the
+        decode launch overlapping it)."""
+        self.abi.gdn_decode_step_conv(self.pool, 0, self.ids, self.x, self.w, self.y, self.g,
+                                      self.beta, self.o)
+
+    def step_two_calls(self, ev=None):
+        """The same step as two calls; ev brackets the decode launch."""
         a = self.abi
         a.gdn_conv_silu(self.pool, 0, self.ids, self.x, self.w, self.y)
         if ev is not None:
@@ -308,8 +318,14 @@ def sweep_bench(torch, abi, synth, device, steps):
                 abi.gdn_decode_step(pool, layer, ids, q, k, v, gs[j % sets][:N],
                                     bs[j % sets][:N], o[:N])
 
+        def one_call_step(j):
+            for layer in range(L):
+                abi.gdn_decode_step_conv(pool, layer, ids, xs[j % sets][:N], w[layer], y[:N],
+                                         gs[j % sets][:N], bs[j % sets][:N], o[:N])
+
         for j in range(3):
             one_step(j)
+            one_call_step(j)
         E = lambda: torch.cuda.Event(enable_timing=True)
 
         def timed(step_fn):
@@ -324,18 +340,25 @@ def sweep_bench(torch, abi, synth, device, steps):
             return sum(a.elapsed_time(b) for a, b in evs) / 1e3
 
         t = timed(one_step)
-        # the same 36 launches captured once into a CUDA graph and replayed
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            one_step(0)
-        torch.cuda.current_stream().wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            one_step(0)
-        graph.replay()
-        t_graph = timed(lambda j: graph.replay())
-        del graph
+        t_one = timed(one_call_step)
+
+        def graph_time(step_fn):
+            # the step's 36 launches captured once into a CUDA graph and replayed
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                step_fn(0)
+            torch.cuda.current_stream().wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step_fn(0)
+            graph.replay()
+            tg = timed(lambda j: graph.replay())
+            del graph
+            return tg
+
+        t_graph = graph_time(one_step)
+        t_one_graph = graph_time(one_call_step)
         slot_steps = N * steps
         out.append({"n_active": N, "slot_steps_per_s": slot_steps / t,
                     "slot_layer_steps_per_s": slot_steps * L / t,
@@ -343,12 +366,17 @@ def sweep_bench(torch, abi, synth, device, steps):
                     "ms_per_step": t / steps * 1e3,
                     "graph_slot_steps_per_s": slot_steps / t_graph,
                     "graph_state_gbs": slot_steps * L * STATE_BYTES_PER_SLOT_LAYER / t_graph / 1e9,
-                    "graph_ms_per_step": t_graph / steps * 1e3})
+                    "graph_ms_per_step": t_graph / steps * 1e3,
+                    "one_call_slot_steps_per_s": slot_steps / t_one,
+                    "one_call_graph_slot_steps_per_s": slot_steps / t_one_graph,
+                    "one_call_graph_ms_per_step": t_one_graph / steps * 1e3})
     del pool
     return {"workload": "18 stacked GDN layers (decode-step layer shape), 512-slot pool, "
                         f"N active, {steps} decode steps per N, conv+decode per layer, "
                         "L2 flushed between steps; graph_* = the step's 36 launches replayed "
-                        "from one CUDA graph (inputs of step 0 each time)", "points": out}
+                        "from one CUDA graph (inputs of step 0 each time); one_call_* = each "
+                        "layer as one gdn_decode_step_conv call (decode launch overlapping "
+                        "the conv)", "points": out}
 
 
 def verify_bench(torch, abi, synth, device, steps, peak):
@@ -493,6 +521,7 @@ def run_gpu(args, rank, world):
     b = DecodeBench(torch, abi, synth, device)
     for _ in range(max(3, args.warmup)):
         b.step()
+        b.step_two_calls()
         b.step_e2e()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
@@ -505,7 +534,9 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
 
     barrier()
-    t_dev, t_kernel = b.timed(b.step, args.steps, kernel_events=True)
+    t_dev, _ = b.timed(b.step, args.steps)
+    barrier()
+    t_two, t_kernel = b.timed(b.step_two_calls, args.steps, kernel_events=True)
     barrier()
     t_e2e, _ = b.timed(b.step_e2e, args.steps)
     barrier()
@@ -520,7 +551,8 @@ def run_gpu(args, rank, world):
     time.sleep(0.2)
     clk = clocks.stop()
     if dist is not None:
-        t_dev, t_e2e, t_kernel = max_over_ranks([t_dev, t_e2e, t_kernel], dist, device)
+        t_dev, t_e2e, t_two, t_kernel = max_over_ranks([t_dev, t_e2e, t_two, t_kernel], dist,
+                                                       device)
     if rank != 0:
         return None
 
@@ -538,14 +570,21 @@ def run_gpu(args, rank, world):
                    f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": units / t_e2e, "unit": UNIT, "h2d_bytes_per_step": b.h2d,
                 "d2h_bytes_per_step": b.d2h,
-                "note": "pinned host x, g, beta -> device, conv + decode, o -> pinned host"},
+                "note": "pinned host x, g, beta -> device, one-call conv + decode, "
+                        "o -> pinned host"},
+        "two_calls": {"value": units / t_two, "unit": UNIT,
+                      "ms_per_step": t_two / args.steps * 1e3,
+                      "note": "the same step as gdn_conv_silu then gdn_decode_step, "
+                              "an event between them"},
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "hbm", "kernel": "gdn decode_kernel<128, bf16, float>",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(),
                      "peak_kind": f"{peak_kind} (HBM copy, burst)",
                      "algorithmic_bytes_per_launch": DECODE_KERNEL_BYTES_PER_SLOT * b.n,
-                     "kernel_us": kernel_avg * 1e6},
+                     "kernel_us": kernel_avg * 1e6,
+                     "timed_on": "the decode launch of the two-call step (events between "
+                                 "the launches; the one-call step overlaps them)"},
         "clocks": clk,
     }
     if secondary:

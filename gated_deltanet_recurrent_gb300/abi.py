@@ -24,6 +24,7 @@ DEVERR_SLOT, DEVERR_SEQ, DEVERR_COUNT, DEVERR_TIMEOUT = 1, 2, 4, 8
 EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "gdn_pool_reset",
             "gdn_pool_copy",
             "gdn_pool_destroy", "gdn_pool_get_error", "gdn_conv_silu", "gdn_decode_step",
+            "gdn_decode_step_conv",
             "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
             "gdn_spec_verify_deferred", "gdn_prefill_chunked_noalloc", "gdn_prefill_chunked_ckpt",
             "gdn_status_string",
@@ -78,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gdn_conv_silu": (st, [vp, i32, vp, vp, i32, i32, i32, vp, i64, st, vp, vp, vp, i64,
                                vp, vp]),
         "gdn_decode_step": (st, [vp, i32, vp, i32, P(gdn_qkv), vp, st, ctypes.c_float, vp]),
+        "gdn_decode_step_conv": (st, [vp, i32, vp, i32, vp, i64, vp, vp, vp, i64, vp, vp, st,
+                                      vp, st, ctypes.c_float, vp]),
         "gdn_prefill_chunked": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
                                      ctypes.c_float, vp]),
         "gdn_prefill_recurrent": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
@@ -269,6 +272,31 @@ def gdn_decode_step(pool: Pool, layer: int, slot_ids: torch.Tensor, q, k, v, g, 
     _check(load_library().gdn_decode_step(pool.handle, layer, _idx(slot_ids, "slot_ids"),
                                           slot_ids.numel(), ctypes.byref(inp), _ptr(o),
                                           _dt(o), scale, _stream(stream)))
+    return o
+
+
+def gdn_decode_step_conv(pool: Pool, layer: int, slot_ids: torch.Tensor, x: torch.Tensor,
+                         w: torch.Tensor, y: torch.Tensor, g, beta, o: torch.Tensor, bias=None,
+                         scale: float = 1.0, stream=None):
+    """conv + SiLU then the decode step in one call.  x, y [n, conv_ch] (row
+    stride may exceed conv_ch; y is split into q | k | v); w [conv_ch, conv_k]
+    float32; g, beta [n, h_v] in x's dtype; o [n, h_v, dv]."""
+    n = slot_ids.numel()
+    if w.dtype != torch.float32 or not w.is_contiguous():
+        raise GDNError(1, "w must be contiguous float32 [conv_ch, conv_k]")
+    for name, t in (("x", x), ("y", y)):
+        if t.dim() != 2 or t.stride(1) != 1 or t.shape[0] != n:
+            raise GDNError(1, f"{name} must be [n, channels] with unit channel stride")
+    for name, t in (("g", g), ("beta", beta)):
+        if t.shape != (n, pool.desc.h_v) or not t.is_contiguous():
+            raise GDNError(5, f"{name} must be contiguous [n, {pool.desc.h_v}]")
+    dts = {_dt(t) for t in (x, y, g, beta)}
+    if len(dts) != 1:
+        raise GDNError(4, "x, y, g and beta must share one dtype")
+    _check(load_library().gdn_decode_step_conv(
+        pool.handle, layer, _idx(slot_ids, "slot_ids"), n, _ptr(x), x.stride(0), _ptr(w),
+        _ptr(bias), _ptr(y), y.stride(0), _ptr(g), _ptr(beta), dts.pop(), _ptr(o), _dt(o), scale,
+        _stream(stream)))
     return o
 
 

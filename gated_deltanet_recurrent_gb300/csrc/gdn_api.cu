@@ -412,6 +412,50 @@ gdn_status gdn_decode_step(gdn_pool *p, int32_t layer, const int32_t *slot_ids, 
   return ok();
 }
 
+gdn_status gdn_decode_step_conv(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
+                                int32_t n, const void *x, int64_t ld_x, const float *w,
+                                const float *bias, void *y, int64_t ld_y, const void *g,
+                                const void *beta, gdn_dtype dtype, void *o, gdn_dtype o_dtype,
+                                float scale, gdn_stream stream) {
+  gdn_status st = check_pool(p, layer);
+  if (st != GDN_OK) return st;
+  if (n < 0) return fail(GDN_ERR_ARG, "n = %d < 0", n);
+  if (n == 0) return ok();
+  if (n > 65535) return fail(GDN_ERR_SIZE, "n = %d > 65535", n);
+  const gdn_pool_desc &d = p->desc;
+  const int64_t C = d.conv_ch, nqk = (int64_t)d.h_k * d.dk;
+  if (C != 2 * nqk + (int64_t)d.h_v * d.dv)
+    return fail(GDN_ERR_SIZE, "conv_ch = %lld is not 2*h_k*dk + h_v*dv = %lld", (long long)C,
+                (long long)(2 * nqk + (int64_t)d.h_v * d.dv));
+  if (dtype != d.conv_dtype) return fail(GDN_ERR_DTYPE, "dtype differs from the pool's conv_dtype");
+  if (!dtype_ok(o_dtype)) return fail(GDN_ERR_DTYPE, "o dtype must be F32 or BF16");
+  if (!slot_ids || !x || !w || !y || !o)
+    return fail(GDN_ERR_ARG, "slot_ids, x, w, y and o must be non-NULL");
+  if (ld_x == 0) ld_x = C;
+  if (ld_y == 0) ld_y = C;
+  if (ld_x < C || ld_y < C) return fail(GDN_ERR_ARG, "row strides smaller than conv_ch");
+  const size_t es = dtype_size(dtype);
+  unsigned char *yb = static_cast<unsigned char *>(y);
+  const gdn_qkv in{yb, yb + nqk * es, yb + 2 * nqk * es, g, beta, ld_y, ld_y, dtype};
+  gdn::QKV q;
+  if ((st = resolve_qkv(p, &in, n, q))) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d.host_checks) {
+    if ((st = check_slots(p, slot_ids, n, s)) || (st = check_device_ptr(x, "x")) ||
+        (st = check_device_ptr(w, "w")) || (bias && (st = check_device_ptr(bias, "bias"))) ||
+        (st = check_device_ptr(o, "o")))
+      return st;
+  }
+  gdn::SeqIndex seq{slot_ids, nullptr, n, n};
+  cudaError_t e = gdn::launch_conv_silu(p->view, layer, seq, 1, x, ld_x, w, bias, y, ld_y,
+                                        nullptr, s);
+  if (e != cudaSuccess) return cuda_fail(e, "conv launch");
+  e = gdn::launch_decode(p->view, p->has_tmap ? &p->tmap : nullptr, layer, slot_ids, n, q, o,
+                         o_dtype, scale, s, /*after_conv=*/true);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return ok();
+}
+
 gdn_status gdn_spec_verify(gdn_pool *p, int32_t layer, const int32_t *slot_ids, int32_t n,
                            int32_t T, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
                            const int32_t *accept_len, float scale, gdn_stream stream) {

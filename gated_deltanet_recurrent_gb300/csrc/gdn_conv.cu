@@ -6,6 +6,9 @@
 // Token blocks of one sequence run in parallel; only block 0 reads the old
 // cache (kTokBlock >= conv_k - 1), and the same thread writes the new cache
 // after it has read the old one, so one launch updates caches in place.
+// Each conv CTA first allows a programmatic dependent launch that follows it
+// (the decode of the same step) to start; such a dependent waits for the conv
+// grid to complete before it reads anything the conv writes.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -20,6 +23,7 @@ __global__ void __launch_bounds__(kConvThreads)
     conv_silu_kernel(PoolView p, int layer, SeqIndex seq, const T *__restrict__ x, int64_t ld_x,
                      const float *__restrict__ w, const float *__restrict__ bias,
                      T *__restrict__ y, int64_t ld_y, const int32_t *__restrict__ advance) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int c = blockIdx.x * kConvThreads + threadIdx.x;
   const int i = blockIdx.z;
   const int slot = seq.slot_ids[i];
@@ -140,6 +144,7 @@ __global__ void __launch_bounds__(kConvThreads)
                          int64_t ld_x, const float *__restrict__ w,
                          const float *__restrict__ bias, T *__restrict__ y, int64_t ld_y,
                          const int32_t *__restrict__ advance) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int V = Vec16<T>::N;
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * V;
   const int i = blockIdx.z;

@@ -24,7 +24,10 @@ using rows::dispatch;
 // its whole tile in flight from its first cycle while its threads normalise
 // q and k; rows are then read from shared memory, updated, and stored back
 // with 128-bit streaming stores.  grid (ceil(dv / R), h_v, n).
-template <int DK, typename TI, typename TO>
+// AFTER_CONV: launched as a programmatic dependent of the conv that writes q,
+// k and v; the tile fetch is issued before the grid-dependency wait, every
+// read of the token inputs after it.
+template <int DK, typename TI, typename TO, bool AFTER_CONV>
 __global__ void __launch_bounds__(kThreads)
     decode_bulk_kernel(PoolView p, int layer, const int32_t *__restrict__ slot_ids, QKV in,
                        TO *__restrict__ o, float scale) {
@@ -58,6 +61,9 @@ __global__ void __launch_bounds__(kThreads)
     mbar_arrive_expect_tx(&bar, bytes);
     bulk_g2s(tile, S, bytes, &bar);
   }
+  // Returns once the prerequisite grid has completed and its memory is
+  // visible (immediately when there is none).
+  if (AFTER_CONV) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int lane = tid & 31, warp = tid >> 5;
   const int sub = lane % LPR, grp = lane / LPR;
@@ -122,19 +128,34 @@ __global__ void __launch_bounds__(kThreads)
 
 template <int DK, typename TI, typename TO>
 cudaError_t launch_decode_t(const PoolView &p, int layer, const int32_t *slot_ids, int n,
-                            const QKV &in, void *o, float scale, cudaStream_t s) {
-constexpr int R = kBulkBytes / (DK * 4);
+                            const QKV &in, void *o, float scale, cudaStream_t s,
+                            bool after_conv) {
+  constexpr int R = kBulkBytes / (DK * 4);
   dim3 grid((p.dv + R - 1) / R, p.h_v, n);
-  decode_bulk_kernel<DK, TI, TO><<<grid, kThreads, 0, s>>>(p, layer, slot_ids, in,
-                                                             static_cast<TO *>(o), scale);
-  return cudaGetLastError();
+  if (!after_conv) {
+    decode_bulk_kernel<DK, TI, TO, false><<<grid, kThreads, 0, s>>>(p, layer, slot_ids, in,
+                                                                    static_cast<TO *>(o), scale);
+    return cudaGetLastError();
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_bulk_kernel<DK, TI, TO, true>, p, layer, slot_ids, in,
+                            static_cast<TO *>(o), scale);
 }
 
 template <int DK, typename TI, typename TO>
 struct DecodeF {
   static cudaError_t run(const PoolView &p, int layer, const int32_t *slot_ids, int n,
-                         const QKV &in, void *o, float scale, cudaStream_t s) {
-    return launch_decode_t<DK, TI, TO>(p, layer, slot_ids, n, in, o, scale, s);
+                         const QKV &in, void *o, float scale, cudaStream_t s, bool after_conv) {
+    return launch_decode_t<DK, TI, TO>(p, layer, slot_ids, n, in, o, scale, s, after_conv);
   }
 };
 
@@ -142,13 +163,14 @@ struct DecodeF {
 
 cudaError_t launch_decode(const PoolView &p, const void *tmap, int layer,
                           const int32_t *slot_ids, int n, const QKV &in, void *o,
-                          gdn_dtype o_dtype, float scale, cudaStream_t s) {
+                          gdn_dtype o_dtype, float scale, cudaStream_t s, bool after_conv) {
   // The tensor-map path of the verify kernel (T = 1, always committing) computes
   // the same step but keeps 64 KiB per CTA in flight, three CTAs per SM; the
   // 16 KiB bulk tiles above sustain more bytes in flight per SM, so decode
   // does not use the map.
   (void)tmap;
-  return dispatch<DecodeF>(p.dk, in.dtype, o_dtype, p, layer, slot_ids, n, in, o, scale, s);
+  return dispatch<DecodeF>(p.dk, in.dtype, o_dtype, p, layer, slot_ids, n, in, o, scale, s,
+                           after_conv);
 }
 
 }  // namespace gdn

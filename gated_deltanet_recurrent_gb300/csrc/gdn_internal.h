@@ -64,9 +64,16 @@ cudaError_t launch_conv_silu(const PoolView &p, int layer, const SeqIndex &seq,
                              const float *w, const float *bias, void *y, int64_t ld_y,
                              const int32_t *advance, cudaStream_t s);
 
+// The conv kernels let a programmatic dependent launch that follows them start
+// as soon as every conv CTA is running.  after_conv: launch the decode kernel
+// as such a dependent of the kernel before it on `s`; it fetches its state
+// tiles first and reads q, k, v, g and beta only once that kernel has completed
+// and its writes are visible.  Only for a decode whose preceding launch on `s`
+// is the conv of the same step (it writes neither the state nor slot_ids).
 cudaError_t launch_decode(const PoolView &p, const void *tmap, int layer,
                           const int32_t *slot_ids, int n, const QKV &in, void *o,
-                          gdn_dtype o_dtype, float scale, cudaStream_t s);
+                          gdn_dtype o_dtype, float scale, cudaStream_t s,
+                          bool after_conv = false);
 
 // Speculative verify of T new drafts per slot.  Normal mode: commit at
 // accept_len[i] (or after all T with commit_all).  Deferred mode (prev.q set):

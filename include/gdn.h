@@ -183,6 +183,28 @@ gdn_status gdn_decode_step(gdn_pool *pool, int32_t layer, const int32_t *slot_id
                            const gdn_qkv *in, void *o, gdn_dtype o_dtype, float scale,
                            gdn_stream stream);
 
+/* The whole decode step of one layer in one call: gdn_conv_silu in decode
+ * mode (one token per slot) on x, writing y, then gdn_decode_step reading q,
+ * k and v out of y (b70-optimization-lab research plan, "What the research
+ * found": batch-1 decode is latency- and launch-bound, so conv, SiLU and the
+ * q/k norm are folded into the decode call).  y: [n][conv_ch] in `dtype` with
+ * row stride ld_y (0: conv_ch), split as q = y[:, 0 : h_k*dk],
+ * k = y[:, h_k*dk : 2*h_k*dk], v = y[:, 2*h_k*dk :]; the pool's conv_ch must
+ * be 2*h_k*dk + h_v*dv (else GDN_ERR_SIZE).  x: [n][conv_ch] with row stride
+ * ld_x (0: conv_ch); x, y, g and beta are all in `dtype`, which must be the
+ * pool's conv_dtype (else GDN_ERR_DTYPE); w, bias as in gdn_conv_silu; o, g,
+ * beta, scale as in gdn_decode_step.  Results, cache and state are those of
+ * the two calls made one after the other.  The decode launch overlaps the
+ * conv: it is a programmatic dependent launch that fetches its state tiles
+ * (which the conv does not touch) before it waits for the conv grid to
+ * complete and reads y.  Caller owns every buffer; on an error nothing is
+ * launched. */
+gdn_status gdn_decode_step_conv(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
+                                int32_t n, const void *x, int64_t ld_x, const float *w,
+                                const float *bias, void *y, int64_t ld_y, const void *g,
+                                const void *beta, gdn_dtype dtype, void *o, gdn_dtype o_dtype,
+                                float scale, gdn_stream stream);
+
 /* Chunked prefill of packed variable-length sequences (b70-optimization-lab
  * research plan, "What the research found": the chunked delta rule with the
  * (I+A)^{-1} UT transform; ai-infra-handbooks Qwen3.5 project, "What to do",
