@@ -17,7 +17,9 @@ Sources (page title and section):
   [P3] ai-infra-handbooks, "Project: adding the hybrid model Qwen3.5":
        "What to do", State row -- one conv cache and one recurrent state per
        request slot, zero for a new request, carried across chunked-prefill
-       chunks.
+       chunks.  "Why it is worth doing" names the model's two kinds of
+       RMSNorm; the output one (gated_rmsnorm below) is not written out
+       there, so its formula is a reading (see that function).
 
 The pages name the recurrence but never write it out.  The rule used is the
 gated delta rule of Gated DeltaNet, for each value head:
@@ -195,6 +197,26 @@ def spec_verify(S0, q, k, v, g, beta, accept_len=None, scale=1.0, eps=L2_EPS):
         if t + 1 == a:
             keep = S.copy()
     return o, keep
+
+
+# ------------------------------------------------------ output gated RMSNorm
+
+def gated_rmsnorm(o, z, w, eps=1e-6):
+    """Output gated RMSNorm of a GDN layer [P3, "Why it is worth doing": the
+    model has two kinds of RMSNorm; the formula is not printed there].
+    Reading: each row (one token, one value head) of o is divided by its root
+    mean square over the last axis (eps added inside the square root), scaled
+    by the per-channel weight w and gated by SiLU of the matching row of z.
+    o, z [..., d]; w [d]."""
+    o, z, w = _f64(o), _f64(z), _f64(w)
+    out = np.empty_like(o)
+    rows_o = o.reshape(-1, o.shape[-1])
+    rows_z = z.reshape(-1, z.shape[-1])
+    rows_out = out.reshape(-1, o.shape[-1])
+    for r in range(rows_o.shape[0]):
+        mean_square = np.mean(rows_o[r] * rows_o[r])
+        rows_out[r] = rows_o[r] / np.sqrt(mean_square + eps) * w * silu(rows_z[r])
+    return out
 
 
 # -------------------------------------------------------------------- the pool

@@ -21,6 +21,10 @@ Map (oracle function -> pins):
                   prefix it closes; outputs and final state equal prefill
   OraclePool      N slots == each alone; reset == fresh; prefill split
                   invariance across pieces (chunked-prefill state carry)
+  gated_rmsnorm   rows of unit root mean square reduce to o * w * silu(z)
+                  with silu from scipy's expit; scale invariance (eps = 0);
+                  unit mean square of out / (w silu(z)); z = 0 gives 0; a
+                  zero row with eps > 0 gives 0; planted mistakes are caught
 """
 import os
 from fractions import Fraction
@@ -580,3 +584,60 @@ def test_pool_prefill_checkpoints_are_prefix_states():
             np.testing.assert_allclose(a.S[0, d], S_ref, rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(a.S[0, [3, 4]], S0[0, [3, 4]])
 
+
+
+# ----------------------------------------------------------- gated RMSNorm
+
+def test_gated_rmsnorm_reduces_to_the_gate_on_unit_rms_rows():
+    """Rows of +-1 have root mean square 1, so with eps = 0 the norm is the
+    identity and the result is o * w * z * expit(z) (scipy's logistic)."""
+    from scipy.special import expit
+    rng = np.random.default_rng(90)
+    o = rng.choice([-1.0, 1.0], size=(5, 3, 24))
+    z = rng.standard_normal((5, 3, 24)) * 3
+    w = rng.standard_normal(24)
+    np.testing.assert_allclose(O.gated_rmsnorm(o, z, w, eps=0.0), o * w * z * expit(z),
+                               rtol=1e-13, atol=1e-15)
+
+
+def test_gated_rmsnorm_invariants():
+    rng = np.random.default_rng(91)
+    o = rng.standard_normal((7, 40))
+    z = rng.standard_normal((7, 40))
+    w = rng.uniform(0.5, 2.0, 40)
+    out = O.gated_rmsnorm(o, z, w, eps=0.0)
+    # scale invariance of the norm
+    np.testing.assert_allclose(O.gated_rmsnorm(4.25 * o, z, w, eps=0.0), out, rtol=1e-13)
+    # divided by the weight and the gate, every row has mean square exactly 1
+    from scipy.special import expit
+    normed = out / (w * z * expit(z))
+    np.testing.assert_allclose(np.mean(normed ** 2, axis=-1), 1.0, rtol=1e-12)
+    # a closed gate (z = 0) gives zero; a zero row with eps > 0 gives zero
+    assert np.all(O.gated_rmsnorm(o, np.zeros_like(z), w) == 0.0)
+    assert np.all(O.gated_rmsnorm(np.zeros_like(o), z, w, eps=1e-6) == 0.0)
+
+
+def test_gated_rmsnorm_pins_catch_planted_mistakes():
+    """A sum instead of a mean, a sigmoid gate, or a dropped weight each break
+    one of the pins above."""
+    from scipy.special import expit
+    rng = np.random.default_rng(92)
+    o = rng.choice([-1.0, 1.0], size=(3, 16))
+    z = rng.standard_normal((3, 16))
+    w = rng.uniform(0.5, 2.0, 16)
+    want = o * w * z * expit(z)
+
+    def sum_not_mean(o, z, w, eps=1e-6):
+        o, z = np.asarray(o, float), np.asarray(z, float)
+        return o / np.sqrt(np.sum(o * o, -1, keepdims=True) + eps) * w * O.silu(z)
+
+    def sigmoid_gate(o, z, w, eps=1e-6):
+        o, z = np.asarray(o, float), np.asarray(z, float)
+        return o / np.sqrt(np.mean(o * o, -1, keepdims=True) + eps) * w * expit(z)
+
+    def no_weight(o, z, w, eps=1e-6):
+        o, z = np.asarray(o, float), np.asarray(z, float)
+        return o / np.sqrt(np.mean(o * o, -1, keepdims=True) + eps) * O.silu(z)
+
+    for wrong in (sum_not_mean, sigmoid_gate, no_weight):
+        assert not np.allclose(wrong(o, z, w, eps=0.0), want, rtol=1e-6), wrong.__name__
