@@ -17,7 +17,8 @@ gdn_decode_step), the decode kernel's HBM roofline fraction (timed on the
 decode launch of the two-call step), the oracle timed
 on the host cores (`cpu_baseline`), SM clocks sampled during timing, and
 `secondary` measurements: the 18-layer slot sweep (N = 1 .. 512),
-speculative verify (128 slots, T = 4) and varlen chunked prefill.
+speculative verify (128 slots, T = 4), varlen chunked prefill and the output
+gated RMSNorm.
 
 --impl reference times the float64 CPU oracle on a bounded sample of the same
 workload (the pages publish no runnable implementation of this path).
@@ -60,8 +61,9 @@ def _parse():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--sweep-steps", type=int, default=128)
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--sections", default="sweep,verify,prefill",
-                    help="secondary measurements to run (comma list of sweep, verify, prefill)")
+    ap.add_argument("--sections", default="sweep,verify,prefill,norm",
+                    help="secondary measurements to run (comma list of sweep, verify, prefill, "
+                         "norm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -437,6 +439,33 @@ def verify_bench(torch, abi, synth, device, steps, peak):
             "deferred_hbm_frac": per_def / t_def / 1e9 / peak}
 
 
+def norm_bench(torch, abi, device, steps, peak):
+    """Output gated RMSNorm over 16,384 tokens x 32 value heads x 128: o fp32,
+    z and y bf16 (512 MiB per call, larger than L2, so no flush)."""
+    rows, d = 16384 * 32, 128
+    gen = torch.Generator(device=device).manual_seed(5)
+    o = 0.3 * torch.randn(rows, d, device=device, generator=gen)
+    z = (2.0 * torch.randn(rows, d, device=device, generator=gen)).to(torch.bfloat16)
+    w = 0.5 + torch.rand(d, device=device, generator=gen)
+    y = torch.empty(rows, d, device=device, dtype=torch.bfloat16)
+    for _ in range(3):
+        abi.gdn_gated_rmsnorm(o, z, w, y)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [(E(), E()) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record()
+        abi.gdn_gated_rmsnorm(o, z, w, y)
+        b.record()
+    torch.cuda.synchronize()
+    t = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+    nbytes = rows * d * (4 + 2 + 2) + d * 4
+    return {"workload": "output gated RMSNorm, 16384 tokens x 32 value heads x 128, o fp32, "
+                        "z and y bf16 (512 MiB per call > L2)",
+            "us_per_call": t * 1e6, "algorithmic_gbs": nbytes / t / 1e9,
+            "hbm_frac": nbytes / t / 1e9 / peak}
+
+
 def prefill_bench(torch, abi, synth, device, steps):
     wl = synth.prefill_workload(seed=3)
     s = wl["shape"]
@@ -551,6 +580,8 @@ def run_gpu(args, rank, world):
         secondary["verify"] = verify_bench(torch, abi, synth, device, 50, peak)
     if "prefill" in sections:
         secondary["prefill"] = prefill_bench(torch, abi, synth, device, 5)
+    if "norm" in sections:
+        secondary["norm"] = norm_bench(torch, abi, device, 20, peak)
     time.sleep(0.2)
     clk = clocks.stop()
     if dist is not None:

@@ -24,7 +24,7 @@ DEVERR_SLOT, DEVERR_SEQ, DEVERR_COUNT, DEVERR_TIMEOUT = 1, 2, 4, 8
 EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "gdn_pool_reset",
             "gdn_pool_copy",
             "gdn_pool_destroy", "gdn_pool_get_error", "gdn_conv_silu", "gdn_decode_step",
-            "gdn_decode_step_conv",
+            "gdn_decode_step_conv", "gdn_gated_rmsnorm",
             "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
             "gdn_spec_verify_deferred", "gdn_prefill_chunked_noalloc", "gdn_prefill_chunked_ckpt",
             "gdn_status_string",
@@ -81,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gdn_decode_step": (st, [vp, i32, vp, i32, P(gdn_qkv), vp, st, ctypes.c_float, vp]),
         "gdn_decode_step_conv": (st, [vp, i32, vp, i32, vp, i64, vp, vp, vp, i64, vp, vp, st,
                                       vp, st, ctypes.c_float, vp]),
+        "gdn_gated_rmsnorm": (st, [i64, i32, vp, st, vp, st, vp, ctypes.c_float, vp, st, vp]),
         "gdn_prefill_chunked": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
                                      ctypes.c_float, vp]),
         "gdn_prefill_recurrent": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
@@ -298,6 +299,24 @@ def gdn_decode_step_conv(pool: Pool, layer: int, slot_ids: torch.Tensor, x: torc
         _ptr(bias), _ptr(y), y.stride(0), _ptr(g), _ptr(beta), dts.pop(), _ptr(o), _dt(o), scale,
         _stream(stream)))
     return o
+
+
+def gdn_gated_rmsnorm(o: torch.Tensor, z: torch.Tensor, w: torch.Tensor,
+                      y: Optional[torch.Tensor] = None, eps: float = 1e-6, stream=None):
+    """Output gated RMSNorm over the last axis: o, z, y [..., d] contiguous
+    (each float32 or bf16; y defaults to float32), w [d] float32."""
+    d = o.shape[-1]
+    if y is None:
+        y = torch.empty(o.shape, dtype=torch.float32, device=o.device)
+    for name, t in (("o", o), ("z", z), ("y", y)):
+        if t.shape != o.shape or not t.is_contiguous():
+            raise GDNError(1, f"{name} must be contiguous with o's shape {tuple(o.shape)}")
+    if w.dtype != torch.float32 or not w.is_contiguous() or w.numel() != d:
+        raise GDNError(1, f"w must be contiguous float32 [{d}]")
+    _check(load_library().gdn_gated_rmsnorm(o.numel() // max(d, 1), d, _ptr(o), _dt(o), _ptr(z),
+                                            _dt(z), _ptr(w), eps, _ptr(y), _dt(y),
+                                            _stream(stream)))
+    return y
 
 
 def gdn_prefill_chunked(pool: Pool, layer: int, slot_ids: torch.Tensor,

@@ -5,6 +5,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <cmath>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -453,6 +454,23 @@ gdn_status gdn_decode_step_conv(gdn_pool *p, int32_t layer, const int32_t *slot_
   e = gdn::launch_decode(p->view, p->has_tmap ? &p->tmap : nullptr, layer, slot_ids, n, q, o,
                          o_dtype, scale, s, /*after_conv=*/true);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return ok();
+}
+
+gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t d, const void *o, gdn_dtype o_dtype,
+                             const void *z, gdn_dtype z_dtype, const float *w, float eps,
+                             void *y, gdn_dtype y_dtype, gdn_stream stream) {
+  if (rows < 0) return fail(GDN_ERR_ARG, "rows = %lld < 0", (long long)rows);
+  if (d < 1) return fail(GDN_ERR_ARG, "d = %d < 1", d);
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(GDN_ERR_ARG, "eps must be finite and >= 0");
+  if (!dtype_ok(o_dtype) || !dtype_ok(z_dtype) || !dtype_ok(y_dtype))
+    return fail(GDN_ERR_DTYPE, "o, z and y dtypes must be F32 or BF16");
+  if (rows == 0) return ok();
+  if (!o || !z || !w || !y) return fail(GDN_ERR_ARG, "o, z, w and y must be non-NULL");
+  if (rows > INT64_MAX / d) return fail(GDN_ERR_SIZE, "rows * d overflows");
+  cudaError_t e = gdn::launch_gated_rmsnorm(o, o_dtype, z, z_dtype, w, eps, y, y_dtype, rows, d,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gated RMSNorm launch");
   return ok();
 }
 

@@ -56,6 +56,12 @@ struct Checkpoints {
 cudaError_t launch_pool_reset(const PoolView &p, const int32_t *slot_ids, int n,
                               cudaStream_t s);
 
+// y[r][j] = o[r][j] * rsqrt(mean_j o[r][j]^2 + eps) * w[j] * silu(z[r][j]) over
+// rows x d contiguous elements.
+cudaError_t launch_gated_rmsnorm(const void *o, gdn_dtype ot, const void *z, gdn_dtype zt,
+                                 const float *w, float eps, void *y, gdn_dtype yt, int64_t rows,
+                                 int d, cudaStream_t s);
+
 cudaError_t launch_pool_copy(const PoolView &p, const int32_t *src, const int32_t *dst, int n,
                              cudaStream_t s);
 

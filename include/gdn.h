@@ -205,6 +205,20 @@ gdn_status gdn_decode_step_conv(gdn_pool *pool, int32_t layer, const int32_t *sl
                                 const void *beta, gdn_dtype dtype, void *o, gdn_dtype o_dtype,
                                 float scale, gdn_stream stream);
 
+/* Output gated RMSNorm of the layer (ai-infra-handbooks Qwen3.5 project, "Why
+ * it is worth doing": the model's two kinds of RMSNorm; the formula is not
+ * written out there, and the one used is the plain reading): for each of
+ * `rows` rows (one token and value head each) of d elements,
+ *     y[r][j] = o[r][j] / sqrt(mean_j o[r][j]^2 + eps) * w[j] * silu(z[r][j]).
+ * o (the recurrence output), z (the gate), y: [rows][d] contiguous, each in
+ * its own dtype (GDN_F32 or GDN_BF16); w: [d] float32; eps >= 0 and finite
+ * (a row of zeros needs eps > 0).  y may not overlap o or z.  No pool is
+ * involved.  rows == 0 is a no-op; d < 1, a NULL pointer or a bad dtype is
+ * GDN_ERR_ARG / GDN_ERR_DTYPE and nothing is launched. */
+gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t d, const void *o, gdn_dtype o_dtype,
+                             const void *z, gdn_dtype z_dtype, const float *w, float eps,
+                             void *y, gdn_dtype y_dtype, gdn_stream stream);
+
 /* Chunked prefill of packed variable-length sequences (b70-optimization-lab
  * research plan, "What the research found": the chunked delta rule with the
  * (I+A)^{-1} UT transform; ai-infra-handbooks Qwen3.5 project, "What to do",
