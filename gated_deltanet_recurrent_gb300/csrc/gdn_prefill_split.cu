@@ -809,13 +809,13 @@ __global__ void __launch_bounds__(NT, 1)
       const float4 x = *reinterpret_cast<const float4 *>(QK + tc::core_off(64 + i, 4 * k4, D));
       const float d = sDte[i];
       const float v0 = d * x.x, v1 = d * x.y, v2 = d * x.z, v3 = d * x.w;
-      // round 1 (xor 2): lanes 0,1 keep columns 0,1 and take rows 2,3's; lanes 2,3 the rest
+      // stage 1 (xor 2): lanes 0,1 keep columns 0,1 and take rows 2,3's; lanes 2,3 the rest
       const bool hi2 = (l4 & 2) != 0;
       const float r0 = __shfl_xor_sync(0xffffffffu, hi2 ? v0 : v2, 2);
       const float r1 = __shfl_xor_sync(0xffffffffu, hi2 ? v1 : v3, 2);
       const float a0 = hi2 ? r0 : v0, a1 = hi2 ? r1 : v1;
       const float a2 = hi2 ? v2 : r0, a3 = hi2 ? v3 : r1;
-      // round 2 (xor 1): 2 x 2 transposes
+      // stage 2 (xor 1): 2 x 2 transposes
       const bool hi1 = (l4 & 1) != 0;
       const float s0 = __shfl_xor_sync(0xffffffffu, hi1 ? a0 : a1, 1);
       const float s1 = __shfl_xor_sync(0xffffffffu, hi1 ? a2 : a3, 1);

@@ -63,7 +63,7 @@ typedef enum {
   GDN_ERR_DUP_SLOT = 3,    /* a slot id repeated within one call (host check) */
   GDN_ERR_DTYPE = 4,       /* dtype not supported for this argument */
   GDN_ERR_SIZE = 5,        /* buffer too small, malformed cu_seqlens, length/T out of range */
-  GDN_ERR_UNSUPPORTED = 6, /* a shape this build has no kernel for (see gdn_pool_create) */
+  GDN_ERR_UNSUPPORTED = 6, /* a shape the library has no kernel for (see gdn_pool_create) */
   GDN_ERR_CUDA = 7         /* a CUDA runtime call failed (gdn_last_error_message has it) */
 } gdn_status;
 
