@@ -101,3 +101,32 @@ def test_no_compute_path_through_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b|gdn_oracle|oracle/",
                                      text, flags=re.M), f
+
+
+def test_one_call_decode_step_on_a_null_pool_fails_cleanly(lib):
+    st = lib.gdn_decode_step_conv(None, 0, None, 1, None, 0, None, None, None, 0, None, None,
+                                  abi.GDN_BF16, None, abi.GDN_F32, 1.0, None)
+    assert abi.STATUS[st] == "GDN_ERR_ARG"
+    assert "pool" in lib.gdn_last_error_message().decode()
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(rows=-1), "GDN_ERR_ARG"),
+    (dict(d=0), "GDN_ERR_ARG"),
+    (dict(eps=-1e-6), "GDN_ERR_ARG"),
+    (dict(eps=float("inf")), "GDN_ERR_ARG"),
+    (dict(eps=float("nan")), "GDN_ERR_ARG"),
+    (dict(o_dtype=7), "GDN_ERR_DTYPE"),
+    (dict(y_dtype=2), "GDN_ERR_DTYPE"),
+    (dict(o=None), "GDN_ERR_ARG"),             # rows > 0 needs every pointer
+    (dict(rows=0, o=None, z=None, w=None, y=None), "GDN_OK"),   # empty: no-op
+])
+def test_gated_rmsnorm_argument_checks(lib, args, status):
+    """Validation runs before any CUDA call (fake non-NULL pointers are never
+    dereferenced on these paths)."""
+    a = dict(rows=4, d=16, o=0x1000, o_dtype=abi.GDN_F32, z=0x2000, z_dtype=abi.GDN_BF16,
+             w=0x3000, eps=1e-6, y=0x4000, y_dtype=abi.GDN_F32)
+    a.update(args)
+    st = lib.gdn_gated_rmsnorm(a["rows"], a["d"], a["o"], a["o_dtype"], a["z"], a["z_dtype"],
+                               a["w"], a["eps"], a["y"], a["y_dtype"], None)
+    assert abi.STATUS[st] == status
