@@ -611,7 +611,7 @@ def run_gpu(args, rank, world):
                       "note": "the same step as gdn_conv_silu then gdn_decode_step, "
                               "an event between them"},
         "gpu_launches": 2 * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "gdn decode_kernel<128, bf16, float>",
+        "roofline": {"bound": "hbm", "kernel": "decode_bulk_kernel<128, bf16, float, false>",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(),
                      "peak_kind": f"{peak_kind} (HBM copy, burst)",
