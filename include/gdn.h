@@ -197,8 +197,9 @@ gdn_status gdn_decode_step(gdn_pool *pool, int32_t layer, const int32_t *slot_id
  * the two calls made one after the other.  The decode launch overlaps the
  * conv: it is a programmatic dependent launch that fetches its state tiles
  * (which the conv does not touch) before it waits for the conv grid to
- * complete and reads y.  Caller owns every buffer; on an error nothing is
- * launched. */
+ * complete and reads y.  Caller owns every buffer.  An argument or host-check
+ * error launches nothing; GDN_ERR_CUDA from the second launch leaves the conv
+ * (cache advanced, y written) launched without its decode. */
 gdn_status gdn_decode_step_conv(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
                                 int32_t n, const void *x, int64_t ld_x, const float *w,
                                 const float *bias, void *y, int64_t ld_y, const void *g,
