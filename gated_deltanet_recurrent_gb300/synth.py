@@ -217,3 +217,44 @@ SWEEP_SLOTS = (1, 4, 8, 16, 32, 64, 128, 256, 512)
 def sweep_slot_order(seed: int = 2, n_slots: int = 512) -> np.ndarray:
     """Slot-sweep order: the first N entries are the active slots at size N."""
     return np.random.default_rng(seed).permutation(n_slots).astype(np.int32)
+
+
+def gate_inputs(rng: np.random.Generator, n_tokens: int, h_v: int, dtype: str = "f32"):
+    """g, beta [n_tokens, h_v] with the recipe of token_inputs:
+    beta = sigmoid(N(0,1)), g = -softplus(N(0,1))."""
+    zb = rng.standard_normal((n_tokens, h_v))
+    zg = rng.standard_normal((n_tokens, h_v))
+    return cast(-np.logaddexp(0.0, zg), dtype), cast(1.0 / (1.0 + np.exp(-zb)), dtype)
+
+
+def sweep_workload(seed: int = 2, n_layers: int = 18, n_slots: int = 512,
+                   n_states: int = 512, table_rows: int = 4096,
+                   shape: LayerShape = GDN_LAYER, dtype: str = "bf16") -> dict:
+    """Inputs of the stacked-layer slot sweep.
+
+    Fresh draws for every (step, layer, slot) of 128 steps would be 19 GB of
+    conv inputs, so each step's rows are picked from seeded tables instead:
+    x [table_rows, conv_ch], g and beta [table_rows, h_v], row indices from
+    sweep_rows(seed, step, layer, n).  The initial state and conv cache of
+    layer l, slot s are entry state_index[l, s] of n_states seeded draws; the
+    index is a permutation per layer, so the slots of one layer all start
+    from different states.  Active slots at size N: order[:N]."""
+    assert n_states >= n_slots
+    rng = np.random.default_rng([seed, 0])
+    states = random_states(rng, n_states, shape)
+    caches = random_conv_cache(rng, n_states, shape, dtype)
+    state_index = np.stack([rng.permutation(n_states)[:n_slots] for _ in range(n_layers)])
+    x = conv_input(rng, table_rows, shape.conv_ch, dtype)
+    g, beta = gate_inputs(rng, table_rows, shape.h_v, dtype)
+    w = np.stack([conv_weights(rng, shape.conv_ch, shape.conv_k) for _ in range(n_layers)])
+    return {"shape": shape, "n_layers": n_layers, "n_slots": n_slots,
+            "order": sweep_slot_order(seed, n_slots), "state_table": states,
+            "cache_table": caches, "state_index": state_index.astype(np.int64),
+            "x": x, "g": g, "beta": beta, "conv_w": w, "table_rows": table_rows,
+            "seed": seed, "dtype": dtype}
+
+
+def sweep_rows(seed: int, step: int, layer: int, n: int, table_rows: int) -> np.ndarray:
+    """Table rows of the inputs of `step` in `layer`: entry i is the row of
+    the i-th active slot (order[i])."""
+    return np.random.default_rng([seed, 1, step, layer]).integers(0, table_rows, n)

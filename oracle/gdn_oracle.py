@@ -83,6 +83,37 @@ def conv_silu(x, cache, w, bias=None, advance=None):
     return y, new_cache
 
 
+# ------------------------------------------------- storage formats (rounding)
+
+def round_binary(x, p, emin, emax):
+    """Round to the nearest value of a binary floating-point format with p
+    significant bits (the leading one included), normal exponents emin..emax
+    and subnormals below 2^emin, ties to the even significand; magnitudes
+    beyond the format's range become infinities.  This is round-to-nearest-even
+    as IEEE 754 defines it, applied once, straight from float64.
+
+    Used where the layer stores an intermediate in a narrower format: the
+    conv output in bf16 activations, and the recurrent state of a pool that
+    keeps it in half precision."""
+    x = _f64(x)
+    _, E = np.frexp(np.abs(x))                 # |x| = m 2^E with m in [0.5, 1)
+    e = np.maximum(E - 1, emin)                # exponent of the leading bit
+    ulp = np.exp2(e - (p - 1))                 # spacing of the format at |x|
+    r = np.round(x / ulp) * ulp                # np.round rounds halves to even
+    top = (2.0 - 2.0 ** (1 - p)) * 2.0 ** emax
+    return np.where(np.abs(r) > top, np.copysign(np.inf, x), r)
+
+
+def round_bf16(x):
+    """bfloat16: 8 significant bits, exponents -126..127."""
+    return round_binary(x, 8, -126, 127)
+
+
+def round_f16(x):
+    """IEEE binary16: 11 significant bits, exponents -14..15."""
+    return round_binary(x, 11, -14, 15)
+
+
 # ------------------------------------------------------------ gated delta rule
 
 def l2_normalize(x, eps=L2_EPS):

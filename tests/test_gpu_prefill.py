@@ -14,6 +14,7 @@ from gated_deltanet_recurrent_gb300 import abi, synth
 from oracle import gdn_oracle as O
 from tests.gpu_util import (assert_close_bf16, assert_maxrel, dev, dev_i32, host, tok_dev,
                             tok_np)
+from tests.oracle_par import recurrent_many
 
 pytestmark = pytest.mark.gpu
 
@@ -314,7 +315,9 @@ def _head_sample(tok, heads, group):
 def test_prefill_varlen_pieces_full_size_sampled_heads(entry):
     """8 sequences with lengths uniform in [512, 8192], fed in 2048-token
     pieces with the state carried between calls; bf16 in and out; half the
-    slots start from zero, half from N(0, 0.1)."""
+    slots start from zero, half from N(0, 0.1).  The first piece-call is
+    checked on all 32 value heads (outputs and the states it leaves); the
+    whole sequences through the last call on value heads 0, 17 and 31."""
     wl = synth.prefill_workload(seed=3)
     s = wl["shape"]
     lens, cu = wl["lengths"], wl["cu_seqlens"]
@@ -324,6 +327,7 @@ def test_prefill_varlen_pieces_full_size_sampled_heads(entry):
     pool.state[0, lid] = dev(wl["states"])
     tok_all = {n: dev(wl["tok"][n], "bf16") for n in ("q", "k", "v", "g", "beta")}
     o = torch.empty(int(cu[-1]), s.h_v, s.dv, device="cuda", dtype=torch.bfloat16)
+    first = None
     for idx, starts, ln in synth.prefill_calls(lens, wl["piece"]):
         rows = np.concatenate([np.arange(cu[i] + st, cu[i] + st + l)
                                for i, st, l in zip(idx, starts, ln)])
@@ -333,8 +337,27 @@ def test_prefill_varlen_pieces_full_size_sampled_heads(entry):
         PREFILL[entry](pool, 0, dev_i32(ids[idx]), dev_i32(synth.cu_seqlens_of(ln)),
                        *packed, ob, max_seqlen=max(ln))
         o[rt] = ob
-    heads = [0, 17, 31]
+        if first is None:                     # the first piece-call, every head
+            first = (host(ob), host(pool.state[0, lid]), ln)
     group = s.h_v // s.h_k
+    # all 32 value heads of the first piece-call (the first 2048 tokens of
+    # every sequence, 15,204 tokens): one oracle task per sequence and key head
+    o1, S1, ln1 = first
+    tasks, where = [], []
+    for i in range(len(lens)):
+        lo = int(cu[i])
+        for kh in range(s.h_k):
+            hs = list(range(kh * group, (kh + 1) * group))
+            sl = slice(lo, lo + ln1[i])
+            tasks.append((wl["states"][i][hs], wl["tok"]["q"][sl, kh:kh + 1],
+                          wl["tok"]["k"][sl, kh:kh + 1], wl["tok"]["v"][sl][:, hs],
+                          wl["tok"]["g"][sl][:, hs], wl["tok"]["beta"][sl][:, hs]))
+            where.append((i, hs))
+    off = synth.cu_seqlens_of(ln1)
+    for (i, hs), (S_ref, o_ref) in zip(where, recurrent_many(tasks)):
+        assert_close_bf16(o1[off[i]:off[i + 1]][:, hs], o_ref, what=f"call 0 o seq {i} heads {hs}")
+        assert_close_bf16(S1[i][hs], S_ref, what=f"call 0 S seq {i} heads {hs}")
+    heads = [0, 17, 31]
     sub = _head_sample(wl["tok"], heads, group)
     for i in range(len(lens)):
         lo, hi = cu[i], cu[i + 1]

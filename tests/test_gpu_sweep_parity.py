@@ -1,0 +1,197 @@
+"""GPU parity of the 18-layer slot sweep at its full shape: 18 stacked GDN
+layers (32 value heads sharing 16 key heads, K = V = 128, conv_k = 4 over
+8192 channels, bf16 activations, fp32 state), a 512-slot pool (19.3 GB of
+state) with all 512 slots active in the sweep's slot order, 128 decode steps
+with new inputs every step.
+
+Two twin pools run the same steps: one with eager calls (gdn_conv_silu, then
+gdn_decode_step, per layer), one by replaying a CUDA graph of the one-call
+step (gdn_decode_step_conv per layer).  The two must agree bit for bit (same
+kernels, same inputs), and both are compared with the float64 oracle:
+
+  * every slot of layers 0, 9 and 17: the outputs of steps 0 and 1 and the
+    states after step 1 (all heads);
+  * a fixed sample of 16 slots in every layer, one key head and its two value
+    heads each (a different head per slot and layer): the outputs of all 128
+    steps and the states after the last one.
+
+The full check is therefore sampled after step 1, as stated.
+
+Tolerance.  The conv output y is stored in bf16 (the layer's activation
+dtype), so the oracle rounds its float64 conv output to bf16 before the split
+(round-to-nearest-even, oracle.round_bf16).  The GPU rounds its float32 conv
+result; the two roundings differ when a value lies within float32 error of a
+bf16 rounding boundary, which moves one q, k or v element by one bf16 unit
+(2^-8 relative).  Such a flip moves a state row by about
+2^-8 * beta * |v_r| * |k_j| -- a few 1e-4 against max|S| ~ 0.5 -- so the
+float32 bar (1e-4 * max) does not apply to this chained bf16 layer; the
+bf16-input criterion |gpu - ref| <= 1e-2 + 1e-2 |ref| does, and max|gpu - ref|
+is further held to 5e-3 * max|ref| per compared tensor."""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_recurrent_gb300 import abi, synth
+from oracle import gdn_oracle as O
+from tests.gpu_util import assert_close_bf16, assert_maxrel, host
+
+pytestmark = pytest.mark.gpu
+
+STEPS = 128
+FULL_LAYERS = (0, 9, 17)
+FULL_STEPS = 2
+N_SAMPLE = 16
+
+
+def _check(got, ref, what):
+    assert_close_bf16(got, ref, what=what)
+    assert_maxrel(got, ref, 5e-3, what)
+
+
+def _split(y, s):
+    nq = s.h_k * s.dk
+    return (y[:nq].reshape(s.h_k, s.dk), y[nq:2 * nq].reshape(s.h_k, s.dk),
+            y[2 * nq:].reshape(s.h_v, s.dv))
+
+
+def _sample_channels(s, kh):
+    """conv channels of key head kh (q and k) and of its value heads."""
+    group = s.h_v // s.h_k
+    nq = s.h_k * s.dk
+    heads = list(range(kh * group, (kh + 1) * group))
+    ch = np.concatenate([np.arange(kh * s.dk, (kh + 1) * s.dk),
+                         nq + np.arange(kh * s.dk, (kh + 1) * s.dk),
+                         2 * nq + np.arange(heads[0] * s.dv, (heads[-1] + 1) * s.dv)])
+    return heads, ch
+
+
+def test_sweep_18_layers_512_slots_eager_and_graph_match_oracle():
+    wl = synth.sweep_workload(seed=2)
+    s, L, P = wl["shape"], wl["n_layers"], wl["n_slots"]
+    N = P
+    order = wl["order"]
+    group = s.h_v // s.h_k
+    nq = s.h_k * s.dk
+    dev = torch.device("cuda")
+    bf = torch.bfloat16
+
+    table = torch.from_numpy(wl["state_table"]).to(dev)
+    ctable = torch.from_numpy(wl["cache_table"]).to(dev, bf)
+    sidx = torch.from_numpy(wl["state_index"]).to(dev)
+    pools = [abi.Pool.for_shape(s, L, P, conv_dtype=bf, host_checks=False) for _ in range(2)]
+    epool, gpool = pools
+    ids = torch.from_numpy(order).to(dev)
+    xt = torch.from_numpy(wl["x"]).to(dev, bf)
+    gt = torch.from_numpy(wl["g"]).to(dev, bf)
+    bt = torch.from_numpy(wl["beta"]).to(dev, bf)
+    w = [torch.from_numpy(wl["conv_w"][l]).to(dev) for l in range(L)]
+
+    # static inputs and outputs of the captured one-call step
+    sx = [torch.empty(N, s.conv_ch, device=dev, dtype=bf) for _ in range(L)]
+    sg = [torch.empty(N, s.h_v, device=dev, dtype=bf) for _ in range(L)]
+    sb = [torch.empty(N, s.h_v, device=dev, dtype=bf) for _ in range(L)]
+    sy = [torch.empty(N, s.conv_ch, device=dev, dtype=bf) for _ in range(L)]
+    so = [torch.empty(N, s.h_v, s.dv, device=dev) for _ in range(L)]
+    ey = [torch.empty_like(t) for t in sy]
+    eo = [torch.empty_like(t) for t in so]
+
+    def graph_step(stream):
+        for l in range(L):
+            abi.gdn_decode_step_conv(gpool, l, ids, sx[l], w[l], sy[l], sg[l], sb[l], so[l],
+                                     stream=stream)
+
+    def eager_step():
+        for l in range(L):
+            abi.gdn_conv_silu(epool, l, ids, sx[l], w[l], ey[l])
+            q = ey[l][:, :nq].view(N, s.h_k, s.dk)
+            k = ey[l][:, nq:2 * nq].view(N, s.h_k, s.dk)
+            v = ey[l][:, 2 * nq:].view(N, s.h_v, s.dv)
+            abi.gdn_decode_step(epool, l, ids, q, k, v, sg[l], sb[l], eo[l])
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            graph_step(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for p in pools:                       # initial states (capture ran nothing)
+        for l in range(L):
+            p.state[l] = table[sidx[l]]
+            p.conv[l] = ctable[sidx[l]]
+    del table, ctable
+    torch.cuda.synchronize()
+
+    rng = np.random.default_rng(20)
+    pos = np.sort(rng.choice(N, N_SAMPLE, replace=False))
+    pos_dev = torch.from_numpy(pos).to(dev)
+    # oracle chains of the sample: (position, layer) -> [heads, channels, S, X]
+    chains = {}
+    for j, i in enumerate(pos):
+        slot = int(order[i])
+        for l in range(L):
+            heads, ch = _sample_channels(s, (3 * j + 5 * l) % s.h_k)
+            e = wl["state_index"][l, slot]
+            chains[(j, l)] = [heads, ch, wl["state_table"][e][heads].astype(np.float64),
+                              wl["cache_table"][e][ch].astype(np.float64)]
+    full_o = {l: [] for l in FULL_LAYERS}
+    S_after = {}
+
+    for step in range(STEPS):
+        rows = [synth.sweep_rows(wl["seed"], step, l, N, wl["table_rows"]) for l in range(L)]
+        for l in range(L):
+            r = torch.from_numpy(rows[l]).to(dev)
+            sx[l].copy_(xt[r])
+            sg[l].copy_(gt[r])
+            sb[l].copy_(bt[r])
+        eager_step()
+        graph.replay()
+        o_samp = host(torch.stack([eo[l][pos_dev] for l in range(L)]))
+        for l in range(L):
+            assert torch.equal(so[l], eo[l]), f"step {step} layer {l}: graph vs eager outputs"
+        if step < FULL_STEPS:
+            for l in FULL_LAYERS:
+                full_o[l].append(host(eo[l]))
+        if step == FULL_STEPS - 1:
+            for l in FULL_LAYERS:
+                S_after[l] = epool.state[l].cpu().numpy()
+        # the sampled chains, one step
+        for (j, l), c in chains.items():
+            heads, ch, S, X = c
+            i = pos[j]
+            rr = rows[l][i]
+            y, c[3] = O.conv_silu(wl["x"][rr:rr + 1, ch], X, wl["conv_w"][l][ch])
+            y = O.round_bf16(y[0])
+            q, k, v = y[:s.dk][None], y[s.dk:2 * s.dk][None], y[2 * s.dk:].reshape(group, s.dv)
+            c[2], o_ref = O.gdn_step(S, q, k, v, wl["g"][rr][heads], wl["beta"][rr][heads])
+            _check(o_samp[l, j][heads], o_ref, f"o step {step} layer {l} slot {order[i]}")
+
+    torch.cuda.synchronize()
+    assert torch.equal(epool.state, gpool.state), "graph vs eager states"
+    assert torch.equal(epool.conv, gpool.conv), "graph vs eager conv caches"
+    for (j, l), (heads, ch, S, X) in chains.items():
+        slot = int(order[pos[j]])
+        got = host(epool.state[l, slot][heads])
+        _check(got, S, f"S after {STEPS} steps, layer {l} slot {slot}")
+    assert abi.gdn_pool_get_error(epool) == 0
+    assert abi.gdn_pool_get_error(gpool) == 0
+    del pools, epool, gpool
+    torch.cuda.empty_cache()
+
+    # every slot of layers 0, 9, 17: outputs of the first two steps, states after them
+    for l in FULL_LAYERS:
+        rows = [synth.sweep_rows(wl["seed"], st, l, N, wl["table_rows"])
+                for st in range(FULL_STEPS)]
+        for i in range(N):
+            slot = int(order[i])
+            e = wl["state_index"][l, slot]
+            S = wl["state_table"][e]
+            X = wl["cache_table"][e]
+            for st in range(FULL_STEPS):
+                rr = rows[st][i]
+                y, X = O.conv_silu(wl["x"][rr:rr + 1], X, wl["conv_w"][l])
+                q, k, v = _split(O.round_bf16(y[0]), s)
+                S, o_ref = O.gdn_step(S, q, k, v, wl["g"][rr], wl["beta"][rr])
+                _check(full_o[l][st][i], o_ref, f"o step {st} layer {l} slot {slot}")
+            _check(S_after[l][slot], S, f"S after step {FULL_STEPS} layer {l} slot {slot}")

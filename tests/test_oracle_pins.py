@@ -25,6 +25,10 @@ Map (oracle function -> pins):
                   with silu from scipy's expit; scale invariance (eps = 0);
                   unit mean square of out / (w silu(z)); z = 0 gives 0; a
                   zero row with eps > 0 gives 0; planted mistakes are caught
+  round_bf16 /
+  round_f16       torch's float32 -> bfloat16 and numpy's float64 -> float16
+                  conversions (library routines) on values spanning the
+                  subnormal, normal and overflow ranges; hand-worked ties
 """
 import os
 from fractions import Fraction
@@ -641,3 +645,38 @@ def test_gated_rmsnorm_pins_catch_planted_mistakes():
 
     for wrong in (sum_not_mean, sigmoid_gate, no_weight):
         assert not np.allclose(wrong(o, z, w, eps=0.0), want, rtol=1e-6), wrong.__name__
+
+
+# ------------------------------------------------------- storage formats
+
+def test_round_bf16_matches_torch_conversion():
+    """torch converts float32 to bfloat16 with round-to-nearest-even; on
+    float32 inputs (one rounding, no double rounding) it is the definition."""
+    rng = np.random.default_rng(90)
+    x = rng.standard_normal(100000) * np.exp2(rng.integers(-140, 129, 100000))
+    x = x.astype(np.float32)
+    x = x[np.isfinite(x)]
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(O.round_bf16(x.astype(np.float64)), ref)
+
+
+def test_round_f16_matches_numpy_conversion():
+    rng = np.random.default_rng(91)
+    x = rng.standard_normal(100000) * np.exp2(rng.integers(-30, 18, 100000))
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(O.round_f16(x), ref)
+
+
+def test_round_bf16_hand_worked_ties_and_range():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: the even significand is 1.
+    # 1 + 3 2^-8 lies halfway between 1 + 2^-7 and 1 + 2^-6: even is 1 + 2^-6.
+    # 2^-134 is half the smallest subnormal (2^-133): ties to 0.
+    # 1.5 2^-133 is halfway between 2^-133 and 2^-132: even is 2^-132.
+    x = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 2.0 ** -134,
+                  1.5 * 2.0 ** -133, 3.4e38])
+    want = np.array([1.0, 1 + 2.0 ** -6, -1.0, 0.0, 2.0 ** -132, np.inf])
+    np.testing.assert_array_equal(O.round_bf16(x), want)
+    # the largest finite bf16 is (2 - 2^-7) 2^127 and stays put
+    top = (2 - 2.0 ** -7) * 2.0 ** 127
+    assert O.round_bf16(np.array([top]))[0] == top

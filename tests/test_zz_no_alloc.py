@@ -62,3 +62,38 @@ def test_noalloc_prefill_refuses_calls_beyond_its_array():
     torch.cuda.synchronize()
     assert torch.equal(pool.state, before)
     assert bool((o == 0).all())
+
+
+def test_noalloc_prefill_on_a_side_stream_small_call_then_larger_call():
+    """A smaller call followed by a larger one (more sequences, more chunks,
+    bf16 outputs), both on a non-default stream: the second call must read
+    nothing the first left in the shared array."""
+    rng = np.random.default_rng(52)
+    shape = synth.LayerShape(8, 4, 128, 128, 16, 4)
+    ids = [np.array([2], dtype=np.int32), np.array([4, 1, 0, 6], dtype=np.int32)]
+    S0 = synth.random_states(rng, 7, shape)
+    pools = {}
+    for name in ("noalloc", "chunked"):
+        pool = abi.Pool.for_shape(shape, 1, 7, conv_dtype=torch.float32)
+        pool.state[0] = dev(S0)
+        pools[name] = pool
+    fns = {"noalloc": abi.gdn_prefill_chunked_noalloc, "chunked": abi.gdn_prefill_chunked}
+    side = torch.cuda.Stream()
+    for call, (sid, lens, odt) in enumerate(((ids[0], [70], torch.float32),
+                                             (ids[1], [300, 5, 129, 64], torch.bfloat16))):
+        cu = synth.cu_seqlens_of(lens)
+        tok = tok_dev(synth.token_inputs(rng, int(cu[-1]), shape, "bf16"), "bf16")
+        sid_d, cu_d = dev_i32(sid), dev_i32(cu)
+        side.wait_stream(torch.cuda.current_stream())      # inputs copied on the default stream
+        outs = {}
+        with torch.cuda.stream(side):
+            for name, pool in pools.items():
+                o = torch.empty(int(cu[-1]), shape.h_v, shape.dv, device="cuda", dtype=odt)
+                fns[name](pool, 0, sid_d, cu_d, *tok, o, max_seqlen=max(lens), stream=side)
+                outs[name] = o
+        side.synchronize()
+        assert_maxrel(host(outs["noalloc"]), host(outs["chunked"]), 1e-5, f"o, call {call}")
+        assert_maxrel(host(pools["noalloc"].state), host(pools["chunked"].state), 1e-5,
+                      f"S, call {call}")
+    for pool in pools.values():
+        assert abi.gdn_pool_get_error(pool) == 0
