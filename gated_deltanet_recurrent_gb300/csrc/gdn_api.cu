@@ -16,6 +16,7 @@ struct gdn_pool {
   gdn::PoolView view;
   gdn_pool_desc desc;
   int device;
+  int sm_count;
   bool has_tmap;
   alignas(64) CUtensorMap tmap;  // the state as a [rows][dk] float32 tensor (TMA)
   cudaMemPool_t work_pool;       // stream-ordered prefill workspaces (kept until destroy)
@@ -251,20 +252,32 @@ gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t st
         (st = check_device_ptr(conv_mem, "conv_mem")))
       return st;
   }
+  // one allocation: the error word, then the one-call decode step's tickets
+  // (one per layer, slot and key head), all zero
+  const size_t n_ticks = (size_t)desc->n_layers * desc->n_slots * desc->h_k;
+  const size_t aux_bytes = (1 + n_ticks) * sizeof(unsigned int);
   unsigned int *err = nullptr;
-  e = cudaMalloc(&err, sizeof(unsigned int));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
-  e = cudaMemset(err, 0, sizeof(unsigned int));
+  e = cudaMalloc(&err, aux_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word and tickets)");
+  e = cudaMemset(err, 0, aux_bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaFree(err);
-    return cuda_fail(e, "cudaMemset(error word)");
+    return cuda_fail(e, "cudaMemset(error word and tickets)");
+  }
+  int sm_count = 0;
+  e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    cudaFree(err);
+    return cuda_fail(e, "cudaDeviceGetAttribute(multiprocessor count)");
   }
   gdn_pool *p = new gdn_pool;
   p->desc = *desc;
   p->device = dev;
+  p->sm_count = sm_count;
   p->view = gdn::PoolView{static_cast<float *>(state_mem), conv_mem, err,
                           desc->n_layers, desc->n_slots, desc->h_v, desc->h_k, desc->dk,
-                          desc->dv, desc->conv_ch, desc->conv_k, desc->conv_dtype};
+                          desc->dv, desc->conv_ch, desc->conv_k, desc->conv_dtype, err + 1};
   p->has_tmap = encode_state_map(p);
   cudaMemPoolProps props = {};
   props.allocType = cudaMemAllocationTypePinned;
@@ -288,7 +301,7 @@ gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t st
 gdn_status gdn_pool_destroy(gdn_pool *p) {
   if (!p) return ok();
   cudaError_t e = cudaDeviceSynchronize();
-  cudaError_t e2 = cudaFree(p->view.err);
+  cudaError_t e2 = cudaFree(p->view.err);  // the error word and the tickets
   cudaError_t e3 = cudaMemPoolDestroy(p->work_pool);
   if (e2 == cudaSuccess) e2 = e3;
   delete p;
@@ -447,9 +460,22 @@ gdn_status gdn_decode_step_conv(gdn_pool *p, int32_t layer, const int32_t *slot_
         (st = check_device_ptr(o, "o")))
       return st;
   }
+  // One fused kernel while its whole grid is resident at once (small n: one
+  // launch and one wave).  Beyond that its CTAs each recompute their key
+  // head's q and k conv, and the conv launch followed by the decode as a
+  // programmatic dependent launch (the decode fetches its state tiles while
+  // the conv runs) is faster.
+  int64_t resident = 0;
+  cudaError_t e = gdn::decode_conv_resident_ctas(p->view, dtype, o_dtype, p->sm_count, &resident);
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  if (gdn::decode_grid_ctas(p->view, n) <= resident) {
+    e = gdn::launch_decode_conv(p->view, layer, slot_ids, n, x, ld_x, w, bias, y, ld_y, g, beta,
+                                dtype, o, o_dtype, scale, s);
+    if (e != cudaSuccess) return cuda_fail(e, "conv + decode launch");
+    return ok();
+  }
   gdn::SeqIndex seq{slot_ids, nullptr, n, n};
-  cudaError_t e = gdn::launch_conv_silu(p->view, layer, seq, 1, x, ld_x, w, bias, y, ld_y,
-                                        nullptr, s);
+  e = gdn::launch_conv_silu(p->view, layer, seq, 1, x, ld_x, w, bias, y, ld_y, nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "conv launch");
   e = gdn::launch_decode(p->view, p->has_tmap ? &p->tmap : nullptr, layer, slot_ids, n, q, o,
                          o_dtype, scale, s, /*after_conv=*/true);

@@ -126,6 +126,319 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// ---- conv + SiLU, q/k norm and the decode step in one kernel ----
+//
+// Same grid and state streaming as decode_bulk_kernel.  While its state tile
+// is in flight, each CTA computes the conv + SiLU outputs it needs itself:
+// the 2*DK q and k channels of its key head and the R v channels of its rows,
+// from x, the slot's conv cache and the taps, rounded to the activation dtype
+// exactly as the conv kernel stores y.  Outputs, y, cache and state are
+// bit-identical to the conv kernel followed by the decode kernel.  Loads that
+// do not depend on the slot id (x, taps, g, beta) are issued before it.
+//
+// Cache update without a grid-wide wait.  A v channel is read by one CTA,
+// which shifts its cache in place.  A q/k channel is read by the `readers`
+// CTAs that share the key head (value heads of the group x row blocks), so
+// its old cache must stay readable until all of them have read it: after its
+// reads each CTA takes a ticket for the key head (p.ticks[layer][slot][hk]),
+// and the CTA that draws the last one writes the shifted q/k cache (its old
+// values are still in its registers) and puts the ticket back to 0.  No CTA
+// waits on another; every launch leaves every ticket at 0 (an entry skipped
+// for a bad slot id draws none).  The ticket is taken by one thread after a
+// CTA barrier (the barrier orders the other threads' cache reads before it,
+// as in a grid-wide barrier) and its result is read only after the state
+// update, so the round trip stays off the decode's critical path.  The first
+// value head of the group, row block 0, writes the q/k part of y.
+constexpr int kMaxConvK = 8;
+
+template <typename T>
+__device__ __forceinline__ float round_to(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ float round_to<bf16>(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// One conv channel of one token: taps, raw input and the cached inputs, for
+// a conv width W <= WM.
+template <int WM>
+struct ConvTap {
+  float w[WM];
+  float b, x;
+  float hist[WM - 1];  // the W - 1 cached inputs, oldest first
+};
+
+template <int WM, typename T>
+__device__ __forceinline__ void tap_load(ConvTap<WM> &t, const T *xrow, const float *w,
+                                         const float *bias, int c, int W) {
+  const float *wc = w + (int64_t)c * W;
+  if (WM == 4 && W == 4 && ((uintptr_t)wc & 15) == 0) {
+    const float4 w4 = *reinterpret_cast<const float4 *>(wc);
+    t.w[0] = w4.x; t.w[1] = w4.y; t.w[2] = w4.z; t.w[WM - 1] = w4.w;
+  } else {
+#pragma unroll
+    for (int m = 0; m < WM; ++m)
+      if (m < W) t.w[m] = wc[m];
+  }
+  t.b = bias ? bias[c] : 0.f;
+  t.x = Elem<T>::load1(xrow + c);
+}
+
+template <int WM, typename T>
+__device__ __forceinline__ void tap_load_cache(ConvTap<WM> &t, const T *cache, int c, int W) {
+  const T *cc = cache + (int64_t)c * (W - 1);
+#pragma unroll
+  for (int m = 0; m < WM - 1; ++m)
+    if (m < W - 1) t.hist[m] = Elem<T>::load1(cc + m);
+}
+
+// The conv kernel's arithmetic, in its order, rounded to T as y is stored.
+template <int WM, typename T>
+__device__ __forceinline__ float tap_conv(const ConvTap<WM> &t, int W) {
+  float wl = 0.f;  // t.w[W - 1], selected without a dynamic register index
+#pragma unroll
+  for (int m = 0; m < WM; ++m)
+    if (m == W - 1) wl = t.w[m];
+  float u = t.b + wl * t.x;
+#pragma unroll
+  for (int m = 0; m < WM - 1; ++m)
+    if (m < W - 1) u += t.w[m] * t.hist[m];
+  return round_to<T>(silu(u));
+}
+
+struct ConvStep {
+  const void *x;
+  int64_t ld_x;
+  const float *w;
+  const float *bias;
+  void *y;
+  int64_t ld_y;
+  const void *g, *beta;
+};
+
+// WM: the largest conv width this instantiation handles (4: exactly 4).
+template <int DK, typename TI, typename TO, int WM>
+__global__ void __launch_bounds__(kThreads)
+    decode_conv_kernel(PoolView p, int layer, const int32_t *__restrict__ slot_ids, ConvStep cs,
+                       TO *__restrict__ o, float scale) {
+  constexpr int R = kBulkBytes / (DK * 4);
+  constexpr int LPR = DK / 4, RPP = 32 / LPR;
+  constexpr int RPW = R / (kThreads / 32);
+  constexpr int U = 4;
+  constexpr int PASSES = RPW / (RPP * U);
+  constexpr int NQK = (2 * DK + kThreads - 1) / kThreads;  // q/k channels per thread
+  constexpr int NV = (R + kThreads - 1) / kThreads;         // v channels per thread
+  constexpr int kTicketThread = kThreads - 1;
+  static_assert(PASSES >= 1 && RPW % (RPP * U) == 0, "row mapping");
+  __shared__ __align__(128) float4 tile[kBulkBytes / 16];
+  __shared__ __align__(16) float sqk[2 * DK];   // conv outputs of q | k (this key head)
+  __shared__ float sv[R];                       // conv outputs of this CTA's v rows
+  __shared__ TI snew[2 * DK][WM - 1];           // q/k cache after this token (if last)
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_last;
+
+  const int i = blockIdx.z;
+  const int h = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int slot = slot_ids[i];
+  const int group = p.h_v / p.h_k;
+  const int hk = h / group;
+  const int W = WM == 4 ? 4 : p.conv_k;
+  const int nq = p.h_k * DK;
+  const int r0 = blockIdx.x * R;
+  const int nrows = min(R, p.dv - r0);
+  // slot-independent inputs first
+  const int64_t gb = (int64_t)i * p.h_v + h;
+  const float graw = Elem<TI>::load1(static_cast<const TI *>(cs.g) + gb);
+  const float beta = Elem<TI>::load1(static_cast<const TI *>(cs.beta) + gb);
+  const TI *xrow = static_cast<const TI *>(cs.x) + (int64_t)i * cs.ld_x;
+  auto qk_channel = [&](int j) { return (j < DK ? 0 : nq) + hk * DK + j % DK; };
+  ConvTap<WM> tq[NQK], tv[NV];
+#pragma unroll
+  for (int e = 0; e < NQK; ++e) {
+    const int j = tid + e * kThreads;
+    if (j < 2 * DK) tap_load<WM, TI>(tq[e], xrow, cs.w, cs.bias, qk_channel(j), W);
+  }
+#pragma unroll
+  for (int e = 0; e < NV; ++e) {
+    const int r = tid + e * kThreads;
+    if (r < nrows) tap_load<WM, TI>(tv[e], xrow, cs.w, cs.bias, 2 * nq + h * p.dv + r0 + r, W);
+  }
+  if (slot < 0 || slot >= p.n_slots) {
+    if (blockIdx.x == 0 && h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
+    return;
+  }
+  float *S = state_head(p, layer, slot, h) + (int64_t)r0 * DK;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)nrows * DK * 4;
+    mbar_arrive_expect_tx(&bar, bytes);
+    bulk_g2s(tile, S, bytes, &bar);
+  }
+
+  TI *cache = static_cast<TI *>(p.conv) +
+              ((int64_t)layer * p.n_slots + slot) * p.conv_ch * (W - 1);
+  TI *yrow = static_cast<TI *>(cs.y) + (int64_t)i * cs.ld_y;
+  const bool y_qk_writer = blockIdx.x == 0 && h % group == 0;
+#pragma unroll
+  for (int e = 0; e < NQK; ++e) {
+    const int j = tid + e * kThreads;
+    if (j < 2 * DK) tap_load_cache<WM, TI>(tq[e], cache, qk_channel(j), W);
+  }
+#pragma unroll
+  for (int e = 0; e < NV; ++e) {
+    const int r = tid + e * kThreads;
+    if (r < nrows) tap_load_cache<WM, TI>(tv[e], cache, 2 * nq + h * p.dv + r0 + r, W);
+  }
+#pragma unroll
+  for (int e = 0; e < NQK; ++e) {
+    const int j = tid + e * kThreads;
+    if (j < 2 * DK) {
+      const float yv = tap_conv<WM, TI>(tq[e], W);
+      sqk[j] = yv;
+      if (y_qk_writer) Elem<TI>::store1(yrow + qk_channel(j), yv);
+      // the shifted cache (hist[1 .. W-2], x), kept for the ticket's winner
+#pragma unroll
+      for (int m = 0; m < WM - 2; ++m)
+        if (m < W - 2) Elem<TI>::store1(&snew[j][m], tq[e].hist[m + 1]);
+      Elem<TI>::store1(&snew[j][W - 2], tq[e].x);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < NV; ++e) {
+    const int r = tid + e * kThreads;
+    if (r < nrows) {
+      const int c = 2 * nq + h * p.dv + r0 + r;
+      const float yv = tap_conv<WM, TI>(tv[e], W);
+      sv[r] = yv;
+      Elem<TI>::store1(yrow + c, yv);
+      // this CTA is the only reader of its v channels: shift in place
+      TI *cc = cache + (int64_t)c * (W - 1);
+#pragma unroll
+      for (int m = 0; m < WM - 2; ++m)
+        if (m < W - 2) Elem<TI>::store1(cc + m, tv[e].hist[m + 1]);
+      Elem<TI>::store1(cc + (W - 2), tv[e].x);
+    }
+  }
+  __syncthreads();  // every thread's q/k cache reads are done; sqk, sv, snew complete
+  unsigned int *ticket = p.ticks + ((int64_t)layer * p.n_slots + slot) * p.h_k + hk;
+  unsigned int prev = 0;
+  if (tid == kTicketThread) {
+    __threadfence();
+    prev = atomicAdd(ticket, 1u);  // read only after the state update
+  }
+
+  const int lane = tid & 31, warp = tid >> 5;
+  const int sub = lane % LPR, grp = lane / LPR;
+  float4 q4 = reinterpret_cast<const float4 *>(sqk)[sub];
+  float4 k4 = reinterpret_cast<const float4 *>(sqk + DK)[sub];
+  const float kk = group_sum<LPR>(dot4(k4, k4));
+  const float qq = group_sum<LPR>(dot4(q4, q4));
+  k4 = scale4(rsqrtf(kk + kL2Eps), k4);
+  q4 = scale4(rsqrtf(qq + kL2Eps), q4);
+  const float alpha = expf(graw);
+  TO *op = o + gb * p.dv + r0;
+
+  if (mbar_wait_bounded(&bar, 0)) {
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+      float4 s[U];
+      float acc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int rl = warp * RPW + (ps * U + u) * RPP + grp;
+        s[u] = rl < nrows ? tile[rl * (DK / 4) + sub] : make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[u] = dot4(s[u], k4);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = group_sum<LPR>(acc[u]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int rl = warp * RPW + (ps * U + u) * RPP + grp;
+        const float vr = rl < nrows ? sv[rl] : 0.f;
+        const float d = beta * (vr - alpha * acc[u]);
+        s[u] = axpby4(alpha, s[u], d, k4);
+        acc[u] = dot4(s[u], q4);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = group_sum<LPR>(acc[u]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int rl = warp * RPW + (ps * U + u) * RPP + grp;
+        if (rl < nrows) {
+          __stcs(reinterpret_cast<float4 *>(S + (int64_t)rl * DK) + sub, s[u]);
+          if (sub == 0) Elem<TO>::store1(op + rl, scale * acc[u]);
+        }
+      }
+    }
+  } else {
+    if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
+    mbar_wait_bounded(&bar, 0);  // give the copy a second bounded chance before going on
+  }
+
+  // the last of the key head's readers writes the shifted q/k cache
+  if (tid == kTicketThread) {
+    const int readers = group * (int)gridDim.x;
+    const int last = prev == (unsigned int)(readers - 1);
+    if (last) {
+      atomicExch(ticket, 0u);
+      __threadfence();
+    }
+    s_last = last;
+  }
+  __syncthreads();
+  if (s_last) {
+    for (int e = tid; e < 2 * DK * (W - 1); e += kThreads) {
+      const int j = e / (W - 1), m = e % (W - 1);
+      cache[(int64_t)qk_channel(j) * (W - 1) + m] = snew[j][m];
+    }
+  }
+}
+
+template <int DK, typename TI, typename TO>
+struct DecodeConvF {
+  static cudaError_t run(const PoolView &p, int layer, const int32_t *slot_ids, int n,
+                         const ConvStep &cs, void *o, float scale, cudaStream_t s) {
+    constexpr int R = kBulkBytes / (DK * 4);
+    dim3 grid((p.dv + R - 1) / R, p.h_v, n);
+    if (p.conv_k == 4)
+      decode_conv_kernel<DK, TI, TO, 4><<<grid, kThreads, 0, s>>>(p, layer, slot_ids, cs,
+                                                                   static_cast<TO *>(o), scale);
+    else
+      decode_conv_kernel<DK, TI, TO, kMaxConvK><<<grid, kThreads, 0, s>>>(
+          p, layer, slot_ids, cs, static_cast<TO *>(o), scale);
+    return cudaGetLastError();
+  }
+};
+
+// CTAs of the fused kernel one SM holds at once (looked up once per
+// instantiation; every device this library runs on is the same part).
+template <int DK, typename TI, typename TO>
+struct DecodeConvOcc {
+  static cudaError_t run(const PoolView &p, int *per_sm) {
+    static int occ4 = -1, occ8 = -1;
+    int &occ = p.conv_k == 4 ? occ4 : occ8;
+    if (occ < 0) {
+      int v = 0;
+      const cudaError_t e =
+          p.conv_k == 4
+              ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &v, decode_conv_kernel<DK, TI, TO, 4>, kThreads, 0)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &v, decode_conv_kernel<DK, TI, TO, kMaxConvK>, kThreads, 0);
+      if (e != cudaSuccess) return e;
+      occ = v;
+    }
+    *per_sm = occ;
+    return cudaSuccess;
+  }
+};
+
 template <int DK, typename TI, typename TO>
 cudaError_t launch_decode_t(const PoolView &p, int layer, const int32_t *slot_ids, int n,
                             const QKV &in, void *o, float scale, cudaStream_t s,
@@ -171,6 +484,29 @@ cudaError_t launch_decode(const PoolView &p, const void *tmap, int layer,
   (void)tmap;
   return dispatch<DecodeF>(p.dk, in.dtype, o_dtype, p, layer, slot_ids, n, in, o, scale, s,
                            after_conv);
+}
+
+cudaError_t decode_conv_resident_ctas(const PoolView &p, gdn_dtype dtype, gdn_dtype o_dtype,
+                                      int sm_count, int64_t *ctas) {
+  int per_sm = 0;
+  const cudaError_t e = dispatch<DecodeConvOcc>(p.dk, dtype, o_dtype, p, &per_sm);
+  *ctas = (int64_t)per_sm * sm_count;
+  return e;
+}
+
+int64_t decode_grid_ctas(const PoolView &p, int n) {
+  const int R = kBulkBytes / (p.dk * 4);
+  return (int64_t)((p.dv + R - 1) / R) * p.h_v * n;
+}
+
+cudaError_t launch_decode_conv(const PoolView &p, int layer, const int32_t *slot_ids, int n,
+                              const void *x, int64_t ld_x, const float *w, const float *bias,
+                              void *y, int64_t ld_y, const void *g, const void *beta,
+                              gdn_dtype dtype, void *o, gdn_dtype o_dtype, float scale,
+                              cudaStream_t s) {
+  if (p.ticks == nullptr || p.conv_k > kMaxConvK) return cudaErrorInvalidValue;
+  const ConvStep cs{x, ld_x, w, bias, y, ld_y, g, beta};
+  return dispatch<DecodeConvF>(p.dk, dtype, o_dtype, p, layer, slot_ids, n, cs, o, scale, s);
 }
 
 }  // namespace gdn

@@ -26,6 +26,7 @@ struct PoolView {
   unsigned int *err;       // device error word
   int n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k;
   gdn_dtype conv_dtype;
+  unsigned int *ticks;     // [n_layers][n_slots][h_k] tickets of the one-call decode step
   GDN_HD int64_t state_slot_elems() const { return (int64_t)h_v * dv * dk; }
   GDN_HD int64_t conv_slot_elems() const { return (int64_t)conv_ch * (conv_k - 1); }
 };
@@ -80,6 +81,22 @@ cudaError_t launch_decode(const PoolView &p, const void *tmap, int layer,
                           const int32_t *slot_ids, int n, const QKV &in, void *o,
                           gdn_dtype o_dtype, float scale, cudaStream_t s,
                           bool after_conv = false);
+
+// conv + SiLU, the q/k norm and the decode step of one layer in one kernel
+// (one token per slot): y = conv(x) split as q | k | v.  Results, y, cache and
+// state equal launch_conv_silu followed by launch_decode, bit for bit.  Needs
+// conv_ch == 2*h_k*dk + h_v*dv and p.ticks (all zero between launches).
+// CTAs of the decode kernels' grid for n slots, and how many CTAs of the fused
+// conv + decode kernel the device (sm_count SMs) holds resident at once.
+int64_t decode_grid_ctas(const PoolView &p, int n);
+cudaError_t decode_conv_resident_ctas(const PoolView &p, gdn_dtype dtype, gdn_dtype o_dtype,
+                                      int sm_count, int64_t *ctas);
+
+cudaError_t launch_decode_conv(const PoolView &p, int layer, const int32_t *slot_ids, int n,
+                               const void *x, int64_t ld_x, const float *w, const float *bias,
+                               void *y, int64_t ld_y, const void *g, const void *beta,
+                               gdn_dtype dtype, void *o, gdn_dtype o_dtype, float scale,
+                               cudaStream_t s);
 
 // Speculative verify of T new drafts per slot.  Normal mode: commit at
 // accept_len[i] (or after all T with commit_all).  Deferred mode (prev.q set):

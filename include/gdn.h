@@ -193,13 +193,20 @@ gdn_status gdn_decode_step(gdn_pool *pool, int32_t layer, const int32_t *slot_id
  * be 2*h_k*dk + h_v*dv (else GDN_ERR_SIZE).  x: [n][conv_ch] with row stride
  * ld_x (0: conv_ch); x, y, g and beta are all in `dtype`, which must be the
  * pool's conv_dtype (else GDN_ERR_DTYPE); w, bias as in gdn_conv_silu; o, g,
- * beta, scale as in gdn_decode_step.  Results, cache and state are those of
- * the two calls made one after the other.  The decode launch overlaps the
- * conv: it is a programmatic dependent launch that fetches its state tiles
- * (which the conv does not touch) before it waits for the conv grid to
- * complete and reads y.  Caller owns every buffer.  An argument or host-check
- * error launches nothing; GDN_ERR_CUDA from the second launch leaves the conv
- * (cache advanced, y written) launched without its decode. */
+ * beta, scale as in gdn_decode_step.  Results, y, cache and state are those
+ * of the two calls made one after the other, bit for bit.
+ * Two forms, chosen by size: while the decode grid (h_v * ceil(dv / rows per
+ * CTA) CTAs per slot) fits on the device at once, ONE kernel does it all --
+ * each CTA convolves the q/k channels of its key head and the v channels of
+ * its state rows itself while its state tile is in flight, and the last of
+ * the CTAs sharing a key head (a per-slot ticket in pool memory, no waiting)
+ * shifts that head's q/k cache.  Larger calls launch the conv and then the
+ * decode as its programmatic dependent launch, which fetches its state tiles
+ * (untouched by the conv) before it waits for the conv grid to complete and
+ * reads y.  Caller owns every buffer.  An argument or host-check error
+ * launches nothing; GDN_ERR_CUDA from the second launch of the two-launch
+ * form leaves the conv (cache advanced, y written) launched without its
+ * decode. */
 gdn_status gdn_decode_step_conv(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
                                 int32_t n, const void *x, int64_t ld_x, const float *w,
                                 const float *bias, void *y, int64_t ld_y, const void *g,

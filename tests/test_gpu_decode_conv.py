@@ -1,5 +1,7 @@
 """gdn_decode_step_conv: conv + SiLU and the decode step of one layer in one
-call, the decode launch overlapping the conv (programmatic dependent launch).
+call -- one fused kernel while its grid fits the GPU at once (few slots),
+else the conv launch with the decode as its programmatic dependent launch.
+Both forms are exercised (the decode-step layer with 4 and with 64 slots).
 
 Checked through the C ABI over three consecutive steps:
   * y against the float64 oracle's conv + SiLU (bf16: |got - ref| <= 1e-2 +
@@ -28,6 +30,12 @@ CASES = {
     # decode-step layer shape: 32/16 heads, K = V = 128, 64 of 256 slots, bf16
     "gdn_layer_bf16": dict(shape=synth.GDN_LAYER, n_slots=256, n_active=64, dtype="bf16",
                            pad_x=0, pad_y=0, bias=False, layer=0, n_layers=1),
+    # the same layer with 4 slots: one fused kernel
+    "gdn_layer_bf16_few": dict(shape=synth.GDN_LAYER, n_slots=256, n_active=4, dtype="bf16",
+                               pad_x=0, pad_y=0, bias=False, layer=0, n_layers=1),
+    # conv width 3 (the generic-width fused kernel), float32
+    "small_f32_w3": dict(shape=synth.LayerShape(4, 2, 32, 32, 256, 3), n_slots=9, n_active=5,
+                         dtype="f32", pad_x=0, pad_y=0, bias=True, layer=1, n_layers=2),
     # small heads in float32, second layer of two, with a conv bias
     "small_f32": dict(shape=synth.LayerShape(4, 2, 32, 32, 256, 4), n_slots=9, n_active=5,
                       dtype="f32", pad_x=0, pad_y=0, bias=True, layer=1, n_layers=2),
@@ -153,3 +161,40 @@ def test_decode_step_conv_argument_checks():
     torch.cuda.synchronize()
     assert torch.equal(pool.state, before[0]) and torch.equal(pool.conv, before[1])
     assert bool((o == 0).all()) and bool((y == 0).all())
+
+
+def test_decode_step_conv_alternating_forms_keep_the_cache_consistent():
+    """Steps with 4, 64, 4, 64 active slots of one pool (fused kernel, then
+    the launch pair, alternately; the fused kernel's tickets must end every
+    launch at zero) match a twin pool stepped with the two separate calls,
+    bit for bit."""
+    shape = synth.GDN_LAYER
+    rng = np.random.default_rng(66)
+    ids_all = rng.choice(256, 64, replace=False).astype(np.int32)
+    one, two = (_pool(shape, 1, 256, torch.bfloat16) for _ in range(2))
+    gen = torch.Generator(device="cuda").manual_seed(6)
+    one.state.normal_(0.0, 0.1, generator=gen)
+    one.conv.copy_(torch.randn(one.conv.shape, device="cuda", generator=gen))
+    two.state.copy_(one.state)
+    two.conv.copy_(one.conv)
+    w = dev(synth.conv_weights(rng, shape.conv_ch, shape.conv_k))
+    nq = shape.h_k * shape.dk
+    for step, n in enumerate((4, 64, 4, 64, 4)):
+        ids = dev_i32(ids_all[:n])
+        x = dev(synth.conv_input(rng, n, shape.conv_ch, "bf16"), "bf16")
+        tok = synth.token_inputs(rng, n, shape, "bf16")
+        g, b = dev(tok["g"], "bf16"), dev(tok["beta"], "bf16")
+        y1 = torch.empty(n, shape.conv_ch, device="cuda", dtype=torch.bfloat16)
+        y2 = torch.empty_like(y1)
+        o1 = torch.empty(n, shape.h_v, shape.dv, device="cuda")
+        o2 = torch.empty_like(o1)
+        abi.gdn_decode_step_conv(one, 0, ids, x, w, y1, g, b, o1)
+        abi.gdn_conv_silu(two, 0, ids, x, w, y2)
+        abi.gdn_decode_step(two, 0, ids, y2[:, :nq].view(n, shape.h_k, shape.dk),
+                            y2[:, nq:2 * nq].view(n, shape.h_k, shape.dk),
+                            y2[:, 2 * nq:].view(n, shape.h_v, shape.dv), g, b, o2)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2) and torch.equal(o1, o2), f"step {step} (n = {n})"
+        assert torch.equal(one.state, two.state), f"step {step}: state"
+        assert torch.equal(one.conv, two.conv), f"step {step}: conv cache"
+    assert abi.gdn_pool_get_error(one) == 0
