@@ -7,18 +7,21 @@ Headline (one JSON line on stdout): decode slot-steps/s for one GDN layer
 over 8192 channels, bf16 activations) on a 256-slot pool with 64 active slot
 ids drawn at random.  One step = one gdn_decode_step_conv call: the conv +
 SiLU over the 64 new tokens, then the decode step reading q, k, v straight
-out of the conv output (its launch overlapping the conv).  L2 is flushed (a
-512 MiB write) between timed steps, outside the timed events.
+out of the conv output.  L2 is flushed (a 512 MiB write) between timed steps,
+outside the timed events.
 
-Also in the line: the same metric end to end through the C ABI with inputs
-copied from pinned host memory and outputs copied back inside the timed
-region (`e2e`), the same step as two calls (`two_calls`: gdn_conv_silu, then
-gdn_decode_step), the decode kernel's HBM roofline fraction (timed on the
-decode launch of the two-call step), the oracle timed
-on the host cores (`cpu_baseline`), SM clocks sampled during timing, and
+Also in the line: the same metric end to end through the C ABI with every
+step's inputs copied from pinned host memory and its output copied back inside
+the timed regions (`e2e`; the copies run on a second stream, double-buffered,
+overlapping the neighbouring steps' compute), the same step as two calls
+(`two_calls`: gdn_conv_silu, then gdn_decode_step), the decode kernel's HBM
+roofline fraction (timed on the decode launch of the two-call step), the
+oracle timed on the host cores (`cpu_baseline`: one thread and all cores;
+decode, prefill and verify), SM clocks sampled during timing, and
 `secondary` measurements: the 18-layer slot sweep (N = 1 .. 512),
-speculative verify (128 slots, T = 4), varlen chunked prefill and the output
-gated RMSNorm.
+speculative verify (128 slots, T = 4), varlen chunked prefill with its
+roofline, the output gated RMSNorm, and the decode step on pools that store
+the state in bf16 / binary16.
 
 --impl reference times the float64 CPU oracle on a bounded sample of the same
 workload (the pages publish no runnable implementation of this path).
@@ -51,6 +54,22 @@ DECODE_KERNEL_BYTES_PER_SLOT = STATE_BYTES_PER_SLOT_LAYER + 2 * 16 * 128 * 2 + 3
     + 2 * 32 * 2 + 32 * 128 * 4
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_decode_pool256_active64.md")
 DECODE_SOURCE = os.path.join(ROOT, "gated_deltanet_recurrent_gb300", "csrc", "gdn_decode.cu")
+PREFILL_SUMMARY = os.path.join(ROOT, "profiles", "gdn_prefill_split_varlen8_piece2048.md")
+PREFILL_SOURCE = os.path.join(ROOT, "gated_deltanet_recurrent_gb300", "csrc",
+                              "gdn_prefill_split.cu")
+# chunked prefill, algorithmic work per token and value head (chunk 64, K = V = 128,
+# triangular blocks exploited): the state-side products run on the tensor cores
+# in tf32 (Delta = F T^T 16,640; W S0^T, Q S0^T, state update 3 x 32,768;
+# P Delta 8,320), the key-side Gram products in bf16 (K K^T 8,064 + Q K^T 8,320),
+# forming T on the CUDA cores (~1,365)
+PREFILL_FLOPS_TF32 = 16640 + 3 * 32768 + 8320
+PREFILL_FLOPS_BF16 = 8064 + 8320
+PREFILL_FLOPS_SIMT = 1365
+# bytes per token: q, k (16 x 128 each), v (32 x 128), g, beta (32 each) in bf16,
+# o (32 x 128) out in bf16; plus the state read and written once per
+# (sequence, call): 2 x 32 x 128 x 128 x 4 bytes
+PREFILL_BYTES_PER_TOKEN = 2 * (2 * 16 * 128 + 32 * 128 + 2 * 32) + 2 * 32 * 128
+PREFILL_STATE_BYTES_PER_SEQ_CALL = STATE_BYTES_PER_SLOT_LAYER
 
 
 def _parse():
@@ -61,12 +80,12 @@ def _parse():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--sweep-steps", type=int, default=128)
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--sections", default="sweep,verify,prefill,norm",
+    ap.add_argument("--sections", default="sweep,verify,prefill,norm,half",
                     help="secondary measurements to run (comma list of sweep, verify, prefill, "
-                         "norm)")
+                         "norm, half)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     return ap.parse_args()
 
 
@@ -102,12 +121,138 @@ def _oracle_decode_sample(n_slots_per_step: int, steps: int, warmup: int):
     return time.perf_counter() - t0, steps * m
 
 
+_WL = {}
+
+
+def _workloads(n_tok=None):
+    """The oracle baseline's inputs, built once per process: the decode and
+    spec-verify workloads, and 8 prefill sequences of n_tok tokens drawn with
+    the varlen-prefill workload's recipe."""
+    from gated_deltanet_recurrent_gb300 import synth
+    if "decode" not in _WL:
+        _WL["decode"] = synth.decode_workload(seed=1)
+        _WL["verify"] = synth.verify_workload(seed=4, n_decode=0)
+    if n_tok is not None and _WL.get("prefill_tokens") != n_tok:
+        _WL["prefill"] = synth.prefill_workload(seed=3, lengths=[n_tok] * 8)
+        _WL["prefill_tokens"] = n_tok
+    return _WL
+
+
+def _decode_slots_task(args):
+    """(slot indices, steps) -> (seconds, slot-steps): the oracle's conv +
+    decode over those slots of the decode workload, `steps` times."""
+    idx, steps = args
+    import numpy as np
+    from oracle import gdn_oracle as O
+    wl = _workloads()["decode"]
+    s = wl["shape"]
+    nq = s.h_k * s.dk
+    S = {i: wl["states"][i].astype(np.float64) for i in idx}
+    X = {i: wl["conv_cache"][i].astype(np.float64) for i in idx}
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for i in idx:
+            y, X[i] = O.conv_silu(wl["x"][i:i + 1], X[i], wl["conv_w"])
+            y = y[0]
+            S[i], _ = O.gdn_step(S[i], y[:nq].reshape(s.h_k, s.dk),
+                                 y[nq:2 * nq].reshape(s.h_k, s.dk),
+                                 y[2 * nq:].reshape(s.h_v, s.dv),
+                                 wl["tok"]["g"][i], wl["tok"]["beta"][i])
+    return time.perf_counter() - t0, steps * len(idx)
+
+
+def _prefill_task(args):
+    """(sequence, chunk or None) -> (seconds, tokens): the oracle's prefill of
+    one sample sequence (all heads), token by token (chunk None) or in the
+    chunked form."""
+    seq, chunk = args
+    from oracle import gdn_oracle as O
+    wl = _WL["prefill"]
+    lo, hi = int(wl["cu_seqlens"][seq]), int(wl["cu_seqlens"][seq + 1])
+    tok = [wl["tok"][k][lo:hi] for k in ("q", "k", "v", "g", "beta")]
+    t0 = time.perf_counter()
+    if chunk is None:
+        O.gdn_recurrent(wl["states"][seq], *tok)
+    else:
+        O.gdn_chunked(wl["states"][seq], *tok, chunk=chunk)
+    return time.perf_counter() - t0, hi - lo
+
+
+def _verify_task(args):
+    """(slot indices, repeats) -> (seconds, slot-verifies): the oracle's
+    speculative verify with commit (T = 4) of those slots of the verify
+    workload."""
+    idx, reps = args
+    from oracle import gdn_oracle as O
+    wl = _workloads()["verify"]
+    T = wl["T"]
+    d = wl["draft"]
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        for i in idx:
+            sl = slice(i * T, (i + 1) * T)
+            O.spec_verify(wl["states"][i], d["q"][sl], d["k"][sl], d["v"][sl], d["g"][sl],
+                          d["beta"][sl], wl["accept_len"][i])
+    return time.perf_counter() - t0, reps * len(idx)
+
+
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _timed_parallel(pool, fn, tasks):
+    """Wall time of running tasks on the pool; returns (seconds, units)."""
+    t0 = time.perf_counter()
+    res = pool.map(fn, tasks, chunksize=1)
+    return time.perf_counter() - t0, sum(u for _, u in res)
+
+
 def _cpu_baseline_child(seconds: float):
-    # calibrate one step of 8 slots, then run for about `seconds`
-    dt, _ = _oracle_decode_sample(8, 1, 0)
+    """The oracle on the host cores: one thread, then every core (one spawned
+    worker process per core, each on its own slots or sequence), for decode,
+    prefill (token by token and chunked) and verify.  About `seconds` of
+    wall time per one-thread measurement; inputs are built before timing."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    out = {"cpu_model": _cpu_model(), "nproc": cores}
+    _workloads(32)
+    # decode: calibrate one step of 8 slots, then run for about `seconds`
+    dt, _ = _decode_slots_task((list(range(8)), 1))
     steps = max(1, int(seconds / max(dt, 1e-6)))
-    dt, units = _oracle_decode_sample(8, steps, 1)
-    print(json.dumps({"value": units / dt, "seconds": dt, "units": units, "steps": steps}))
+    dt, units = _decode_slots_task((list(range(8)), steps))
+    out["decode_1t"] = {"value": units / dt, "seconds": dt, "units": units, "steps": steps}
+    # prefill: sequences sized for about seconds / 2 token by token
+    t1, _ = _prefill_task((0, None))
+    n_tok = max(64, min(2048, int(seconds / 2 / max(t1 / 32, 1e-6))))
+    _workloads(n_tok)
+    dt, units = _prefill_task((0, None))
+    out["prefill_tbt_1t"] = {"value": units / dt, "seconds": dt, "tokens": units}
+    dt, units = _prefill_task((0, 64))
+    out["prefill_chunked_1t"] = {"value": units / dt, "seconds": dt, "tokens": units}
+    # verify
+    dv, _ = _verify_task(([0], 1))
+    reps = max(1, int(seconds / 2 / max(dv * 8, 1e-6)))
+    dt, units = _verify_task((list(range(8)), reps))
+    out["verify_1t"] = {"value": units / dt, "seconds": dt, "units": units}
+    with mp.get_context("spawn").Pool(cores, initializer=_workloads, initargs=(n_tok,)) as pool:
+        pool.map(_verify_task, [([0], 1)] * cores, chunksize=1)   # workers up
+        dt, units = _timed_parallel(pool, _decode_slots_task,
+                                    [([w % 64], steps * 8) for w in range(cores)])
+        out["decode_all"] = {"value": units / dt, "seconds": dt, "units": units}
+        dt, units = _timed_parallel(pool, _prefill_task, [(w % 8, None) for w in range(cores)])
+        out["prefill_tbt_all"] = {"value": units / dt, "seconds": dt, "tokens": units}
+        dt, units = _timed_parallel(pool, _verify_task,
+                                    [([w % 128], reps * 8) for w in range(cores)])
+        out["verify_all"] = {"value": units / dt, "seconds": dt, "units": units}
+    print(json.dumps(out))
 
 
 def _cpu_env():
@@ -121,14 +266,31 @@ def _cpu_env():
 def cpu_baseline(seconds: float):
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
                         "--cpu-seconds", str(seconds)], capture_output=True, text=True,
-                       env=_cpu_env(), cwd=ROOT, timeout=600)
+                       env=_cpu_env(), cwd=ROOT, timeout=900)
     if r.returncode != 0:
         return {"error": r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"float64 numpy oracle, conv+SiLU then gated delta rule, on 8 of the 64 "
-                      f"active slots of the decode workload for {d['steps']} steps "
-                      f"({d['units']} slot-steps, {d['seconds']:.1f} s), single thread"}
+    one, allc = d["decode_1t"], d["decode_all"]
+    return {"value": allc["value"], "unit": UNIT, "cores": d["nproc"], "kind": "oracle",
+            "cpu_model": d["cpu_model"],
+            "sample": f"float64 numpy oracle, conv+SiLU then gated delta rule on the decode "
+                      f"workload: {d['nproc']} worker processes (one per core), each on its "
+                      f"own slot for {one['steps'] * 8} steps ({allc['units']} slot-steps, "
+                      f"{allc['seconds']:.1f} s wall)",
+            "single_thread": {"value": one["value"], "unit": UNIT, "cores": 1,
+                              "sample": f"8 slots x {one['steps']} steps, "
+                                        f"{one['seconds']:.1f} s"},
+            "prefill": {"unit": "tokens/s",
+                        "token_by_token_1t": d["prefill_tbt_1t"]["value"],
+                        "chunked_1t": d["prefill_chunked_1t"]["value"],
+                        "token_by_token_all_cores": d["prefill_tbt_all"]["value"],
+                        "sample": f"sequences of {d['prefill_tbt_1t']['tokens']} tokens drawn "
+                                  f"with the varlen-prefill recipe (32/16 heads, K = V = 128, "
+                                  f"bf16 values); all cores: one sequence per worker"},
+            "verify": {"unit": "slot-verifies/s", "one_thread": d["verify_1t"]["value"],
+                       "all_cores": d["verify_all"]["value"],
+                       "sample": "verify with commit, T = 4, slots of the spec-verify "
+                                 "workload"}}
 
 
 # ------------------------------------------------------------------- clocks
@@ -178,17 +340,18 @@ def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
-        return d["hbm_gbs"], d.get("bf16_tflops"), "measured"
+        return d["hbm_gbs"], d.get("bf16_tflops") or 1900.0, "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, 1900.0, "fallback"
 
 
-def _profiled_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode source."""
+def _profile_fields(summary, source):
+    """Machine-read fields ('- key: `value`' lines) of a committed ncu summary,
+    or None unless it was taken on the current kernel source (its
+    source_sha256_16 field matches)."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-        sha = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()[:16]
+        text = open(summary).read()
+        sha = hashlib.sha256(open(source, "rb").read()).hexdigest()[:16]
     except OSError:
         return None
     fields = {}
@@ -196,62 +359,81 @@ def _profiled_traffic():
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_sha256_16") != sha:
-        return None
+    return fields if fields.get("source_sha256_16") == sha else None
+
+
+def _profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode source."""
+    f = _profile_fields(PROFILE_SUMMARY, DECODE_SOURCE)
     try:
-        return float(fields["dram_bytes_per_launch"])
+        return float(f["dram_bytes_per_launch"]) if f else None
     except (KeyError, ValueError):
         return None
 
 
 class DecodeBench:
-    def __init__(self, torch, abi, synth, device):
+    def __init__(self, torch, abi, synth, device, state_dtype=None):
         self.torch = torch
         self.abi = abi
         wl = synth.decode_workload(seed=1)
         self.shape = s = wl["shape"]
         self.n = n = len(wl["slot_ids"])
         t = lambda a, dt=torch.bfloat16: torch.from_numpy(a).to(device=device, dtype=dt)
+        sdt = state_dtype or torch.float32
         self.pool = abi.Pool.for_shape(s, 1, wl["n_slots"], conv_dtype=torch.bfloat16,
-                                       host_checks=False, device=device)
+                                       host_checks=False, device=device, state_dtype=sdt)
         gen = torch.Generator(device=device).manual_seed(1)
-        self.pool.state.normal_(0.0, 0.1, generator=gen)
+        self.pool.state.copy_(torch.randn(self.pool.state.shape, device=device,
+                                          generator=gen).mul_(0.1).to(sdt))
         lid = torch.from_numpy(wl["slot_ids"]).long().to(device)
-        self.pool.state[0, lid] = t(wl["states"], torch.float32)
+        self.pool.state[0, lid] = t(wl["states"], torch.float32).to(sdt)
         self.pool.conv[0, lid] = t(wl["conv_cache"])
         self.ids = torch.from_numpy(wl["slot_ids"]).to(device)
         # x, g and beta of a step are packed into one bf16 buffer (x first, each
-        # part 16-byte aligned), so the end-to-end leg stages them with one copy
+        # part 16-byte aligned), so the end-to-end leg stages them with one copy;
+        # two such buffers (and two o) let step i+1's inputs and step i-1's
+        # output move while step i computes
         nx, ng = n * s.conv_ch, n * s.h_v
-        self.inputs = torch.empty(nx + 2 * ng, device=device, dtype=torch.bfloat16)
-        self.x = self.inputs[:nx].view(n, s.conv_ch)
-        self.g = self.inputs[nx:nx + ng].view(n, s.h_v)
-        self.beta = self.inputs[nx + ng:].view(n, s.h_v)
-        self.x.copy_(t(wl["x"]))
-        self.g.copy_(t(wl["tok"]["g"]))
-        self.beta.copy_(t(wl["tok"]["beta"]))
+        self.nx, self.ng = nx, ng
+        self.inputs = [torch.empty(nx + 2 * ng, device=device, dtype=torch.bfloat16)
+                       for _ in range(2)]
+        for buf in self.inputs:
+            buf[:nx].copy_(t(wl["x"]).reshape(-1))
+            buf[nx:nx + ng].copy_(t(wl["tok"]["g"]).reshape(-1))
+            buf[nx + ng:].copy_(t(wl["tok"]["beta"]).reshape(-1))
+        self.x, self.g, self.beta = self.parts(0)
         self.w = t(wl["conv_w"], torch.float32)
         self.y = torch.empty(n, s.conv_ch, device=device, dtype=torch.bfloat16)
         nq = s.h_k * s.dk
         self.q = self.y[:, :nq].view(n, s.h_k, s.dk)
         self.k = self.y[:, nq:2 * nq].view(n, s.h_k, s.dk)
         self.v = self.y[:, 2 * nq:].view(n, s.h_v, s.dv)
-        self.o = torch.empty(n, s.h_v, s.dv, device=device)
+        self.os = [torch.empty(n, s.h_v, s.dv, device=device) for _ in range(2)]
+        self.o = self.os[0]
         self.flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
-        # pinned host buffers for the end-to-end leg
-        self.inputs_h = self.inputs.cpu().pin_memory()
-        self.o_h = torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
-        self.h2d = self.inputs_h.numel() * self.inputs_h.element_size()
-        self.d2h = self.o_h.numel() * self.o_h.element_size()
+        # pinned host buffers for the end-to-end leg (one per step parity)
+        self.inputs_h = [b.cpu().pin_memory() for b in self.inputs]
+        self.o_h = [torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
+                    for _ in range(2)]
+        self.h2d = self.inputs_h[0].numel() * self.inputs_h[0].element_size()
+        self.d2h = self.o_h[0].numel() * self.o_h[0].element_size()
+        self.copy_stream = torch.cuda.Stream(device=device)
+
+    def parts(self, j):
+        s, n, nx, ng = self.shape, self.n, self.nx, self.ng
+        b = self.inputs[j]
+        return b[:nx].view(n, s.conv_ch), b[nx:nx + ng].view(n, s.h_v), b[nx + ng:].view(n, s.h_v)
 
     def flush(self):
         self.flush_buf.zero_()
 
-    def step(self):
+    def step(self, j=0):
         """The decode step of the layer as one call (conv + SiLU, then the
-        decode launch overlapping it)."""
-        self.abi.gdn_decode_step_conv(self.pool, 0, self.ids, self.x, self.w, self.y, self.g,
-                                      self.beta, self.o)
+        decode), on input buffer j."""
+        x, g, beta = self.parts(j)
+        self.abi.gdn_decode_step_conv(self.pool, 0, self.ids, x, self.w, self.y, g, beta,
+                                      self.os[j])
 
     def step_two_calls(self, ev=None):
         """The same step as two calls; ev brackets the decode launch."""
@@ -263,11 +445,6 @@ class DecodeBench:
                           self.o)
         if ev is not None:
             ev[1].record()
-
-    def step_e2e(self):
-        self.inputs.copy_(self.inputs_h, non_blocking=True)
-        self.step()
-        self.o_h.copy_(self.o, non_blocking=True)
 
     def timed(self, fn, steps, kernel_events=False):
         torch = self.torch
@@ -286,6 +463,75 @@ class DecodeBench:
         total = sum(a.elapsed_time(b) for a, b in evs) / 1e3
         ktime = sum(a.elapsed_time(b) for a, b in kev) / 1e3 if kernel_events else None
         return total, ktime
+
+    def timed_e2e(self, steps):
+        """End to end through the C ABI from pinned host memory: every step's
+        packed inputs are copied host -> device and its o device -> host, on a
+        copy stream, overlapped with the neighbouring steps' compute.  The
+        timed region of step i holds its compute and the copies of steps
+        i + 1 (in) and i - 1 (out): the compute stream waits for both before
+        the region's end event, and a region's copies start only after its
+        start event, so no copy runs in the untimed L2 flush between regions.
+        A last region holds the final output copy.  Returns seconds."""
+        torch = self.torch
+        cs, cp = torch.cuda.current_stream(), self.copy_stream
+        E = lambda t=True: torch.cuda.Event(enable_timing=t)
+        starts = [E() for _ in range(steps + 1)]
+        ends = [E() for _ in range(steps + 1)]
+        h2d_done = [E(False) for _ in range(steps + 1)]
+
+        def h2d(i):
+            self.inputs[i % 2].copy_(self.inputs_h[i % 2], non_blocking=True)
+            h2d_done[i].record(cp)
+
+        def d2h(i):
+            self.o_h[i % 2].copy_(self.os[i % 2], non_blocking=True)
+
+        torch.cuda.synchronize()
+        for i in range(steps + 1):
+            self.flush()
+            starts[i].record(cs)
+            cp.wait_event(starts[i])
+            with torch.cuda.stream(cp):
+                if i == 0:
+                    h2d(0)
+                if i > 0:
+                    d2h(i - 1)
+                if i + 1 < steps:
+                    h2d(i + 1)
+            if i < steps:
+                cs.wait_event(h2d_done[i])
+                self.step(i % 2)
+            cs.wait_stream(cp)
+            ends[i].record(cs)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3
+
+
+def half_state_bench(torch, abi, synth, device, steps, peak):
+    """The decode-step workload on pools storing the state in bf16 / f16
+    (float32 arithmetic): one-call step and the decode kernel alone."""
+    out = {}
+    for name, dt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        b = DecodeBench(torch, abi, synth, device, state_dtype=dt)
+        for _ in range(3):
+            b.step()
+            b.step_two_calls()
+        torch.cuda.synchronize()
+        t_one, _ = b.timed(b.step, steps)
+        _, t_kernel = b.timed(b.step_two_calls, steps, kernel_events=True)
+        per_slot = DECODE_KERNEL_BYTES_PER_SLOT - STATE_BYTES_PER_SLOT_LAYER // 2
+        gbs = per_slot * b.n * steps / t_kernel / 1e9
+        out[name] = {"slot_steps_per_s": b.n * steps / t_one,
+                     "us_per_step": t_one / steps * 1e6,
+                     "decode_kernel_us": t_kernel / steps * 1e6,
+                     "decode_algorithmic_bytes_per_launch": per_slot * b.n,
+                     "decode_gbs": gbs, "decode_hbm_frac": gbs / peak}
+        del b
+    out["workload"] = ("decode step workload (64 of 256 slots, one layer, bf16 activations) "
+                       "on a pool storing the state in bf16 / binary16, float32 arithmetic; "
+                       "L2 flushed between steps")
+    return out
 
 
 def sweep_bench(torch, abi, synth, device, steps):
@@ -466,7 +712,7 @@ def norm_bench(torch, abi, device, steps, peak):
             "hbm_frac": nbytes / t / 1e9 / peak}
 
 
-def prefill_bench(torch, abi, synth, device, steps):
+def prefill_bench(torch, abi, synth, device, steps, hbm_peak, bf16_peak):
     wl = synth.prefill_workload(seed=3)
     s = wl["shape"]
     lens = wl["lengths"]
@@ -518,14 +764,36 @@ def prefill_bench(torch, abi, synth, device, steps):
     except abi.GDNError as e:
         return {"unavailable": str(e)}
     total = int(cu[-1])
+    pass_s = t / steps
+    seq_calls = sum(int(c[0].numel()) for c in calls)
+    nbytes = total * PREFILL_BYTES_PER_TOKEN + seq_calls * PREFILL_STATE_BYTES_PER_SEQ_CALL
+    heads = s.h_v
+    f_tf32 = total * heads * PREFILL_FLOPS_TF32
+    f_bf16 = total * heads * PREFILL_FLOPS_BF16
+    flops = f_tf32 + f_bf16 + total * heads * PREFILL_FLOPS_SIMT
+    # lower bounds on the pass: HBM traffic at the copy peak, tensor work at the
+    # dense bf16 peak (tf32 runs at half of it on this part)
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    t_tc = f_tf32 / (bf16_peak * 0.5e12) + f_bf16 / (bf16_peak * 1e12)
+    prof = _profile_fields(PREFILL_SUMMARY, PREFILL_SOURCE) or {}
+    roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "algorithmic_bytes_per_pass": nbytes, "algorithmic_flops_per_pass": flops,
+            "arithmetic_intensity": flops / nbytes,
+            "achieved_gbs": nbytes / pass_s / 1e9, "achieved_tflops": flops / pass_s / 1e12,
+            "roofline_ms": max(t_hbm, t_tc) * 1e3, "frac": max(t_hbm, t_tc) / pass_s,
+            "peaks": f"HBM {hbm_peak:.0f} GB/s, bf16 {bf16_peak:.0f} TFLOP/s, tf32 half of "
+                     f"bf16 (MEASURED_PEAKS.json)",
+            "tensor_pipe_pct_state_walk": prof.get("tensor_pipe_pct_seq"),
+            "tensor_pipe_pct_key_side": prof.get("tensor_pipe_pct_prep"),
+            "dram_bytes_first_call": prof.get("dram_bytes_call0")}
     return {"workload": f"varlen chunked prefill, decode-step layer shape, 8 sequences "
                         f"(lengths {lens}), pieces of 2048 tokens with the state carried "
                         f"between calls, bf16 in/out, chunk 64",
-            "tokens_per_s": total * steps / t, "ms_per_pass": t / steps * 1e3,
-            "calls_per_pass": len(calls),
+            "tokens_per_s": total * steps / t, "ms_per_pass": pass_s * 1e3,
+            "calls_per_pass": len(calls), "tokens_per_pass": total,
             "single_launch_tokens_per_s": total * steps / t_single,
             "token_by_token_tokens_per_s": total * steps / t_rec,
-            "speedup_over_token_by_token": t_rec / t}
+            "speedup_over_token_by_token": t_rec / t, "roofline": roof}
 
 
 def max_over_ranks(values, dist, device):
@@ -548,13 +816,13 @@ def run_gpu(args, rank, world):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
-    peak, _, peak_kind = _peaks()
+    peak, tc_peak, peak_kind = _peaks()
 
     b = DecodeBench(torch, abi, synth, device)
     for _ in range(max(3, args.warmup)):
         b.step()
         b.step_two_calls()
-        b.step_e2e()
+    b.timed_e2e(max(3, args.warmup))
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
@@ -570,7 +838,7 @@ def run_gpu(args, rank, world):
     barrier()
     t_two, t_kernel = b.timed(b.step_two_calls, args.steps, kernel_events=True)
     barrier()
-    t_e2e, _ = b.timed(b.step_e2e, args.steps)
+    t_e2e = b.timed_e2e(args.steps)
     barrier()
     secondary = {}
     sections = set() if args.no_secondary else set(args.sections.split(","))
@@ -579,9 +847,11 @@ def run_gpu(args, rank, world):
     if "verify" in sections:
         secondary["verify"] = verify_bench(torch, abi, synth, device, 50, peak)
     if "prefill" in sections:
-        secondary["prefill"] = prefill_bench(torch, abi, synth, device, 5)
+        secondary["prefill"] = prefill_bench(torch, abi, synth, device, 5, peak, tc_peak)
     if "norm" in sections:
         secondary["norm"] = norm_bench(torch, abi, device, 20, peak)
+    if "half" in sections:
+        secondary["half_state"] = half_state_bench(torch, abi, synth, device, 50, peak)
     time.sleep(0.2)
     clk = clocks.stop()
     if dist is not None:
@@ -604,8 +874,10 @@ def run_gpu(args, rank, world):
                    f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": units / t_e2e, "unit": UNIT, "h2d_bytes_per_step": b.h2d,
                 "d2h_bytes_per_step": b.d2h,
-                "note": "pinned host x|g|beta (one packed buffer, one copy) -> device, "
-                        "one-call conv + decode, o -> pinned host"},
+                "note": "per step: pinned host x|g|beta (one packed buffer, one copy) -> "
+                        "device, one-call conv + decode, o -> pinned host; copies on a "
+                        "second stream, double-buffered, overlapping the neighbouring "
+                        "steps' compute inside the timed regions"},
         "two_calls": {"value": units / t_two, "unit": UNIT,
                       "ms_per_step": t_two / args.steps * 1e3,
                       "note": "the same step as gdn_conv_silu then gdn_decode_step, "

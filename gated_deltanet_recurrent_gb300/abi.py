@@ -16,7 +16,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
 
-GDN_F32, GDN_BF16 = 0, 1
+GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SLOT", 3: "GDN_ERR_DUP_SLOT",
           4: "GDN_ERR_DTYPE", 5: "GDN_ERR_SIZE", 6: "GDN_ERR_UNSUPPORTED", 7: "GDN_ERR_CUDA"}
 DEVERR_SLOT, DEVERR_SEQ, DEVERR_COUNT, DEVERR_TIMEOUT = 1, 2, 4, 8
@@ -44,7 +44,7 @@ class gdn_pool_desc(ctypes.Structure):
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
                 ("conv_ch", ctypes.c_int32), ("conv_k", ctypes.c_int32),
                 ("conv_dtype", ctypes.c_int), ("host_checks", ctypes.c_int32),
-                ("prefill_workspace_max", ctypes.c_uint64)]
+                ("prefill_workspace_max", ctypes.c_uint64), ("state_dtype", ctypes.c_int)]
 
 
 class gdn_qkv(ctypes.Structure):
@@ -163,18 +163,25 @@ def _qkv(pool: "Pool", q, k, v, g, beta) -> gdn_qkv:
                    ld_q, ld_v, dts.pop())
 
 
+_STATE_DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
+
+
 class Pool:
     """A pool handle plus the torch tensors holding its state and conv cache:
-    state [n_layers, n_slots, h_v, dv, dk] float32, conv [n_layers, n_slots,
-    conv_ch, conv_k-1] in conv_dtype.  Both start at zero."""
+    state [n_layers, n_slots, h_v, dv, dk] in state_dtype (float32, or
+    bfloat16 / float16 storage), conv [n_layers, n_slots, conv_ch, conv_k-1]
+    in conv_dtype.  Both start at zero."""
 
     def __init__(self, n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k,
                  conv_dtype=torch.bfloat16, host_checks=True, device="cuda",
-                 prefill_workspace_max=0):
+                 prefill_workspace_max=0, state_dtype=torch.float32):
+        if state_dtype not in _STATE_DTYPES:
+            raise GDNError(4, f"unsupported state dtype {state_dtype}")
         self.desc = gdn_pool_desc(n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k,
                                   GDN_F32 if conv_dtype == torch.float32 else GDN_BF16,
-                                  1 if host_checks else 0, prefill_workspace_max)
-        self.state = torch.zeros((n_layers, n_slots, h_v, dv, dk), dtype=torch.float32,
+                                  1 if host_checks else 0, prefill_workspace_max,
+                                  _STATE_DTYPES[state_dtype])
+        self.state = torch.zeros((n_layers, n_slots, h_v, dv, dk), dtype=state_dtype,
                                  device=device)
         self.conv = torch.zeros((n_layers, n_slots, conv_ch, conv_k - 1), dtype=conv_dtype,
                                 device=device)
@@ -182,10 +189,10 @@ class Pool:
 
     @classmethod
     def for_shape(cls, shape, n_layers, n_slots, conv_dtype=torch.bfloat16, host_checks=True,
-                  device="cuda", prefill_workspace_max=0):
+                  device="cuda", prefill_workspace_max=0, state_dtype=torch.float32):
         return cls(n_layers, n_slots, shape.h_v, shape.h_k, shape.dk, shape.dv,
                    shape.conv_ch, shape.conv_k, conv_dtype, host_checks, device,
-                   prefill_workspace_max)
+                   prefill_workspace_max, state_dtype)
 
     def set_host_checks(self, on: bool):
         """Recreate the handle with host checks switched on or off (same memory)."""

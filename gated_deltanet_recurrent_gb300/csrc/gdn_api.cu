@@ -57,6 +57,8 @@ gdn_status check_desc(const gdn_pool_desc *d) {
   if (d->h_v % d->h_k != 0) return fail(GDN_ERR_ARG, "h_v (%d) is not a multiple of h_k (%d)",
                                         d->h_v, d->h_k);
   if (!dtype_ok(d->conv_dtype)) return fail(GDN_ERR_DTYPE, "conv_dtype must be F32 or BF16");
+  if (d->state_dtype != GDN_F32 && d->state_dtype != GDN_BF16 && d->state_dtype != GDN_F16)
+    return fail(GDN_ERR_DTYPE, "state_dtype must be F32, BF16 or F16");
   if (!dk_supported(d->dk)) return fail(GDN_ERR_UNSUPPORTED, "dk=%d (supported: 16,32,64,128)",
                                         d->dk);
   if (d->dv % 4 != 0 || d->dv > 4096) return fail(GDN_ERR_UNSUPPORTED,
@@ -177,7 +179,7 @@ gdn_status resolve_qkv(const gdn_pool *p, const gdn_qkv *in, int64_t tokens, gdn
 // point, so the library does not link libcuda.  Returns false if unavailable.
 bool encode_state_map(gdn_pool *p) {
   const gdn_pool_desc &d = p->desc;
-  if (d.dk != 128 || d.dv != 128) return false;
+  if (d.dk != 128 || d.dv != 128 || d.state_dtype != GDN_F32) return false;
   const uint64_t rows = (uint64_t)d.n_layers * d.n_slots * d.h_v * d.dv;
   if (rows > 0x7fffffffull) return false;
   void *fn = nullptr;
@@ -221,7 +223,8 @@ const char *gdn_last_error_message(void) { return g_last_msg.c_str(); }
 
 size_t gdn_pool_state_bytes(const gdn_pool_desc *d) {
   if (!d || d->n_layers < 0 || d->n_slots < 0) return 0;
-  return (size_t)d->n_layers * d->n_slots * d->h_v * d->dv * d->dk * sizeof(float);
+  return (size_t)d->n_layers * d->n_slots * d->h_v * d->dv * d->dk *
+         (d->state_dtype == GDN_F32 ? sizeof(float) : 2);
 }
 
 size_t gdn_pool_conv_bytes(const gdn_pool_desc *d) {
@@ -277,7 +280,8 @@ gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t st
   p->sm_count = sm_count;
   p->view = gdn::PoolView{static_cast<float *>(state_mem), conv_mem, err,
                           desc->n_layers, desc->n_slots, desc->h_v, desc->h_k, desc->dk,
-                          desc->dv, desc->conv_ch, desc->conv_k, desc->conv_dtype, err + 1};
+                          desc->dv, desc->conv_ch, desc->conv_k, desc->conv_dtype, err + 1,
+                          desc->state_dtype};
   p->has_tmap = encode_state_map(p);
   cudaMemPoolProps props = {};
   props.allocType = cudaMemAllocationTypePinned;

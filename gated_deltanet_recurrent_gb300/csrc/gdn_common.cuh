@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,6 +37,44 @@ struct Elem<bf16> {
   static __device__ __forceinline__ float load1(const bf16 *p) { return __bfloat162float(*p); }
   static __device__ __forceinline__ void store1(bf16 *p, float x) { *p = __float2bfloat16_rn(x); }
 };
+
+// ---- state storage: float32, or bf16 / f16 elements converted to and from
+// float32 registers (round to nearest even on every store) ----
+
+// four consecutive state elements starting at element e (a multiple of 4) of
+// `base` (global or shared memory)
+__device__ __forceinline__ float4 state_ld4(const void *base, int64_t e, gdn_dtype sd) {
+  if (sd == GDN_F32) return reinterpret_cast<const float4 *>(base)[e / 4];
+  const uint2 r = reinterpret_cast<const uint2 *>(base)[e / 4];
+  if (sd == GDN_BF16)
+    return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u),
+                       __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// store four state elements at element e; STREAM: evict-first global store
+template <bool STREAM>
+__device__ __forceinline__ void state_st4(void *base, int64_t e, float4 v, gdn_dtype sd) {
+  if (sd == GDN_F32) {
+    float4 *p = reinterpret_cast<float4 *>(base) + e / 4;
+    if (STREAM) __stcs(p, v); else *p = v;
+    return;
+  }
+  uint2 r;
+  if (sd == GDN_BF16) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    r.x = *reinterpret_cast<const unsigned *>(&a);
+    r.y = *reinterpret_cast<const unsigned *>(&b);
+  } else {
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    r.x = *reinterpret_cast<const unsigned *>(&a);
+    r.y = *reinterpret_cast<const unsigned *>(&b);
+  }
+  uint2 *p = reinterpret_cast<uint2 *>(base) + e / 4;
+  if (STREAM) __stcs(p, r); else *p = r;
+}
 
 __device__ __forceinline__ float dot4(const float4 a, const float4 b) {
   return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;

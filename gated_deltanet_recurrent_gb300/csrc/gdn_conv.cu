@@ -280,10 +280,10 @@ __global__ void reset_kernel(PoolView p, const int32_t *__restrict__ slot_ids) {
   }
   const int64_t start = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  float4 *st = reinterpret_cast<float4 *>(p.state + ((int64_t)layer * p.n_slots + slot) *
-                                                        p.state_slot_elems());
-  const int64_t n4 = p.state_slot_elems() / 4;  // dk is a multiple of 4
-  for (int64_t e = start; e < n4; e += stride) st[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // the slot's state as 16-byte words (dk * element size is a multiple of 16)
+  uint4 *st = reinterpret_cast<uint4 *>(p.state_at(p.state_head_elem(layer, slot, 0)));
+  const int64_t n16 = p.state_slot_elems() * p.state_esz() / 16;
+  for (int64_t e = start; e < n16; e += stride) st[e] = make_uint4(0u, 0u, 0u, 0u);
   const int64_t nc = p.conv_slot_elems();
   const int64_t coff = ((int64_t)layer * p.n_slots + slot) * nc;
   if (p.conv_dtype == GDN_F32)
@@ -304,10 +304,10 @@ __global__ void copy_kernel(PoolView p, const int32_t *__restrict__ src,
   }
   const int64_t start = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t per = p.state_slot_elems();
-  const float4 *sa = reinterpret_cast<const float4 *>(p.state + ((int64_t)layer * p.n_slots + a) * per);
-  float4 *sb = reinterpret_cast<float4 *>(p.state + ((int64_t)layer * p.n_slots + b) * per);
-  for (int64_t e = start; e < per / 4; e += stride) sb[e] = sa[e];
+  const int64_t n16 = p.state_slot_elems() * p.state_esz() / 16;
+  const uint4 *sa = reinterpret_cast<const uint4 *>(p.state_at(p.state_head_elem(layer, a, 0)));
+  uint4 *sb = reinterpret_cast<uint4 *>(p.state_at(p.state_head_elem(layer, b, 0)));
+  for (int64_t e = start; e < n16; e += stride) sb[e] = sa[e];
   const int64_t nc = p.conv_slot_elems();
   if (p.conv_dtype == GDN_F32) {
     const float *ca = static_cast<const float *>(p.conv) + ((int64_t)layer * p.n_slots + a) * nc;

@@ -17,21 +17,23 @@ namespace {
 
 using rows::kThreads;
 using rows::kBulkBytes;
-using rows::state_head;
 using rows::dispatch;
 
-// Bulk-staged decode: the CTA's 16 KiB state tile (R rows of one head) is fetched by one cp.async.bulk onto an mbarrier, so every CTA has
-// its whole tile in flight from its first cycle while its threads normalise
-// q and k; rows are then read from shared memory, updated, and stored back
-// with 128-bit streaming stores.  grid (ceil(dv / R), h_v, n).
+// Bulk-staged decode: the CTA's 16 KiB state tile (R rows of one head: 32 of
+// float32 or 64 of a bf16 / f16 state at dk = 128) is fetched by one cp.async.bulk onto
+// an mbarrier, so every CTA has its whole tile in flight from its first cycle
+// while its threads normalise q and k; rows are then read from shared memory,
+// widened to float32, updated, and stored back (rounded to the state's
+// storage type) with streaming stores.  grid (ceil(dv / R), h_v, n).
 // AFTER_CONV: launched as a programmatic dependent of the conv that writes q,
 // k and v; the tile fetch is issued before the grid-dependency wait, every
 // read of the token inputs after it.
-template <int DK, typename TI, typename TO, bool AFTER_CONV>
-__global__ void __launch_bounds__(kThreads)
+// HALF: the pool stores its state in bf16 or f16 (else float32, no branch).
+template <int DK, typename TI, typename TO, bool AFTER_CONV, bool HALF>
+__global__ void __launch_bounds__(kThreads, HALF ? 9 : 10)
     decode_bulk_kernel(PoolView p, int layer, const int32_t *__restrict__ slot_ids, QKV in,
                        TO *__restrict__ o, float scale) {
-  constexpr int R = kBulkBytes / (DK * 4);        // rows per CTA
+  constexpr int R = kBulkBytes / (DK * (HALF ? 2 : 4));  // rows per CTA: a 16 KiB tile
   constexpr int LPR = DK / 4, RPP = 32 / LPR;
   constexpr int RPW = R / (kThreads / 32);        // rows per warp
   constexpr int U = 4;
@@ -50,14 +52,15 @@ __global__ void __launch_bounds__(kThreads)
   }
   const int r0 = blockIdx.x * R;
   const int nrows = min(R, p.dv - r0);
-  float *S = state_head(p, layer, slot, h) + (int64_t)r0 * DK;
+  char *S = p.state_at(p.state_head_elem(layer, slot, h) + (int64_t)r0 * DK);
+  const gdn_dtype sd = HALF ? p.state_dtype : GDN_F32;
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_fence_init();
   }
   __syncthreads();
   if (tid == 0) {
-    const uint32_t bytes = (uint32_t)nrows * DK * 4;
+    const uint32_t bytes = (uint32_t)nrows * DK * p.state_esz();
     mbar_arrive_expect_tx(&bar, bytes);
     bulk_g2s(tile, S, bytes, &bar);
   }
@@ -102,7 +105,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int rl = warp * RPW + (ps * U + u) * RPP + grp;
-      s[u] = rl < nrows ? tile[rl * (DK / 4) + sub] : make_float4(0.f, 0.f, 0.f, 0.f);
+      s[u] = rl < nrows ? state_ld4(tile, (int64_t)rl * DK + 4 * sub, sd)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
       acc[u] = dot4(s[u], k4);
     }
 #pragma unroll
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int u = 0; u < U; ++u) {
       const int rl = warp * RPW + (ps * U + u) * RPP + grp;
       if (rl < nrows) {
-        __stcs(reinterpret_cast<float4 *>(S + (int64_t)rl * DK) + sub, s[u]);
+        state_st4<true>(S, (int64_t)rl * DK + 4 * sub, s[u], sd);
         if (sub == 0) Elem<TO>::store1(op + rl, scale * acc[u]);
       }
     }
@@ -269,14 +273,15 @@ __global__ void __launch_bounds__(kThreads)
     if (blockIdx.x == 0 && h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
     return;
   }
-  float *S = state_head(p, layer, slot, h) + (int64_t)r0 * DK;
+  char *S = p.state_at(p.state_head_elem(layer, slot, h) + (int64_t)r0 * DK);
+  const gdn_dtype sd = p.state_dtype;
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_fence_init();
   }
   __syncthreads();
   if (tid == 0) {
-    const uint32_t bytes = (uint32_t)nrows * DK * 4;
+    const uint32_t bytes = (uint32_t)nrows * DK * p.state_esz();
     mbar_arrive_expect_tx(&bar, bytes);
     bulk_g2s(tile, S, bytes, &bar);
   }
@@ -352,7 +357,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int rl = warp * RPW + (ps * U + u) * RPP + grp;
-        s[u] = rl < nrows ? tile[rl * (DK / 4) + sub] : make_float4(0.f, 0.f, 0.f, 0.f);
+        s[u] = rl < nrows ? state_ld4(tile, (int64_t)rl * DK + 4 * sub, sd)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
         acc[u] = dot4(s[u], k4);
       }
 #pragma unroll
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int u = 0; u < U; ++u) {
         const int rl = warp * RPW + (ps * U + u) * RPP + grp;
         if (rl < nrows) {
-          __stcs(reinterpret_cast<float4 *>(S + (int64_t)rl * DK) + sub, s[u]);
+          state_st4<true>(S, (int64_t)rl * DK + 4 * sub, s[u], sd);
           if (sub == 0) Elem<TO>::store1(op + rl, scale * acc[u]);
         }
       }
@@ -443,11 +449,16 @@ template <int DK, typename TI, typename TO>
 cudaError_t launch_decode_t(const PoolView &p, int layer, const int32_t *slot_ids, int n,
                             const QKV &in, void *o, float scale, cudaStream_t s,
                             bool after_conv) {
-  constexpr int R = kBulkBytes / (DK * 4);
+  const bool half = p.state_dtype != GDN_F32;
+  const int R = kBulkBytes / (DK * (half ? 2 : 4));
   dim3 grid((p.dv + R - 1) / R, p.h_v, n);
   if (!after_conv) {
-    decode_bulk_kernel<DK, TI, TO, false><<<grid, kThreads, 0, s>>>(p, layer, slot_ids, in,
-                                                                    static_cast<TO *>(o), scale);
+    if (half)
+      decode_bulk_kernel<DK, TI, TO, false, true><<<grid, kThreads, 0, s>>>(
+          p, layer, slot_ids, in, static_cast<TO *>(o), scale);
+    else
+      decode_bulk_kernel<DK, TI, TO, false, false><<<grid, kThreads, 0, s>>>(
+          p, layer, slot_ids, in, static_cast<TO *>(o), scale);
     return cudaGetLastError();
   }
   cudaLaunchAttribute attr[1];
@@ -460,8 +471,11 @@ cudaError_t launch_decode_t(const PoolView &p, int layer, const int32_t *slot_id
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_bulk_kernel<DK, TI, TO, true>, p, layer, slot_ids, in,
-                            static_cast<TO *>(o), scale);
+  if (half)
+    return cudaLaunchKernelEx(&cfg, decode_bulk_kernel<DK, TI, TO, true, true>, p, layer,
+                              slot_ids, in, static_cast<TO *>(o), scale);
+  return cudaLaunchKernelEx(&cfg, decode_bulk_kernel<DK, TI, TO, true, false>, p, layer,
+                            slot_ids, in, static_cast<TO *>(o), scale);
 }
 
 template <int DK, typename TI, typename TO>

@@ -21,14 +21,24 @@ constexpr int kChunk = 64;          // prefill chunk length
 constexpr int kMaxVerifyT = 32;     // drafts per slot in one verify call
 
 struct PoolView {
-  float *state;            // [n_layers][n_slots][h_v][dv][dk]
+  float *state;            // [n_layers][n_slots][h_v][dv][dk] of state_dtype (base address)
   void *conv;              // [n_layers][n_slots][conv_ch][conv_k-1]
   unsigned int *err;       // device error word
   int n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k;
   gdn_dtype conv_dtype;
   unsigned int *ticks;     // [n_layers][n_slots][h_k] tickets of the one-call decode step
+  gdn_dtype state_dtype;   // GDN_F32, or GDN_BF16 / GDN_F16 storage (fp32 arithmetic)
   GDN_HD int64_t state_slot_elems() const { return (int64_t)h_v * dv * dk; }
   GDN_HD int64_t conv_slot_elems() const { return (int64_t)conv_ch * (conv_k - 1); }
+  GDN_HD int state_esz() const { return state_dtype == GDN_F32 ? 4 : 2; }
+  // element index of row 0 of head h of (layer, slot)
+  GDN_HD int64_t state_head_elem(int layer, int slot, int h) const {
+    return ((int64_t)layer * n_slots + slot) * state_slot_elems() + (int64_t)h * dv * dk;
+  }
+  // address of state element e
+  GDN_HD char *state_at(int64_t e) const {
+    return reinterpret_cast<char *>(state) + e * state_esz();
+  }
 };
 
 struct QKV {

@@ -353,11 +353,14 @@ size_t prefill_workspace_bytes(const PoolView &p, const SeqIndex &seq, const QKV
 cudaError_t launch_prefill(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in,
                            void *o, gdn_dtype o_dtype, float scale, void *work,
                            cudaStream_t s) {
+  if (tc_shape(p, in) && work != nullptr)
+    return launch_prefill_split(p, layer, seq, in, o, o_dtype, scale, work, s);
+  // a bf16 / f16 state is read and written by the two-launch path above and by
+  // the token-by-token kernel; the single-launch chunked kernels keep float32
+  if (p.state_dtype != GDN_F32)
+    return launch_prefill_recurrent(p, layer, seq, in, o, o_dtype, scale, s);
   if (p.dk != p.dv) return cudaErrorNotSupported;
-  if (tc_shape(p, in)) {
-    if (work != nullptr) return launch_prefill_split(p, layer, seq, in, o, o_dtype, scale, work, s);
-    return launch_prefill_tc(p, layer, seq, in, o, o_dtype, scale, s);
-  }
+  if (tc_shape(p, in)) return launch_prefill_tc(p, layer, seq, in, o, o_dtype, scale, s);
   switch (p.dk) {
     case 16: return launch_prefill_d<16>(p, layer, seq, in, o, o_dtype, scale, s);
     case 32: return launch_prefill_d<32>(p, layer, seq, in, o, o_dtype, scale, s);

@@ -690,8 +690,8 @@ __global__ void __launch_bounds__(NT, 1)
     return;
   }
   const int hk = h / (p.h_v / p.h_k);
-  float *Sg = p.state + ((int64_t)layer * p.n_slots + slot) * p.state_slot_elems() +
-              (int64_t)h * D * D;
+  const gdn_dtype sd = p.state_dtype;
+  char *Sg = p.state_at(p.state_head_elem(layer, slot, h));  // float32, bf16 or f16 elements
   const float *wsq = work + ((int64_t)off[si] * p.h_v + h) * (2 * TILE);  // chunk 0's tiles
   const int64_t wstep = (int64_t)p.h_v * (2 * TILE);                      // next chunk
 
@@ -712,14 +712,14 @@ __global__ void __launch_bounds__(NT, 1)
   }
   const uint32_t tm = tmem_slot;
   const uint32_t lrow = tm + ((uint32_t)(32 * quad) << 16);
-  {  // state row `row`, column half `half` -> TMEM
-    const float4 *src = reinterpret_cast<const float4 *>(Sg + (int64_t)row * D + 64 * half);
+  {  // state row `row`, column half `half` -> TMEM (float32)
+    const int64_t e0 = (int64_t)row * D + 64 * half;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       float v[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float4 x = src[c * 4 + j];
+        const float4 x = state_ld4(Sg, e0 + (c * 4 + j) * 4, sd);
         v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
       }
       tc::tmem_st16(lrow + T_S + 64 * half + c * 16, v);
@@ -936,16 +936,17 @@ __global__ void __launch_bounds__(NT, 1)
       if (ds >= p.n_slots) {
         if (tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
       } else if (ds >= 0) {
-        float4 *dst = reinterpret_cast<float4 *>(
-            p.state + ((int64_t)layer * p.n_slots + ds) * p.state_slot_elems() +
-            ((int64_t)h * D + row) * D + 64 * half);
+        char *dst = p.state_at(p.state_head_elem(layer, ds, h));
+        const int64_t e0 = (int64_t)row * D + 64 * half;
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           float v[16];
           tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, v);
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4)
-            dst[cb * 4 + j4] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+            state_st4<false>(dst, e0 + (cb * 4 + j4) * 4,
+                             make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]),
+                             sd);
         }
       }
     }
@@ -980,14 +981,15 @@ __global__ void __launch_bounds__(NT, 1)
   }
 
   if (alive) {
-    float4 *dst = reinterpret_cast<float4 *>(Sg + (int64_t)row * D + 64 * half);
+    const int64_t e0 = (int64_t)row * D + 64 * half;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       float v[16];
       tc::tmem_ld16(lrow + T_S + 64 * half + c * 16, v);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        dst[c * 4 + j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        state_st4<false>(Sg, e0 + (c * 4 + j) * 4,
+                         make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), sd);
     }
   } else {
     if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);

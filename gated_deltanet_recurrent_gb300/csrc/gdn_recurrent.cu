@@ -5,7 +5,8 @@
 // form is measured against, and it has no chunk-size or head-dim constraint.
 //
 // CTA = 32 state rows of one (sequence, value head); each row lives in the
-// registers of 4 lanes (dk/4 columns each) for the whole call.  Tokens are
+// registers of 4 lanes (dk/4 columns each) for the whole call, in float32
+// whatever the pool's storage type (rounded back once, at the end).  Tokens are
 // staged 32 at a time (normalised q, k; this CTA's slice of v; alpha, beta);
 // per token each row does p = s.k, s = alpha s + beta (v - alpha p) k,
 // o = s.q, with 2-shuffle reductions over its 4 lanes.
@@ -52,14 +53,14 @@ __global__ void __launch_bounds__(kRT)
   const int r = r0 + rl;
   const bool live = r < p.dv;
   const int rot = rho % C4;                  // chunk rotation per row (bank spread)
-  float *Srow = p.state + ((int64_t)layer * p.n_slots + slot) * p.state_slot_elems() +
-                ((int64_t)h * p.dv + (live ? r : 0)) * DK;
+  const gdn_dtype sd = p.state_dtype;
+  char *Srow = p.state_at(p.state_head_elem(layer, slot, h) + (int64_t)(live ? r : 0) * DK);
 
   float4 s[C4];
 #pragma unroll
   for (int j = 0; j < C4; ++j) {
     const int cj = ((j + rot) % C4) * LPR + sub;
-    s[j] = live ? reinterpret_cast<const float4 *>(Srow)[cj] : make_float4(0.f, 0.f, 0.f, 0.f);
+    s[j] = live ? state_ld4(Srow, 4 * cj, sd) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
   const TI *qg = static_cast<const TI *>(in.q);
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kRT)
 #pragma unroll
     for (int j = 0; j < C4; ++j) {
       const int cj = ((j + rot) % C4) * LPR + sub;
-      reinterpret_cast<float4 *>(Srow)[cj] = s[j];
+      state_st4<false>(Srow, 4 * cj, s[j], sd);
     }
   }
 }

@@ -8,7 +8,6 @@ namespace gdn {
 namespace {
 
 using rows::kThreads;
-using rows::state_head;
 using rows::dispatch;
 
 constexpr int kTileBytes = 32768;  // state tile per CTA (one bulk copy)
@@ -27,8 +26,10 @@ constexpr int kTileBytes = 32768;  // state tile per CTA (one bulk copy)
 // (tokens 1-based here; the code is 0-based).  The 2T dot products are
 // independent, so each row is split over only 4 lanes (2-shuffle reductions)
 // and the state row is rebuilt once, at the accepted length, instead of
-// being updated T times.  The CTA's 16 KiB state tile arrives by one bulk
-// copy while the tokens are staged.  grid (ceil(dv / R), h_v, n).
+// being updated T times.  The CTA's state tile (32 KiB of float32, 16 KiB of
+// a bf16 / f16 state, widened to float32 as rows are read and rounded back
+// when they are written) arrives by one bulk copy while the tokens are
+// staged.  grid (ceil(dv / R), h_v, n).
 template <int DK, int TMAX, typename TI, typename TO>
 __global__ void __launch_bounds__(kThreads)
     rows_kernel(PoolView p, int layer, VerifyArgs va, TO *__restrict__ o) {
@@ -91,14 +92,15 @@ __global__ void __launch_bounds__(kThreads)
   };
   const int r0 = blockIdx.x * R;
   const int nrows = min(R, p.dv - r0);
-  float *S = state_head(p, layer, slot, h) + (int64_t)r0 * DK;
+  char *S = p.state_at(p.state_head_elem(layer, slot, h) + (int64_t)r0 * DK);
+  const gdn_dtype sd = p.state_dtype;
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_fence_init();
   }
   __syncthreads();
   if (tid == 0) {
-    const uint32_t bytes = (uint32_t)nrows * DK * 4;
+    const uint32_t bytes = (uint32_t)nrows * DK * p.state_esz();
     mbar_arrive_expect_tx(&bar, bytes);
     bulk_g2s(tile, S, bytes, &bar);
   }
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int j = 0; j < C4; ++j) {
       const int cj = ((j + rot) % C4) * LPR + sub;   // float4 index within the row
-      s[j] = live ? tile[rl * (DK / 4) + cj] : make_float4(0.f, 0.f, 0.f, 0.f);
+      s[j] = live ? state_ld4(tile, (int64_t)rl * DK + 4 * cj, sd) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if constexpr (TMAX <= 8) {
       // fully unrolled: per-row scalars in registers
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(kThreads)
           for (int ii = 0; ii < TMAX; ++ii)
             if (ii < a) acc = axpby4(1.f, acc, Dm[a * (T + 1) + ii + 1] * dl[ii],
                                      sk4[ii * (DK / 4) + cj]);
-          __stcs(reinterpret_cast<float4 *>(S + (int64_t)rl * DK) + cj, acc);
+          state_st4<true>(S, (int64_t)rl * DK + 4 * cj, acc, sd);
         }
       }
     } else {
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(kThreads)
           for (int ii = 0; ii < a; ++ii)
             acc = axpby4(1.f, acc, Dm[a * (T + 1) + ii + 1] * rdl[rs + ii],
                          sk4[ii * (DK / 4) + cj]);
-          __stcs(reinterpret_cast<float4 *>(S + (int64_t)rl * DK) + cj, acc);
+          state_st4<true>(S, (int64_t)rl * DK + 4 * cj, acc, sd);
         }
       }
       __syncwarp();

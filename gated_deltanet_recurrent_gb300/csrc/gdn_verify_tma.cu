@@ -284,7 +284,8 @@ cudaError_t launch_t(const PoolView &p, const CUtensorMap &tmap, int layer, cons
 
 cudaError_t launch_verify_tma(const PoolView &p, const void *tmap, int layer,
                               const VerifyArgs &va, void *o, gdn_dtype o_dtype, cudaStream_t s) {
-  if (tmap == nullptr || p.dk != D || p.dv != D || va.T + va.T_prev > TMX)
+  if (tmap == nullptr || p.state_dtype != GDN_F32 || p.dk != D || p.dv != D ||
+      va.T + va.T_prev > TMX)
     return cudaErrorNotSupported;
   const CUtensorMap &m = *static_cast<const CUtensorMap *>(tmap);
   if (va.in.dtype == GDN_F32 && o_dtype == GDN_F32) return launch_t<float, float>(p, m, layer, va, o, s);

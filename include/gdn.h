@@ -12,7 +12,7 @@
  * Per value head h of a slot, with key head h' = h / (h_v / h_k), each token
  * applies the gated delta rule
  *     S <- alpha * S (I - beta k k^T) + beta v k^T,      o = scale * S q
- * where S is [dv][dk] float32, q and k are L2-normalised inside the kernels
+ * where S is [dv][dk] (float32 arithmetic), q and k are L2-normalised inside the kernels
  * (x / sqrt(sum x^2 + 1e-6)), alpha = exp(g) with g <= 0 given per token and
  * value head, and o is read from the updated state.
  *
@@ -35,8 +35,9 @@
  *    trap.  Repeated slot ids in one call are not detected on the device and
  *    give unspecified results for those slots.
  *  - n == 0 / empty sequences are valid no-ops.
- *  - The state layout is [n_layers][n_slots][h_v][dv][dk] float32 and the conv
- *    cache [n_layers][n_slots][conv_ch][conv_k-1] in conv_dtype, oldest input
+ *  - The state layout is [n_layers][n_slots][h_v][dv][dk] in the pool's
+ *    state_dtype (float32 unless chosen otherwise) and the conv cache
+ *    [n_layers][n_slots][conv_ch][conv_k-1] in conv_dtype, oldest input
  *    first; both are plain caller memory, so a state can be written, read,
  *    copied or saved with ordinary memcpy.
  *  - Not thread-safe per pool: calls on one pool from several host threads
@@ -67,7 +68,9 @@ typedef enum {
   GDN_ERR_CUDA = 7         /* a CUDA runtime call failed (gdn_last_error_message has it) */
 } gdn_status;
 
-typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+/* Element types.  Activations (q, k, v, g, beta, x, y, o) and the conv cache
+ * are GDN_F32 or GDN_BF16; the recurrent state may also be GDN_F16. */
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1, GDN_F16 = 2 } gdn_dtype;
 
 /* Bits of the pool's device error word. */
 #define GDN_DEVERR_SLOT 1u   /* an entry with an out-of-range slot id was skipped */
@@ -95,6 +98,19 @@ typedef struct {
    * value head); 0 means 8 GiB.  Calls that would need more, or whose
    * workspace cannot be allocated, run the single-launch kernel instead. */
   uint64_t prefill_workspace_max;
+  /* Storage type of the recurrent state: GDN_F32, or a half-precision state
+   * (GDN_BF16 / GDN_F16) that halves the state's memory and its HBM traffic
+   * (baseRT issue #31, "Why this looks tractable": the gdn_mp_factor_f16 /
+   * gdn_mp_scan_f16 kernels; the pages do not say what they compute, and the
+   * reading used here is half-precision storage with float32 arithmetic).  A
+   * kernel widens the stored state to float32, keeps it in float32 for the
+   * whole call, and rounds it to nearest-even once when it writes it back (a
+   * decode step: every token; a prefill call: at the end of each sequence
+   * and at each checkpoint; a verify: at commit).  Every entry point accepts
+   * such a pool; chunked prefill runs its two-launch tensor-core path where
+   * that applies (dk = dv = 128 with a workspace) and the token-by-token
+   * kernel otherwise, and verify runs its CUDA-core kernel. */
+  gdn_dtype state_dtype;
 } gdn_pool_desc;
 
 /* Per-token inputs of the recurrence for `tokens` tokens.
@@ -121,10 +137,11 @@ size_t gdn_pool_conv_bytes(const gdn_pool_desc *desc);
  * slot dimension that page asks for).  Wraps caller memory: state_mem and
  * conv_mem (256-byte aligned device memory of at least the sizes above) are
  * NOT cleared -- call gdn_pool_reset for new requests, or write states
- * directly.  The pool allocates a 4-byte device error word and owns a
- * stream-ordered memory pool from which chunked prefill takes its workspace
- * (kept for reuse until gdn_pool_destroy).  On success *out receives the
- * handle. */
+ * directly.  The pool allocates a small zeroed device array (the error word
+ * and 4 bytes per layer, slot and key head for gdn_decode_step_conv) and owns
+ * a stream-ordered memory pool from which chunked prefill takes its
+ * workspace (kept for reuse until gdn_pool_destroy).  On success *out
+ * receives the handle. */
 gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t state_bytes,
                            void *conv_mem, size_t conv_bytes, gdn_pool **out);
 

@@ -255,13 +255,28 @@ def gated_rmsnorm(o, z, w, eps=1e-6):
 class OraclePool:
     """Slot-indexed pool: per layer and slot a float64 state [H_v, V, K] and a
     conv cache [C, W-1] [P1 "Why this looks tractable"; P3 "What to do",
-    State row].  Slots are independent; a new request starts from zero."""
+    State row].  Slots are independent; a new request starts from zero.
 
-    def __init__(self, n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k):
+    state_round: None (the state is kept exactly), or round_bf16 / round_f16
+    for a pool that stores its state in half precision [P1, "Why this looks
+    tractable" names gdn_mp_factor_f16 and gdn_mp_scan_f16 without saying what
+    they compute; the reading taken is half-precision storage of the state
+    with full-precision arithmetic].  Within one call a slot's state is
+    carried unrounded; it is rounded when the call stores it: after each
+    decode step, at the end of each prefill sequence, at each prefill
+    checkpoint, and at a verify's commit."""
+
+    def __init__(self, n_layers, n_slots, h_v, h_k, dk, dv, conv_ch, conv_k,
+                 state_round=None):
         self.h_v, self.h_k, self.dk, self.dv = h_v, h_k, dk, dv
         self.conv_ch, self.conv_k = conv_ch, conv_k
         self.S = np.zeros((n_layers, n_slots, h_v, dv, dk))
         self.X = np.zeros((n_layers, n_slots, conv_ch, conv_k - 1))
+        self.state_round = state_round
+
+    def _store(self, S):
+        """The state as the pool stores it."""
+        return S if self.state_round is None else self.state_round(S)
 
     def reset(self, slot_ids):
         for s in slot_ids:
@@ -288,8 +303,8 @@ class OraclePool:
         """One token per active slot; q, k [N, H_k, K], v [N, H_v, V]."""
         o = np.empty((len(slot_ids), self.h_v, self.dv))
         for i, s in enumerate(slot_ids):
-            self.S[layer, s], o[i] = gdn_step(
-                self.S[layer, s], q[i], k[i], v[i], g[i], beta[i], scale, eps)
+            S, o[i] = gdn_step(self.S[layer, s], q[i], k[i], v[i], g[i], beta[i], scale, eps)
+            self.S[layer, s] = self._store(S)
         return o
 
     def prefill(self, layer, slot_ids, cu_seqlens, q, k, v, g, beta,
@@ -303,9 +318,10 @@ class OraclePool:
             args = (self.S[layer, s], q[lo:hi], k[lo:hi], v[lo:hi],
                     g[lo:hi], beta[lo:hi])
             if chunk is None:
-                self.S[layer, s], o[lo:hi] = gdn_recurrent(*args, scale, eps)
+                S, o[lo:hi] = gdn_recurrent(*args, scale, eps)
             else:
-                self.S[layer, s], o[lo:hi] = gdn_chunked(*args, scale, chunk, eps)
+                S, o[lo:hi] = gdn_chunked(*args, scale, chunk, eps)
+            self.S[layer, s] = self._store(S)
         return o
 
     def prefill_checkpointed(self, layer, slot_ids, cu_seqlens, q, k, v, g, beta,
@@ -326,8 +342,8 @@ class OraclePool:
                 if n_done % ckpt_every == 0:
                     j = n_done // ckpt_every - 1
                     if j < len(ckpt_slots[i]) and ckpt_slots[i][j] >= 0:
-                        self.S[layer, ckpt_slots[i][j]] = S
-            self.S[layer, s] = S
+                        self.S[layer, ckpt_slots[i][j]] = self._store(S)
+            self.S[layer, s] = self._store(S)
         return o
 
     def spec_verify(self, layer, slot_ids, T, q, k, v, g, beta,
@@ -342,8 +358,8 @@ class OraclePool:
             a = None if accept_len is None else accept_len[i]
             o[i], S_keep = spec_verify(self.S[layer, s], q[sl], k[sl], v[sl],
                                        g[sl], beta[sl], a, scale, eps)
-            if accept_len is not None:
-                self.S[layer, s] = S_keep
+            if accept_len is not None and a > 0:
+                self.S[layer, s] = self._store(S_keep)
         return o
 
     def spec_verify_deferred(self, layer, slot_ids, T, q, k, v, g, beta,
@@ -357,13 +373,14 @@ class OraclePool:
         n = len(slot_ids)
         o = np.empty((n, T, self.h_v, self.dv))
         for i, s in enumerate(slot_ids):
+            S = self.S[layer, s]
             if prev is not None:
                 pq, pk, pv, pg, pb = prev
                 for t in range(int(prev_accept[i])):
                     r = i * T_prev + t
-                    self.S[layer, s], _ = gdn_step(self.S[layer, s], pq[r], pk[r], pv[r],
-                                                   pg[r], pb[r], scale, eps)
+                    S, _ = gdn_step(S, pq[r], pk[r], pv[r], pg[r], pb[r], scale, eps)
+                if int(prev_accept[i]) > 0:
+                    self.S[layer, s] = self._store(S)
             sl = slice(i * T, (i + 1) * T)
-            o[i], _ = spec_verify(self.S[layer, s], q[sl], k[sl], v[sl], g[sl], beta[sl],
-                                  None, scale, eps)
+            o[i], _ = spec_verify(S, q[sl], k[sl], v[sl], g[sl], beta[sl], None, scale, eps)
         return o

@@ -680,3 +680,60 @@ def test_round_bf16_hand_worked_ties_and_range():
     # the largest finite bf16 is (2 - 2^-7) 2^127 and stays put
     top = (2 - 2.0 ** -7) * 2.0 ** 127
     assert O.round_bf16(np.array([top]))[0] == top
+
+
+# -------------------------------------------- half-precision state storage
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_half_state_pool_stores_representable_states_within_half_an_ulp(fmt):
+    """A pool with half-precision state storage keeps every stored state
+    exactly representable in the format, and each store is the exact result
+    rounded to nearest: within half a unit in the last place (2^-8 relative
+    for bf16's 8 significant bits, 2^-11 for binary16's 11; subnormal f16
+    values within half of 2^-24)."""
+    rnd, p = (O.round_bf16, 8) if fmt == "bf16" else (O.round_f16, 11)
+    rng = np.random.default_rng(92)
+    shape = synth.LayerShape(2, 1, 8, 8, 4, 4)
+    pool = O.OraclePool(1, 3, shape.h_v, shape.h_k, shape.dk, shape.dv, 4, 4, state_round=rnd)
+    pool.S[0, 1] = rnd(synth.random_states(rng, 1, shape)[0])
+    for step in range(4):
+        tok = synth.token_inputs(rng, 1, shape, "f32")
+        S_before = pool.S[0, 1].copy()
+        pool.decode_step(0, [1], *tok_np_(tok))
+        exact, _ = O.gdn_step(S_before, *(tok[n][0] for n in ("q", "k", "v", "g", "beta")))
+        np.testing.assert_array_equal(rnd(pool.S[0, 1]), pool.S[0, 1])
+        err = np.abs(pool.S[0, 1] - exact)
+        tiny = 2.0 ** -25 if fmt == "f16" else 0.0
+        assert np.all(err <= 2.0 ** -p * np.abs(exact) + tiny)
+        assert np.any(err > 0), "the state was not rounded"
+
+
+def tok_np_(tok):
+    return [tok[n] for n in ("q", "k", "v", "g", "beta")]
+
+
+def test_half_state_rounds_at_call_boundaries_not_per_token():
+    """Within a call the state is carried unrounded: a prefill call of L
+    tokens equals the exact recurrence over them followed by ONE rounding,
+    whereas L decode calls round after every token.  With beta = 0 and g = 0
+    (alpha = 1) a stored state passes through any call bit for bit."""
+    rng = np.random.default_rng(93)
+    shape = synth.LayerShape(2, 2, 8, 8, 4, 4)
+    S0 = O.round_bf16(synth.random_states(rng, 1, shape)[0])
+    tok = synth.token_inputs(rng, 12, shape, "f32")
+    a = O.OraclePool(1, 2, 2, 2, 8, 8, 4, 4, state_round=O.round_bf16)
+    b = O.OraclePool(1, 2, 2, 2, 8, 8, 4, 4, state_round=O.round_bf16)
+    a.S[0, 0] = S0
+    b.S[0, 0] = S0
+    a.prefill(0, [0], [0, 12], *tok_np_(tok))
+    for t in range(12):
+        b.decode_step(0, [0], *(x[t:t + 1] for x in tok_np_(tok)))
+    exact, _ = O.gdn_recurrent(S0, *tok_np_(tok))
+    np.testing.assert_array_equal(a.S[0, 0], O.round_bf16(exact))
+    assert not np.array_equal(a.S[0, 0], b.S[0, 0]), "per-token rounding must differ"
+    assert np.max(np.abs(a.S[0, 0] - b.S[0, 0])) <= 2.0 ** -6 * np.max(np.abs(exact))
+    still = {n: x.copy() for n, x in tok.items()}
+    still["beta"][:] = 0.0
+    still["g"][:] = 0.0
+    a.prefill(0, [0], [0, 12], *tok_np_(still))
+    np.testing.assert_array_equal(a.S[0, 0], O.round_bf16(exact))
