@@ -20,8 +20,8 @@ oracle timed on the host cores (`cpu_baseline`: one thread and all cores;
 decode, prefill and verify), SM clocks sampled during timing, and
 `secondary` measurements: the 18-layer slot sweep (N = 1 .. 512),
 speculative verify (128 slots, T = 4), varlen chunked prefill with its
-roofline, the output gated RMSNorm, and the decode step on pools that store
-the state in bf16 / binary16.
+roofline, the output gated RMSNorm, the decode step on pools that store the
+state in bf16 / binary16, and the layer's input projection (gdn_in_proj).
 
 --impl reference times the float64 CPU oracle on a bounded sample of the same
 workload (the pages publish no runnable implementation of this path).
@@ -80,9 +80,9 @@ def _parse():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--sweep-steps", type=int, default=128)
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--sections", default="sweep,verify,prefill,norm,half",
+    ap.add_argument("--sections", default="sweep,verify,prefill,norm,half,in_proj",
                     help="secondary measurements to run (comma list of sweep, verify, prefill, "
-                         "norm, half)")
+                         "norm, half, in_proj)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
@@ -534,6 +534,54 @@ def half_state_bench(torch, abi, synth, device, steps, peak):
     return out
 
 
+def in_proj_bench(torch, abi, synth, device, steps, hbm_peak, bf16_peak):
+    """gdn_in_proj on the layer's projection (hidden 2048 -> q | k | v, gate z,
+    beta and decay logits = 12,352 outputs), bf16 in, bf16 out: a decode step
+    (64 tokens, weight-read bound) and a prefill piece (16,384 tokens,
+    tensor bound).  L2 flushed between timed calls.  torch.matmul (cuBLAS) on
+    the same operands is timed beside it as context only."""
+    hidden, n_out = 2048, 2 * 16 * 128 + 2 * 32 * 128 + 2 * 32
+    gen = torch.Generator(device=device).manual_seed(7)
+    w = (torch.randn(n_out, hidden, device=device, generator=gen) / hidden ** 0.5).bfloat16()
+    pool = abi.Pool.for_shape(synth.LayerShape(2, 1, 16, 16, 64, 4), 1, 1,
+                              conv_dtype=torch.float32, host_checks=False, device=device)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    out = {}
+    for name, tokens in (("decode_64", 64), ("prefill_16384", 16384)):
+        x = torch.randn(tokens, hidden, device=device, generator=gen).bfloat16()
+        y = torch.empty(tokens, n_out, device=device, dtype=torch.bfloat16)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            evs = [(E(), E()) for _ in range(steps)]
+            torch.cuda.synchronize()
+            for a, b in evs:
+                flush.zero_()
+                a.record()
+                fn()
+                b.record()
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+
+        t = timed(lambda: abi.gdn_in_proj(pool, x, w, y))
+        t_lib = timed(lambda: torch.matmul(x, w.t(), out=y))
+        flops = 2.0 * tokens * hidden * n_out
+        nbytes = 2.0 * (tokens * hidden + n_out * hidden + tokens * n_out)
+        t_roof = max(flops / (bf16_peak * 1e12), nbytes / (hbm_peak * 1e9))
+        out[name] = {"tokens": tokens, "us_per_call": t * 1e6, "tflops": flops / t / 1e12,
+                     "gbs": nbytes / t / 1e9,
+                     "bound": "tensor" if flops / (bf16_peak * 1e12) >= nbytes / (hbm_peak * 1e9)
+                     else "hbm",
+                     "roofline_frac": t_roof / t, "library_matmul_us": t_lib * 1e6}
+    del pool
+    out["workload"] = (f"input projection, hidden {hidden} -> {n_out} outputs (q|k|v 8192, gate "
+                       f"4096, beta and decay logits 64), bf16 in/out, float32 accumulation; "
+                       f"library_matmul_us: torch.matmul on the same operands (context)")
+    return out
+
+
 def sweep_bench(torch, abi, synth, device, steps):
     """18 stacked layers, N active slots of a 512-slot pool, `steps` decode
     steps per N; L2 flushed between steps."""
@@ -852,6 +900,8 @@ def run_gpu(args, rank, world):
         secondary["norm"] = norm_bench(torch, abi, device, 20, peak)
     if "half" in sections:
         secondary["half_state"] = half_state_bench(torch, abi, synth, device, 50, peak)
+    if "in_proj" in sections:
+        secondary["in_proj"] = in_proj_bench(torch, abi, synth, device, 20, peak, tc_peak)
     time.sleep(0.2)
     clk = clocks.stop()
     if dist is not None:

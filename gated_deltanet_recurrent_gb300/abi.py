@@ -24,7 +24,7 @@ DEVERR_SLOT, DEVERR_SEQ, DEVERR_COUNT, DEVERR_TIMEOUT = 1, 2, 4, 8
 EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "gdn_pool_reset",
             "gdn_pool_copy",
             "gdn_pool_destroy", "gdn_pool_get_error", "gdn_conv_silu", "gdn_decode_step",
-            "gdn_decode_step_conv", "gdn_gated_rmsnorm",
+            "gdn_decode_step_conv", "gdn_gated_rmsnorm", "gdn_in_proj",
             "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
             "gdn_spec_verify_deferred", "gdn_prefill_chunked_noalloc", "gdn_prefill_chunked_ckpt",
             "gdn_status_string",
@@ -82,6 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gdn_decode_step_conv": (st, [vp, i32, vp, i32, vp, i64, vp, vp, vp, i64, vp, vp, st,
                                       vp, st, ctypes.c_float, vp]),
         "gdn_gated_rmsnorm": (st, [i64, i32, vp, st, vp, st, vp, ctypes.c_float, vp, st, vp]),
+        "gdn_in_proj": (st, [vp, i64, i32, i32, vp, i64, vp, i64, vp, i64, st, vp]),
         "gdn_prefill_chunked": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
                                      ctypes.c_float, vp]),
         "gdn_prefill_recurrent": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
@@ -306,6 +307,25 @@ def gdn_decode_step_conv(pool: Pool, layer: int, slot_ids: torch.Tensor, x: torc
         _ptr(bias), _ptr(y), y.stride(0), _ptr(g), _ptr(beta), dts.pop(), _ptr(o), _dt(o), scale,
         _stream(stream)))
     return o
+
+
+def gdn_in_proj(pool: Pool, x: torch.Tensor, w: torch.Tensor,
+                y: Optional[torch.Tensor] = None, stream=None):
+    """y = x w^T: x [tokens, hidden] bf16, w [n_out, hidden] bf16 (unit
+    column strides), y [tokens, n_out] float32 or bf16 (default float32)."""
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise GDNError(4, "x and w must be bf16")
+    if x.dim() != 2 or w.dim() != 2 or x.stride(1) != 1 or w.stride(1) != 1 or \
+            x.shape[1] != w.shape[1]:
+        raise GDNError(1, "x [tokens, hidden] and w [n_out, hidden] with unit column strides")
+    if y is None:
+        y = torch.empty(x.shape[0], w.shape[0], dtype=torch.float32, device=x.device)
+    if y.dim() != 2 or y.stride(1) != 1 or tuple(y.shape) != (x.shape[0], w.shape[0]):
+        raise GDNError(1, "y must be [tokens, n_out] with a unit column stride")
+    _check(load_library().gdn_in_proj(pool.handle, x.shape[0], x.shape[1], w.shape[0], _ptr(x),
+                                      x.stride(0), _ptr(w), w.stride(0), _ptr(y), y.stride(0),
+                                      _dt(y), _stream(stream)))
+    return y
 
 
 def gdn_gated_rmsnorm(o: torch.Tensor, z: torch.Tensor, w: torch.Tensor,

@@ -23,7 +23,7 @@ LIB = os.path.join(PKG, "libgdn.so")
 
 SOURCES = ["gdn_api.cu", "gdn_conv.cu", "gdn_decode.cu", "gdn_verify.cu", "gdn_prefill.cu",
            "gdn_prefill_tc.cu", "gdn_recurrent.cu", "gdn_verify_tma.cu",
-           "gdn_prefill_split.cu", "gdn_norm.cu"]
+           "gdn_prefill_split.cu", "gdn_norm.cu", "gdn_in_proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "-Xptxas", "-v", "--expt-relaxed-constexpr"]

@@ -487,6 +487,41 @@ gdn_status gdn_decode_step_conv(gdn_pool *p, int32_t layer, const int32_t *slot_
   return ok();
 }
 
+gdn_status gdn_in_proj(gdn_pool *p, int64_t tokens, int32_t hidden, int32_t n_out,
+                       const void *x, int64_t ld_x, const void *w, int64_t ld_w, void *y,
+                       int64_t ld_y, gdn_dtype y_dtype, gdn_stream stream) {
+  gdn_status st = check_pool(p, 0);
+  if (st != GDN_OK) return st;
+  if (tokens < 0 || hidden < 1 || n_out < 1)
+    return fail(GDN_ERR_ARG, "tokens = %lld, hidden = %d, n_out = %d", (long long)tokens, hidden,
+                n_out);
+  if (!dtype_ok(y_dtype)) return fail(GDN_ERR_DTYPE, "y dtype must be F32 or BF16");
+  if (tokens == 0) return ok();
+  if (tokens > INT32_MAX) return fail(GDN_ERR_SIZE, "tokens = %lld > 2^31 - 1", (long long)tokens);
+  if (!x || !w || !y) return fail(GDN_ERR_ARG, "x, w and y must be non-NULL");
+  if (ld_x == 0) ld_x = hidden;
+  if (ld_w == 0) ld_w = hidden;
+  if (ld_y == 0) ld_y = n_out;
+  if (ld_x < hidden || ld_w < hidden || ld_y < n_out)
+    return fail(GDN_ERR_ARG, "row strides smaller than a row");
+  const size_t ye = dtype_size(y_dtype);
+  if ((uintptr_t)x % 16 || (uintptr_t)w % 16 || (uintptr_t)y % 16 || (ld_x * 2) % 16 ||
+      (ld_w * 2) % 16 || (ld_y * (int64_t)ye) % 16)
+    return fail(GDN_ERR_ARG, "x, w and y rows must start 16-byte aligned (pointers and strides)");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->desc.host_checks) {
+    if ((st = check_device_ptr(x, "x")) || (st = check_device_ptr(w, "w")) ||
+        (st = check_device_ptr(y, "y")))
+      return st;
+  }
+  const cudaError_t e = gdn::launch_in_proj(tokens, n_out, hidden, x, ld_x, w, ld_w, y, ld_y,
+                                            y_dtype, p->view.err, p->sm_count, s);
+  if (e == cudaErrorInvalidValue)
+    return fail(GDN_ERR_UNSUPPORTED, "no tensor map for these operands (driver entry point)");
+  if (e != cudaSuccess) return cuda_fail(e, "input projection launch");
+  return ok();
+}
+
 gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t d, const void *o, gdn_dtype o_dtype,
                              const void *z, gdn_dtype z_dtype, const float *w, float eps,
                              void *y, gdn_dtype y_dtype, gdn_stream stream) {

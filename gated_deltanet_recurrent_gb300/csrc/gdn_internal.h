@@ -73,6 +73,13 @@ cudaError_t launch_gated_rmsnorm(const void *o, gdn_dtype ot, const void *z, gdn
                                  const float *w, float eps, void *y, gdn_dtype yt, int64_t rows,
                                  int d, cudaStream_t s);
 
+// y[t][n] = sum_h x[t][h] * w[n][h]: bf16 x [M][K] (row stride ld_x) and w
+// [N][K] (ld_w), float32 accumulation, y [M][N] (ld_y) in y_dtype; timeouts
+// set GDN_DEVERR_TIMEOUT in *err.  Rows and strides 16-byte aligned.
+cudaError_t launch_in_proj(int64_t M, int N, int K, const void *x, int64_t ld_x, const void *w,
+                           int64_t ld_w, void *y, int64_t ld_y, gdn_dtype y_dtype,
+                           unsigned int *err, int sm_count, cudaStream_t s);
+
 cudaError_t launch_pool_copy(const PoolView &p, const int32_t *src, const int32_t *dst, int n,
                              cudaStream_t s);
 

@@ -230,6 +230,24 @@ gdn_status gdn_decode_step_conv(gdn_pool *pool, int32_t layer, const int32_t *sl
                                 const void *beta, gdn_dtype dtype, void *o, gdn_dtype o_dtype,
                                 float scale, gdn_stream stream);
 
+/* Input projection of the layer (baseRT issue #31, "Why this looks
+ * tractable": the gdn_in_proj kernel, named there without its formula; the
+ * plain reading is the layer's linear projection of the hidden states):
+ *     y[t][n] = sum_h x[t][h] * w[n][h]     for t < tokens, n < n_out,
+ * with x [tokens][hidden] and w [n_out][hidden] in bf16 (row strides ld_x,
+ * ld_w elements; 0: hidden), float32 accumulation, and y [tokens][n_out] in
+ * y_dtype (GDN_F32 or GDN_BF16, rounded to nearest-even; row stride ld_y,
+ * 0: n_out).  The rows of w stack whatever the layer projects to (q | k | v
+ * for gdn_conv_silu, the output gate, the beta and decay logits); the
+ * library applies no activation.  Pointers and row strides must be 16-byte
+ * aligned (GDN_ERR_ARG otherwise).  Runs on the tensor cores (tcgen05, TMA
+ * tensor maps); the pool supplies the device and the error word
+ * (GDN_DEVERR_TIMEOUT if a bounded wait gives up) and is otherwise unused.
+ * tokens == 0 is a no-op. */
+gdn_status gdn_in_proj(gdn_pool *pool, int64_t tokens, int32_t hidden, int32_t n_out,
+                       const void *x, int64_t ld_x, const void *w, int64_t ld_w, void *y,
+                       int64_t ld_y, gdn_dtype y_dtype, gdn_stream stream);
+
 /* Output gated RMSNorm of the layer (ai-infra-handbooks Qwen3.5 project, "Why
  * it is worth doing": the model's two kinds of RMSNorm; the formula is not
  * written out there, and the one used is the plain reading): for each of

@@ -230,6 +230,16 @@ def spec_verify(S0, q, k, v, g, beta, accept_len=None, scale=1.0, eps=L2_EPS):
     return o, keep
 
 
+# ------------------------------------------------------------ input projection
+
+def in_proj(x, w):
+    """Input projection of the layer [P1, "Why this looks tractable" names
+    gdn_in_proj without its formula; the reading is the layer's linear map of
+    the hidden states]: y[t][n] = sum_h x[t][h] w[n][h], x [T, hidden],
+    w [n_out, hidden] (one row per output channel), in float64."""
+    return _f64(x) @ _f64(w).T
+
+
 # ------------------------------------------------------ output gated RMSNorm
 
 def gated_rmsnorm(o, z, w, eps=1e-6):

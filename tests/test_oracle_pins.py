@@ -25,6 +25,8 @@ Map (oracle function -> pins):
                   with silu from scipy's expit; scale invariance (eps = 0);
                   unit mean square of out / (w silu(z)); z = 0 gives 0; a
                   zero row with eps > 0 gives 0; planted mistakes are caught
+  in_proj         brute-force sums over small integers; one-hot rows pick
+                  columns of w (catches a transposed weight)
   round_bf16 /
   round_f16       torch's float32 -> bfloat16 and numpy's float64 -> float16
                   conversions (library routines) on values spanning the
@@ -737,3 +739,18 @@ def test_half_state_rounds_at_call_boundaries_not_per_token():
     still["g"][:] = 0.0
     a.prefill(0, [0], [0, 12], *tok_np_(still))
     np.testing.assert_array_equal(a.S[0, 0], O.round_bf16(exact))
+
+
+# ------------------------------------------------------- input projection
+
+def test_in_proj_brute_force_and_orientation():
+    rng = np.random.default_rng(94)
+    x = rng.integers(-3, 4, (5, 7)).astype(float)
+    w = rng.integers(-3, 4, (6, 7)).astype(float)
+    want = np.array([[sum(x[t, h] * w[n, h] for h in range(7)) for n in range(6)]
+                     for t in range(5)])
+    np.testing.assert_array_equal(O.in_proj(x, w), want)
+    # a one-hot hidden state selects one input column of every weight row
+    e = np.zeros((1, 7))
+    e[0, 2] = 1.0
+    np.testing.assert_array_equal(O.in_proj(e, w)[0], w[:, 2])
