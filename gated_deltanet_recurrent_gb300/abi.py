@@ -20,10 +20,12 @@ GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_ARG", 2: "GDN_ERR_SLOT", 3: "GDN_ERR_DUP_SLOT",
           4: "GDN_ERR_DTYPE", 5: "GDN_ERR_SIZE", 6: "GDN_ERR_UNSUPPORTED", 7: "GDN_ERR_CUDA"}
 DEVERR_SLOT, DEVERR_SEQ, DEVERR_COUNT, DEVERR_TIMEOUT = 1, 2, 4, 8
+TEST_DECODE_WAIT_TIMEOUT = 1
 
 EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "gdn_pool_reset",
             "gdn_pool_copy",
-            "gdn_pool_destroy", "gdn_pool_get_error", "gdn_conv_silu", "gdn_decode_step",
+            "gdn_pool_destroy", "gdn_pool_get_error", "gdn_pool_set_test_flags", "gdn_conv_silu",
+            "gdn_decode_step",
             "gdn_decode_step_conv", "gdn_gated_rmsnorm", "gdn_in_proj",
             "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
             "gdn_spec_verify_deferred", "gdn_prefill_chunked_noalloc", "gdn_prefill_chunked_ckpt",
@@ -76,6 +78,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gdn_pool_copy": (st, [vp, vp, vp, i32, vp]),
         "gdn_pool_destroy": (st, [vp]),
         "gdn_pool_get_error": (st, [vp, P(ctypes.c_uint32)]),
+        "gdn_pool_set_test_flags": (st, [vp, ctypes.c_uint32]),
         "gdn_conv_silu": (st, [vp, i32, vp, vp, i32, i32, i32, vp, i64, st, vp, vp, vp, i64,
                                vp, vp]),
         "gdn_decode_step": (st, [vp, i32, vp, i32, P(gdn_qkv), vp, st, ctypes.c_float, vp]),
@@ -253,6 +256,11 @@ def gdn_pool_get_error(pool: Pool) -> int:
     err = ctypes.c_uint32(0)
     _check(load_library().gdn_pool_get_error(pool.handle, ctypes.byref(err)))
     return err.value
+
+
+def gdn_pool_set_test_flags(pool: Pool, flags: int):
+    """Test hook of the C ABI (see gdn.h); 0 restores normal operation."""
+    _check(load_library().gdn_pool_set_test_flags(pool.handle, flags))
 
 
 def gdn_conv_silu(pool: Pool, layer: int, slot_ids: torch.Tensor, x: torch.Tensor,

@@ -281,7 +281,7 @@ gdn_status gdn_pool_create(const gdn_pool_desc *desc, void *state_mem, size_t st
   p->view = gdn::PoolView{static_cast<float *>(state_mem), conv_mem, err,
                           desc->n_layers, desc->n_slots, desc->h_v, desc->h_k, desc->dk,
                           desc->dv, desc->conv_ch, desc->conv_k, desc->conv_dtype, err + 1,
-                          desc->state_dtype};
+                          desc->state_dtype, 0u};
   p->has_tmap = encode_state_map(p);
   cudaMemPoolProps props = {};
   props.allocType = cudaMemAllocationTypePinned;
@@ -311,6 +311,14 @@ gdn_status gdn_pool_destroy(gdn_pool *p) {
   delete p;
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree(error word)");
+  return ok();
+}
+
+gdn_status gdn_pool_set_test_flags(gdn_pool *p, uint32_t flags) {
+  if (!p) return fail(GDN_ERR_ARG, "pool is NULL");
+  if (flags & ~(uint32_t)GDN_TEST_DECODE_WAIT_TIMEOUT)
+    return fail(GDN_ERR_ARG, "unknown test flags 0x%x", flags);
+  p->view.test_flags = flags;
   return ok();
 }
 

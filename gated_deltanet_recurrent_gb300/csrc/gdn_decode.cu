@@ -61,7 +61,10 @@ __global__ void __launch_bounds__(kThreads, HALF ? 9 : 10)
   __syncthreads();
   if (tid == 0) {
     const uint32_t bytes = (uint32_t)nrows * DK * p.state_esz();
-    mbar_arrive_expect_tx(&bar, bytes);
+    // test hook: expect 16 bytes the copy never delivers, so the bounded wait
+    // below runs out after the copy itself has landed
+    const uint32_t extra = (p.test_flags & GDN_TEST_DECODE_WAIT_TIMEOUT) ? 16u : 0u;
+    mbar_arrive_expect_tx(&bar, bytes + extra);
     bulk_g2s(tile, S, bytes, &bar);
   }
   // Returns once the prerequisite grid has completed and its memory is
@@ -282,7 +285,10 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   if (tid == 0) {
     const uint32_t bytes = (uint32_t)nrows * DK * p.state_esz();
-    mbar_arrive_expect_tx(&bar, bytes);
+    // test hook: expect 16 bytes the copy never delivers, so the bounded wait
+    // below runs out after the copy itself has landed
+    const uint32_t extra = (p.test_flags & GDN_TEST_DECODE_WAIT_TIMEOUT) ? 16u : 0u;
+    mbar_arrive_expect_tx(&bar, bytes + extra);
     bulk_g2s(tile, S, bytes, &bar);
   }
 

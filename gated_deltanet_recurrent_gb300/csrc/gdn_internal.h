@@ -28,6 +28,7 @@ struct PoolView {
   gdn_dtype conv_dtype;
   unsigned int *ticks;     // [n_layers][n_slots][h_k] tickets of the one-call decode step
   gdn_dtype state_dtype;   // GDN_F32, or GDN_BF16 / GDN_F16 storage (fp32 arithmetic)
+  uint32_t test_flags;     // GDN_TEST_* bits (gdn_pool_set_test_flags); 0 in normal use
   GDN_HD int64_t state_slot_elems() const { return (int64_t)h_v * dv * dk; }
   GDN_HD int64_t conv_slot_elems() const { return (int64_t)conv_ch * (conv_k - 1); }
   GDN_HD int state_esz() const { return state_dtype == GDN_F32 ? 4 : 2; }

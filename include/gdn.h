@@ -160,14 +160,29 @@ gdn_status gdn_pool_reset(gdn_pool *pool, const int32_t *slot_ids, int32_t n, gd
 gdn_status gdn_pool_copy(gdn_pool *pool, const int32_t *src_slots, const int32_t *dst_slots,
                          int32_t n, gdn_stream stream);
 
-/* Release the handle, its error word and its workspace memory pool (caller
- * memory is left alone).
+/* State cache destroy (baseRT issue #31, "Why this looks tractable":
+ * GDNStateCache::destroy).  Releases the handle, its error word and tickets
+ * and its workspace memory pool (caller memory is left alone).
  * Synchronises the device before freeing. NULL is a no-op. */
 gdn_status gdn_pool_destroy(gdn_pool *pool);
 
 /* Wait for the device, return the device error word (GDN_DEVERR_* bits
- * accumulated since the last call) in *dev_err and clear it. */
+ * accumulated since the last call) in *dev_err and clear it.  The pages have
+ * no counterpart: baseRT issue #31 ("Why this looks tractable") names only
+ * GDNStateCache::{create,destroy}; the word is how kernels that never trap
+ * report a skipped entry or an expired wait. */
 gdn_status gdn_pool_get_error(gdn_pool *pool, uint32_t *dev_err);
+
+/* Test hook (no counterpart on the pages; 0 in normal use).  With
+ * GDN_TEST_DECODE_WAIT_TIMEOUT set, the decode kernels of this pool
+ * (gdn_decode_step, gdn_decode_step_conv) make each CTA's copy barrier expect
+ * 16 bytes more than its state-tile copy delivers: the copy lands, the
+ * bounded wait runs out (a second or two), the CTA sets GDN_DEVERR_TIMEOUT,
+ * leaves its state rows and its rows of o unwritten and exits with no copy
+ * in flight.  It exercises the error path of the waits without a fault; flags
+ * other than that bit are GDN_ERR_ARG. */
+#define GDN_TEST_DECODE_WAIT_TIMEOUT 1u
+gdn_status gdn_pool_set_test_flags(gdn_pool *pool, uint32_t flags);
 
 /* Causal depthwise conv of width conv_k followed by SiLU (baseRT issue #31,
  * "Why this looks tractable": gdn_conv_silu), on each sequence's slot cache.
