@@ -18,7 +18,9 @@ overlapping the neighbouring steps' compute), the same step as two calls
 roofline fraction (timed on the decode launch of the two-call step), the
 oracle timed on the host cores (`cpu_baseline`: one thread and all cores;
 decode, prefill and verify), SM clocks sampled during timing, and
-`secondary` measurements: the 18-layer slot sweep (N = 1 .. 512),
+`steady_state` (back-to-back steps over rotating slot sets, no flush), and
+`secondary` measurements: the 18-layer slot sweep (N = 1 .. 512), one layer
+at N = 1 .. 16 (the small-N latency path),
 speculative verify (128 slots, T = 4), varlen chunked prefill with its
 roofline, the output gated RMSNorm, the decode step on pools that store the
 state in bf16 / binary16, and the layer's input projection (gdn_in_proj).
@@ -80,9 +82,9 @@ def _parse():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--sweep-steps", type=int, default=128)
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--sections", default="sweep,verify,prefill,norm,half,in_proj",
-                    help="secondary measurements to run (comma list of sweep, verify, prefill, "
-                         "norm, half, in_proj)")
+    ap.add_argument("--sections", default="sweep,small_n,verify,prefill,norm,half,in_proj",
+                    help="secondary measurements to run (comma list of sweep, small_n, verify, "
+                         "prefill, norm, half, in_proj)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
@@ -464,6 +466,36 @@ class DecodeBench:
         ktime = sum(a.elapsed_time(b) for a, b in kev) / 1e3 if kernel_events else None
         return total, ktime
 
+    def timed_steady(self, steps):
+        """Back-to-back one-call steps with no flush, rotating over four
+        disjoint sets of 64 slots (the active set, then the other 192 slots of
+        the pool): 512 MiB of state, four times L2, so each step streams its
+        state from HBM while the previous step's dirty lines drain, as in a
+        long run.  One timed region over all steps; returns seconds."""
+        torch = self.torch
+        if not hasattr(self, "slot_sets"):
+            rest = sorted(set(range(self.pool.state.shape[1])) - set(self.ids.tolist()))
+            self.slot_sets = [self.ids] + [
+                torch.tensor(rest[64 * j:64 * (j + 1)], dtype=torch.int32, device=self.ids.device)
+                for j in range(3)]
+        x, g, beta = self.parts(0)
+
+        def one(j):
+            self.abi.gdn_decode_step_conv(self.pool, 0, self.slot_sets[j % 4], x, self.w, self.y,
+                                          g, beta, self.os[0])
+
+        for j in range(8):
+            one(j)
+        E = lambda: torch.cuda.Event(enable_timing=True)
+        a, b = E(), E()
+        torch.cuda.synchronize()
+        a.record()
+        for j in range(steps):
+            one(j)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3
+
     def timed_e2e(self, steps):
         """End to end through the C ABI from pinned host memory: every step's
         packed inputs are copied host -> device and its o device -> host, on a
@@ -532,6 +564,64 @@ def half_state_bench(torch, abi, synth, device, steps, peak):
                        "on a pool storing the state in bf16 / binary16, float32 arithmetic; "
                        "L2 flushed between steps")
     return out
+
+
+def small_n_bench(torch, abi, synth, device, steps):
+    """One layer of the decode-step shape on a 256-slot pool with N = 1, 4, 8,
+    16 active slots: the one-call step (one fused kernel while its grid fits
+    the GPU at once) eager, and replayed from a CUDA graph of that one call.
+    L2 flushed between steps."""
+    s = synth.GDN_LAYER
+    pool = abi.Pool.for_shape(s, 1, 256, conv_dtype=torch.bfloat16, host_checks=False,
+                              device=device)
+    gen = torch.Generator(device=device).manual_seed(11)
+    pool.state.normal_(0.0, 0.1, generator=gen)
+    order = torch.from_numpy(synth.sweep_slot_order(2, 256)).to(device)
+    w = 0.25 * torch.randn(s.conv_ch, s.conv_k, device=device, generator=gen)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    out = []
+    for N in (1, 4, 8, 16):
+        ids = order[:N].contiguous()
+        x = torch.randn(N, s.conv_ch, device=device, generator=gen).bfloat16()
+        g = (-torch.nn.functional.softplus(torch.randn(N, s.h_v, device=device,
+                                                       generator=gen))).bfloat16()
+        bt = torch.sigmoid(torch.randn(N, s.h_v, device=device, generator=gen)).bfloat16()
+        y = torch.empty(N, s.conv_ch, device=device, dtype=torch.bfloat16)
+        o = torch.empty(N, s.h_v, s.dv, device=device)
+        step = lambda st=None: abi.gdn_decode_step_conv(pool, 0, ids, x, w, y, g, bt, o,
+                                                          stream=st)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            evs = [(E(), E()) for _ in range(steps)]
+            torch.cuda.synchronize()
+            for a, b in evs:
+                flush.zero_()
+                a.record()
+                fn()
+                b.record()
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+
+        t_eager = timed(step)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                step(side)
+        torch.cuda.current_stream().wait_stream(side)
+        t_graph = timed(graph.replay)
+        del graph
+        out.append({"n_active": N, "us_per_step_eager": t_eager * 1e6,
+                    "us_per_step_graph": t_graph * 1e6,
+                    "state_gbs_graph": N * STATE_BYTES_PER_SLOT_LAYER / t_graph / 1e9})
+    del pool
+    return {"workload": "one layer of the decode-step shape, 256-slot pool, N active, the "
+                        "one-call step (median of the steps), L2 flushed between steps",
+            "points": out}
 
 
 def in_proj_bench(torch, abi, synth, device, steps, hbm_peak, bf16_peak):
@@ -888,6 +978,8 @@ def run_gpu(args, rank, world):
     barrier()
     t_e2e = b.timed_e2e(args.steps)
     barrier()
+    t_steady = b.timed_steady(max(args.steps, 64))
+    barrier()
     secondary = {}
     sections = set() if args.no_secondary else set(args.sections.split(","))
     if "sweep" in sections:
@@ -900,6 +992,8 @@ def run_gpu(args, rank, world):
         secondary["norm"] = norm_bench(torch, abi, device, 20, peak)
     if "half" in sections:
         secondary["half_state"] = half_state_bench(torch, abi, synth, device, 50, peak)
+    if "small_n" in sections:
+        secondary["small_n"] = small_n_bench(torch, abi, synth, device, 50)
     if "in_proj" in sections:
         secondary["in_proj"] = in_proj_bench(torch, abi, synth, device, 20, peak, tc_peak)
     time.sleep(0.2)
@@ -928,6 +1022,10 @@ def run_gpu(args, rank, world):
                         "device, one-call conv + decode, o -> pinned host; copies on a "
                         "second stream, double-buffered, overlapping the neighbouring "
                         "steps' compute inside the timed regions"},
+        "steady_state": {"value": b.n * max(args.steps, 64) * world / t_steady, "unit": UNIT,
+                         "ms_per_step": t_steady / max(args.steps, 64) * 1e3,
+                         "note": "back-to-back one-call steps, no flush, rotating over four "
+                                 "disjoint 64-slot sets of the pool (512 MiB of state)"},
         "two_calls": {"value": units / t_two, "unit": UNIT,
                       "ms_per_step": t_two / args.steps * 1e3,
                       "note": "the same step as gdn_conv_silu then gdn_decode_step, "
