@@ -369,8 +369,9 @@ gdn_status gdn_spec_verify_deferred(gdn_pool *pool, int32_t layer, const int32_t
  * allocator.  A call needing more than 64 MiB -- about 32 KiB per 64-token
  * chunk per value head, counting (tokens / 64 + sequences) chunks -- returns
  * GDN_ERR_SIZE and launches nothing.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture.  Every call shares the one array: calls whose work
+ * array's device address (cudaGetSymbolAddress) and keeps it for the process:
+ * make that first call before any stream capture, and do not call it again on
+ * a device after cudaDeviceReset.  Every call shares the one array: calls whose work
  * overlaps on the GPU (other streams, other threads, other pools of the same
  * device) race on it and must be serialised by the caller. */
 gdn_status gdn_prefill_chunked_noalloc(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
