@@ -7,7 +7,8 @@ held to max|gpu - ref| <= 1e-5 * max|ref|; a bf16 y is additionally rounded
 once, |gpu - ref| <= 2^-8 |ref| + 1e-5 max|ref| elementwise.  Shapes cover a
 decode step (64 tokens), ragged token counts (M tails), output widths that
 are not a multiple of the tile (N tails) and hidden sizes that are not a
-multiple of the 64-wide K block (zero-filled K tails)."""
+multiple of the 64-wide K block (zero-filled K tails), on each of the three
+kernel forms (chosen by the number of output tiles)."""
 import numpy as np
 import pytest
 import torch
@@ -33,9 +34,12 @@ def _inputs(rng, tokens, hidden, n_out):
     return x, w
 
 
+# 64 / 300 tokens: 96-column tiles (one wave); 512: 128-column tiles, two CTAs
+# per SM; 2048: the persistent kernel (128 x 256 tiles, double-buffered TMEM)
 @pytest.mark.parametrize("tokens,hidden,n_out", [(64, HIDDEN, N_OUT), (300, HIDDEN, N_OUT),
-                                                 (2048, HIDDEN, N_OUT), (1, 64, 16),
-                                                 (130, 200, 72), (257, 1000, 344)])
+                                                 (512, HIDDEN, N_OUT), (2048, HIDDEN, N_OUT),
+                                                 (1, 64, 16), (130, 200, 72), (257, 1000, 344),
+                                                 (2000, 520, 3000)])
 @pytest.mark.parametrize("ydt", ["f32", "bf16"])
 def test_in_proj_matches_oracle(tokens, hidden, n_out, ydt):
     rng = np.random.default_rng(tokens + hidden + n_out)
