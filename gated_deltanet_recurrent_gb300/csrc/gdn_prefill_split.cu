@@ -801,7 +801,7 @@ __global__ void __launch_bounds__(NT, 1)
   // xor-shuffle rounds, and each stores 4 consecutive tokens of one k.
   auto build_kt = [&](int c0s) {
     const int l4 = lane & 3;
-#pragma unroll 2
+#pragma unroll 4
     for (int it = 0; it < 8; ++it) {
       const int blk = it * 8 + warp;                 // 8 token groups x 8 k-quad groups
       const int i = 8 * (blk & 7) + (lane & 7);
@@ -870,29 +870,33 @@ __global__ void __launch_bounds__(NT, 1)
     const int i0 = 32 * half;
     {
       const int v = row;
+      // this thread's 32 columns of E and D3, all four loads under one wait
+      float e[32], d3[32];
+      tc::tmem_ld16x4(lrow + T_E + i0, lrow + T_E + i0 + 16, lrow + T_D3 + i0,
+                      lrow + T_D3 + i0 + 16, e, d3);
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         const int t0 = i0 + 16 * cb;
-        float e[16], d3[16], f[16];
-        tc::tmem_ld16(lrow + T_E + t0, e);
-        tc::tmem_ld16(lrow + T_D3 + t0, d3);
+        float f[16], dd[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int t = t0 + j;
-          d3[j] *= sGam[t];
-          f[j] = XU[t * XS + v] - sBeta[t] * sGam[t] * e[j];
+          dd[j] = d3[16 * cb + j] * sGam[t];
+          f[j] = XU[t * XS + v] - sBeta[t] * sGam[t] * e[16 * cb + j];
         }
         tc::tmem_st16(lrow + T_F + t0, f);
-        tc::tmem_st16(lrow + T_D4 + t0, d3);
+        tc::tmem_st16(lrow + T_D4 + t0, dd);
       }
       const float gn = sGam[C - 1];
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        float sv[16];
-        tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, sv);
+      for (int cb = 0; cb < 2; ++cb) {
+        float sv[32];
+        const uint32_t sc = lrow + T_S + 64 * half + 32 * cb;
+        tc::tmem_ld32(sc, sc + 16, sv);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) sv[j] *= gn;
-        tc::tmem_st16(lrow + T_S + 64 * half + 16 * cb, sv);
+        for (int j = 0; j < 32; ++j) sv[j] *= gn;
+        tc::tmem_st16(sc, sv);
+        tc::tmem_st16(sc + 16, sv + 16);
       }
       tc::tmem_st_wait();
     }
@@ -963,18 +967,13 @@ __global__ void __launch_bounds__(NT, 1)
     // outputs o[t][v] = scale D4[v][t] (gamma_t S Q^T + Delta^T P^T), this warp's half of t
     {
       const int v = row;
-      TO *ob = o + (lo + c0) * p.h_v * D + (int64_t)h * D + v;
+      const int64_t ostep = (int64_t)p.h_v * D;
+      TO *ob = o + (lo + c0 + i0) * ostep + (int64_t)h * D + v;
+      float d4[32];
+      tc::tmem_ld32(lrow + T_D4 + i0, lrow + T_D4 + i0 + 16, d4);
 #pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        const int t0 = i0 + 16 * cb;
-        float d4[16];
-        tc::tmem_ld16(lrow + T_D4 + t0, d4);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = t0 + j;
-          if (t < n) Elem<TO>::store1(ob + (int64_t)t * p.h_v * D, scale * d4[j]);
-        }
-      }
+      for (int j = 0; j < 32; ++j)
+        if (i0 + j < n) Elem<TO>::store1(ob + (int64_t)j * ostep, scale * d4[j]);
     }
     if (!last) build_kt(c0 + C);
     tc::fence_before_sync();

@@ -163,6 +163,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr0, uint32_t taddr1, floa
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Four 16-column loads (two 32-column pieces) of this thread's TMEM lane under
+// one wait: a = columns [a0, a0 + 16) and [a1, a1 + 16), b likewise.
+__device__ __forceinline__ void tmem_ld16x4(uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1,
+                                            float *a, float *b) {
+  uint32_t r[64];
+#define GDN_LD16(ADDR, OFF)                                                                       \
+  asm volatile(                                                                                  \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"    \
+      "%14,%15}, [%16];"                                                                         \
+      : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]),                   \
+        "=r"(r[OFF + 4]), "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7]),                   \
+        "=r"(r[OFF + 8]), "=r"(r[OFF + 9]), "=r"(r[OFF + 10]), "=r"(r[OFF + 11]),                 \
+        "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]), "=r"(r[OFF + 15])                \
+      : "r"(ADDR))
+  GDN_LD16(a0, 0);
+  GDN_LD16(a1, 16);
+  GDN_LD16(b0, 32);
+  GDN_LD16(b1, 48);
+#undef GDN_LD16
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    a[j] = __uint_as_float(r[j]);
+    b[j] = __uint_as_float(r[32 + j]);
+  }
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
