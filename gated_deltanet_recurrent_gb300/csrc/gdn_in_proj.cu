@@ -197,8 +197,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
 // ---- persistent form for many tiles (prefill-sized token counts) ----
 //
 // One CTA per SM walks the output tiles t = blockIdx.x, blockIdx.x + grid, ...
-// (128 x 256 each, consecutive CTAs on the same column block, so a W tile is
-// read from L2 by neighbours).  The producer and MMA threads run across tile
+// (128 x 256 each, column block fastest: the CTAs in flight cover a few row
+// blocks of x and all of W, which stays resident in L2).  The producer and MMA threads run across tile
 // boundaries through one 4-stage ring (48 KiB per stage); the accumulator is
 // double-buffered in TMEM (2 x 256 columns), so the four epilogue warps drain
 // tile i while the MMAs of tile i + 1 run.  Barriers: full / empty per stage
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int64_t g = 0, issued = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const int m0 = (t % m_tiles) * kBM, n0 = (t / m_tiles) * kPBN;
+      const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kPBN;
       for (int kb = 0; kb < KB; ++kb, ++g) {
         const int s = (int)(g % S);
         const int64_t u = g / S;
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const int m0 = (t % m_tiles) * kBM, n0 = (t / m_tiles) * kPBN;
+      const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kPBN;
       const int row = m0 + 32 * quad + lane;
       TO *yrow = y + (int64_t)row * ld_y + n0;
       const uint32_t acc = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)(b * kPBN);

@@ -34,12 +34,13 @@ def _inputs(rng, tokens, hidden, n_out):
     return x, w
 
 
-# 64 / 300 tokens: 96-column tiles (one wave); 512: 128-column tiles, two CTAs
-# per SM; 2048: the persistent kernel (128 x 256 tiles, double-buffered TMEM)
+# 64 / 300 tokens: 96-column tiles (one wave); 512, 2000: 128-column tiles, two
+# CTAs per SM; 2048 and 4100 (with M, N and K tails): the persistent kernel
+# (128 x 256 tiles, double-buffered TMEM)
 @pytest.mark.parametrize("tokens,hidden,n_out", [(64, HIDDEN, N_OUT), (300, HIDDEN, N_OUT),
                                                  (512, HIDDEN, N_OUT), (2048, HIDDEN, N_OUT),
                                                  (1, 64, 16), (130, 200, 72), (257, 1000, 344),
-                                                 (2000, 520, 3000)])
+                                                 (2000, 520, 3000), (4100, 200, 4904)])
 @pytest.mark.parametrize("ydt", ["f32", "bf16"])
 def test_in_proj_matches_oracle(tokens, hidden, n_out, ydt):
     rng = np.random.default_rng(tokens + hidden + n_out)
