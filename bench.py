@@ -1024,6 +1024,10 @@ def run_gpu(args, rank, world):
                         "steps' compute inside the timed regions"},
         "steady_state": {"value": b.n * max(args.steps, 64) * world / t_steady, "unit": UNIT,
                          "ms_per_step": t_steady / max(args.steps, 64) * 1e3,
+                         "step_algorithmic_gbs": DECODE_KERNEL_BYTES_PER_SLOT * b.n
+                         * max(args.steps, 64) / t_steady / 1e9,
+                         "step_hbm_frac": DECODE_KERNEL_BYTES_PER_SLOT * b.n * max(args.steps, 64)
+                         / t_steady / 1e9 / peak,
                          "note": "back-to-back one-call steps, no flush, rotating over four "
                                  "disjoint 64-slot sets of the pool (512 MiB of state)"},
         "two_calls": {"value": units / t_two, "unit": UNIT,
