@@ -186,21 +186,27 @@ __device__ __forceinline__ void tma2(void *dst, const CUtensorMap *m, int x, int
       : "memory");
 }
 
-// One thread: the chunk's q, k, v halves (and g, beta) onto rbar.
-__device__ __forceinline__ void prefetch_raw(const InMaps &m, bool gb, int h, int hk,
-                                             int64_t tok0, unsigned char *raw, uint64_t *rbar) {
-  mbar_arrive_expect_tx(rbar, kRawQKV + (gb ? 2 * kRawGB : 0));
+// One thread: the chunk's q and k halves (and g, beta) onto rbar.
+__device__ __forceinline__ void prefetch_qk(const InMaps &m, bool gb, int h, int hk,
+                                            int64_t tok0, unsigned char *raw, uint64_t *rbar) {
+  mbar_arrive_expect_tx(rbar, 4 * kRawHalf + (gb ? 2 * kRawGB : 0));
   const int z = (int)tok0;
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     tma3(raw + (0 + hf) * kRawHalf, &m.q, 64 * hf, hk, z, rbar);
     tma3(raw + (2 + hf) * kRawHalf, &m.k, 64 * hf, hk, z, rbar);
-    tma3(raw + (4 + hf) * kRawHalf, &m.v, 64 * hf, h, z, rbar);
   }
   if (gb) {
     tma2(raw + kRawQKV, &m.g, h & ~7, z, rbar);
     tma2(raw + kRawQKV + kRawGB, &m.b, h & ~7, z, rbar);
   }
+}
+// One thread: the chunk's v halves onto vbar.
+__device__ __forceinline__ void prefetch_v(const InMaps &m, int h, int64_t tok0,
+                                           unsigned char *raw, uint64_t *vbar) {
+  mbar_arrive_expect_tx(vbar, 2 * kRawHalf);
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) tma3(raw + (4 + hf) * kRawHalf, &m.v, 64 * hf, h, (int)tok0, vbar);
 }
 
 // Elements 4c .. 4c+3 of token t of a [64][128] bf16 tile stored as two swizzled halves.
@@ -213,9 +219,10 @@ __device__ __forceinline__ float4 raw_load4(const unsigned char *tile, int t, in
                      __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
 }
 
-// stage_rows from the raw tiles (same mapping and arithmetic).
+// stage_rows from the raw tiles (same mapping and arithmetic), without v: the
+// state kernel reads v from the raw tile itself.
 __device__ __forceinline__ void stage_rows_raw(const unsigned char *raw, int n, float gt, float bt,
-                                               float *QK, float *XU, float *sG, float *sBeta) {
+                                               float *QK, float *sG, float *sBeta) {
   const int lane = threadIdx.x & 31;
   const int cg = lane >> 3;
   const int t = stage_token();
@@ -237,12 +244,6 @@ __device__ __forceinline__ void stage_rows_raw(const unsigned char *raw, int n, 
     for (int j = 0; j < D / 16; ++j)
       *reinterpret_cast<float4 *>(QK + tc::core_off(64 * which + t, 4 * (cg + 4 * j), D)) =
           scale4(xs, x4[j]);
-  }
-#pragma unroll
-  for (int j = 0; j < D / 16; ++j) {
-    const int c = cg + 4 * j;
-    const float4 v4 = real ? raw_load4(raw + 4 * kRawHalf, t, c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4 *>(XU + t * XS + 4 * c) = scale4(bt, v4);
   }
   if (cg == 0) {
     sG[t] = gt;
@@ -621,21 +622,33 @@ __global__ void __launch_bounds__(NT, 2)
 // --------------------------------------------------------------- state side
 // shared-memory map of seq_kernel (bytes)
 constexpr int S_QK = 0;                        // [Q;K] core tile 128 x 128
-constexpr int S_XU = S_QK + 128 * D * 4;       // beta v (plain 64 x XS)
-constexpr int S_PT = S_XU + C * XS * 4;        // P tile (from the workspace)
+constexpr int S_OS = S_QK + 128 * D * 4;       // outputs of a chunk, [64 tokens][128], for
+                                               // whole-row stores (up to 32 KiB)
+constexpr int S_PT = S_OS + C * XS * 4;        // P tile (from the workspace)
 constexpr int S_KT = S_PT + TILE * 4;          // Ktil^T tile [k][i], 128 x 64, right after P:
                                                // [P; Ktil^T] is one 192-row B operand
 constexpr int S_TT = S_KT + D * C * 4;         // T tile (from the workspace)
 constexpr int S_SC = S_TT + TILE * 4;          // G, gamma, beta, e^{G_n - G}
-constexpr int S_RAW = S_SC + 4 * C * 4;        // raw bf16 q, k, v of the next chunk
+constexpr int S_RAW = S_SC + 4 * C * 4;        // raw bf16 q, k, v (tensor-map rows), or else
+                                               // beta v (plain 64 x XS float32)
+constexpr int kXUBytes = C * XS * 4;
 template <typename TI>
-constexpr int seq_smem() { return S_RAW + (std::is_same<TI, bf16>::value ? kRawBytes : 0); }
+constexpr int seq_smem() {
+  return S_RAW + (std::is_same<TI, bf16>::value ? kRawBytes : kXUBytes);
+}
+static_assert(kRawBytes >= kXUBytes && C * D * 4 <= S_PT - S_OS, "shared-memory regions");
 static_assert(S_PT % 16 == 0 && S_KT == S_PT + TILE * 4 && S_TT % 16 == 0 && S_RAW % 16 == 0,
               "tile alignment");
 static_assert(S_RAW + kRawBytes <= 227 * 1024, "shared memory");
 
-// Thread that issues the bulk and tensor-map copies (warp 6), away from the
-// MMA-issuing thread 0 and the scan warp 7, so no warp carries two serial jobs.
+// Roles in seq_kernel: warps 0..7 compute (warp w reads TMEM lanes
+// 32 (w % 4) .. +31, column half w / 4) and meet on named barrier 1; warp 8
+// issues the MMA groups and the P / T tile copies.  The compute warps hand
+// work to warp 8 through mbarriers with one arrival per warp, so a thread that
+// stalls issuing a long MMA group holds up no CUDA-core work.
+constexpr int kMmaWarp = 8;
+constexpr int NTS = NT + 32;
+// Compute thread that issues the tensor-map copies of the raw rows (warp 6).
 constexpr int kCopier = 192;
 
 // TMEM columns
@@ -644,8 +657,37 @@ constexpr int kCopier = 192;
 constexpr uint32_t T_D4 = 0, T_S = 64, T_D3 = 192, T_E = 256, T_F = 320, T_DD = 384;
 constexpr uint32_t SEQ_TMEM = 512;
 
+__device__ __forceinline__ void cw_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The 256 compute threads meet; true when p holds for every one of them.
+__device__ __forceinline__ bool cw_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, 256, a;\n\tselp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
+// Bounded wait that also gives up as soon as the other role has failed.
+__device__ __forceinline__ bool wait_live(uint64_t *bar, uint32_t parity,
+                                          const volatile int *dead) {
+  for (uint32_t it = 0; it < (1u << 20); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*dead) return false;
+  }
+  return false;
+}
+// This warp's TMEM stores have completed (each lane waited) and its operand
+// writes to shared memory are fenced for the tensor core: one arrival.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+  tc::fence_before_sync();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 template <typename TI, typename TO>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NTS, 1)
     seq_kernel(PoolView p, int layer, SeqIndex seq, QKV in, TO *__restrict__ o, float scale,
                const int32_t *__restrict__ off, int64_t cap, const float *__restrict__ work,
                const __grid_constant__ InMaps maps, int raw_rows, int raw_gb, Checkpoints ck) {
@@ -653,7 +695,8 @@ __global__ void __launch_bounds__(NT, 1)
   const bool RAW = std::is_same<TI, bf16>::value && raw_rows != 0;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *QK = reinterpret_cast<float *>(smem + S_QK);
-  float *XU = reinterpret_cast<float *>(smem + S_XU);
+  TO *OS = reinterpret_cast<TO *>(smem + S_OS);
+  float *XU = reinterpret_cast<float *>(smem + S_RAW);  // beta v when the rows are staged
   unsigned char *RW = smem + S_RAW + ((1024u - (smem_addr(smem + S_RAW) & 1023u)) & 1023u);
   const bool GB = RAW && raw_gb != 0;  // g, beta come with the tensor-map copies too
   float *PT = reinterpret_cast<float *>(smem + S_PT);
@@ -663,14 +706,15 @@ __global__ void __launch_bounds__(NT, 1)
   float *sGam = sG + C;
   float *sBeta = sGam + C;
   float *sDte = sBeta + C;
-  __shared__ __align__(8) uint64_t bar;    // MMA completion
-  __shared__ __align__(8) uint64_t tbar;   // P / T tiles landed
-  __shared__ __align__(8) uint64_t rbar;   // raw q, k, v rows landed
+  __shared__ __align__(8) uint64_t b_ed3, b_dd, b_upd;  // MMA groups done
+  __shared__ __align__(8) uint64_t tbar, rbar, vbar;     // P / T tiles, raw q k, raw v landed
+  __shared__ __align__(8) uint64_t f_rdy, g_rdy, s_rdy;  // compute warps -> MMA warp
   __shared__ uint32_t tmem_slot;
+  __shared__ int dead;  // set by the role that gave up waiting
 
   const int h = blockIdx.x, si = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int quad = warp & 3, half = warp >> 2;
+  const int quad = warp & 3, half = (warp >> 2) & 1;
   const int row = 32 * quad + lane;
   const int slot = seq.slot_ids[si];
   const bool first = h == 0 && tid == 0;
@@ -689,6 +733,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (first) raise_error(p.err, GDN_DEVERR_SEQ);  // overlapping sequences
     return;
   }
+  const int nch = (len + C - 1) / C;
   const int hk = h / (p.h_v / p.h_k);
   const gdn_dtype sd = p.state_dtype;
   char *Sg = p.state_at(p.state_head_elem(layer, slot, h));  // float32, bf16 or f16 elements
@@ -697,305 +742,390 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (warp == 0) tc::tmem_alloc(&tmem_slot, SEQ_TMEM);
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    mbar_init(&b_ed3, 1);
+    mbar_init(&b_dd, 1);
+    mbar_init(&b_upd, 1);
     mbar_init(&tbar, 1);
     mbar_init(&rbar, 1);
+    mbar_init(&vbar, 1);
+    mbar_init(&f_rdy, 8);
+    mbar_init(&g_rdy, 8);
+    mbar_init(&s_rdy, 8);
+    dead = 0;
     mbar_fence_init();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (tid == kCopier) {  // chunk 0's P and T tiles
-    mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
-    bulk_g2s(PT, wsq, kTileBytes, &tbar);
-    bulk_g2s(TT, wsq + TILE, kTileBytes, &tbar);
-  }
   const uint32_t tm = tmem_slot;
-  const uint32_t lrow = tm + ((uint32_t)(32 * quad) << 16);
-  {  // state row `row`, column half `half` -> TMEM (float32)
-    const int64_t e0 = (int64_t)row * D + 64 * half;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 x = state_ld4(Sg, e0 + (c * 4 + j) * 4, sd);
-        v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
-      }
-      tc::tmem_st16(lrow + T_S + 64 * half + c * 16, v);
-    }
-    tc::tmem_st_wait();
-  }
+  volatile int *vdead = &dead;
 
-  const TI *qg = static_cast<const TI *>(in.q);
-  const TI *kg = static_cast<const TI *>(in.k);
-  const TI *vg = static_cast<const TI *>(in.v);
-  const uint32_t qk_s = smem_addr(QK);
-  const uint32_t pt_s = smem_addr(PT);
-  const uint32_t tt_s = smem_addr(TT);
-  constexpr uint32_t SBO_D = tc::sbo_bytes(D);
-  constexpr uint32_t SBO_C = tc::sbo_bytes(C);
-  constexpr uint32_t KSTEP = 2 * tc::kLBO;
-  uint32_t phase = 0, tphase = 0, rphase = 0;
-  bool alive = true;
-  float g_next = 0.f, b_next = 0.f;  // this thread's g, beta of the next chunk to stage (RAW)
-
-  // Stage chunk c0s into QK, XU and the scalars (then start fetching the one
-  // after it), and form its cumulative decays.  Ends with the tile writes
-  // fenced for the tensor core; the caller's next barrier publishes them.
-  auto stage_next = [&](int c0s) {
-    const int ns = min(C, len - c0s);
-    if (RAW) {
-      alive = __syncthreads_and(alive && mbar_wait_bounded(&rbar, rphase));
-      rphase ^= 1;
-      if (GB) {  // this head's column of the [64][8] g and beta tiles (padded tokens 0)
-        const int t = stage_token();
-        const bf16 *gt8 = reinterpret_cast<const bf16 *>(RW + kRawQKV);
-        g_next = t < ns ? __bfloat162float(gt8[t * 8 + (h & 7)]) : 0.f;
-        b_next = t < ns ? __bfloat162float(gt8[C * 8 + t * 8 + (h & 7)]) : 0.f;
-      }
-      stage_rows_raw(RW, ns, g_next, b_next, QK, XU, sG, sBeta);
-    } else {
-      stage_chunk<TI, true>(in, p, h, hk, lo + c0s, ns, QK, XU, sG, sBeta);
-    }
-    __syncthreads();
-    if (RAW && c0s + C < len) {  // the raw copy is consumed: fetch the next chunk's
-      const int nn = min(C, len - c0s - C);
-      if (tid == kCopier) prefetch_raw(maps, GB, h, hk, lo + c0s + C, RW, &rbar);
-      if (!GB) load_gb<TI>(in, p, h, lo + c0s + C, nn, g_next, b_next);
-    }
-    if (warp == 7) {  // cumulative log-decay (padded tokens carry g = 0)
-      const float a = sG[2 * lane], b = sG[2 * lane + 1];
-      float incl = a + b;
-#pragma unroll
-      for (int sh = 1; sh < 32; sh <<= 1) {
-        const float up = __shfl_up_sync(0xffffffffu, incl, sh);
-        if (lane >= sh) incl += up;
-      }
-      const float g0 = incl - b;
-      const float gl = __shfl_sync(0xffffffffu, incl, 31);
-      sG[2 * lane] = g0;
-      sG[2 * lane + 1] = incl;
-      sGam[2 * lane] = expf(g0);
-      sGam[2 * lane + 1] = expf(incl);
-      sDte[2 * lane] = expf(gl - g0);
-      sDte[2 * lane + 1] = expf(gl - incl);
-    }
-    tc::fence_async_smem();
-  };
-  // [D3 | E] = S [Q;K]^T (A = S from TMEM; M 128, N 128, K 128), one commit
-  auto issue_ed3 = [&]() {
-    if (tid == 0) {
-      constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j)
-        tc::mma_ts(tm + T_D3, tm + T_S + j * 8,
-                   tc::smem_desc(qk_s + j * KSTEP, tc::kLBO, SBO_D), id, j > 0);
-      tc::mma_commit(&bar);
-    }
-  };
-  // The Ktil^T tile of the staged chunk (needs its sDte), and rows `ahead`
-  // chunks further on pulled towards L2.
-  // Each thread reads 4 consecutive k of one token (a 16-byte piece of the K
-  // core tile), the 4 lanes of a quad transpose their 4 x 4 block with two
-  // xor-shuffle rounds, and each stores 4 consecutive tokens of one k.
-  auto build_kt = [&](int c0s) {
-    const int l4 = lane & 3;
-#pragma unroll 4
-    for (int it = 0; it < 8; ++it) {
-      const int blk = it * 8 + warp;                 // 8 token groups x 8 k-quad groups
-      const int i = 8 * (blk & 7) + (lane & 7);
-      const int k4 = 4 * (blk >> 3) + (lane >> 3);   // columns 4 k4 .. 4 k4 + 3
-      const float4 x = *reinterpret_cast<const float4 *>(QK + tc::core_off(64 + i, 4 * k4, D));
-      const float d = sDte[i];
-      const float v0 = d * x.x, v1 = d * x.y, v2 = d * x.z, v3 = d * x.w;
-      // stage 1 (xor 2): lanes 0,1 keep columns 0,1 and take rows 2,3's; lanes 2,3 the rest
-      const bool hi2 = (l4 & 2) != 0;
-      const float r0 = __shfl_xor_sync(0xffffffffu, hi2 ? v0 : v2, 2);
-      const float r1 = __shfl_xor_sync(0xffffffffu, hi2 ? v1 : v3, 2);
-      const float a0 = hi2 ? r0 : v0, a1 = hi2 ? r1 : v1;
-      const float a2 = hi2 ? v2 : r0, a3 = hi2 ? v3 : r1;
-      // stage 2 (xor 1): 2 x 2 transposes
-      const bool hi1 = (l4 & 1) != 0;
-      const float s0 = __shfl_xor_sync(0xffffffffu, hi1 ? a0 : a1, 1);
-      const float s1 = __shfl_xor_sync(0xffffffffu, hi1 ? a2 : a3, 1);
-      const float4 w = hi1 ? make_float4(s0, a1, s1, a3) : make_float4(a0, s0, a2, s1);
-      // lane l4 now holds column k = 4 k4 + l4 of tokens ib .. ib + 3
-      const int ib = 8 * (blk & 7) + (lane & 4);
-      *reinterpret_cast<float4 *>(KT + tc::core_off(4 * k4 + l4, ib, C)) = w;
-    }
-    const int t = tid & (C - 1);
-    const int64_t tok = lo + c0s + (RAW ? 3 * C : 2 * C) + t;
-    if (tok < hi) {
-      constexpr int LINES = (D * (int)sizeof(TI) + 127) / 128;
-      const char *qr = reinterpret_cast<const char *>(qg + tok * in.ld_qk + (int64_t)hk * D);
-      const char *kr = reinterpret_cast<const char *>(kg + tok * in.ld_qk + (int64_t)hk * D);
-      const char *vr = reinterpret_cast<const char *>(vg + tok * in.ld_v + (int64_t)h * D);
-      for (int l = tid >> 6; l < 3 * LINES; l += NT / C) {
-        const char *base = l < LINES ? qr : (l < 2 * LINES ? kr : vr);
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 128 * (l % LINES)));
-      }
-    }
-    tc::fence_async_smem();
-  };
-
-  // chunk 0: stage, start E and D3, build its Ktil^T while they run
-  if (RAW) {
-    if (tid == kCopier) prefetch_raw(maps, GB, h, hk, lo, RW, &rbar);
-    if (!GB) load_gb<TI>(in, p, h, lo, min(C, len), g_next, b_next);
-  }
-  stage_next(0);
-  tc::fence_before_sync();
-  alive = __syncthreads_and(alive);
-  tc::fence_after_sync();
-  if (alive) {
-    issue_ed3();
-    build_kt(0);
-  }
-
-  // Per chunk the state chain is E/D3 -> F -> Delta -> state update -> next
-  // E/D3; the next chunk's staging runs under the state update, and this
-  // chunk's outputs and the next chunk's Ktil^T under the next E/D3.
-  for (int c0 = 0; c0 < len && alive; c0 += C) {
-    const int n = min(C, len - c0);
-    const bool last = c0 + C >= len;
-    alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));  // E, D3 done
-    if (!alive) break;
-    phase ^= 1;
-    tc::fence_after_sync();
-
-    // F[v][t] = beta_t v_t[v] - beta_t gamma_t E[v][t] into TMEM; the output's state
-    // part gamma_t (S Q^T)[v][t] into the D4 columns (the Delta^T P^T MMA adds to it);
-    // S <- gamma_n S
-    const int i0 = 32 * half;
-    {
-      const int v = row;
-      // this thread's 32 columns of E and D3, all four loads under one wait
-      float e[32], d3[32];
-      tc::tmem_ld16x4(lrow + T_E + i0, lrow + T_E + i0 + 16, lrow + T_D3 + i0,
-                      lrow + T_D3 + i0 + 16, e, d3);
-#pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        const int t0 = i0 + 16 * cb;
-        float f[16], dd[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = t0 + j;
-          dd[j] = d3[16 * cb + j] * sGam[t];
-          f[j] = XU[t * XS + v] - sBeta[t] * sGam[t] * e[16 * cb + j];
-        }
-        tc::tmem_st16(lrow + T_F + t0, f);
-        tc::tmem_st16(lrow + T_D4 + t0, dd);
-      }
-      const float gn = sGam[C - 1];
-#pragma unroll 1
-      for (int cb = 0; cb < 2; ++cb) {
-        float sv[32];
-        const uint32_t sc = lrow + T_S + 64 * half + 32 * cb;
-        tc::tmem_ld32(sc, sc + 16, sv);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] *= gn;
-        tc::tmem_st16(sc, sv);
-        tc::tmem_st16(sc + 16, sv + 16);
-      }
-      tc::tmem_st_wait();
-    }
-    tc::fence_before_sync();
-    alive = __syncthreads_and(mbar_wait_bounded(&tbar, tphase));  // P, T tiles landed
-    if (!alive) break;
-    tphase ^= 1;
-    tc::fence_after_sync();
-
-    // Delta^T = F T^T  (A = F from TMEM, M 128, N 64, K 64)
-    if (tid == 0) {
-#pragma unroll
-      for (int j = 0; j < C / 8; ++j)
-        tc::mma_ts(tm + T_DD, tm + T_F + j * 8, tc::smem_desc(tt_s + j * KSTEP, tc::kLBO, SBO_C),
-                   tc::idesc_tf32(128, 64), j > 0);
-      tc::mma_commit(&bar);
-    }
-    alive = __syncthreads_and(mbar_wait_bounded(&bar, phase));
-    if (!alive) break;
-    phase ^= 1;
-    tc::fence_after_sync();
-
-    // [D4 | S] += Delta^T [P; Ktil^T]^T: D4 (onto gamma S Q^T) and the state update in one
-    // N = 192 chain; K = 64
-    if (tid == 0) {
-#pragma unroll
-      for (int j = 0; j < C / 8; ++j)
-        tc::mma_ts(tm + T_D4, tm + T_DD + j * 8, tc::smem_desc(pt_s + j * KSTEP, tc::kLBO, SBO_C),
-                   tc::idesc_tf32(128, 192), 1);
-      tc::mma_commit(&bar);
-    }
-    if (!last) stage_next(c0 + C);  // QK, XU and the scalars are free; the MMAs do not read them
-    tc::fence_before_sync();
-    alive = __syncthreads_and(alive && mbar_wait_bounded(&bar, phase));  // D4, new state ready
-    if (!alive) break;
-    phase ^= 1;
-    tc::fence_after_sync();
-    if (ck.every > 0 && c0 + C <= len && (c0 + C) % ck.every == 0) {  // checkpoint: copy S out
-      const int j = (c0 + C) / ck.every - 1;
-      const int ds = j < ck.per_seq ? ck.slots[(int64_t)si * ck.per_seq + j] : -1;
-      if (ds >= p.n_slots) {
-        if (tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
-      } else if (ds >= 0) {
-        char *dst = p.state_at(p.state_head_elem(layer, ds, h));
-        const int64_t e0 = (int64_t)row * D + 64 * half;
-#pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-          float v[16];
-          tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, v);
-#pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4)
-            state_st4<false>(dst, e0 + (cb * 4 + j4) * 4,
-                             make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]),
-                             sd);
-        }
-      }
-    }
-    if (!last) {
-      if (tid == kCopier) {  // the tiles are free again: fetch the next chunk's
-        const float *src = wsq + (int64_t)(c0 / C + 1) * wstep;
+  if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA warp
+    // Per chunk c: [F_c staged, P/T tiles] -> Delta^T = F T^T -> [S scaled,
+    // Ktil^T] -> [D4 | S] += Delta^T [P; Ktil^T]^T -> next tiles; [chunk c+1
+    // staged] -> [D3 | E] of chunk c+1.  Lane 0 issues; the warp waits together.
+    const uint32_t qk_s = smem_addr(QK), pt_s = smem_addr(PT), tt_s = smem_addr(TT);
+    constexpr uint32_t SBO_D = tc::sbo_bytes(D);
+    constexpr uint32_t SBO_C = tc::sbo_bytes(C);
+    constexpr uint32_t KSTEP = 2 * tc::kLBO;
+    const bool leader = lane == 0;
+    auto all_lanes = [](bool x) { return __all_sync(0xffffffffu, x) != 0; };
+    auto load_tiles = [&](int c) {  // P and T tiles of chunk c onto tbar
+      if (leader) {
+        const float *src = wsq + (int64_t)c * wstep;
         mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
         bulk_g2s(PT, src, kTileBytes, &tbar);
         bulk_g2s(TT, src + TILE, kTileBytes, &tbar);
       }
+    };
+    // [D3 | E] = S [Q;K]^T  (A = S from TMEM; M 128, N 128, K 128)
+    auto issue_ed3 = [&]() {
+      if (leader) {
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j)
+          tc::mma_ts(tm + T_D3, tm + T_S + j * 8,
+                     tc::smem_desc(qk_s + j * KSTEP, tc::kLBO, SBO_D), tc::idesc_tf32(128, 128),
+                     j > 0);
+        tc::mma_commit(&b_ed3);
+      }
+      __syncwarp();
+    };
+    int n_ed3 = 0, n_dd = 0, n_upd = 0, n_t = 1;  // groups issued, tile loads armed
+    load_tiles(0);
+    bool ok = all_lanes(wait_live(&s_rdy, 0, vdead));  // chunk 0 staged, state in TMEM
+    if (ok) {
+      tc::fence_after_sync();
       issue_ed3();
+      n_ed3 = 1;
     }
-
-    // outputs o[t][v] = scale D4[v][t] (gamma_t S Q^T + Delta^T P^T), this warp's half of t
-    {
-      const int v = row;
-      const int64_t ostep = (int64_t)p.h_v * D;
-      TO *ob = o + (lo + c0 + i0) * ostep + (int64_t)h * D + v;
-      float d4[32];
-      tc::tmem_ld32(lrow + T_D4 + i0, lrow + T_D4 + i0 + 16, d4);
+    for (int c = 0; ok && c < nch; ++c) {
+      const uint32_t par = c & 1;
+      ok = all_lanes(wait_live(&f_rdy, par, vdead) && wait_live(&tbar, par, vdead));
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (leader) {  // Delta^T = F T^T  (A = F from TMEM; M 128, N 64, K 64)
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (i0 + j < n) Elem<TO>::store1(ob + (int64_t)j * ostep, scale * d4[j]);
+        for (int j = 0; j < C / 8; ++j)
+          tc::mma_ts(tm + T_DD, tm + T_F + j * 8,
+                     tc::smem_desc(tt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 64),
+                     j > 0);
+        tc::mma_commit(&b_dd);
+      }
+      __syncwarp();
+      ++n_dd;
+      ok = all_lanes(wait_live(&b_dd, par, vdead) && wait_live(&g_rdy, par, vdead));
+      if (!ok) break;
+      tc::fence_after_sync();
+      // [D4 | S] += Delta^T [P; Ktil^T]^T: D4 (onto gamma S Q^T) and the state update in
+      // one N = 192 chain; K = 64
+      if (leader) {
+#pragma unroll
+        for (int j = 0; j < C / 8; ++j)
+          tc::mma_ts(tm + T_D4, tm + T_DD + j * 8,
+                     tc::smem_desc(pt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 192),
+                     1);
+        tc::mma_commit(&b_upd);
+      }
+      __syncwarp();
+      ++n_upd;
+      ok = all_lanes(wait_live(&b_upd, par, vdead));
+      if (!ok || c + 1 == nch) break;
+      load_tiles(c + 1);  // both tiles are free again
+      ++n_t;
+      ok = all_lanes(wait_live(&s_rdy, (c + 1) & 1, vdead));
+      if (!ok) break;
+      tc::fence_after_sync();
+      issue_ed3();
+      ++n_ed3;
     }
-    if (!last) build_kt(c0 + C);
-    tc::fence_before_sync();
-  }
-
-  if (alive) {
-    const int64_t e0 = (int64_t)row * D + 64 * half;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      float v[16];
-      tc::tmem_ld16(lrow + T_S + 64 * half + c * 16, v);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        state_st4<false>(Sg, e0 + (c * 4 + j) * 4,
-                         make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), sd);
+    if (!ok) {
+      if (leader) {
+        *vdead = 1;
+        raise_error(p.err, GDN_DEVERR_TIMEOUT);
+      }
+      // at most one group per barrier and one tile load can be in flight: let
+      // them finish before TMEM and shared memory are released
+      if (n_ed3) mbar_wait_bounded(&b_ed3, (n_ed3 - 1) & 1);
+      if (n_dd) mbar_wait_bounded(&b_dd, (n_dd - 1) & 1);
+      if (n_upd) mbar_wait_bounded(&b_upd, (n_upd - 1) & 1);
+      mbar_wait_bounded(&tbar, (n_t - 1) & 1);
     }
   } else {
-    if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
-    // give outstanding MMA groups and tile copies a second bounded chance to finish
-    mbar_wait_bounded(&bar, phase);
-    mbar_wait_bounded(&tbar, tphase);
-    if (RAW) mbar_wait_bounded(&rbar, rphase);
+    // ----------------------------------------------------------- compute warps
+    const uint32_t lrow = tm + ((uint32_t)(32 * quad) << 16);
+    {  // state row `row`, column half `half` -> TMEM (float32)
+      const int64_t e0 = (int64_t)row * D + 64 * half;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 x = state_ld4(Sg, e0 + (c * 4 + j) * 4, sd);
+          v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+        }
+        tc::tmem_st16(lrow + T_S + 64 * half + c * 16, v);
+      }
+      tc::tmem_st_wait();
+    }
+
+    const bool ovec = ((uintptr_t)o & 15) == 0;  // output rows start 16-byte aligned
+    const TI *qg = static_cast<const TI *>(in.q);
+    const TI *kg = static_cast<const TI *>(in.k);
+    const TI *vg = static_cast<const TI *>(in.v);
+    int n_r = 0, n_v = 0;  // raw q k and raw v loads armed
+    bool alive = true;
+    float g_next = 0.f, b_next = 0.f;  // this thread's g, beta of the next chunk to stage (RAW)
+
+    // Stage chunk c0s into QK (and XU unless v comes by tensor map) and the
+    // scalars (then start fetching the next q, k), and form its cumulative
+    // decays.  Ends with the tile writes fenced for the tensor core.
+    auto stage_next = [&](int c0s) {
+      const int ns = min(C, len - c0s);
+      if (RAW) {
+        alive = cw_and(alive && wait_live(&rbar, (c0s / C) & 1, vdead));
+        if (GB) {  // this head's column of the [64][8] g and beta tiles (padded tokens 0)
+          const int t = stage_token();
+          const bf16 *gt8 = reinterpret_cast<const bf16 *>(RW + kRawQKV);
+          g_next = t < ns ? __bfloat162float(gt8[t * 8 + (h & 7)]) : 0.f;
+          b_next = t < ns ? __bfloat162float(gt8[C * 8 + t * 8 + (h & 7)]) : 0.f;
+        }
+        stage_rows_raw(RW, ns, g_next, b_next, QK, sG, sBeta);
+      } else {
+        stage_chunk<TI, true>(in, p, h, hk, lo + c0s, ns, QK, XU, sG, sBeta);
+      }
+      cw_sync();
+      if (alive && RAW && c0s + C < len) {  // the raw copy is consumed: fetch the next chunk's
+        const int nn = min(C, len - c0s - C);
+        if (tid == kCopier) prefetch_qk(maps, GB, h, hk, lo + c0s + C, RW, &rbar);
+        ++n_r;
+        if (!GB) load_gb<TI>(in, p, h, lo + c0s + C, nn, g_next, b_next);
+      }
+      if (warp == 7) {  // cumulative log-decay (padded tokens carry g = 0)
+        const float a = sG[2 * lane], b = sG[2 * lane + 1];
+        float incl = a + b;
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+          const float up = __shfl_up_sync(0xffffffffu, incl, sh);
+          if (lane >= sh) incl += up;
+        }
+        const float g0 = incl - b;
+        const float gl = __shfl_sync(0xffffffffu, incl, 31);
+        sG[2 * lane] = g0;
+        sG[2 * lane + 1] = incl;
+        sGam[2 * lane] = expf(g0);
+        sGam[2 * lane + 1] = expf(incl);
+        sDte[2 * lane] = expf(gl - g0);
+        sDte[2 * lane + 1] = expf(gl - incl);
+      }
+      tc::fence_async_smem();
+    };
+    // The Ktil^T tile of the staged chunk (needs its sDte), and rows `ahead`
+    // chunks further on pulled towards L2.
+    // Each thread reads 4 consecutive k of one token (a 16-byte piece of the K
+    // core tile), the 4 lanes of a quad transpose their 4 x 4 block with two
+    // xor-shuffle rounds, and each stores 4 consecutive tokens of one k.
+    auto build_kt = [&](int c0s) {
+      const int l4 = lane & 3;
+#pragma unroll 4
+      for (int it = 0; it < 8; ++it) {
+        const int blk = it * 8 + warp;                 // 8 token groups x 8 k-quad groups
+        const int i = 8 * (blk & 7) + (lane & 7);
+        const int k4 = 4 * (blk >> 3) + (lane >> 3);   // columns 4 k4 .. 4 k4 + 3
+        const float4 x = *reinterpret_cast<const float4 *>(QK + tc::core_off(64 + i, 4 * k4, D));
+        const float d = sDte[i];
+        const float v0 = d * x.x, v1 = d * x.y, v2 = d * x.z, v3 = d * x.w;
+        // stage 1 (xor 2): lanes 0,1 keep columns 0,1 and take rows 2,3's; lanes 2,3 the rest
+        const bool hi2 = (l4 & 2) != 0;
+        const float r0 = __shfl_xor_sync(0xffffffffu, hi2 ? v0 : v2, 2);
+        const float r1 = __shfl_xor_sync(0xffffffffu, hi2 ? v1 : v3, 2);
+        const float a0 = hi2 ? r0 : v0, a1 = hi2 ? r1 : v1;
+        const float a2 = hi2 ? v2 : r0, a3 = hi2 ? v3 : r1;
+        // stage 2 (xor 1): 2 x 2 transposes
+        const bool hi1 = (l4 & 1) != 0;
+        const float s0 = __shfl_xor_sync(0xffffffffu, hi1 ? a0 : a1, 1);
+        const float s1 = __shfl_xor_sync(0xffffffffu, hi1 ? a2 : a3, 1);
+        const float4 w = hi1 ? make_float4(s0, a1, s1, a3) : make_float4(a0, s0, a2, s1);
+        // lane l4 now holds column k = 4 k4 + l4 of tokens ib .. ib + 3
+        const int ib = 8 * (blk & 7) + (lane & 4);
+        *reinterpret_cast<float4 *>(KT + tc::core_off(4 * k4 + l4, ib, C)) = w;
+      }
+      const int t = tid & (C - 1);
+      const int64_t tok = lo + c0s + (RAW ? 3 * C : 2 * C) + t;
+      if (tok < hi) {
+        constexpr int LINES = (D * (int)sizeof(TI) + 127) / 128;
+        const char *qr = reinterpret_cast<const char *>(qg + tok * in.ld_qk + (int64_t)hk * D);
+        const char *kr = reinterpret_cast<const char *>(kg + tok * in.ld_qk + (int64_t)hk * D);
+        const char *vr = reinterpret_cast<const char *>(vg + tok * in.ld_v + (int64_t)h * D);
+        for (int l = tid >> 6; l < 3 * LINES; l += NT / C) {
+          const char *base = l < LINES ? qr : (l < 2 * LINES ? kr : vr);
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(base + 128 * (l % LINES)));
+        }
+      }
+      tc::fence_async_smem();
+    };
+
+    // chunk 0: stage it and hand it (with the state) to the MMA warp, then build
+    // its Ktil^T while [D3 | E] runs
+    if (RAW) {
+      if (tid == kCopier) {
+        prefetch_qk(maps, GB, h, hk, lo, RW, &rbar);
+        prefetch_v(maps, h, lo, RW, &vbar);
+      }
+      n_r = n_v = 1;
+      if (!GB) load_gb<TI>(in, p, h, lo, min(C, len), g_next, b_next);
+    }
+    stage_next(0);
+    alive = cw_and(alive);
+    if (alive) warp_arrive(&s_rdy);
+    if (alive) build_kt(0);
+
+    // Per chunk the state chain is [D3 | E] -> F -> Delta -> state update ->
+    // next [D3 | E]; the next chunk is staged under the Delta MMAs, and this
+    // chunk's outputs and the next Ktil^T under the next [D3 | E].
+    for (int c = 0; c < nch && alive; ++c) {
+      const int c0 = c * C;
+      const uint32_t par = c & 1;
+      const int n = min(C, len - c0);
+      const bool last = c + 1 == nch;
+      alive = cw_and(wait_live(&b_ed3, par, vdead) &&    // [D3 | E] done, v landed
+                     (!RAW || wait_live(&vbar, par, vdead)));
+      if (!alive) break;
+      tc::fence_after_sync();
+
+      // F[v][t] = beta_t v_t[v] - beta_t gamma_t E[v][t] into TMEM; the output's state
+      // part gamma_t (S Q^T)[v][t] into the D4 columns (the Delta^T P^T MMA adds to it)
+      const int i0 = 32 * half;
+      {
+        const int v = row;
+        // element (t, v) of the raw v tile: half v / 64, 128-byte row t, swizzled 16-byte piece
+        const unsigned char *vr = RW + (4 + (v >> 6)) * kRawHalf + (v & 7) * 2;
+        const int vpiece = (v & 63) >> 3;
+        // this thread's 32 columns of E and D3, all four loads under one wait
+        float e[32], d3[32];
+        tc::tmem_ld16x4(lrow + T_E + i0, lrow + T_E + i0 + 16, lrow + T_D3 + i0,
+                        lrow + T_D3 + i0 + 16, e, d3);
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+          const int t0 = i0 + 16 * cb;
+          float f[16], dd[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = t0 + j;
+            dd[j] = d3[16 * cb + j] * sGam[t];
+            float bv;  // beta_t v_t[v] (0 for padded tokens)
+            if (RAW) {
+              const uint32_t u = *reinterpret_cast<const unsigned short *>(
+                  vr + t * 128 + ((vpiece ^ (t & 7)) << 4));
+              bv = t < n ? sBeta[t] * __uint_as_float(u << 16) : 0.f;
+            } else {
+              bv = XU[t * XS + v];
+            }
+            f[j] = bv - sBeta[t] * sGam[t] * e[16 * cb + j];
+          }
+          tc::tmem_st16(lrow + T_F + t0, f);
+          tc::tmem_st16(lrow + T_D4 + t0, dd);
+        }
+        tc::tmem_st_wait();
+      }
+      warp_arrive(&f_rdy);
+      {  // S <- gamma_n S, under Delta^T = F T^T (which reads neither)
+        const float gn = sGam[C - 1];
+#pragma unroll 1
+        for (int cb = 0; cb < 2; ++cb) {
+          float sv[32];
+          const uint32_t sc = lrow + T_S + 64 * half + 32 * cb;
+          tc::tmem_ld32(sc, sc + 16, sv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sv[j] *= gn;
+          tc::tmem_st16(sc, sv);
+          tc::tmem_st16(sc + 16, sv + 16);
+        }
+        tc::tmem_st_wait();
+      }
+      warp_arrive(&g_rdy);  // (this chunk's Ktil^T was fenced when it was built)
+
+      if (!last) {
+        cw_sync();  // every warp is past its reads of v (XU), gamma and beta
+        if (RAW && alive) {  // the raw v tile is free: fetch the next chunk's
+          if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RW, &vbar);
+          ++n_v;
+        }
+        stage_next(c0 + C);
+        if (alive) warp_arrive(&s_rdy);
+      }
+      alive = cw_and(alive && wait_live(&b_upd, par, vdead));  // D4, new state ready
+      if (!alive) break;
+      tc::fence_after_sync();
+      if (ck.every > 0 && c0 + C <= len && (c0 + C) % ck.every == 0) {  // checkpoint: copy S out
+        const int j = (c0 + C) / ck.every - 1;
+        const int ds = j < ck.per_seq ? ck.slots[(int64_t)si * ck.per_seq + j] : -1;
+        if (ds >= p.n_slots) {
+          if (tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
+        } else if (ds >= 0) {
+          char *dst = p.state_at(p.state_head_elem(layer, ds, h));
+          const int64_t e0 = (int64_t)row * D + 64 * half;
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {
+            float v[16];
+            tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, v);
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4)
+              state_st4<false>(dst, e0 + (cb * 4 + j4) * 4,
+                               make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]),
+                               sd);
+          }
+        }
+      }
+
+      // outputs o[t][v] = scale D4[v][t] (gamma_t S Q^T + Delta^T P^T): this warp's half
+      // of t into the [t][v] staging tile, then whole 16-byte pieces of token rows out
+      {
+        const int v = row;
+        const int64_t ostep = (int64_t)p.h_v * D;
+        float d4[32];
+        tc::tmem_ld32(lrow + T_D4 + i0, lrow + T_D4 + i0 + 16, d4);
+        if (ovec) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) Elem<TO>::store1(OS + (i0 + j) * D + v, scale * d4[j]);
+          cw_sync();
+          constexpr int VEC = 16 / (int)sizeof(TO), PIECES = D / VEC;  // per token row
+          TO *ob = o + (lo + c0) * ostep + (int64_t)h * D;
+          for (int e = tid; e < n * PIECES; e += NT) {
+            const int t = e / PIECES, pc = e % PIECES;
+            *reinterpret_cast<uint4 *>(ob + t * ostep + pc * VEC) =
+                *reinterpret_cast<const uint4 *>(OS + t * D + pc * VEC);
+          }
+        } else {
+          TO *ob = o + (lo + c0 + i0) * ostep + (int64_t)h * D + v;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (i0 + j < n) Elem<TO>::store1(ob + (int64_t)j * ostep, scale * d4[j]);
+        }
+      }
+      if (!last) build_kt(c0 + C);
+    }
+
+    if (alive) {
+      const int64_t e0 = (int64_t)row * D + 64 * half;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[16];
+        tc::tmem_ld16(lrow + T_S + 64 * half + c * 16, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          state_st4<false>(Sg, e0 + (c * 4 + j) * 4,
+                           make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), sd);
+      }
+    } else {
+      *vdead = 1;
+      if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
+      // raw-row loads still in flight land before shared memory is released
+      if (RAW && tid == kCopier) {
+        if (n_r > 0) mbar_wait_bounded(&rbar, (n_r - 1) & 1);
+        if (n_v > 0) mbar_wait_bounded(&vbar, (n_v - 1) & 1);
+      }
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1077,7 +1207,7 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   constexpr int smem = seq_smem<TI>();
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(p.h_v, seq.n_seqs), NT, smem, s>>>(p, layer, seq, in, static_cast<TO *>(o),
+  kern<<<dim3(p.h_v, seq.n_seqs), NTS, smem, s>>>(p, layer, seq, in, static_cast<TO *>(o),
                                                      scale, off, nc, tiles, maps, raw ? 1 : 0,
                                                      gb ? 1 : 0, ck);
   return cudaGetLastError();
