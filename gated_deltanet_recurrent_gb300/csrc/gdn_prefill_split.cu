@@ -163,6 +163,7 @@ __device__ __forceinline__ void stage_chunk(const QKV &in, const PoolView &p, in
 // [64 tokens][8 heads] bf16 (the 8-head group holding this head).
 struct InMaps {
   CUtensorMap q, k, v, g, b;   // q, k, v: {128, heads, tokens}; g, b: {h_v, tokens}
+  CUtensorMap o;               // bf16 outputs {128, h_v, tokens}, stores of whole chunks
 };
 constexpr int kRawHalf = C * 64 * 2;            // 8 KiB
 constexpr int kRawGB = C * 8 * 2;               // 1 KiB
@@ -186,6 +187,27 @@ __device__ __forceinline__ void tma2(void *dst, const CUtensorMap *m, int x, int
       : "memory");
 }
 
+// Tensor-map store of a shared-memory box (one thread), and the bulk-group
+// commit / waits that order it: .read once the source may be overwritten, the
+// full wait before the block exits.
+__device__ __forceinline__ void tma3_store(const CUtensorMap *m, int x, int y, int z,
+                                           const void *src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // One thread: the chunk's q and k halves (and g, beta) onto rbar.
 __device__ __forceinline__ void prefetch_qk(const InMaps &m, bool gb, int h, int hk,
                                             int64_t tok0, unsigned char *raw, uint64_t *rbar) {
@@ -201,12 +223,30 @@ __device__ __forceinline__ void prefetch_qk(const InMaps &m, bool gb, int h, int
     tma2(raw + kRawQKV + kRawGB, &m.b, h & ~7, z, rbar);
   }
 }
-// One thread: the chunk's v halves onto vbar.
+// One thread: the chunk's v halves to vdst, vdst + kRawHalf onto vbar.
 __device__ __forceinline__ void prefetch_v(const InMaps &m, int h, int64_t tok0,
-                                           unsigned char *raw, uint64_t *vbar) {
+                                           unsigned char *vdst, uint64_t *vbar) {
   mbar_arrive_expect_tx(vbar, 2 * kRawHalf);
 #pragma unroll
-  for (int hf = 0; hf < 2; ++hf) tma3(raw + (4 + hf) * kRawHalf, &m.v, 64 * hf, h, (int)tok0, vbar);
+  for (int hf = 0; hf < 2; ++hf) tma3(vdst + hf * kRawHalf, &m.v, 64 * hf, h, (int)tok0, vbar);
+}
+// One thread: the chunk's q and k halves into a [q h0 | k h0 | q h1 | k h1]
+// buffer (each half-pair a 128-row [Q;K] operand block) and, with gb, g and
+// beta to gbt, gbt + kRawGB, all onto bar.
+__device__ __forceinline__ void prefetch_qk_pairs(const InMaps &m, bool gb, int h, int hk,
+                                                  int64_t tok0, unsigned char *qk,
+                                                  unsigned char *gbt, uint64_t *bar) {
+  mbar_arrive_expect_tx(bar, 4 * kRawHalf + (gb ? 2 * kRawGB : 0));
+  const int z = (int)tok0;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    tma3(qk + (2 * hf) * kRawHalf, &m.q, 64 * hf, hk, z, bar);
+    tma3(qk + (2 * hf + 1) * kRawHalf, &m.k, 64 * hf, hk, z, bar);
+  }
+  if (gb) {
+    tma2(gbt, &m.g, h & ~7, z, bar);
+    tma2(gbt + kRawGB, &m.b, h & ~7, z, bar);
+  }
 }
 
 // Elements 4c .. 4c+3 of token t of a [64][128] bf16 tile stored as two swizzled halves.
@@ -970,7 +1010,7 @@ __global__ void __launch_bounds__(NTS, 1)
     if (RAW) {
       if (tid == kCopier) {
         prefetch_qk(maps, GB, h, hk, lo, RW, &rbar);
-        prefetch_v(maps, h, lo, RW, &vbar);
+        prefetch_v(maps, h, lo, RW + 4 * kRawHalf, &vbar);
       }
       n_r = n_v = 1;
       if (!GB) load_gb<TI>(in, p, h, lo, min(C, len), g_next, b_next);
@@ -1048,7 +1088,7 @@ __global__ void __launch_bounds__(NTS, 1)
       if (!last) {
         cw_sync();  // every warp is past its reads of v (XU), gamma and beta
         if (RAW && alive) {  // the raw v tile is free: fetch the next chunk's
-          if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RW, &vbar);
+          if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RW + 4 * kRawHalf, &vbar);
           ++n_v;
         }
         stage_next(c0 + C);
@@ -1133,11 +1173,568 @@ __global__ void __launch_bounds__(NTS, 1)
   if (warp == 0) tc::tmem_dealloc(tm, SEQ_TMEM);
 }
 
+// ------------------------------------------------- state side, bf16 rows
+// The state walk for bf16 q, k, v whose rows arrive by tensor-map copies.
+// [D3 | E] = S [Q;K]^T runs on kind::f16 over the raw tiles themselves (the
+// exact input values, two chunks of q, k buffered ahead), with the state as
+// a bf16 pair S = S_hi + S_lo (each rounded to nearest; the pair carries
+// about 16 significant bits, more than a tf32 operand) packed into the free
+// F and Delta columns of TMEM; the L2 norms of q and k scale the products'
+// columns.  Delta^T = F T^T and the N = 192 output / state update stay on
+// kind::tf32 as in seq_kernel; so do the roles of the nine warps.
+
+// shared-memory map of seq_bf16_kernel (bytes from a 1024-byte aligned base)
+constexpr int kQKBuf = 4 * kRawHalf;            // raw [q h0 | k h0 | q h1 | k h1], 32 KiB
+constexpr int B_QK = 0;                         // two q, k buffers (chunk c in buffer c % 2)
+constexpr int B_V = B_QK + 2 * kQKBuf;          // raw v [v h0 | v h1]
+constexpr int B_GB = B_V + 2 * kRawHalf;        // two raw g, beta buffers [g | beta]
+constexpr int B_OS = B_GB + 4 * kRawGB;         // outputs of a chunk, [64 tokens][128]
+constexpr int B_PT = B_OS + C * D * 4;          // P tile
+constexpr int B_KT = B_PT + TILE * 4;           // Ktil^T tile, right after P
+constexpr int B_TT = B_KT + D * C * 4;          // T tile
+constexpr int B_SC = B_TT + TILE * 4;           // per-token scalars, 8 x 64 floats
+constexpr int kSeqBf16Smem = B_SC + 8 * C * 4 + 1024;  // + alignment slack
+static_assert(B_V % 1024 == 0 && B_GB % 128 == 0 && B_PT % 16 == 0 && B_KT == B_PT + TILE * 4,
+              "tile alignment");
+static_assert(kSeqBf16Smem <= 227 * 1024, "shared memory");
+
+// Elements 4c .. 4c+3 of row t of a 64 x 128 bf16 operand held as two 64-column
+// swizzled halves `stride` bytes apart.
+__device__ __forceinline__ uint2 raw_piece(const unsigned char *half0, int stride, int t, int c) {
+  const int col = (4 * c) & 63;
+  return *reinterpret_cast<const uint2 *>(half0 + ((4 * c) >> 6) * stride + t * 128 +
+                                          ((((col >> 3) ^ (t & 7))) << 4) + (col & 7) * 2);
+}
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+template <typename TO>
+__global__ void __launch_bounds__(NTS, 1)
+    seq_bf16_kernel(PoolView p, int layer, SeqIndex seq, QKV in, TO *__restrict__ o, float scale,
+                    const int32_t *__restrict__ off, int64_t cap, const float *__restrict__ work,
+                    const __grid_constant__ InMaps maps, int raw_gb, int o_map,
+                    Checkpoints ck) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char *sm = smem + ((1024u - (smem_addr(smem) & 1023u)) & 1023u);
+  const bool GB = raw_gb != 0;  // g, beta come with the tensor-map copies too
+  unsigned char *RQK = sm + B_QK;
+  unsigned char *RV = sm + B_V;
+  unsigned char *RGB = sm + B_GB;
+  TO *OS = reinterpret_cast<TO *>(sm + B_OS);
+  // staged outputs: bf16 as two 64-column halves of [64 tokens][64] in the
+  // 128-byte swizzle (the output map's boxes); float32 as plain [64][128] rows
+  constexpr bool OB16 = std::is_same<TO, bf16>::value;
+  constexpr int kOSRow = D;
+  static_assert(B_OS % 1024 == 0, "output staging alignment");
+  float *PT = reinterpret_cast<float *>(sm + B_PT);
+  float *KT = reinterpret_cast<float *>(sm + B_KT);
+  float *TT = reinterpret_cast<float *>(sm + B_TT);
+  float *sG = reinterpret_cast<float *>(sm + B_SC);  // g, then (scan) nothing further
+  float *sGam = sG + C;    // gamma_t = e^{G_t}
+  float *sBeta = sGam + C;
+  float *sRq = sBeta + C;  // 1 / |q_t|, 1 / |k_t|
+  float *sRk = sRq + C;
+  float *sQ = sRk + C;     // gamma_t / |q_t|            (scales column t of S Q^T)
+  float *sK = sQ + C;      // beta_t gamma_t / |k_t|     (scales column t of S K^T)
+  float *sKt = sK + C;     // e^{G_n - G_t} / |k_t|      (scales token t of Ktil)
+  __shared__ __align__(8) uint64_t b_ed3, b_dd, b_upd;  // MMA groups done
+  __shared__ __align__(8) uint64_t tbar, vbar;           // P / T tiles, raw v landed
+  __shared__ __align__(8) uint64_t rbar[2];              // raw q, k (g, beta) buffers landed
+  __shared__ __align__(8) uint64_t f_rdy, g_rdy, s_rdy;  // compute warps -> MMA warp
+  __shared__ uint32_t tmem_slot;
+  __shared__ int dead;  // set by the role that gave up waiting
+
+  const int h = blockIdx.x, si = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int quad = warp & 3, half = (warp >> 2) & 1;
+  const int row = 32 * quad + lane;
+  const int slot = seq.slot_ids[si];
+  const bool first = h == 0 && tid == 0;
+  if (slot < 0 || slot >= p.n_slots) {
+    if (first) raise_error(p.err, GDN_DEVERR_SLOT);
+    return;
+  }
+  const int64_t lo = seq.cu_seqlens[si], hi = seq.cu_seqlens[si + 1];
+  if (hi < lo || lo < 0 || hi > seq.total_tokens) {
+    if (first) raise_error(p.err, GDN_DEVERR_SEQ);
+    return;
+  }
+  const int len = (int)(hi - lo);
+  if (len == 0) return;
+  if (off[si] < 0 || off[si + 1] > cap || off[si + 1] - off[si] != (len + C - 1) / C) {
+    if (first) raise_error(p.err, GDN_DEVERR_SEQ);  // overlapping sequences
+    return;
+  }
+  const int nch = (len + C - 1) / C;
+  const int hk = h / (p.h_v / p.h_k);
+  const gdn_dtype sd = p.state_dtype;
+  char *Sg = p.state_at(p.state_head_elem(layer, slot, h));  // float32, bf16 or f16 elements
+  const float *wsq = work + ((int64_t)off[si] * p.h_v + h) * (2 * TILE);  // chunk 0's tiles
+  const int64_t wstep = (int64_t)p.h_v * (2 * TILE);                      // next chunk
+
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, SEQ_TMEM);
+  if (tid == 0) {
+    mbar_init(&b_ed3, 1);
+    mbar_init(&b_dd, 1);
+    mbar_init(&b_upd, 1);
+    mbar_init(&tbar, 1);
+    mbar_init(&vbar, 1);
+    mbar_init(&rbar[0], 1);
+    mbar_init(&rbar[1], 1);
+    mbar_init(&f_rdy, 8);
+    mbar_init(&g_rdy, 8);
+    mbar_init(&s_rdy, 8);
+    dead = 0;
+    mbar_fence_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = tmem_slot;
+  volatile int *vdead = &dead;
+
+  if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA warp
+    const uint32_t pt_s = smem_addr(PT), tt_s = smem_addr(TT);
+    constexpr uint32_t SBO_C = tc::sbo_bytes(C);
+    constexpr uint32_t KSTEP = 2 * tc::kLBO;
+    const bool leader = lane == 0;
+    auto all_lanes = [](bool x) { return __all_sync(0xffffffffu, x) != 0; };
+    auto load_tiles = [&](int c) {  // P and T tiles of chunk c onto tbar
+      if (leader) {
+        const float *src = wsq + (int64_t)c * wstep;
+        mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
+        bulk_g2s(PT, src, kTileBytes, &tbar);
+        bulk_g2s(TT, src + TILE, kTileBytes, &tbar);
+      }
+    };
+    // [D3 | E] = (S_hi + S_lo) [Q;K]^T over the raw rows of chunk c: M 128, N 128,
+    // K 128 in steps of 16 (four 32-byte steps inside each swizzled 64-column half)
+    auto issue_ed3 = [&](int c) {
+      if (leader) {
+        const uint32_t b0 = smem_addr(RQK + (c & 1) * kQKBuf);
+        constexpr uint32_t id = tc::idesc_bf16(128, 128);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t bd = tc::smem_desc_sw128(b0 + (ks >> 2) * 2 * kRawHalf + 32 * (ks & 3));
+          tc::mma_ts_f16(tm + T_D3, tm + T_F + 8 * ks, bd, id, ks > 0);
+          tc::mma_ts_f16(tm + T_D3, tm + T_DD + 8 * ks, bd, id, 1);
+        }
+        tc::mma_commit(&b_ed3);
+      }
+      __syncwarp();
+    };
+    int n_ed3 = 0, n_dd = 0, n_upd = 0, n_t = 1;  // groups issued, tile loads armed
+    load_tiles(0);
+    bool ok = all_lanes(wait_live(&s_rdy, 0, vdead) && wait_live(&rbar[0], 0, vdead));
+    if (ok) {
+      tc::fence_after_sync();
+      issue_ed3(0);
+      n_ed3 = 1;
+    }
+    for (int c = 0; ok && c < nch; ++c) {
+      const uint32_t par = c & 1;
+      ok = all_lanes(wait_live(&f_rdy, par, vdead) && wait_live(&tbar, par, vdead));
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (leader) {  // Delta^T = F T^T  (A = F from TMEM; M 128, N 64, K 64)
+#pragma unroll
+        for (int j = 0; j < C / 8; ++j)
+          tc::mma_ts(tm + T_DD, tm + T_F + j * 8,
+                     tc::smem_desc(tt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 64),
+                     j > 0);
+        tc::mma_commit(&b_dd);
+      }
+      __syncwarp();
+      ++n_dd;
+      ok = all_lanes(wait_live(&b_dd, par, vdead) && wait_live(&g_rdy, par, vdead));
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (leader) {  // [D4 | S] += Delta^T [P; Ktil^T]^T  (N 192, K 64)
+#pragma unroll
+        for (int j = 0; j < C / 8; ++j)
+          tc::mma_ts(tm + T_D4, tm + T_DD + j * 8,
+                     tc::smem_desc(pt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 192),
+                     1);
+        tc::mma_commit(&b_upd);
+      }
+      __syncwarp();
+      ++n_upd;
+      ok = all_lanes(wait_live(&b_upd, par, vdead));
+      if (!ok || c + 1 == nch) break;
+      load_tiles(c + 1);  // both tiles are free again
+      ++n_t;
+      ok = all_lanes(wait_live(&s_rdy, (c + 1) & 1, vdead) &&
+                     wait_live(&rbar[(c + 1) & 1], ((c + 1) >> 1) & 1, vdead));
+      if (!ok) break;
+      tc::fence_after_sync();
+      issue_ed3(c + 1);
+      ++n_ed3;
+    }
+    if (!ok) {
+      if (leader) {
+        *vdead = 1;
+        raise_error(p.err, GDN_DEVERR_TIMEOUT);
+      }
+      if (n_ed3) mbar_wait_bounded(&b_ed3, (n_ed3 - 1) & 1);
+      if (n_dd) mbar_wait_bounded(&b_dd, (n_dd - 1) & 1);
+      if (n_upd) mbar_wait_bounded(&b_upd, (n_upd - 1) & 1);
+      mbar_wait_bounded(&tbar, (n_t - 1) & 1);
+    }
+  } else {
+    // ----------------------------------------------------------- compute warps
+    const uint32_t lrow = tm + ((uint32_t)(32 * quad) << 16);
+    const bool ovec = ((uintptr_t)o & 15) == 0;  // output rows start 16-byte aligned
+    {  // state row `row`, column half `half` -> TMEM (float32)
+      const int64_t e0 = (int64_t)row * D + 64 * half;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 x = state_ld4(Sg, e0 + (c * 4 + j) * 4, sd);
+          v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+        }
+        tc::tmem_st16(lrow + T_S + 64 * half + c * 16, v);
+      }
+      tc::tmem_st_wait();
+    }
+    int n_r0 = 0, n_r1 = 0, n_v = 0;  // raw loads armed per barrier
+    bool alive = true;
+    float g_next = 0.f, b_next = 0.f;  // this thread's g, beta of the next chunk (without GB)
+
+    // copier: q, k (g, beta) of chunk c into buffer c % 2
+    auto fetch_qk = [&](int c) {
+      const int b = c & 1;
+      if (tid == kCopier)
+        prefetch_qk_pairs(maps, GB, h, hk, lo + (int64_t)c * C, RQK + b * kQKBuf,
+                          RGB + b * 2 * kRawGB, &rbar[b]);
+      if (b) ++n_r1; else ++n_r0;
+    };
+    // Per-token scalars of chunk c: the L2 norms of its raw q and k rows, g and
+    // beta, then (warp 7) the cumulative decays and the column scales.
+    auto stage_scalars = [&](int c) {
+      const int ns = min(C, len - c * C), b = c & 1;
+      alive = cw_and(alive && wait_live(&rbar[b], (c >> 1) & 1, vdead));
+      const unsigned char *qk = RQK + b * kQKBuf;
+      const int t = stage_token(), part = lane >> 3;
+      float qq = 0.f, kk = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const uint2 qv = raw_piece(qk, 2 * kRawHalf, t, part + 4 * m);
+        const uint2 kv = raw_piece(qk + kRawHalf, 2 * kRawHalf, t, part + 4 * m);
+        const float a0 = bf_lo(qv.x), a1 = bf_hi(qv.x), a2 = bf_lo(qv.y), a3 = bf_hi(qv.y);
+        const float b0 = bf_lo(kv.x), b1 = bf_hi(kv.x), b2 = bf_lo(kv.y), b3 = bf_hi(kv.y);
+        qq += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+        kk += b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
+      }
+      qq += __shfl_xor_sync(0xffffffffu, qq, 8);
+      qq += __shfl_xor_sync(0xffffffffu, qq, 16);
+      kk += __shfl_xor_sync(0xffffffffu, kk, 8);
+      kk += __shfl_xor_sync(0xffffffffu, kk, 16);
+      float gt = g_next, bt = b_next;
+      if (GB) {  // this head's column of the [64][8] g and beta tiles (padded tokens 0)
+        const bf16 *g8 = reinterpret_cast<const bf16 *>(RGB + b * 2 * kRawGB);
+        gt = t < ns ? __bfloat162float(g8[t * 8 + (h & 7)]) : 0.f;
+        bt = t < ns ? __bfloat162float(g8[C * 8 + t * 8 + (h & 7)]) : 0.f;
+      }
+      if (part == 0) {
+        sRq[t] = rsqrtf(qq + kL2Eps);
+        sRk[t] = rsqrtf(kk + kL2Eps);
+        sG[t] = gt;
+        sBeta[t] = bt;
+      }
+      cw_sync();
+      if (warp == 7) {  // cumulative log-decay (padded tokens carry g = 0) and the scales
+        const float a = sG[2 * lane], bb = sG[2 * lane + 1];
+        float incl = a + bb;
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+          const float up = __shfl_up_sync(0xffffffffu, incl, sh);
+          if (lane >= sh) incl += up;
+        }
+        const float gl = __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * lane + e;
+          const float G = e == 0 ? incl - bb : incl;
+          const float gam = expf(G);
+          sGam[i] = gam;
+          sQ[i] = gam * sRq[i];
+          sK[i] = sBeta[i] * gam * sRk[i];
+          sKt[i] = expf(gl - G) * sRk[i];
+        }
+      }
+    };
+    // S (float32) -> the bf16 pair S_hi at the F columns and S_lo at the Delta
+    // columns, packed two per column (lower k in the low half), for the next
+    // [D3 | E], and S <- gn S in place for the next state update (which the
+    // pair does not see).  Arrives on s_rdy once all of it is in TMEM.
+    auto split_scale = [&](float gn) {
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        float sv[32], hp[16], lp[16];
+        const uint32_t sc = lrow + T_S + 64 * half + 32 * cb;
+        tc::tmem_ld32(sc, sc + 16, sv);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float s0 = sv[2 * m], s1 = sv[2 * m + 1];
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(s0, s1);
+          const float2 hf = __bfloat1622float2(h2);
+          const __nv_bfloat162 l2 = __floats2bfloat162_rn(s0 - hf.x, s1 - hf.y);
+          hp[m] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h2));
+          lp[m] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&l2));
+        }
+        tc::tmem_st16(lrow + T_F + 32 * half + 16 * cb, hp);
+        tc::tmem_st16(lrow + T_DD + 32 * half + 16 * cb, lp);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] *= gn;
+        tc::tmem_st16(sc, sv);
+        tc::tmem_st16(sc + 16, sv + 16);
+      }
+      tc::tmem_st_wait();
+      warp_arrive(&s_rdy);
+    };
+    // Ktil^T of chunk c (tokens past the chunk's end zero) from its raw k rows.
+    // A warp task is one
+    // token quad x 32 consecutive k (one k per lane): four 16-bit reads (one
+    // per token, 64 contiguous bytes of a swizzled row per warp), scaled, and
+    // one 16-byte store (a quarter-warp fills one core matrix).
+    auto build_kt = [&](int c) {
+      const int nn = min(C, len - c * C);
+      const unsigned char *kb = RQK + (c & 1) * kQKBuf + kRawHalf;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int task = it * 8 + warp;
+        const int tq = task & 15, k = 32 * (task >> 4) + lane;
+        const unsigned char *kc = kb + (k >> 6) * 2 * kRawHalf + (k & 7) * 2;
+        const int piece = (k & 63) >> 3;
+        const float4 d4 = *reinterpret_cast<const float4 *>(sKt + 4 * tq);
+        const float d[4] = {d4.x, d4.y, d4.z, d4.w};
+        float w[4];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+          const int i = 4 * tq + ii;
+          const uint32_t u =
+              *reinterpret_cast<const unsigned short *>(kc + i * 128 + ((piece ^ (i & 7)) << 4));
+          w[ii] = d[ii] * __uint_as_float(u << 16);
+          if (nn < C && i >= nn) w[ii] = 0.f;
+        }
+        *reinterpret_cast<float4 *>(KT + tc::core_off(k, 4 * tq, C)) =
+            make_float4(w[0], w[1], w[2], w[3]);
+      }
+      tc::fence_async_smem();
+    };
+    // F[v][t] = beta_t v_t[v] - (beta_t gamma_t / |k_t|) (S K^T)[v][t] and the
+    // output's state part (gamma_t / |q_t|) (S Q^T)[v][t] into TMEM, this
+    // thread's 32 tokens; padded tokens (FULL false) give 0
+    auto f_pass = [&](auto full, int n, int i0) {
+      constexpr bool FULL = decltype(full)::value;
+      const int v = row;
+      const unsigned char *vr = RV + (v >> 6) * kRawHalf + (v & 7) * 2;
+      const int vpiece = (v & 63) >> 3;
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        const int t0 = i0 + 16 * cb;
+        float ed[32], f[16], dd[16];  // ed: 16 columns of E, then the same of D3
+        tc::tmem_ld32(lrow + T_E + t0, lrow + T_D3 + t0, ed);
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {  // four tokens' scalars per vector load
+          const float4 b4 = *reinterpret_cast<const float4 *>(sBeta + t0 + 4 * j4);
+          const float4 q4 = *reinterpret_cast<const float4 *>(sQ + t0 + 4 * j4);
+          const float4 k4 = *reinterpret_cast<const float4 *>(sK + t0 + 4 * j4);
+          const float be[4] = {b4.x, b4.y, b4.z, b4.w}, qs[4] = {q4.x, q4.y, q4.z, q4.w};
+          const float ks[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * j4 + jj, t = t0 + j;
+            const uint32_t u = *reinterpret_cast<const unsigned short *>(
+                vr + t * 128 + ((vpiece ^ (t & 7)) << 4));
+            const float bv = be[jj] * __uint_as_float(u << 16);
+            dd[j] = ed[16 + j] * qs[jj];
+            f[j] = bv - ks[jj] * ed[j];
+            if (!FULL && t >= n) dd[j] = f[j] = 0.f;
+          }
+        }
+        tc::tmem_st16(lrow + T_F + t0, f);
+        tc::tmem_st16(lrow + T_D4 + t0, dd);
+      }
+      tc::tmem_st_wait();
+    };
+
+    // chunk 0 (and 1) on their way; chunk 0's scalars, split state, scaled
+    // state and Ktil^T to the MMA warp
+    if (tid == kCopier) prefetch_v(maps, h, lo, RV, &vbar);
+    n_v = 1;
+    fetch_qk(0);
+    if (nch > 1) fetch_qk(1);
+    if (!GB) load_gb<bf16>(in, p, h, lo, min(C, len), g_next, b_next);
+    stage_scalars(0);
+    if (!GB && nch > 1) load_gb<bf16>(in, p, h, lo + C, min(C, len - C), g_next, b_next);
+    alive = cw_and(alive);  // the scan's results are visible
+    if (alive) {
+      split_scale(sGam[C - 1]);
+      build_kt(0);
+      warp_arrive(&g_rdy);
+    }
+
+    // Per chunk c: [D3 | E] -> F -> (MMA warp: Delta, state update) while the
+    // next chunk's scalars are staged -> split and scale the new state (the
+    // next [D3 | E] starts) -> outputs and the next Ktil^T under it.
+    for (int c = 0; c < nch && alive; ++c) {
+      const int c0 = c * C;
+      const uint32_t par = c & 1;
+      const int n = min(C, len - c0);
+      const bool last = c + 1 == nch;
+      alive = cw_and(wait_live(&b_ed3, par, vdead) &&    // [D3 | E] done, v landed
+                     wait_live(&vbar, par, vdead));
+      if (!alive) break;
+      tc::fence_after_sync();
+      if (c + 2 < nch) fetch_qk(c + 2);  // buffer c % 2 is free: [D3 | E] and Ktil^T are done
+
+      const int i0 = 32 * half;
+      if (n == C) f_pass(std::true_type(), n, i0); else f_pass(std::false_type(), n, i0);
+      warp_arrive(&f_rdy);
+
+      if (!last) {
+        cw_sync();  // every warp is past its reads of v and of this chunk's scalars
+        if (alive) {  // the raw v tile is free: fetch the next chunk's
+          if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RV, &vbar);
+          ++n_v;
+        }
+        stage_scalars(c + 1);
+        if (!GB && c + 2 < nch)
+          load_gb<bf16>(in, p, h, lo + c0 + 2 * C, min(C, len - c0 - 2 * C), g_next, b_next);
+      }
+      if (tid == kCopier) bulk_wait_read();  // the last output store has read its staging
+      alive = cw_and(alive && wait_live(&b_upd, par, vdead));  // D4, new state ready
+      if (!alive) break;
+      tc::fence_after_sync();
+      if (ck.every > 0 && c0 + C <= len && (c0 + C) % ck.every == 0) {  // checkpoint: copy S out
+        const int j = (c0 + C) / ck.every - 1;
+        const int ds = j < ck.per_seq ? ck.slots[(int64_t)si * ck.per_seq + j] : -1;
+        if (ds >= p.n_slots) {
+          if (tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
+        } else if (ds >= 0) {
+          char *dst = p.state_at(p.state_head_elem(layer, ds, h));
+          const int64_t e0 = (int64_t)row * D + 64 * half;
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {
+            float v[16];
+            tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, v);
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4)
+              state_st4<false>(dst, e0 + (cb * 4 + j4) * 4,
+                               make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]),
+                               sd);
+          }
+        }
+      }
+      if (!last) split_scale(sGam[C - 1]);  // the next [D3 | E] starts here
+
+      // outputs o[t][v] = scale D4[v][t]: this warp's half of t into the [t][v] staging
+      // tile, then whole 16-byte pieces of token rows out
+      {
+        const int v = row;
+        const int64_t ostep = (int64_t)p.h_v * D;
+        float d4[32];
+        tc::tmem_ld32(lrow + T_D4 + i0, lrow + T_D4 + i0 + 16, d4);
+        if (ovec) {
+          if constexpr (OB16) {
+            // lanes v, v ^ 1 swap one value per token pair (j, j + 4) of each group of
+            // 8: the even lane writes (v, v + 1) of token j, the odd lane (v - 1, v) of
+            // token j + 4; the two rows differ in the swizzle's bit 2, so the two
+            // halves of the warp store to disjoint banks
+            const bool odd = (lane & 1) != 0;
+            unsigned char *oh = reinterpret_cast<unsigned char *>(OS) + (v >> 6) * kRawHalf +
+                                (v & 6) * 2;
+            const int vp = (v & 63) >> 3;
+#pragma unroll
+            for (int j8 = 0; j8 < 32; j8 += 8)
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const int j = j8 + jj;
+                const float a = scale * d4[j], b = scale * d4[j + 4];
+                const float x = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+                const int t = i0 + j + (odd ? 4 : 0);
+                *reinterpret_cast<__nv_bfloat162 *>(oh + t * 128 + ((vp ^ (t & 7)) << 4)) =
+                    odd ? __floats2bfloat162_rn(x, b) : __floats2bfloat162_rn(a, x);
+              }
+            tc::fence_async_smem();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) OS[(i0 + j) * kOSRow + v] = scale * d4[j];
+          }
+          cw_sync();
+          if (OB16 && o_map != 0 && n == C) {  // a whole chunk: two tensor-map stores
+            if (tid == kCopier) {
+              tma3_store(&maps.o, 0, h, (int)(lo + c0), OS);
+              tma3_store(&maps.o, 64, h, (int)(lo + c0),
+                         reinterpret_cast<unsigned char *>(OS) + kRawHalf);
+              bulk_commit();
+            }
+          } else {
+            constexpr int VEC = 16 / (int)sizeof(TO), PIECES = D / VEC;  // per token row
+            TO *ob = o + (lo + c0) * ostep + (int64_t)h * D;
+            for (int e = tid; e < n * PIECES; e += NT) {
+              const int t = e / PIECES, pc = e % PIECES;
+              const unsigned char *src =
+                  OB16 ? reinterpret_cast<const unsigned char *>(OS) + (pc >> 3) * kRawHalf +
+                             t * 128 + (((pc & 7) ^ (t & 7)) << 4)
+                       : reinterpret_cast<const unsigned char *>(OS + t * kOSRow + pc * VEC);
+              *reinterpret_cast<uint4 *>(ob + t * ostep + pc * VEC) =
+                  *reinterpret_cast<const uint4 *>(src);
+            }
+          }
+        } else {
+          TO *ob = o + (lo + c0 + i0) * ostep + (int64_t)h * D + v;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (i0 + j < n) Elem<TO>::store1(ob + (int64_t)j * ostep, scale * d4[j]);
+        }
+      }
+      if (!last) {
+        build_kt(c + 1);
+        warp_arrive(&g_rdy);  // the next state update's operands: scaled S, Ktil^T
+      }
+    }
+
+    if (tid == kCopier) bulk_wait_all();  // output stores complete before the block exits
+    if (alive) {
+      const int64_t e0 = (int64_t)row * D + 64 * half;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[16];
+        tc::tmem_ld16(lrow + T_S + 64 * half + c * 16, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          state_st4<false>(Sg, e0 + (c * 4 + j) * 4,
+                           make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]), sd);
+      }
+    } else {
+      *vdead = 1;
+      if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
+      if (tid == kCopier) {  // raw loads still in flight land before shared memory is released
+        if (n_r0 > 0) mbar_wait_bounded(&rbar[0], (n_r0 - 1) & 1);
+        if (n_r1 > 0) mbar_wait_bounded(&rbar[1], (n_r1 - 1) & 1);
+        if (n_v > 0) mbar_wait_bounded(&vbar, (n_v - 1) & 1);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tm, SEQ_TMEM);
+}
+
 // Tensor maps for the bf16 inputs of a call: q, k {128, h_k, tokens} and v
 // {128, h_v, tokens} with boxes {64, 1, 64} in the 128-byte swizzle (rows and
 // strides 16-byte aligned), and g, beta {h_v, tokens} with boxes {8, 64} when
 // their rows are 16-byte aligned too (gb).  False: stage from global memory.
-bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMaps &m, bool &gb) {
+// With o_bf16 (a bf16 output tensor [tokens][h_v][128]) also its map, boxes
+// {64, 1, 64} in the 128-byte swizzle, when it starts 16-byte aligned (om).
+bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMaps &m, bool &gb,
+                    const void *o_bf16, bool &om) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -1149,7 +1746,7 @@ bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMap
     }
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }();
-  gb = false;
+  gb = om = false;
   if (encode == nullptr) return false;
   const size_t es = 2;
   auto a16 = [](const void *x) { return (uintptr_t)x % 16 == 0; };
@@ -1180,6 +1777,8 @@ bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMap
     };
     gb = map2(&m.g, in.g) && map2(&m.b, in.beta);
   }
+  if (o_bf16 != nullptr && a16(o_bf16))
+    om = map3(&m.o, o_bf16, p.h_v, (int64_t)p.h_v * D);
   return true;
 }
 
@@ -1194,7 +1793,10 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   if (e != cudaSuccess) return e;
   InMaps maps;
   bool gb = false;
-  const bool raw = std::is_same<TI, bf16>::value && encode_in_maps(p, seq, in, maps, gb);
+  bool om = false;
+  const bool raw = std::is_same<TI, bf16>::value &&
+                   encode_in_maps(p, seq, in, maps, gb,
+                                  std::is_same<TO, bf16>::value ? o : nullptr, om);
   auto prep = prep_kernel<TI>;
   constexpr int prep_bytes = prep_smem<TI>();
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_bytes);
@@ -1203,6 +1805,15 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   prep<<<dim3((unsigned)nc, p.h_k * npair), NT, prep_bytes, s>>>(p, seq, in, off, tiles, maps,
                                                                   raw ? 1 : 0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (raw) {  // bf16 rows by tensor map: [D3 | E] on kind::f16 over the raw rows
+    auto kern = seq_bf16_kernel<TO>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSeqBf16Smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(p.h_v, seq.n_seqs), NTS, kSeqBf16Smem, s>>>(
+        p, layer, seq, in, static_cast<TO *>(o), scale, off, nc, tiles, maps, gb ? 1 : 0,
+        om ? 1 : 0, ck);
+    return cudaGetLastError();
+  }
   auto kern = seq_kernel<TI, TO>;
   constexpr int smem = seq_smem<TI>();
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -118,6 +118,18 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// D (+)= A B^T, kind::f16 with bf16 operands: A from TMEM (two 16-bit
+// elements per 32-bit column, the lower K index in the low half), B by
+// shared-memory descriptor.
+__device__ __forceinline__ void mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // arrive once on `bar` when every tcgen05.mma issued so far by this thread is done
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
