@@ -1176,12 +1176,15 @@ __global__ void __launch_bounds__(NTS, 1)
 // ------------------------------------------------- state side, bf16 rows
 // The state walk for bf16 q, k, v whose rows arrive by tensor-map copies.
 // [D3 | E] = S [Q;K]^T runs on kind::f16 over the raw tiles themselves (the
-// exact input values, two chunks of q, k buffered ahead), with the state as
-// a bf16 pair S = S_hi + S_lo (each rounded to nearest; the pair carries
-// about 16 significant bits, more than a tf32 operand) packed into the free
-// F and Delta columns of TMEM; the L2 norms of q and k scale the products'
-// columns.  Delta^T = F T^T and the N = 192 output / state update stay on
-// kind::tf32 as in seq_kernel; so do the roles of the nine warps.
+// exact input values, two chunks of q, k buffered ahead: bf16 operands,
+// float32 accumulation), with the state rounded to nearest bf16 and packed
+// two per column into the free F columns of TMEM; the L2 norms of q and k
+// scale the products' columns.  Delta^T = F T^T and the N = 192 output /
+// state update stay on kind::tf32 as in seq_kernel; so do the roles of the
+// nine warps.  The state's carried value stays float32 in TMEM: only this
+// product sees it rounded, and its rounding is not the dominant error (a
+// second bf16 term for the remainder left the errors against the float64
+// recurrence unchanged to four digits).
 
 // shared-memory map of seq_bf16_kernel (bytes from a 1024-byte aligned base)
 constexpr int kQKBuf = 4 * kRawHalf;            // raw [q h0 | k h0 | q h1 | k h1], 32 KiB
@@ -1308,7 +1311,7 @@ __global__ void __launch_bounds__(NTS, 1)
         bulk_g2s(TT, src + TILE, kTileBytes, &tbar);
       }
     };
-    // [D3 | E] = (S_hi + S_lo) [Q;K]^T over the raw rows of chunk c: M 128, N 128,
+    // [D3 | E] = S_bf16 [Q;K]^T over the raw rows of chunk c: M 128, N 128,
     // K 128 in steps of 16 (four 32-byte steps inside each swizzled 64-column half)
     auto issue_ed3 = [&](int c) {
       if (leader) {
@@ -1318,7 +1321,6 @@ __global__ void __launch_bounds__(NTS, 1)
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t bd = tc::smem_desc_sw128(b0 + (ks >> 2) * 2 * kRawHalf + 32 * (ks & 3));
           tc::mma_ts_f16(tm + T_D3, tm + T_F + 8 * ks, bd, id, ks > 0);
-          tc::mma_ts_f16(tm + T_D3, tm + T_DD + 8 * ks, bd, id, 1);
         }
         tc::mma_commit(&b_ed3);
       }
@@ -1466,27 +1468,23 @@ __global__ void __launch_bounds__(NTS, 1)
         }
       }
     };
-    // S (float32) -> the bf16 pair S_hi at the F columns and S_lo at the Delta
-    // columns, packed two per column (lower k in the low half), for the next
-    // [D3 | E], and S <- gn S in place for the next state update (which the
-    // pair does not see).  Arrives on s_rdy once all of it is in TMEM.
+    // S (float32) -> S_bf16 at the F columns, packed two per column (lower k in
+    // the low half), for the next [D3 | E], and S <- gn S in place for the next
+    // state update (which S_bf16 does not see).  Arrives on s_rdy once all of
+    // it is in TMEM.
     auto split_scale = [&](float gn) {
 #pragma unroll 1
       for (int cb = 0; cb < 2; ++cb) {
-        float sv[32], hp[16], lp[16];
+        float sv[32], hp[16];
         const uint32_t sc = lrow + T_S + 64 * half + 32 * cb;
         tc::tmem_ld32(sc, sc + 16, sv);
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
           const float s0 = sv[2 * m], s1 = sv[2 * m + 1];
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(s0, s1);
-          const float2 hf = __bfloat1622float2(h2);
-          const __nv_bfloat162 l2 = __floats2bfloat162_rn(s0 - hf.x, s1 - hf.y);
           hp[m] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h2));
-          lp[m] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&l2));
         }
         tc::tmem_st16(lrow + T_F + 32 * half + 16 * cb, hp);
-        tc::tmem_st16(lrow + T_DD + 32 * half + 16 * cb, lp);
 #pragma unroll
         for (int j = 0; j < 32; ++j) sv[j] *= gn;
         tc::tmem_st16(sc, sv);

@@ -212,7 +212,7 @@ def test_prefill_two_launch_rows_not_16_byte_aligned():
     elements, allowed: rows need 8-byte alignment) cannot arrive by tensor
     map; the state kernel then stages them from global memory as normalised
     float32 rows (tf32 operands), where aligned rows feed the bf16 products
-    directly (kind::f16 with the state as a bf16 hi + lo pair).  Both paths
+    directly (kind::f16, the state operand rounded to bf16).  Both paths
     agree with the oracle, and with each other, within the tensor-core bound
     5e-3 * max|ref|."""
     rng = np.random.default_rng(45)
