@@ -552,6 +552,11 @@ __global__ void __launch_bounds__(NT, 2)
     }
     sG[2 * lane] = incl - b;
     sG[2 * lane + 1] = incl;
+    // cf[i] = e^{G_e - G_i} / |k_i|, e the last token of i's 16-token block (so at
+    // most 1 / |k_i|): the column factor of P and A left of the diagonal blocks
+    const float Ge = __shfl_sync(0xffffffffu, incl, (lane & ~7) | 7);
+    XS_[2 * lane] = rk[2 * lane] * __expf(Ge - (incl - b));
+    XS_[2 * lane + 1] = rk[2 * lane + 1] * __expf(Ge - incl);
   }
   tc::fence_async_smem();
   tc::fence_before_sync();
@@ -601,45 +606,57 @@ __global__ void __launch_bounds__(NT, 2)
   float *Pg = work + ((int64_t)cidx * p.h_v + h) * (2 * TILE);
   float *Tg = Pg + TILE;
   if (alive && live) {
+    // rows 0..63: P[t][i] = e^{G_t - G_i} q~_t.k~_i (i <= t), to the workspace;
+    // rows 64..127: A[t][i] = beta_t e^{G_t - G_i} k~_t.k~_i (i < t), to smem.
+    // Warp w (w % 2 = q2) holds rows t = 32 q2 .. 32 q2 + 31 of one of them.
+    // Columns of the 16-token blocks left of its rows (q2 = 1: i < 32) take
+    // e^{G_t - G_i} = e^{G_t - G_e} e^{G_e - G_i} with e the block's last token
+    // (both factors at most 1, so no overflow at any decay); the warp's own 32
+    // columns take the exact exponential; columns right of them are zero.
     const int row = 32 * quad + lane;
-    if (quad >= 2) {  // rows 64..127: A[t][i] = beta_t e^{G_t - G_i} k~_t.k~_i, i < t
-      const int t = row - 64;
-      const float bt = sBeta[t] * rk[t], gt = sG[t];
+    const bool isA = quad >= 2;
+    const int t = isA ? row - 64 : row;
+    const int q2 = quad & 1;
+    const float sc = isA ? sBeta[t] * rk[t] : rq[t];
+    const float gt = sG[t];
+    const float *cf = XS_;
+    auto put = [&](int i, float4 x) {
+      if (isA) *reinterpret_cast<float4 *>(AP + t * AS + i) = x;
+      else *reinterpret_cast<float4 *>(Pg + tc::core_off(t, i, C)) = x;
+    };
+    if (q2 == 1) {
+      const float rf0 = sc * __expf(gt - sG[15]), rf1 = sc * __expf(gt - sG[31]);
+      float v2[32];
+      tc::tmem_ld32(lrow, lrow + 16, v2);
 #pragma unroll
-      for (int cp = 0; cp < 2; ++cp) {
-        float v2[32];
-        tc::tmem_ld32(lrow + 32 * cp, lrow + 32 * cp + 16, v2);
-#pragma unroll
-        for (int j2 = 0; j2 < 32; j2 += 4) {
-          const int i = 32 * cp + j2, j = j2;
-          const float *v = v2;
-          float4 a;
-          a.x = i + 0 < t ? bt * rk[i + 0] * __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
-          a.y = i + 1 < t ? bt * rk[i + 1] * __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
-          a.z = i + 2 < t ? bt * rk[i + 2] * __expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
-          a.w = i + 3 < t ? bt * rk[i + 3] * __expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
-          *reinterpret_cast<float4 *>(AP + t * AS + i) = a;
-        }
+      for (int j2 = 0; j2 < 32; j2 += 4) {
+        const float rf = j2 < 16 ? rf0 : rf1;
+        const float4 c4 = *reinterpret_cast<const float4 *>(cf + j2);
+        put(j2, make_float4(rf * c4.x * v2[j2], rf * c4.y * v2[j2 + 1], rf * c4.z * v2[j2 + 2],
+                            rf * c4.w * v2[j2 + 3]));
       }
-    } else {  // rows 0..63: P[t][i] = e^{G_t - G_i} q~_t.k~_i, i <= t, to the workspace
-      const int t = row;
-      const float qt = rq[t], gt = sG[t];
+    }
+    {
+      const int cb = 32 * q2;
+      const int lim = isA ? t : t + 1;  // columns i < lim are kept
+      float v2[32];
+      tc::tmem_ld32(lrow + cb, lrow + cb + 16, v2);
 #pragma unroll
-      for (int cp = 0; cp < 2; ++cp) {
-        float v2[32];
-        tc::tmem_ld32(lrow + 32 * cp, lrow + 32 * cp + 16, v2);
-#pragma unroll
-        for (int j2 = 0; j2 < 32; j2 += 4) {
-          const int i = 32 * cp + j2, j = j2;
-          const float *v = v2;
-          float4 pv;
-          pv.x = i + 0 <= t ? qt * rk[i + 0] * __expf(gt - sG[i + 0]) * v[j + 0] : 0.f;
-          pv.y = i + 1 <= t ? qt * rk[i + 1] * __expf(gt - sG[i + 1]) * v[j + 1] : 0.f;
-          pv.z = i + 2 <= t ? qt * rk[i + 2] * __expf(gt - sG[i + 2]) * v[j + 2] : 0.f;
-          pv.w = i + 3 <= t ? qt * rk[i + 3] * __expf(gt - sG[i + 3]) * v[j + 3] : 0.f;
-          *reinterpret_cast<float4 *>(Pg + tc::core_off(t, i, C)) = pv;
-        }
+      for (int j2 = 0; j2 < 32; j2 += 4) {
+        const int i = cb + j2;
+        const float4 r4 = *reinterpret_cast<const float4 *>(rk + i);
+        const float4 g4 = *reinterpret_cast<const float4 *>(sG + i);
+        float4 x;
+        x.x = i + 0 < lim ? sc * r4.x * __expf(gt - g4.x) * v2[j2 + 0] : 0.f;
+        x.y = i + 1 < lim ? sc * r4.y * __expf(gt - g4.y) * v2[j2 + 1] : 0.f;
+        x.z = i + 2 < lim ? sc * r4.z * __expf(gt - g4.z) * v2[j2 + 2] : 0.f;
+        x.w = i + 3 < lim ? sc * r4.w * __expf(gt - g4.w) * v2[j2 + 3] : 0.f;
+        put(i, x);
       }
+    }
+    if (q2 == 0 && !isA) {  // P's zero columns 32..63 (A's upper part is never read)
+#pragma unroll
+      for (int j2 = 0; j2 < 32; j2 += 4) put(32 + j2, make_float4(0.f, 0.f, 0.f, 0.f));
     }
   } else if (!alive) {
     if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
