@@ -370,47 +370,90 @@ __device__ __forceinline__ void invert_unit_lower(const float *A, float *T, floa
     for (int r = 0; r < 16; ++r) T[(16 * bb + r) * AS + 16 * bb + j] = x[r];
   }
   group_sync(bar);
+  // The products below run over the whole K range, fully unrolled, with two
+  // partial sums each: the triangular factors' zero upper parts add exact
+  // zeros, and every thread gets the same work.
   const int which = tt >> 6, r = (tt >> 2) & 15, q0 = 4 * (tt & 3);
   const int b = 2 * which;
-  {  // X_b = A_{b+1,b} T_{b,b}   (T_{b,b}[k][c] = 0 for k < c)
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  {  // X_b = A_{b+1,b} T_{b,b}
     const float *ar = A + (16 * (b + 1) + r) * AS + 16 * b;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = q0; k < 16; ++k)
-      x = axpby4(1.f, x, ar[k], *reinterpret_cast<const float4 *>(T + (16 * b + k) * AS + 16 * b + q0));
-    *reinterpret_cast<float4 *>(X + which * 256 + r * 16 + q0) = x;
+    const float *tb = T + (16 * b) * AS + 16 * b + q0;
+    float4 x0 = z4, x1 = z4;
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+      const float4 a4 = *reinterpret_cast<const float4 *>(ar + k);
+      x0 = axpby4(1.f, x0, a4.x, *reinterpret_cast<const float4 *>(tb + (k + 0) * AS));
+      x1 = axpby4(1.f, x1, a4.y, *reinterpret_cast<const float4 *>(tb + (k + 1) * AS));
+      x0 = axpby4(1.f, x0, a4.z, *reinterpret_cast<const float4 *>(tb + (k + 2) * AS));
+      x1 = axpby4(1.f, x1, a4.w, *reinterpret_cast<const float4 *>(tb + (k + 3) * AS));
+    }
+    *reinterpret_cast<float4 *>(X + which * 256 + r * 16 + q0) = axpby4(1.f, x0, 1.f, x1);
   }
   group_sync(bar);
   {  // T_{b+1,b} = -T_{b+1,b+1} X_b
     const float *tr = T + (16 * (b + 1) + r) * AS + 16 * (b + 1);
-    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k <= r; ++k)
-      y = axpby4(1.f, y, tr[k], *reinterpret_cast<const float4 *>(X + which * 256 + k * 16 + q0));
-    *reinterpret_cast<float4 *>(T + (16 * (b + 1) + r) * AS + 16 * b + q0) = scale4(-1.f, y);
+    const float *xb = X + which * 256 + q0;
+    float4 y0 = z4, y1 = z4;
+#pragma unroll
+    for (int k = 0; k < 16; k += 4) {
+      const float4 t4 = *reinterpret_cast<const float4 *>(tr + k);
+      y0 = axpby4(1.f, y0, t4.x, *reinterpret_cast<const float4 *>(xb + (k + 0) * 16));
+      y1 = axpby4(1.f, y1, t4.y, *reinterpret_cast<const float4 *>(xb + (k + 1) * 16));
+      y0 = axpby4(1.f, y0, t4.z, *reinterpret_cast<const float4 *>(xb + (k + 2) * 16));
+      y1 = axpby4(1.f, y1, t4.w, *reinterpret_cast<const float4 *>(xb + (k + 3) * 16));
+    }
+    *reinterpret_cast<float4 *>(T + (16 * (b + 1) + r) * AS + 16 * b + q0) =
+        axpby4(-1.f, y0, -1.f, y1);
   }
   group_sync(bar);
   const int r0 = 2 * (tt >> 3), c0 = 4 * (tt & 7);
-  {  // Y = A_L T_lo  (rows 32 + r0, 33 + r0; T_lo[k][c] = 0 for k < c)
+  {  // Y = A_L T_lo  (rows 32 + r0, 33 + r0)
     const float *a0 = A + (32 + r0) * AS, *a1 = a0 + AS;
-    float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
-    for (int k = c0; k < 32; ++k) {
-      const float4 tv = *reinterpret_cast<const float4 *>(T + k * AS + c0);
-      y0 = axpby4(1.f, y0, a0[k], tv);
-      y1 = axpby4(1.f, y1, a1[k], tv);
+    float4 y00 = z4, y01 = z4, y10 = z4, y11 = z4;
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+      const float4 u = *reinterpret_cast<const float4 *>(a0 + k);
+      const float4 w = *reinterpret_cast<const float4 *>(a1 + k);
+      const float4 t0 = *reinterpret_cast<const float4 *>(T + (k + 0) * AS + c0);
+      const float4 t1 = *reinterpret_cast<const float4 *>(T + (k + 1) * AS + c0);
+      const float4 t2 = *reinterpret_cast<const float4 *>(T + (k + 2) * AS + c0);
+      const float4 t3 = *reinterpret_cast<const float4 *>(T + (k + 3) * AS + c0);
+      y00 = axpby4(1.f, y00, u.x, t0);
+      y01 = axpby4(1.f, y01, u.y, t1);
+      y10 = axpby4(1.f, y10, w.x, t0);
+      y11 = axpby4(1.f, y11, w.y, t1);
+      y00 = axpby4(1.f, y00, u.z, t2);
+      y01 = axpby4(1.f, y01, u.w, t3);
+      y10 = axpby4(1.f, y10, w.z, t2);
+      y11 = axpby4(1.f, y11, w.w, t3);
     }
-    *reinterpret_cast<float4 *>(X + r0 * 32 + c0) = y0;
-    *reinterpret_cast<float4 *>(X + (r0 + 1) * 32 + c0) = y1;
+    *reinterpret_cast<float4 *>(X + r0 * 32 + c0) = axpby4(1.f, y00, 1.f, y01);
+    *reinterpret_cast<float4 *>(X + (r0 + 1) * 32 + c0) = axpby4(1.f, y10, 1.f, y11);
   }
   group_sync(bar);
-  {  // T_L = -T_hi Y   (T_hi[r0][r0 + 1] = 0)
+  {  // T_L = -T_hi Y  (rows 32 + r0, 33 + r0)
     const float *t0 = T + (32 + r0) * AS + 32, *t1 = t0 + AS;
-    float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
-    for (int k = 0; k <= r0 + 1; ++k) {
-      const float4 xv = *reinterpret_cast<const float4 *>(X + k * 32 + c0);
-      y0 = axpby4(1.f, y0, t0[k], xv);
-      y1 = axpby4(1.f, y1, t1[k], xv);
+    float4 y00 = z4, y01 = z4, y10 = z4, y11 = z4;
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+      const float4 u = *reinterpret_cast<const float4 *>(t0 + k);
+      const float4 w = *reinterpret_cast<const float4 *>(t1 + k);
+      const float4 x0 = *reinterpret_cast<const float4 *>(X + (k + 0) * 32 + c0);
+      const float4 x1 = *reinterpret_cast<const float4 *>(X + (k + 1) * 32 + c0);
+      const float4 x2 = *reinterpret_cast<const float4 *>(X + (k + 2) * 32 + c0);
+      const float4 x3 = *reinterpret_cast<const float4 *>(X + (k + 3) * 32 + c0);
+      y00 = axpby4(1.f, y00, u.x, x0);
+      y01 = axpby4(1.f, y01, u.y, x1);
+      y10 = axpby4(1.f, y10, w.x, x0);
+      y11 = axpby4(1.f, y11, w.y, x1);
+      y00 = axpby4(1.f, y00, u.z, x2);
+      y01 = axpby4(1.f, y01, u.w, x3);
+      y10 = axpby4(1.f, y10, w.z, x2);
+      y11 = axpby4(1.f, y11, w.w, x3);
     }
-    *reinterpret_cast<float4 *>(T + (32 + r0) * AS + c0) = scale4(-1.f, y0);
-    *reinterpret_cast<float4 *>(T + (33 + r0) * AS + c0) = scale4(-1.f, y1);
+    *reinterpret_cast<float4 *>(T + (32 + r0) * AS + c0) = axpby4(-1.f, y00, -1.f, y01);
+    *reinterpret_cast<float4 *>(T + (33 + r0) * AS + c0) = axpby4(-1.f, y10, -1.f, y11);
   }
   group_sync(bar);
 }
@@ -669,7 +712,9 @@ __global__ void __launch_bounds__(NT, 2)
   if (!alive || !live) return;
 
   invert_unit_lower(AP, TP, XS_, tt, 1 + wg);
-  for (int e = tt; e < C * (C / 4); e += 128) {  // T tile [t][i] -> workspace
+#pragma unroll
+  for (int it = 0; it < C * (C / 4) / 128; ++it) {  // T tile [t][i] -> workspace
+    const int e = tt + 128 * it;
     const int t = e % C, c4 = e / C;
     *reinterpret_cast<float4 *>(Tg + tc::core_off(t, 4 * c4, C)) =
         *reinterpret_cast<const float4 *>(TP + t * AS + 4 * c4);
