@@ -41,9 +41,12 @@ constexpr int AS = C + 4;   // plain row stride of A and T
 constexpr int TILE = C * C; // floats of one 64 x 64 tile
 constexpr uint32_t kTileBytes = TILE * 4;
 
+// offsets, then the state kernels' sequence order (both int32)
 __host__ __device__ inline size_t offsets_bytes(int n_seqs) {
-  return (((size_t)n_seqs + 1) * 4 + 255) & ~(size_t)255;
+  return (((size_t)n_seqs + 1) * 4 + (size_t)n_seqs * 4 + 255) & ~(size_t)255;
 }
+// Calls of up to this many sequences walk them longest first.
+constexpr int kOrderMax = 256;
 __host__ __device__ inline int64_t max_chunks(int n_seqs, int total_tokens) {
   return (int64_t)total_tokens / C + n_seqs;  // >= sum over sequences of ceil(len / 64)
 }
@@ -56,7 +59,10 @@ __device__ __forceinline__ int seq_chunks(const SeqIndex &seq, int i) {
 
 // offsets[i] = number of chunks before sequence i; offsets[n_seqs] = total.
 // Offsets saturate at cap + 1 (only overlapping sequences can exceed the
-// workspace's cap chunks; the state kernel rejects them).
+// workspace's cap chunks; the state kernel rejects them).  Then order[r]
+// (after offsets[n_seqs]) = the sequence with the r-th most chunks, ties by
+// index, so that the state kernels start the longest sequences first
+// (identity order past kOrderMax sequences).
 __global__ void __launch_bounds__(1024)
     chunk_offsets_kernel(SeqIndex seq, int32_t *off, int64_t cap) {
   __shared__ int64_t part[1024];
@@ -79,6 +85,20 @@ __global__ void __launch_bounds__(1024)
     run += seq_chunks(seq, i);
   }
   if (tid == 1023) off[n] = (int32_t)min(part[1023], cap + 1);
+  int32_t *order = off + n + 1;
+  __shared__ int cnt[kOrderMax];
+  if (n <= kOrderMax) {
+    if (tid < n) cnt[tid] = seq_chunks(seq, tid);
+    __syncthreads();
+    if (tid < n) {
+      const int ci = cnt[tid];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += (cnt[j] > ci || (cnt[j] == ci && j < tid)) ? 1 : 0;
+      order[rank] = tid;
+    }
+  } else {
+    for (int i = tid; i < n; i += 1024) order[i] = i;
+  }
 }
 
 // This thread's token in the staging map below (warp w: tokens 8w .. 8w+7).
@@ -814,7 +834,7 @@ __global__ void __launch_bounds__(NTS, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int dead;  // set by the role that gave up waiting
 
-  const int h = blockIdx.x, si = blockIdx.y;
+  const int h = blockIdx.x, si = off[seq.n_seqs + 1 + blockIdx.y];  // longest first
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quad = warp & 3, half = (warp >> 2) & 1;
   const int row = 32 * quad + lane;
@@ -1309,7 +1329,7 @@ __global__ void __launch_bounds__(NTS, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int dead;  // set by the role that gave up waiting
 
-  const int h = blockIdx.x, si = blockIdx.y;
+  const int h = blockIdx.x, si = off[seq.n_seqs + 1 + blockIdx.y];  // longest first
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quad = warp & 3, half = (warp >> 2) & 1;
   const int row = 32 * quad + lane;
