@@ -1268,18 +1268,28 @@ __global__ void __launch_bounds__(NTS, 1)
 // second bf16 term for the remainder left the errors against the float64
 // recurrence unchanged to four digits).
 
+// TMEM columns of seq_bf16_kernel: [D4a | S | D4b | D3 | E | F | Delta].  The
+// output part alternates between D4a (even chunks: [D4a | S] += Delta [P; Ktil^T])
+// and D4b (odd chunks: [S | D4b] += Delta [Ktil^T; P]), so a chunk's outputs
+// can be read while the next chunk's update runs.  S_bf16 shares F's columns.
+constexpr uint32_t U_D4A = 0, U_S = 64, U_D4B = 192, U_D3 = 256, U_E = 320, U_F = 384,
+                   U_DD = 448;
+__device__ __forceinline__ uint32_t u_d4(int c) { return (c & 1) ? U_D4B : U_D4A; }
+
 // shared-memory map of seq_bf16_kernel (bytes from a 1024-byte aligned base)
 constexpr int kQKBuf = 4 * kRawHalf;            // raw [q h0 | k h0 | q h1 | k h1], 32 KiB
 constexpr int B_QK = 0;                         // two q, k buffers (chunk c in buffer c % 2)
 constexpr int B_V = B_QK + 2 * kQKBuf;          // raw v [v h0 | v h1]
 constexpr int B_GB = B_V + 2 * kRawHalf;        // two raw g, beta buffers [g | beta]
 constexpr int B_OS = B_GB + 4 * kRawGB;         // outputs of a chunk, [64 tokens][128]
-constexpr int B_PT = B_OS + C * D * 4;          // P tile
-constexpr int B_KT = B_PT + TILE * 4;           // Ktil^T tile, right after P
-constexpr int B_TT = B_KT + D * C * 4;          // T tile
+constexpr int B_PT = B_OS + C * D * 4;          // P tile of even chunks
+constexpr int B_KT = B_PT + TILE * 4;           // Ktil^T tile: [P0; Ktil^T] and
+constexpr int B_PT1 = B_KT + D * C * 4;         // [Ktil^T; P1] are contiguous operands
+constexpr int B_TT = B_PT1 + TILE * 4;          // T tile
 constexpr int B_SC = B_TT + TILE * 4;           // per-token scalars, 8 x 64 floats
 constexpr int kSeqBf16Smem = B_SC + 8 * C * 4 + 1024;  // + alignment slack
-static_assert(B_V % 1024 == 0 && B_GB % 128 == 0 && B_PT % 16 == 0 && B_KT == B_PT + TILE * 4,
+static_assert(B_V % 1024 == 0 && B_GB % 128 == 0 && B_PT % 16 == 0 && B_KT == B_PT + TILE * 4 &&
+                  B_PT1 == B_KT + D * C * 4,
               "tile alignment");
 static_assert(kSeqBf16Smem <= 227 * 1024, "shared memory");
 
@@ -1312,6 +1322,7 @@ __global__ void __launch_bounds__(NTS, 1)
   constexpr int kOSRow = D;
   static_assert(B_OS % 1024 == 0, "output staging alignment");
   float *PT = reinterpret_cast<float *>(sm + B_PT);
+  float *PT1 = reinterpret_cast<float *>(sm + B_PT1);
   float *KT = reinterpret_cast<float *>(sm + B_KT);
   float *TT = reinterpret_cast<float *>(sm + B_TT);
   float *sG = reinterpret_cast<float *>(sm + B_SC);  // g, then (scan) nothing further
@@ -1380,7 +1391,7 @@ __global__ void __launch_bounds__(NTS, 1)
 
   if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA warp
-    const uint32_t pt_s = smem_addr(PT), tt_s = smem_addr(TT);
+    const uint32_t pt_s = smem_addr(PT), kt_s = smem_addr(KT), tt_s = smem_addr(TT);
     constexpr uint32_t SBO_C = tc::sbo_bytes(C);
     constexpr uint32_t KSTEP = 2 * tc::kLBO;
     const bool leader = lane == 0;
@@ -1389,7 +1400,7 @@ __global__ void __launch_bounds__(NTS, 1)
       if (leader) {
         const float *src = wsq + (int64_t)c * wstep;
         mbar_arrive_expect_tx(&tbar, 2 * kTileBytes);
-        bulk_g2s(PT, src, kTileBytes, &tbar);
+        bulk_g2s((c & 1) ? PT1 : PT, src, kTileBytes, &tbar);
         bulk_g2s(TT, src + TILE, kTileBytes, &tbar);
       }
     };
@@ -1402,7 +1413,7 @@ __global__ void __launch_bounds__(NTS, 1)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t bd = tc::smem_desc_sw128(b0 + (ks >> 2) * 2 * kRawHalf + 32 * (ks & 3));
-          tc::mma_ts_f16(tm + T_D3, tm + T_F + 8 * ks, bd, id, ks > 0);
+          tc::mma_ts_f16(tm + U_D3, tm + U_F + 8 * ks, bd, id, ks > 0);
         }
         tc::mma_commit(&b_ed3);
       }
@@ -1424,7 +1435,7 @@ __global__ void __launch_bounds__(NTS, 1)
       if (leader) {  // Delta^T = F T^T  (A = F from TMEM; M 128, N 64, K 64)
 #pragma unroll
         for (int j = 0; j < C / 8; ++j)
-          tc::mma_ts(tm + T_DD, tm + T_F + j * 8,
+          tc::mma_ts(tm + U_DD, tm + U_F + j * 8,
                      tc::smem_desc(tt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 64),
                      j > 0);
         tc::mma_commit(&b_dd);
@@ -1434,11 +1445,13 @@ __global__ void __launch_bounds__(NTS, 1)
       ok = all_lanes(wait_live(&b_dd, par, vdead) && wait_live(&g_rdy, par, vdead));
       if (!ok) break;
       tc::fence_after_sync();
-      if (leader) {  // [D4 | S] += Delta^T [P; Ktil^T]^T  (N 192, K 64)
+      if (leader) {  // [D4a | S] += Delta^T [P0; Ktil^T]^T (even c) or
+                     // [S | D4b] += Delta^T [Ktil^T; P1]^T (odd c): N 192, K 64
+        const uint32_t dcol = (c & 1) ? U_S : U_D4A, bsm = (c & 1) ? kt_s : pt_s;
 #pragma unroll
         for (int j = 0; j < C / 8; ++j)
-          tc::mma_ts(tm + T_D4, tm + T_DD + j * 8,
-                     tc::smem_desc(pt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 192),
+          tc::mma_ts(tm + dcol, tm + U_DD + j * 8,
+                     tc::smem_desc(bsm + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 192),
                      1);
         tc::mma_commit(&b_upd);
       }
@@ -1479,7 +1492,7 @@ __global__ void __launch_bounds__(NTS, 1)
           const float4 x = state_ld4(Sg, e0 + (c * 4 + j) * 4, sd);
           v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
         }
-        tc::tmem_st16(lrow + T_S + 64 * half + c * 16, v);
+        tc::tmem_st16(lrow + U_S + 64 * half + c * 16, v);
       }
       tc::tmem_st_wait();
     }
@@ -1558,7 +1571,7 @@ __global__ void __launch_bounds__(NTS, 1)
 #pragma unroll 1
       for (int cb = 0; cb < 2; ++cb) {
         float sv[32], hp[16];
-        const uint32_t sc = lrow + T_S + 64 * half + 32 * cb;
+        const uint32_t sc = lrow + U_S + 64 * half + 32 * cb;
         tc::tmem_ld32(sc, sc + 16, sv);
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
@@ -1566,7 +1579,7 @@ __global__ void __launch_bounds__(NTS, 1)
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(s0, s1);
           hp[m] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&h2));
         }
-        tc::tmem_st16(lrow + T_F + 32 * half + 16 * cb, hp);
+        tc::tmem_st16(lrow + U_F + 32 * half + 16 * cb, hp);
 #pragma unroll
         for (int j = 0; j < 32; ++j) sv[j] *= gn;
         tc::tmem_st16(sc, sv);
@@ -1608,7 +1621,7 @@ __global__ void __launch_bounds__(NTS, 1)
     // F[v][t] = beta_t v_t[v] - (beta_t gamma_t / |k_t|) (S K^T)[v][t] and the
     // output's state part (gamma_t / |q_t|) (S Q^T)[v][t] into TMEM, this
     // thread's 32 tokens; padded tokens (FULL false) give 0
-    auto f_pass = [&](auto full, int n, int i0) {
+    auto f_pass = [&](auto full, int n, int i0, uint32_t d4c) {
       constexpr bool FULL = decltype(full)::value;
       const int v = row;
       const unsigned char *vr = RV + (v >> 6) * kRawHalf + (v & 7) * 2;
@@ -1617,7 +1630,7 @@ __global__ void __launch_bounds__(NTS, 1)
       for (int cb = 0; cb < 2; ++cb) {
         const int t0 = i0 + 16 * cb;
         float ed[32], f[16], dd[16];  // ed: 16 columns of E, then the same of D3
-        tc::tmem_ld32(lrow + T_E + t0, lrow + T_D3 + t0, ed);
+        tc::tmem_ld32(lrow + U_E + t0, lrow + U_D3 + t0, ed);
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4) {  // four tokens' scalars per vector load
           const float4 b4 = *reinterpret_cast<const float4 *>(sBeta + t0 + 4 * j4);
@@ -1636,89 +1649,24 @@ __global__ void __launch_bounds__(NTS, 1)
             if (!FULL && t >= n) dd[j] = f[j] = 0.f;
           }
         }
-        tc::tmem_st16(lrow + T_F + t0, f);
-        tc::tmem_st16(lrow + T_D4 + t0, dd);
+        tc::tmem_st16(lrow + U_F + t0, f);
+        tc::tmem_st16(lrow + d4c + t0, dd);
       }
       tc::tmem_st_wait();
     };
 
-    // chunk 0 (and 1) on their way; chunk 0's scalars, split state, scaled
-    // state and Ktil^T to the MMA warp
-    if (tid == kCopier) prefetch_v(maps, h, lo, RV, &vbar);
-    n_v = 1;
-    fetch_qk(0);
-    if (nch > 1) fetch_qk(1);
-    if (!GB) load_gb<bf16>(in, p, h, lo, min(C, len), g_next, b_next);
-    stage_scalars(0);
-    if (!GB && nch > 1) load_gb<bf16>(in, p, h, lo + C, min(C, len - C), g_next, b_next);
-    alive = cw_and(alive);  // the scan's results are visible
-    if (alive) {
-      split_scale(sGam[C - 1]);
-      build_kt(0);
-      warp_arrive(&g_rdy);
-    }
-
-    // Per chunk c: [D3 | E] -> F -> (MMA warp: Delta, state update) while the
-    // next chunk's scalars are staged -> split and scale the new state (the
-    // next [D3 | E] starts) -> outputs and the next Ktil^T under it.
-    for (int c = 0; c < nch && alive; ++c) {
-      const int c0 = c * C;
-      const uint32_t par = c & 1;
-      const int n = min(C, len - c0);
-      const bool last = c + 1 == nch;
-      alive = cw_and(wait_live(&b_ed3, par, vdead) &&    // [D3 | E] done, v landed
-                     wait_live(&vbar, par, vdead));
-      if (!alive) break;
-      tc::fence_after_sync();
-      if (c + 2 < nch) fetch_qk(c + 2);  // buffer c % 2 is free: [D3 | E] and Ktil^T are done
-
-      const int i0 = 32 * half;
-      if (n == C) f_pass(std::true_type(), n, i0); else f_pass(std::false_type(), n, i0);
-      warp_arrive(&f_rdy);
-
-      if (!last) {
-        cw_sync();  // every warp is past its reads of v and of this chunk's scalars
-        if (alive) {  // the raw v tile is free: fetch the next chunk's
-          if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RV, &vbar);
-          ++n_v;
-        }
-        stage_scalars(c + 1);
-        if (!GB && c + 2 < nch)
-          load_gb<bf16>(in, p, h, lo + c0 + 2 * C, min(C, len - c0 - 2 * C), g_next, b_next);
-      }
-      if (tid == kCopier) bulk_wait_read();  // the last output store has read its staging
-      alive = cw_and(alive && wait_live(&b_upd, par, vdead));  // D4, new state ready
-      if (!alive) break;
-      tc::fence_after_sync();
-      if (ck.every > 0 && c0 + C <= len && (c0 + C) % ck.every == 0) {  // checkpoint: copy S out
-        const int j = (c0 + C) / ck.every - 1;
-        const int ds = j < ck.per_seq ? ck.slots[(int64_t)si * ck.per_seq + j] : -1;
-        if (ds >= p.n_slots) {
-          if (tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
-        } else if (ds >= 0) {
-          char *dst = p.state_at(p.state_head_elem(layer, ds, h));
-          const int64_t e0 = (int64_t)row * D + 64 * half;
-#pragma unroll 1
-          for (int cb = 0; cb < 4; ++cb) {
-            float v[16];
-            tc::tmem_ld16(lrow + T_S + 64 * half + 16 * cb, v);
-#pragma unroll
-            for (int j4 = 0; j4 < 4; ++j4)
-              state_st4<false>(dst, e0 + (cb * 4 + j4) * 4,
-                               make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]),
-                               sd);
-          }
-        }
-      }
-      if (!last) split_scale(sGam[C - 1]);  // the next [D3 | E] starts here
-
-      // outputs o[t][v] = scale D4[v][t]: this warp's half of t into the [t][v] staging
-      // tile, then whole 16-byte pieces of token rows out
+    // outputs of chunk cc, o[t][v] = scale D4[v][t]: this warp's half of t into the
+    // [t][v] staging tile (free once the last tensor-map store has read it), then
+    // whole 16-byte pieces of token rows out
+    auto out_chunk = [&](int cc) {
+      const int c0 = cc * C, n = min(C, len - c0), i0 = 32 * half;
+      if (tid == kCopier) bulk_wait_read();
+      cw_sync();
       {
         const int v = row;
         const int64_t ostep = (int64_t)p.h_v * D;
         float d4[32];
-        tc::tmem_ld32(lrow + T_D4 + i0, lrow + T_D4 + i0 + 16, d4);
+        tc::tmem_ld32(lrow + u_d4(cc) + i0, lrow + u_d4(cc) + i0 + 16, d4);
         if (ovec) {
           if constexpr (OB16) {
             // lanes v, v ^ 1 swap one value per token pair (j, j + 4) of each group of
@@ -1773,19 +1721,93 @@ __global__ void __launch_bounds__(NTS, 1)
             if (i0 + j < n) Elem<TO>::store1(ob + (int64_t)j * ostep, scale * d4[j]);
         }
       }
+    };
+
+    // chunk 0 (and 1) on their way; chunk 0's scalars, split state, scaled
+    // state and Ktil^T to the MMA warp
+    if (tid == kCopier) prefetch_v(maps, h, lo, RV, &vbar);
+    n_v = 1;
+    fetch_qk(0);
+    if (nch > 1) fetch_qk(1);
+    if (!GB) load_gb<bf16>(in, p, h, lo, min(C, len), g_next, b_next);
+    stage_scalars(0);
+    if (!GB && nch > 1) load_gb<bf16>(in, p, h, lo + C, min(C, len - C), g_next, b_next);
+    alive = cw_and(alive);  // the scan's results are visible
+    if (alive) {
+      split_scale(sGam[C - 1]);
+      build_kt(0);
+      warp_arrive(&g_rdy);
+    }
+
+    // Per chunk c: [D3 | E] -> F -> (MMA warp: Delta, state update) while the
+    // next chunk's scalars are staged -> split and scale the new state (the
+    // next [D3 | E] starts) -> outputs and the next Ktil^T under it.
+    for (int c = 0; c < nch && alive; ++c) {
+      const int c0 = c * C;
+      const uint32_t par = c & 1;
+      const int n = min(C, len - c0);
+      const bool last = c + 1 == nch;
+      alive = cw_and(wait_live(&b_ed3, par, vdead) &&    // [D3 | E] done, v landed
+                     wait_live(&vbar, par, vdead));
+      if (!alive) break;
+      tc::fence_after_sync();
+      if (c + 2 < nch) fetch_qk(c + 2);  // buffer c % 2 is free: [D3 | E] and Ktil^T are done
+
+      const int i0 = 32 * half;
+      if (n == C) f_pass(std::true_type(), n, i0, u_d4(c));
+      else f_pass(std::false_type(), n, i0, u_d4(c));
+      warp_arrive(&f_rdy);
+
+      if (!last) {
+        cw_sync();  // every warp is past its reads of v and of this chunk's scalars
+        if (alive) {  // the raw v tile is free: fetch the next chunk's
+          if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RV, &vbar);
+          ++n_v;
+        }
+        stage_scalars(c + 1);
+        if (!GB && c + 2 < nch)
+          load_gb<bf16>(in, p, h, lo + c0 + 2 * C, min(C, len - c0 - 2 * C), g_next, b_next);
+      }
+      if (c > 0) out_chunk(c - 1);  // under this chunk's update: the other D4 buffer
+      alive = cw_and(alive && wait_live(&b_upd, par, vdead));  // D4, new state ready
+      if (!alive) break;
+      tc::fence_after_sync();
+      if (ck.every > 0 && c0 + C <= len && (c0 + C) % ck.every == 0) {  // checkpoint: copy S out
+        const int j = (c0 + C) / ck.every - 1;
+        const int ds = j < ck.per_seq ? ck.slots[(int64_t)si * ck.per_seq + j] : -1;
+        if (ds >= p.n_slots) {
+          if (tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
+        } else if (ds >= 0) {
+          char *dst = p.state_at(p.state_head_elem(layer, ds, h));
+          const int64_t e0 = (int64_t)row * D + 64 * half;
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {
+            float v[16];
+            tc::tmem_ld16(lrow + U_S + 64 * half + 16 * cb, v);
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4)
+              state_st4<false>(dst, e0 + (cb * 4 + j4) * 4,
+                               make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]),
+                               sd);
+          }
+        }
+      }
+      if (!last) split_scale(sGam[C - 1]);  // the next [D3 | E] starts here
+
       if (!last) {
         build_kt(c + 1);
         warp_arrive(&g_rdy);  // the next state update's operands: scaled S, Ktil^T
       }
     }
 
+    if (alive) out_chunk(nch - 1);
     if (tid == kCopier) bulk_wait_all();  // output stores complete before the block exits
     if (alive) {
       const int64_t e0 = (int64_t)row * D + 64 * half;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float v[16];
-        tc::tmem_ld16(lrow + T_S + 64 * half + c * 16, v);
+        tc::tmem_ld16(lrow + U_S + 64 * half + c * 16, v);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           state_st4<false>(Sg, e0 + (c * 4 + j) * 4,
