@@ -60,12 +60,12 @@ PREFILL_SUMMARY = os.path.join(ROOT, "profiles", "gdn_prefill_split_varlen8_piec
 PREFILL_SOURCE = os.path.join(ROOT, "gated_deltanet_recurrent_gb300", "csrc",
                               "gdn_prefill_split.cu")
 # chunked prefill, algorithmic work per token and value head (chunk 64, K = V = 128,
-# triangular blocks exploited): the state-side products run on the tensor cores
-# in tf32 (Delta = F T^T 16,640; W S0^T, Q S0^T, state update 3 x 32,768;
-# P Delta 8,320), the key-side Gram products in bf16 (K K^T 8,064 + Q K^T 8,320),
-# forming T on the CUDA cores (~1,365)
-PREFILL_FLOPS_TF32 = 16640 + 3 * 32768 + 8320
-PREFILL_FLOPS_BF16 = 8064 + 8320
+# triangular blocks exploited): on the tensor cores, in tf32 Delta = F T^T
+# (16,640), the state update (32,768) and P Delta (8,320); in bf16 the state
+# products with the raw rows, S K^T and S Q^T (2 x 32,768), and the key-side Gram
+# products (K K^T 8,064 + Q K^T 8,320); forming T on the CUDA cores (~1,365)
+PREFILL_FLOPS_TF32 = 16640 + 32768 + 8320
+PREFILL_FLOPS_BF16 = 2 * 32768 + 8064 + 8320
 PREFILL_FLOPS_SIMT = 1365
 # bytes per token: q, k (16 x 128 each), v (32 x 128), g, beta (32 each) in bf16,
 # o (32 x 128) out in bf16; plus the state read and written once per
