@@ -19,10 +19,12 @@
 // T tiles with one bulk copy issued a chunk ahead.  The arithmetic is the
 // single-launch kernel's, step for step, so results agree with it.
 //
-// Workspace: (n_seqs + 1) int32 chunk offsets (256-byte aligned), then per
-// (chunk, value head) 32 KiB: the P tile, then the T tile, each 64 x 64 float32
-// in the K-major core-matrix layout of gdn_tc.cuh.  Chunks are numbered
-// sequence by sequence; offsets[i] is the first chunk of sequence i.
+// Workspace: (n_seqs + 1) int32 chunk offsets and the sequence order (256-byte
+// aligned), then per (chunk, value head) 32 KiB: the P tile, then the T tile,
+// each 64 x 64 float32 in the K-major core-matrix layout of gdn_tc.cuh; then,
+// when q and k came by tensor map, per (chunk, key head) 1/|q_t| and 1/|k_t|
+// (2 x 64 float32).  Chunks are numbered sequence by sequence; offsets[i] is
+// the first chunk of sequence i.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -252,11 +254,13 @@ __device__ __forceinline__ void prefetch_v(const InMaps &m, int h, int64_t tok0,
 }
 // One thread: the chunk's q and k halves into a [q h0 | k h0 | q h1 | k h1]
 // buffer (each half-pair a 128-row [Q;K] operand block) and, with gb, g and
-// beta to gbt, gbt + kRawGB, all onto bar.
+// beta to gbt, gbt + kRawGB, all onto bar, which also expects extra_tx bytes
+// of copies the caller issues next.
 __device__ __forceinline__ void prefetch_qk_pairs(const InMaps &m, bool gb, int h, int hk,
                                                   int64_t tok0, unsigned char *qk,
-                                                  unsigned char *gbt, uint64_t *bar) {
-  mbar_arrive_expect_tx(bar, 4 * kRawHalf + (gb ? 2 * kRawGB : 0));
+                                                  unsigned char *gbt, uint64_t *bar,
+                                                  uint32_t extra_tx) {
+  mbar_arrive_expect_tx(bar, 4 * kRawHalf + (gb ? 2 * kRawGB : 0) + extra_tx);
   const int z = (int)tok0;
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
@@ -605,6 +609,11 @@ __global__ void __launch_bounds__(NT, 2)
                           reinterpret_cast<float *>(tile), nullptr, rq, rk);
   }
   __syncthreads();
+  if (TMAQK && pair == 0 && tid < 2 * C) {  // 1/|q_t|, 1/|k_t| for the state kernel
+    float *nb = work + (int64_t)gridDim.x * p.h_v * (2 * TILE) +
+                ((int64_t)cidx * p.h_k + kh) * (2 * C);
+    nb[tid] = tid < C ? rq[tid] : rk[tid - C];
+  }
   if (quad == 0 && tt < 32) {  // warp 4 wg: cumulative log-decay of this head
     const float a = sG[2 * lane], b = sG[2 * lane + 1];
     float incl = a + b;
@@ -1287,21 +1296,13 @@ constexpr int B_KT = B_PT + TILE * 4;           // Ktil^T tile: [P0; Ktil^T] and
 constexpr int B_PT1 = B_KT + D * C * 4;         // [Ktil^T; P1] are contiguous operands
 constexpr int B_TT = B_PT1 + TILE * 4;          // T tile
 constexpr int B_SC = B_TT + TILE * 4;           // per-token scalars, 8 x 64 floats
-constexpr int kSeqBf16Smem = B_SC + 8 * C * 4 + 1024;  // + alignment slack
+constexpr int B_NB = B_SC + 8 * C * 4;           // two norm buffers [1/|q| | 1/|k|]
+constexpr int kSeqBf16Smem = B_NB + 2 * 2 * C * 4 + 1024;  // + alignment slack
 static_assert(B_V % 1024 == 0 && B_GB % 128 == 0 && B_PT % 16 == 0 && B_KT == B_PT + TILE * 4 &&
                   B_PT1 == B_KT + D * C * 4,
               "tile alignment");
 static_assert(kSeqBf16Smem <= 227 * 1024, "shared memory");
 
-// Elements 4c .. 4c+3 of row t of a 64 x 128 bf16 operand held as two 64-column
-// swizzled halves `stride` bytes apart.
-__device__ __forceinline__ uint2 raw_piece(const unsigned char *half0, int stride, int t, int c) {
-  const int col = (4 * c) & 63;
-  return *reinterpret_cast<const uint2 *>(half0 + ((4 * c) >> 6) * stride + t * 128 +
-                                          ((((col >> 3) ^ (t & 7))) << 4) + (col & 7) * 2);
-}
-__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
 template <typename TO>
 __global__ void __launch_bounds__(NTS, 1)
@@ -1328,9 +1329,7 @@ __global__ void __launch_bounds__(NTS, 1)
   float *sG = reinterpret_cast<float *>(sm + B_SC);  // g, then (scan) nothing further
   float *sGam = sG + C;    // gamma_t = e^{G_t}
   float *sBeta = sGam + C;
-  float *sRq = sBeta + C;  // 1 / |q_t|, 1 / |k_t|
-  float *sRk = sRq + C;
-  float *sQ = sRk + C;     // gamma_t / |q_t|            (scales column t of S Q^T)
+  float *sQ = sBeta + 2 * C;  // gamma_t / |q_t|         (scales column t of S Q^T)
   float *sK = sQ + C;      // beta_t gamma_t / |k_t|     (scales column t of S K^T)
   float *sKt = sK + C;     // e^{G_n - G_t} / |k_t|      (scales token t of Ktil)
   __shared__ __align__(8) uint64_t b_ed3, b_dd, b_upd;  // MMA groups done
@@ -1366,6 +1365,9 @@ __global__ void __launch_bounds__(NTS, 1)
   const gdn_dtype sd = p.state_dtype;
   char *Sg = p.state_at(p.state_head_elem(layer, slot, h));  // float32, bf16 or f16 elements
   const float *wsq = work + ((int64_t)off[si] * p.h_v + h) * (2 * TILE);  // chunk 0's tiles
+  // chunk 0's 1/|q_t|, 1/|k_t| (written by the key-side kernel), next chunk 2 C * h_k on
+  const float *wnorm = work + cap * p.h_v * (2 * TILE) + ((int64_t)off[si] * p.h_k + hk) * (2 * C);
+  float *NB = reinterpret_cast<float *>(sm + B_NB);  // two [1/|q| | 1/|k|] buffers
   const int64_t wstep = (int64_t)p.h_v * (2 * TILE);                      // next chunk
 
   if (warp == 0) tc::tmem_alloc(&tmem_slot, SEQ_TMEM);
@@ -1503,32 +1505,20 @@ __global__ void __launch_bounds__(NTS, 1)
     // copier: q, k (g, beta) of chunk c into buffer c % 2
     auto fetch_qk = [&](int c) {
       const int b = c & 1;
-      if (tid == kCopier)
+      if (tid == kCopier) {
         prefetch_qk_pairs(maps, GB, h, hk, lo + (int64_t)c * C, RQK + b * kQKBuf,
-                          RGB + b * 2 * kRawGB, &rbar[b]);
+                          RGB + b * 2 * kRawGB, &rbar[b], 2 * C * 4);
+        bulk_g2s(NB + b * 2 * C, wnorm + (int64_t)c * p.h_k * (2 * C), 2 * C * 4, &rbar[b]);
+      }
       if (b) ++n_r1; else ++n_r0;
     };
-    // Per-token scalars of chunk c: the L2 norms of its raw q and k rows, g and
-    // beta, then (warp 7) the cumulative decays and the column scales.
+    // Per-token scalars of chunk c: g and beta (with the L2 norms of its q and k
+    // rows, which came with them), then (warp 7) the cumulative decays and the
+    // column scales.
     auto stage_scalars = [&](int c) {
       const int ns = min(C, len - c * C), b = c & 1;
       alive = cw_and(alive && wait_live(&rbar[b], (c >> 1) & 1, vdead));
-      const unsigned char *qk = RQK + b * kQKBuf;
       const int t = stage_token(), part = lane >> 3;
-      float qq = 0.f, kk = 0.f;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const uint2 qv = raw_piece(qk, 2 * kRawHalf, t, part + 4 * m);
-        const uint2 kv = raw_piece(qk + kRawHalf, 2 * kRawHalf, t, part + 4 * m);
-        const float a0 = bf_lo(qv.x), a1 = bf_hi(qv.x), a2 = bf_lo(qv.y), a3 = bf_hi(qv.y);
-        const float b0 = bf_lo(kv.x), b1 = bf_hi(kv.x), b2 = bf_lo(kv.y), b3 = bf_hi(kv.y);
-        qq += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
-        kk += b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
-      }
-      qq += __shfl_xor_sync(0xffffffffu, qq, 8);
-      qq += __shfl_xor_sync(0xffffffffu, qq, 16);
-      kk += __shfl_xor_sync(0xffffffffu, kk, 8);
-      kk += __shfl_xor_sync(0xffffffffu, kk, 16);
       float gt = g_next, bt = b_next;
       if (GB) {  // this head's column of the [64][8] g and beta tiles (padded tokens 0)
         const bf16 *g8 = reinterpret_cast<const bf16 *>(RGB + b * 2 * kRawGB);
@@ -1536,8 +1526,6 @@ __global__ void __launch_bounds__(NTS, 1)
         bt = t < ns ? __bfloat162float(g8[C * 8 + t * 8 + (h & 7)]) : 0.f;
       }
       if (part == 0) {
-        sRq[t] = rsqrtf(qq + kL2Eps);
-        sRk[t] = rsqrtf(kk + kL2Eps);
         sG[t] = gt;
         sBeta[t] = bt;
       }
@@ -1557,9 +1545,10 @@ __global__ void __launch_bounds__(NTS, 1)
           const float G = e == 0 ? incl - bb : incl;
           const float gam = expf(G);
           sGam[i] = gam;
-          sQ[i] = gam * sRq[i];
-          sK[i] = sBeta[i] * gam * sRk[i];
-          sKt[i] = expf(gl - G) * sRk[i];
+          const float *nrm = NB + b * 2 * C;  // 1/|q| then 1/|k|
+          sQ[i] = gam * nrm[i];
+          sK[i] = sBeta[i] * gam * nrm[C + i];
+          sKt[i] = expf(gl - G) * nrm[C + i];
         }
       }
     };
@@ -1928,9 +1917,9 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
 
 }  // namespace
 
-size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v) {
+size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v, int h_k) {
   return offsets_bytes(n_seqs) +
-         (size_t)max_chunks(n_seqs, total_tokens) * h_v * 2 * kTileBytes;
+         (size_t)max_chunks(n_seqs, total_tokens) * (h_v * 2 * kTileBytes + h_k * 2 * C * 4);
 }
 
 cudaError_t launch_prefill_split(const PoolView &p, int layer, const SeqIndex &seq,
