@@ -1408,13 +1408,20 @@ __global__ void __launch_bounds__(NTS, 1)
     };
     // [D3 | E] = S_bf16 [Q;K]^T over the raw rows of chunk c: M 128, N 128,
     // K 128 in steps of 16 (four 32-byte steps inside each swizzled 64-column half)
+    // Descriptor bases, built once: a K step adds its byte offset / 16 to the
+    // 14-bit address field (every operand lies below 256 KiB: no carry out).
+    const uint64_t ed3_d0 = tc::smem_desc_sw128(smem_addr(RQK));
+    const uint64_t ed3_d1 = tc::smem_desc_sw128(smem_addr(RQK + kQKBuf));
+    const uint64_t dd_d = tc::smem_desc(tt_s, tc::kLBO, SBO_C);
+    const uint64_t up_d0 = tc::smem_desc(pt_s, tc::kLBO, SBO_C);
+    const uint64_t up_d1 = tc::smem_desc(kt_s, tc::kLBO, SBO_C);
     auto issue_ed3 = [&](int c) {
       if (leader) {
-        const uint32_t b0 = smem_addr(RQK + (c & 1) * kQKBuf);
+        const uint64_t b0 = (c & 1) ? ed3_d1 : ed3_d0;
         constexpr uint32_t id = tc::idesc_bf16(128, 128);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t bd = tc::smem_desc_sw128(b0 + (ks >> 2) * 2 * kRawHalf + 32 * (ks & 3));
+          const uint64_t bd = b0 + (uint64_t)((((ks >> 2) * 2 * kRawHalf) + 32 * (ks & 3)) >> 4);
           tc::mma_ts_f16(tm + U_D3, tm + U_F + 8 * ks, bd, id, ks > 0);
         }
         tc::mma_commit(&b_ed3);
@@ -1437,9 +1444,8 @@ __global__ void __launch_bounds__(NTS, 1)
       if (leader) {  // Delta^T = F T^T  (A = F from TMEM; M 128, N 64, K 64)
 #pragma unroll
         for (int j = 0; j < C / 8; ++j)
-          tc::mma_ts(tm + U_DD, tm + U_F + j * 8,
-                     tc::smem_desc(tt_s + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 64),
-                     j > 0);
+          tc::mma_ts(tm + U_DD, tm + U_F + j * 8, dd_d + (uint64_t)((j * KSTEP) >> 4),
+                     tc::idesc_tf32(128, 64), j > 0);
         tc::mma_commit(&b_dd);
       }
       __syncwarp();
@@ -1449,12 +1455,12 @@ __global__ void __launch_bounds__(NTS, 1)
       tc::fence_after_sync();
       if (leader) {  // [D4a | S] += Delta^T [P0; Ktil^T]^T (even c) or
                      // [S | D4b] += Delta^T [Ktil^T; P1]^T (odd c): N 192, K 64
-        const uint32_t dcol = (c & 1) ? U_S : U_D4A, bsm = (c & 1) ? kt_s : pt_s;
+        const uint32_t dcol = (c & 1) ? U_S : U_D4A;
+        const uint64_t b0 = (c & 1) ? up_d1 : up_d0;
 #pragma unroll
         for (int j = 0; j < C / 8; ++j)
-          tc::mma_ts(tm + dcol, tm + U_DD + j * 8,
-                     tc::smem_desc(bsm + j * KSTEP, tc::kLBO, SBO_C), tc::idesc_tf32(128, 192),
-                     1);
+          tc::mma_ts(tm + dcol, tm + U_DD + j * 8, b0 + (uint64_t)((j * KSTEP) >> 4),
+                     tc::idesc_tf32(128, 192), 1);
         tc::mma_commit(&b_upd);
       }
       __syncwarp();
