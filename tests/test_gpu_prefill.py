@@ -12,7 +12,7 @@ import torch
 
 from gated_deltanet_recurrent_gb300 import abi, synth
 from oracle import gdn_oracle as O
-from tests.gpu_util import (assert_close_bf16, assert_maxrel, dev, dev_i32, host, tok_dev,
+from tests.gpu_util import (assert_close_bf16, assert_maxrel, dev, dev_i32, host, tdtype, tok_dev,
                             tok_np)
 from tests.oracle_par import recurrent_many
 
@@ -396,3 +396,41 @@ def test_prefill_device_guard_and_host_checks():
     assert abi.gdn_pool_get_error(pool) == abi.DEVERR_SLOT
     assert bool((pool.state[0, [0, 2, 3]] == SENTINEL).all())
     assert bool((o[:6] == 0).all())
+
+
+@pytest.mark.parametrize("odt", ["bf16", "f32"])
+def test_prefill_many_sequences_unaligned_outputs(odt):
+    """dk = dv = 128, bf16 tensor-map rows, 300 sequences: more than the state
+    kernel orders longest first (up to 256), so they are walked in index
+    order; lengths 1..40 with a few whole and ragged multi-chunk ones; and an
+    output tensor that does not start 16-byte aligned, so the state kernel
+    stores element by element instead of staging whole rows (and of
+    tensor-map stores for bf16).  Every output and every state against the
+    oracle."""
+    rng = np.random.default_rng(46)
+    shape = synth.LayerShape(2, 1, 128, 128, 16, 4)
+    n = 300
+    lens = rng.integers(1, 41, n)
+    lens[[7, 150, 299]] = [64, 130, 65]
+    ids = rng.permutation(n + 10)[:n].astype(np.int32)
+    cu = synth.cu_seqlens_of(lens)
+    T = int(cu[-1])
+    S0 = synth.random_states(rng, n, shape)
+    tok = synth.token_inputs(rng, T, shape, "bf16")
+    pool = _pool(shape, 1, n + 10)
+    lid = torch.from_numpy(ids).long().cuda()
+    pool.state[0, lid] = dev(S0)
+    tdt = tdtype(odt)
+    buf = torch.zeros(T * shape.h_v * shape.dv + 1, device="cuda", dtype=tdt)
+    o = buf[1:].view(T, shape.h_v, shape.dv)       # one element past a 16-byte boundary
+    abi.gdn_prefill_chunked(pool, 0, dev_i32(ids), dev_i32(cu), *tok_dev(tok, "bf16"), o,
+                            max_seqlen=int(lens.max()))
+    assert abi.gdn_pool_get_error(pool) == 0
+    ref = O.OraclePool(1, n + 10, shape.h_v, shape.h_k, shape.dk, shape.dv, 16, 4)
+    ref.S[0, ids] = S0
+    o_ref = ref.prefill(0, ids, cu, *tok_np(tok))
+    assert_close_bf16(host(o), o_ref, what="o")
+    assert_maxrel(host(o), o_ref, _rel_tol(128), "o")
+    assert_maxrel(host(pool.state[0, lid]), ref.S[0, ids], _rel_tol(128), "S")
+    rest = np.setdiff1d(np.arange(n + 10), ids)
+    assert bool((pool.state[0, torch.from_numpy(rest).long().cuda()] == SENTINEL).all())
