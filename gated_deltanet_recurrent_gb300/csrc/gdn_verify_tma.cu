@@ -57,27 +57,12 @@ __global__ void __launch_bounds__(NT)
     if (h == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
     return;
   }
-  // the head's load goes out first: it does not depend on the draft counts
   const int row0 = ((layer * p.n_slots + slot) * p.h_v + h) * D;  // tensor-map row
   const int hk = h / (p.h_v / p.h_k);
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 32);
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_fence_init();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tm = tmem_slot;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar, TILE);
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-      asm volatile(
-          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-          "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(tile + s * SLAB)),
-          "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(32 * s), "r"(row0), "r"(smem_addr(&bar))
-          : "memory");
   }
 
   int ap = 0;  // pending drafts replayed first (deferred commit only)
@@ -103,22 +88,21 @@ __global__ void __launch_bounds__(NT)
     row = pend ? (int64_t)i * T_old + t : (int64_t)i * T_new + (t - ap);
     return pend ? prv : cur;
   };
-  for (int e = tid; e < (NX - 2 * T) * (D / 4); e += NT) {  // zero the unused X rows
-    const int r = 2 * T + e / (D / 4), c4 = e % (D / 4);
-    *reinterpret_cast<float4 *>(X + tc::core_off(r, 4 * c4, D)) = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
-  // ---- stage the drafts while the head is in flight
-  for (int t = warp; t < T; t += NT / 32) {
-    int64_t tok;
-    const QKV src = src_of(t, tok);
-    float4 q4 = Elem<TI>::load4(static_cast<const TI *>(src.q) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
-    float4 k4 = Elem<TI>::load4(static_cast<const TI *>(src.k) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
-    const float qq = group_sum<32>(dot4(q4, q4));
-    const float kk = group_sum<32>(dot4(k4, k4));
-    *reinterpret_cast<float4 *>(X + tc::core_off(t, 4 * lane, D)) = scale4(rsqrtf(kk + kL2Eps), k4);
-    *reinterpret_cast<float4 *>(X + tc::core_off(T + t, 4 * lane, D)) =
-        scale4(rsqrtf(qq + kL2Eps), q4);
+  // ---- the drafts' loads go out before the head's: they are small and every
+  // step after them waits on them, while the head is needed only by the MMA.
+  // Warp w takes tokens w and w + 4 (q and k rows), thread v its row's v of
+  // each token, threads t < T the gates.
+  float4 q4[2], k4[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int t = warp + 4 * r;
+    q4[r] = k4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < T) {
+      int64_t tok;
+      const QKV src = src_of(t, tok);
+      q4[r] = Elem<TI>::load4(static_cast<const TI *>(src.q) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
+      k4[r] = Elem<TI>::load4(static_cast<const TI *>(src.k) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
+    }
   }
   const int v = tid;  // this thread's state row
   float vr[TMX];
@@ -131,13 +115,47 @@ __global__ void __launch_bounds__(NT)
       vr[t] = Elem<TI>::load1(static_cast<const TI *>(src.v) + tok * src.ld_v + (int64_t)h * D + v);
     }
   }
-  if (tid < T) {  // g_t into sG[t + 1] (summed below), alpha_t, beta_t
+  float gt = 0.f, bt = 0.f;
+  if (tid < T) {
     int64_t tok;
     const QKV src = src_of(tid, tok);
-    const float gt = Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
+    gt = Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
+    bt = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * p.h_v + h);
+  }
+  tc::fence_before_sync();
+  __syncthreads();  // the barrier is initialised
+  tc::fence_after_sync();
+  const uint32_t tm = tmem_slot;
+  if (tid == 0) {  // the head: four tensor-map loads in the 128-byte swizzle
+    mbar_arrive_expect_tx(&bar, TILE);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+          "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(tile + s * SLAB)),
+          "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(32 * s), "r"(row0), "r"(smem_addr(&bar))
+          : "memory");
+  }
+  for (int e = tid; e < (NX - 2 * T) * (D / 4); e += NT) {  // zero the unused X rows
+    const int r = 2 * T + e / (D / 4), c4 = e % (D / 4);
+    *reinterpret_cast<float4 *>(X + tc::core_off(r, 4 * c4, D)) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {  // normalised k and q rows of the [K;Q] tile
+    const int t = warp + 4 * r;
+    if (t < T) {
+      const float qq = group_sum<32>(dot4(q4[r], q4[r]));
+      const float kk = group_sum<32>(dot4(k4[r], k4[r]));
+      *reinterpret_cast<float4 *>(X + tc::core_off(t, 4 * lane, D)) =
+          scale4(rsqrtf(kk + kL2Eps), k4[r]);
+      *reinterpret_cast<float4 *>(X + tc::core_off(T + t, 4 * lane, D)) =
+          scale4(rsqrtf(qq + kL2Eps), q4[r]);
+    }
+  }
+  if (tid < T) {  // g_t into sG[t + 1] (summed below), alpha_t, beta_t
     sG[tid + 1] = gt;
     sal[tid] = expf(gt);
-    sbe[tid] = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * p.h_v + h);
+    sbe[tid] = bt;
   }
   __syncthreads();
   if (tid == 0) {  // G_t = g_0 + ... + g_{t-1}, T <= 8 terms
