@@ -547,6 +547,33 @@ gdn_status gdn_gated_rmsnorm(int64_t rows, int32_t d, const void *o, gdn_dtype o
   return ok();
 }
 
+namespace {
+
+// A verify launch with its drafts staged in a stream-ordered workspace (the
+// tensor-core path, when the pool's memory pool grants it within
+// prefill_workspace_max; otherwise each block stages its own drafts).
+cudaError_t verify_with_stage(gdn_pool *p, int32_t layer, gdn::VerifyArgs &va, void *o,
+                              gdn_dtype o_dtype, cudaStream_t s) {
+  void *stage = nullptr;
+  const uint64_t lim = p->desc.prefill_workspace_max ? p->desc.prefill_workspace_max
+                                                     : (uint64_t)8 << 30;
+  const size_t sb = p->has_tmap ? gdn::verify_stage_workspace_bytes(p->view, va) : 0;
+  if (sb > 0 && sb <= lim && cudaMallocFromPoolAsync(&stage, sb, p->work_pool, s) != cudaSuccess) {
+    cudaGetLastError();
+    stage = nullptr;
+  }
+  va.stage = static_cast<float *>(stage);
+  cudaError_t e =
+      gdn::launch_verify(p->view, p->has_tmap ? &p->tmap : nullptr, layer, va, o, o_dtype, s);
+  if (stage != nullptr) {
+    const cudaError_t ef = cudaFreeAsync(stage, s);
+    if (e == cudaSuccess) e = ef;
+  }
+  return e;
+}
+
+}  // namespace
+
 gdn_status gdn_spec_verify(gdn_pool *p, int32_t layer, const int32_t *slot_ids, int32_t n,
                            int32_t T, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
                            const int32_t *accept_len, float scale, gdn_stream stream) {
@@ -568,9 +595,8 @@ gdn_status gdn_spec_verify(gdn_pool *p, int32_t layer, const int32_t *slot_ids, 
     if (accept_len && (st = check_counts(accept_len, n, nullptr, T, s, "accept_len"))) return st;
     if (o && (st = check_device_ptr(o, "o"))) return st;
   }
-  gdn::VerifyArgs va{slot_ids, n, T, q, accept_len, 0, gdn::QKV{}, 0, nullptr, scale};
-  cudaError_t e =
-      gdn::launch_verify(p->view, p->has_tmap ? &p->tmap : nullptr, layer, va, o, o_dtype, s);
+  gdn::VerifyArgs va{slot_ids, n, T, q, accept_len, 0, gdn::QKV{}, 0, nullptr, scale, nullptr};
+  const cudaError_t e = verify_with_stage(p, layer, va, o, o_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "verify launch");
   return ok();
 }
@@ -606,9 +632,8 @@ gdn_status gdn_spec_verify_deferred(gdn_pool *p, int32_t layer, const int32_t *s
       return st;
   }
   gdn::VerifyArgs va{slot_ids, n, T, q, nullptr, 0, pending ? qp : gdn::QKV{},
-                     pending ? T_prev : 0, pending ? prev_accept : nullptr, scale};
-  cudaError_t e =
-      gdn::launch_verify(p->view, p->has_tmap ? &p->tmap : nullptr, layer, va, o, o_dtype, s);
+                     pending ? T_prev : 0, pending ? prev_accept : nullptr, scale, nullptr};
+  const cudaError_t e = verify_with_stage(p, layer, va, o, o_dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "deferred verify launch");
   return ok();
 }

@@ -132,6 +132,7 @@ struct VerifyArgs {
   int T_prev;
   const int32_t *prev_accept;
   float scale;
+  float *stage;                // workspace for the staged drafts (tensor-core path), or NULL
 };
 
 // tmap: the pool's state tensor map (CUtensorMap), or NULL
@@ -140,6 +141,9 @@ cudaError_t launch_verify(const PoolView &p, const void *tmap, int layer, const 
 
 cudaError_t launch_verify_tma(const PoolView &p, const void *tmap, int layer,
                               const VerifyArgs &va, void *o, gdn_dtype o_dtype, cudaStream_t s);
+// Bytes of the draft-staging workspace the tensor-core verify can use (0: that
+// path does not apply).
+size_t verify_stage_workspace_bytes(const PoolView &p, const VerifyArgs &va);
 
 cudaError_t launch_prefill_recurrent(const PoolView &p, int layer, const SeqIndex &seq,
                                      const QKV &in, void *o, gdn_dtype o_dtype, float scale,

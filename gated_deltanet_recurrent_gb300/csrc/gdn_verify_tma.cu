@@ -33,10 +33,126 @@ constexpr int O_DM = O_KQ + TMX * TMX * 4;   // decay table [9][9]
 constexpr int O_SC = O_DM + 96 * 4;          // alpha, beta, G
 constexpr int SMEM = 1024 + O_SC + 32 * 4;
 
+// ---- draft staging, once per (slot, key head)
+// Workspace of a staged call: per (slot i, key head) a block of kXBlock floats
+// -- the [K;Q] core tile X (normalised k rows 0..T-1, q rows T..2T-1, zero
+// rows up to NX), then KK and KQ -- and after all of those, per (slot i,
+// value head) kGBlock floats: the decay table Dm, then alpha, beta and the
+// cumulative G.  The same arithmetic as the verify kernel's own staging, so
+// both forms give the same bits; the verify kernel bulk-copies its two blocks
+// next to the head instead of loading and reducing the drafts itself.
+constexpr int kXBlock = NX * D + 2 * TMX * TMX;  // 2176 floats (8704 bytes)
+constexpr int kGBlock = 128;                     // 96 (Dm) + 8 + 8 + 16 floats
+static_assert(O_KK == O_X + NX * D * 4 && O_KQ == O_KK + TMX * TMX * 4 &&
+                  O_SC == O_DM + 96 * 4 && (kGBlock - 96) * 4 == 32 * 4,
+              "staged blocks mirror the shared-memory map");
+
+__host__ __device__ inline size_t verify_stage_bytes(int n, int h_k, int h_v) {
+  return (size_t)n * ((size_t)h_k * kXBlock + (size_t)h_v * kGBlock) * 4;
+}
+
+// Token t of slot i: pending draft t (deferred round), or new draft t - ap.
+__device__ __forceinline__ QKV verify_src(const VerifyArgs &va, bool deferred, int ap, int i,
+                                          int t, int64_t &row) {
+  const bool pend = deferred && t < ap;
+  row = pend ? (int64_t)i * va.T_prev + t : (int64_t)i * va.T + (t - ap);
+  return pend ? va.prev : va.in;
+}
+
+// Pending drafts replayed first (deferred round only), clamped as the verify
+// kernel clamps them (which also raises the error).
+__device__ __forceinline__ int verify_pending(const VerifyArgs &va, bool deferred, int i) {
+  if (!deferred) return 0;
+  const int ap = va.prev_accept[i];
+  return ap < 0 ? 0 : (ap > va.T_prev ? va.T_prev : ap);
+}
+
+// grid (h_k, n), 128 threads
+template <typename TI, bool DEFERRED>
+__global__ void __launch_bounds__(NT)
+    verify_stage_kernel(int h_v, int h_k, VerifyArgs va, float *__restrict__ st) {
+  __shared__ __align__(16) float Xs[NX * D];
+  __shared__ float sg[TMX + 1];
+  // the verify grid may start now: it issues its head loads before waiting for
+  // this grid (a programmatic dependent launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int kh = blockIdx.x, i = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ap = verify_pending(va, DEFERRED, i);
+  const int T = ap + va.T;
+  for (int e = tid; e < (NX - 2 * T) * (D / 4); e += NT) {  // zero the unused rows
+    const int r = 2 * T + e / (D / 4), c4 = e % (D / 4);
+    *reinterpret_cast<float4 *>(Xs + tc::core_off(r, 4 * c4, D)) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int t = warp; t < T; t += NT / 32) {
+    int64_t tok;
+    const QKV src = verify_src(va, DEFERRED, ap, i, t, tok);
+    float4 q4 = Elem<TI>::load4(static_cast<const TI *>(src.q) + tok * src.ld_qk + (int64_t)kh * D + 4 * lane);
+    float4 k4 = Elem<TI>::load4(static_cast<const TI *>(src.k) + tok * src.ld_qk + (int64_t)kh * D + 4 * lane);
+    const float qq = group_sum<32>(dot4(q4, q4));
+    const float kk = group_sum<32>(dot4(k4, k4));
+    *reinterpret_cast<float4 *>(Xs + tc::core_off(t, 4 * lane, D)) = scale4(rsqrtf(kk + kL2Eps), k4);
+    *reinterpret_cast<float4 *>(Xs + tc::core_off(T + t, 4 * lane, D)) =
+        scale4(rsqrtf(qq + kL2Eps), q4);
+  }
+  __syncthreads();
+  float *xb = st + ((int64_t)i * h_k + kh) * kXBlock;
+  for (int e = tid; e < NX * D / 4; e += NT)
+    reinterpret_cast<float4 *>(xb)[e] = reinterpret_cast<const float4 *>(Xs)[e];
+  // Gram scalars, four lanes per pair (the verify kernel's reduction order)
+  for (int e0 = 0; e0 < 2 * T * T; e0 += NT / 4) {
+    const int e = e0 + tid / 4, sub4 = tid % 4;
+    float acc = 0.f;
+    const int which = e / (T * T), ii = (e / T) % T, tt = e % T;
+    if (e < 2 * T * T) {
+      const int ry = which ? T + tt : tt;
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const int c = 4 * (4 * j + sub4);
+        acc += dot4(*reinterpret_cast<const float4 *>(Xs + tc::core_off(ii, c, D)),
+                    *reinterpret_cast<const float4 *>(Xs + tc::core_off(ry, c, D)));
+      }
+    }
+    acc = group_sum<4>(acc);
+    if (e < 2 * T * T && sub4 == 0) xb[NX * D + which * TMX * TMX + ii * TMX + tt] = acc;
+  }
+  // per value head of the group: the decay table, alpha, beta, G
+  const int G = h_v / h_k;
+  for (int g = 0; g < G; ++g) {
+    const int h = kh * G + g;
+    float *gbk = st + (int64_t)va.n * h_k * kXBlock + ((int64_t)i * h_v + h) * kGBlock;
+    float gt = 0.f;
+    if (tid < T) {
+      int64_t tok;
+      const QKV src = verify_src(va, DEFERRED, ap, i, tid, tok);
+      gt = Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * h_v + h);
+      gbk[96 + tid] = expf(gt);
+      gbk[104 + tid] = Elem<TI>::load1(static_cast<const TI *>(src.beta) + tok * h_v + h);
+      sg[tid + 1] = gt;
+    }
+    __syncthreads();
+    if (tid == 0) {  // G_t = g_0 + ... + g_{t-1}, T <= 8 terms
+      float acc = 0.f;
+      sg[0] = 0.f;
+#pragma unroll
+      for (int t = 1; t <= TMX; ++t)
+        if (t <= T) sg[t] = (acc += sg[t]);
+    }
+    __syncthreads();
+    if (tid <= T) gbk[112 + tid] = sg[tid];
+    for (int e = tid; e < (T + 1) * (T + 1); e += NT) {
+      const int aa = e / (T + 1), bb = e % (T + 1);
+      gbk[aa * (TMX + 1) + bb] = bb <= aa ? expf(sg[aa] - sg[bb]) : 0.f;
+    }
+    __syncthreads();
+  }
+}
+
 template <typename TI, typename TO, bool DEFERRED>
 __global__ void __launch_bounds__(NT)
     verify_tma_kernel(PoolView p, const __grid_constant__ CUtensorMap tmap, int layer,
-                      VerifyArgs va, TO *__restrict__ o) {
+                      VerifyArgs va, TO *__restrict__ o, const float *__restrict__ staged) {
+  const bool pre = staged != nullptr;  // the drafts were staged by verify_stage_kernel
   extern __shared__ __align__(1024) unsigned char dsm[];
   unsigned char *base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
   unsigned char *tile = base;
@@ -97,7 +213,7 @@ __global__ void __launch_bounds__(NT)
   for (int r = 0; r < 2; ++r) {
     const int t = warp + 4 * r;
     q4[r] = k4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < T) {
+    if (!pre && t < T) {
       int64_t tok;
       const QKV src = src_of(t, tok);
       q4[r] = Elem<TI>::load4(static_cast<const TI *>(src.q) + tok * src.ld_qk + (int64_t)hk * D + 4 * lane);
@@ -116,7 +232,7 @@ __global__ void __launch_bounds__(NT)
     }
   }
   float gt = 0.f, bt = 0.f;
-  if (tid < T) {
+  if (!pre && tid < T) {
     int64_t tok;
     const QKV src = src_of(tid, tok);
     gt = Elem<TI>::load1(static_cast<const TI *>(src.g) + tok * p.h_v + h);
@@ -127,7 +243,7 @@ __global__ void __launch_bounds__(NT)
   tc::fence_after_sync();
   const uint32_t tm = tmem_slot;
   if (tid == 0) {  // the head: four tensor-map loads in the 128-byte swizzle
-    mbar_arrive_expect_tx(&bar, TILE);
+    mbar_arrive_expect_tx(&bar, TILE + (pre ? (kXBlock + kGBlock) * 4 : 0));
 #pragma unroll
     for (int s = 0; s < 4; ++s)
       asm volatile(
@@ -135,7 +251,15 @@ __global__ void __launch_bounds__(NT)
           "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(tile + s * SLAB)),
           "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(32 * s), "r"(row0), "r"(smem_addr(&bar))
           : "memory");
+    if (pre) {  // the staged [K;Q] tile with KK, KQ, and this head's decays and gates,
+                // once the staging grid has completed
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      bulk_g2s(X, staged + ((int64_t)i * p.h_k + hk) * kXBlock, kXBlock * 4, &bar);
+      bulk_g2s(Dm, staged + (int64_t)va.n * p.h_k * kXBlock + ((int64_t)i * p.h_v + h) * kGBlock,
+               kGBlock * 4, &bar);
+    }
   }
+  if (!pre) {
   for (int e = tid; e < (NX - 2 * T) * (D / 4); e += NT) {  // zero the unused X rows
     const int r = 2 * T + e / (D / 4), c4 = e % (D / 4);
     *reinterpret_cast<float4 *>(X + tc::core_off(r, 4 * c4, D)) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -187,6 +311,7 @@ __global__ void __launch_bounds__(NT)
     const int aa = e / (T + 1), bb = e % (T + 1);
     Dm[aa * (TMX + 1) + bb] = bb <= aa ? expf(sG[aa] - sG[bb]) : 0.f;
   }
+  }  // !pre
   tc::fence_async_smem();
   tc::fence_before_sync();
   bool alive = __syncthreads_and(mbar_wait_bounded(&bar, 0));
@@ -290,15 +415,46 @@ template <typename TI, typename TO>
 cudaError_t launch_t(const PoolView &p, const CUtensorMap &tmap, int layer, const VerifyArgs &va,
                      void *o, cudaStream_t s) {
   const bool deferred = va.prev.q != nullptr && va.prev_accept != nullptr;
+  if (va.stage != nullptr) {  // the drafts staged once per (slot, key head)
+    auto stage = deferred ? verify_stage_kernel<TI, true> : verify_stage_kernel<TI, false>;
+    stage<<<dim3(p.h_k, va.n), NT, 0, s>>>(p.h_v, p.h_k, va, va.stage);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   auto kern = deferred ? verify_tma_kernel<TI, TO, true> : verify_tma_kernel<TI, TO, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.h_v, va.n);
-  kern<<<grid, NT, SMEM, s>>>(p, tmap, layer, va, static_cast<TO *>(o));
-  return cudaGetLastError();
+  if (va.stage == nullptr) {
+    kern<<<grid, NT, SMEM, s>>>(p, tmap, layer, va, static_cast<TO *>(o), va.stage);
+    return cudaGetLastError();
+  }
+  // a programmatic dependent of the staging grid: heads load while it runs
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, tmap, layer, va, static_cast<TO *>(o),
+                            static_cast<const float *>(va.stage));
 }
 
 }  // namespace
+
+size_t verify_stage_workspace_bytes(const PoolView &p, const VerifyArgs &va) {
+  // Staged drafts pay off from five tokens per slot (measured on the 128-slot
+  // case: 4 tokens 108.7 -> 113.8 us, a deferred round of up to 8 tokens
+  // 151.9 -> 139.1 us); with fewer, each block stages its own.
+  if (p.state_dtype != GDN_F32 || p.dk != D || p.dv != D || va.T + va.T_prev > TMX ||
+      va.T + va.T_prev <= 4)
+    return 0;
+  return verify_stage_bytes(va.n, p.h_k, p.h_v);
+}
 
 cudaError_t launch_verify_tma(const PoolView &p, const void *tmap, int layer,
                               const VerifyArgs &va, void *o, gdn_dtype o_dtype, cudaStream_t s) {
