@@ -331,7 +331,11 @@ gdn_status gdn_prefill_recurrent(gdn_pool *pool, int32_t layer, const int32_t *s
  * the state after accept_len[i] tokens, written once; 0 leaves it untouched.
  * With accept_len == NULL the pool is only read (verify-then-commit in two
  * calls, the second recomputing from the same inputs).  o and accept_len
- * must not both be NULL.  1 <= T <= 32. */
+ * must not both be NULL.  1 <= T <= 32.  Calls of more than four tokens per
+ * slot on the tensor-core path (dk = dv = 128, float32 state) may take a
+ * stream-ordered workspace for the staged drafts from the pool's memory pool
+ * (within prefill_workspace_max; released on `stream` when the call's work
+ * is done); if it cannot be had, the call runs without it. */
 gdn_status gdn_spec_verify(gdn_pool *pool, int32_t layer, const int32_t *slot_ids, int32_t n,
                            int32_t T, const gdn_qkv *in, void *o, gdn_dtype o_dtype,
                            const int32_t *accept_len, float scale, gdn_stream stream);
@@ -351,7 +355,8 @@ gdn_status gdn_spec_verify(gdn_pool *pool, int32_t layer, const int32_t *slot_id
  * them without new drafts.  prev and prev_accept are both NULL (no pending
  * drafts: outputs only) or both set; prev_accept: [n] int32 in [0, T_prev];
  * prev and in share one dtype.  T >= 1, T_prev >= 0, T + T_prev <= 32: the
- * pending drafts plus this round's fit one 32-token window. */
+ * pending drafts plus this round's fit one 32-token window.  Workspace as in
+ * gdn_spec_verify (staged drafts when T + T_prev > 4). */
 gdn_status gdn_spec_verify_deferred(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
                                     int32_t n, int32_t T, const gdn_qkv *in, void *o,
                                     gdn_dtype o_dtype, int32_t T_prev, const gdn_qkv *prev,
