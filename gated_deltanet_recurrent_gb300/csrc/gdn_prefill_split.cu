@@ -1,4 +1,4 @@
-// Chunked prefill in two launches, for dk = dv = 128 (tcgen05, kind::tf32).
+// Chunked prefill in two launches, for dk = dv = 128 (tcgen05).
 //
 // The chunked delta rule (b70-optimization-lab research plan, "What the
 // research found": the (I+A)^{-1} UT transform) splits each 64-token chunk
@@ -14,10 +14,12 @@
 // Only the state side is sequential along a sequence.  `prep_kernel` runs the
 // key side of every (chunk, value head) of the call in parallel (one CTA
 // each, two CTAs per SM) and writes P and T as ready-made tensor-core operand
-// tiles to a workspace; `seq_kernel` then walks each (sequence, value head)
+// tiles to a workspace; a state kernel then walks each (sequence, value head)
 // chunk by chunk with the state resident in TMEM, fetching each chunk's P and
-// T tiles with one bulk copy issued a chunk ahead.  The arithmetic is the
-// single-launch kernel's, step for step, so results agree with it.
+// T tiles with bulk copies issued ahead: `seq_bf16_kernel` when the bf16 rows
+// can come by tensor map (S [Q;K]^T on kind::f16 over the raw tiles),
+// `seq_kernel` otherwise (rows staged from global memory as float32 operand
+// tiles, kind::tf32).
 //
 // Workspace: (n_seqs + 1) int32 chunk offsets and the sequence order (256-byte
 // aligned), then per (chunk, value head) 32 KiB: the P tile, then the T tile,
@@ -178,19 +180,16 @@ __device__ __forceinline__ void stage_chunk(const QKV &in, const PoolView &p, in
                          in.ld_qk, in.ld_v, n, gt, bt, QK, XU, sG, sBeta);
 }
 
-// Raw bf16 copy of one chunk's q, k and v (and optionally g, beta) in shared
-// memory, loaded by tensor-map copies a chunk ahead (16-byte aligned rows):
-// q, k, v each as two 64-column halves of [64 tokens][64] bf16 in the 128-byte
-// swizzled layout (8 KiB each, 1024-byte aligned), then g and beta as
-// [64 tokens][8 heads] bf16 (the 8-head group holding this head).
+// Tensor maps of a call's bf16 rows (16-byte aligned): q, k and v are fetched
+// as 64-column halves of [64 tokens][64] bf16 in the 128-byte swizzled layout
+// (8 KiB each, 1024-byte aligned), g and beta as [64 tokens][8 heads] bf16
+// (the 8-head group holding a head).
 struct InMaps {
   CUtensorMap q, k, v, g, b;   // q, k, v: {128, heads, tokens}; g, b: {h_v, tokens}
   CUtensorMap o;               // bf16 outputs {128, h_v, tokens}, stores of whole chunks
 };
 constexpr int kRawHalf = C * 64 * 2;            // 8 KiB
 constexpr int kRawGB = C * 8 * 2;               // 1 KiB
-constexpr int kRawQKV = 6 * kRawHalf;
-constexpr int kRawBytes = kRawQKV + 2 * kRawGB + 1024;  // + alignment slack
 
 __device__ __forceinline__ void tma3(void *dst, const CUtensorMap *m, int x, int y, int z,
                                      uint64_t *bar) {
@@ -230,21 +229,6 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// One thread: the chunk's q and k halves (and g, beta) onto rbar.
-__device__ __forceinline__ void prefetch_qk(const InMaps &m, bool gb, int h, int hk,
-                                            int64_t tok0, unsigned char *raw, uint64_t *rbar) {
-  mbar_arrive_expect_tx(rbar, 4 * kRawHalf + (gb ? 2 * kRawGB : 0));
-  const int z = (int)tok0;
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    tma3(raw + (0 + hf) * kRawHalf, &m.q, 64 * hf, hk, z, rbar);
-    tma3(raw + (2 + hf) * kRawHalf, &m.k, 64 * hf, hk, z, rbar);
-  }
-  if (gb) {
-    tma2(raw + kRawQKV, &m.g, h & ~7, z, rbar);
-    tma2(raw + kRawQKV + kRawGB, &m.b, h & ~7, z, rbar);
-  }
-}
 // One thread: the chunk's v halves to vdst, vdst + kRawHalf onto vbar.
 __device__ __forceinline__ void prefetch_v(const InMaps &m, int h, int64_t tok0,
                                            unsigned char *vdst, uint64_t *vbar) {
@@ -270,48 +254,6 @@ __device__ __forceinline__ void prefetch_qk_pairs(const InMaps &m, bool gb, int 
   if (gb) {
     tma2(gbt, &m.g, h & ~7, z, bar);
     tma2(gbt + kRawGB, &m.b, h & ~7, z, bar);
-  }
-}
-
-// Elements 4c .. 4c+3 of token t of a [64][128] bf16 tile stored as two swizzled halves.
-__device__ __forceinline__ float4 raw_load4(const unsigned char *tile, int t, int c) {
-  const int col = (4 * c) & 63;
-  const int chunk = (col >> 3) ^ (t & 7);
-  const uint2 r = *reinterpret_cast<const uint2 *>(tile + ((4 * c) >> 6) * kRawHalf + t * 128 +
-                                                   chunk * 16 + (col & 7) * 2);
-  return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u),
-                     __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
-}
-
-// stage_rows from the raw tiles (same mapping and arithmetic), without v: the
-// state kernel reads v from the raw tile itself.
-__device__ __forceinline__ void stage_rows_raw(const unsigned char *raw, int n, float gt, float bt,
-                                               float *QK, float *sG, float *sBeta) {
-  const int lane = threadIdx.x & 31;
-  const int cg = lane >> 3;
-  const int t = stage_token();
-  const bool real = t < n;
-#pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const unsigned char *tile = raw + 2 * which * kRawHalf;
-    float4 x4[D / 16];
-    float xx = 0.f;
-#pragma unroll
-    for (int j = 0; j < D / 16; ++j) {
-      x4[j] = real ? raw_load4(tile, t, cg + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
-      xx += dot4(x4[j], x4[j]);
-    }
-    xx += __shfl_xor_sync(0xffffffffu, xx, 8);
-    xx += __shfl_xor_sync(0xffffffffu, xx, 16);
-    const float xs = rsqrtf(xx + kL2Eps);
-#pragma unroll
-    for (int j = 0; j < D / 16; ++j)
-      *reinterpret_cast<float4 *>(QK + tc::core_off(64 * which + t, 4 * (cg + 4 * j), D)) =
-          scale4(xs, x4[j]);
-  }
-  if (cg == 0) {
-    sG[t] = gt;
-    sBeta[t] = bt;
   }
 }
 
@@ -760,17 +702,12 @@ constexpr int S_KT = S_PT + TILE * 4;          // Ktil^T tile [k][i], 128 x 64, 
                                                // [P; Ktil^T] is one 192-row B operand
 constexpr int S_TT = S_KT + D * C * 4;         // T tile (from the workspace)
 constexpr int S_SC = S_TT + TILE * 4;          // G, gamma, beta, e^{G_n - G}
-constexpr int S_RAW = S_SC + 4 * C * 4;        // raw bf16 q, k, v (tensor-map rows), or else
-                                               // beta v (plain 64 x XS float32)
-constexpr int kXUBytes = C * XS * 4;
-template <typename TI>
-constexpr int seq_smem() {
-  return S_RAW + (std::is_same<TI, bf16>::value ? kRawBytes : kXUBytes);
-}
-static_assert(kRawBytes >= kXUBytes && C * D * 4 <= S_PT - S_OS, "shared-memory regions");
-static_assert(S_PT % 16 == 0 && S_KT == S_PT + TILE * 4 && S_TT % 16 == 0 && S_RAW % 16 == 0,
+constexpr int S_XU = S_SC + 4 * C * 4;         // beta v (plain 64 x XS float32)
+constexpr int kSeqSmem = S_XU + C * XS * 4;
+static_assert(C * D * 4 <= S_PT - S_OS, "shared-memory regions");
+static_assert(S_PT % 16 == 0 && S_KT == S_PT + TILE * 4 && S_TT % 16 == 0 && S_XU % 16 == 0,
               "tile alignment");
-static_assert(S_RAW + kRawBytes <= 227 * 1024, "shared memory");
+static_assert(kSeqSmem <= 227 * 1024, "shared memory");
 
 // Roles in seq_kernel: warps 0..7 compute (warp w reads TMEM lanes
 // 32 (w % 4) .. +31, column half w / 4) and meet on named barrier 1; warp 8
@@ -821,15 +758,11 @@ template <typename TI, typename TO>
 __global__ void __launch_bounds__(NTS, 1)
     seq_kernel(PoolView p, int layer, SeqIndex seq, QKV in, TO *__restrict__ o, float scale,
                const int32_t *__restrict__ off, int64_t cap, const float *__restrict__ work,
-               const __grid_constant__ InMaps maps, int raw_rows, int raw_gb, Checkpoints ck) {
-  // bf16 rows that are 16-byte aligned: stage from a bulk copy made a chunk ahead
-  const bool RAW = std::is_same<TI, bf16>::value && raw_rows != 0;
+               Checkpoints ck) {
   extern __shared__ __align__(1024) unsigned char smem[];
   float *QK = reinterpret_cast<float *>(smem + S_QK);
   TO *OS = reinterpret_cast<TO *>(smem + S_OS);
-  float *XU = reinterpret_cast<float *>(smem + S_RAW);  // beta v when the rows are staged
-  unsigned char *RW = smem + S_RAW + ((1024u - (smem_addr(smem + S_RAW) & 1023u)) & 1023u);
-  const bool GB = RAW && raw_gb != 0;  // g, beta come with the tensor-map copies too
+  float *XU = reinterpret_cast<float *>(smem + S_XU);
   float *PT = reinterpret_cast<float *>(smem + S_PT);
   float *KT = reinterpret_cast<float *>(smem + S_KT);
   float *TT = reinterpret_cast<float *>(smem + S_TT);
@@ -838,7 +771,7 @@ __global__ void __launch_bounds__(NTS, 1)
   float *sBeta = sGam + C;
   float *sDte = sBeta + C;
   __shared__ __align__(8) uint64_t b_ed3, b_dd, b_upd;  // MMA groups done
-  __shared__ __align__(8) uint64_t tbar, rbar, vbar;     // P / T tiles, raw q k, raw v landed
+  __shared__ __align__(8) uint64_t tbar;                 // P / T tiles landed
   __shared__ __align__(8) uint64_t f_rdy, g_rdy, s_rdy;  // compute warps -> MMA warp
   __shared__ uint32_t tmem_slot;
   __shared__ int dead;  // set by the role that gave up waiting
@@ -877,8 +810,6 @@ __global__ void __launch_bounds__(NTS, 1)
     mbar_init(&b_dd, 1);
     mbar_init(&b_upd, 1);
     mbar_init(&tbar, 1);
-    mbar_init(&rbar, 1);
-    mbar_init(&vbar, 1);
     mbar_init(&f_rdy, 8);
     mbar_init(&g_rdy, 8);
     mbar_init(&s_rdy, 8);
@@ -1004,34 +935,14 @@ __global__ void __launch_bounds__(NTS, 1)
     const TI *qg = static_cast<const TI *>(in.q);
     const TI *kg = static_cast<const TI *>(in.k);
     const TI *vg = static_cast<const TI *>(in.v);
-    int n_r = 0, n_v = 0;  // raw q k and raw v loads armed
     bool alive = true;
-    float g_next = 0.f, b_next = 0.f;  // this thread's g, beta of the next chunk to stage (RAW)
 
-    // Stage chunk c0s into QK (and XU unless v comes by tensor map) and the
-    // scalars (then start fetching the next q, k), and form its cumulative
+    // Stage chunk c0s into QK, XU and the scalars, and form its cumulative
     // decays.  Ends with the tile writes fenced for the tensor core.
     auto stage_next = [&](int c0s) {
       const int ns = min(C, len - c0s);
-      if (RAW) {
-        alive = cw_and(alive && wait_live(&rbar, (c0s / C) & 1, vdead));
-        if (GB) {  // this head's column of the [64][8] g and beta tiles (padded tokens 0)
-          const int t = stage_token();
-          const bf16 *gt8 = reinterpret_cast<const bf16 *>(RW + kRawQKV);
-          g_next = t < ns ? __bfloat162float(gt8[t * 8 + (h & 7)]) : 0.f;
-          b_next = t < ns ? __bfloat162float(gt8[C * 8 + t * 8 + (h & 7)]) : 0.f;
-        }
-        stage_rows_raw(RW, ns, g_next, b_next, QK, sG, sBeta);
-      } else {
-        stage_chunk<TI, true>(in, p, h, hk, lo + c0s, ns, QK, XU, sG, sBeta);
-      }
+      stage_chunk<TI, true>(in, p, h, hk, lo + c0s, ns, QK, XU, sG, sBeta);
       cw_sync();
-      if (alive && RAW && c0s + C < len) {  // the raw copy is consumed: fetch the next chunk's
-        const int nn = min(C, len - c0s - C);
-        if (tid == kCopier) prefetch_qk(maps, GB, h, hk, lo + c0s + C, RW, &rbar);
-        ++n_r;
-        if (!GB) load_gb<TI>(in, p, h, lo + c0s + C, nn, g_next, b_next);
-      }
       if (warp == 7) {  // cumulative log-decay (padded tokens carry g = 0)
         const float a = sG[2 * lane], b = sG[2 * lane + 1];
         float incl = a + b;
@@ -1082,7 +993,7 @@ __global__ void __launch_bounds__(NTS, 1)
         *reinterpret_cast<float4 *>(KT + tc::core_off(4 * k4 + l4, ib, C)) = w;
       }
       const int t = tid & (C - 1);
-      const int64_t tok = lo + c0s + (RAW ? 3 * C : 2 * C) + t;
+      const int64_t tok = lo + c0s + 2 * C + t;
       if (tok < hi) {
         constexpr int LINES = (D * (int)sizeof(TI) + 127) / 128;
         const char *qr = reinterpret_cast<const char *>(qg + tok * in.ld_qk + (int64_t)hk * D);
@@ -1098,14 +1009,6 @@ __global__ void __launch_bounds__(NTS, 1)
 
     // chunk 0: stage it and hand it (with the state) to the MMA warp, then build
     // its Ktil^T while [D3 | E] runs
-    if (RAW) {
-      if (tid == kCopier) {
-        prefetch_qk(maps, GB, h, hk, lo, RW, &rbar);
-        prefetch_v(maps, h, lo, RW + 4 * kRawHalf, &vbar);
-      }
-      n_r = n_v = 1;
-      if (!GB) load_gb<TI>(in, p, h, lo, min(C, len), g_next, b_next);
-    }
     stage_next(0);
     alive = cw_and(alive);
     if (alive) warp_arrive(&s_rdy);
@@ -1119,8 +1022,7 @@ __global__ void __launch_bounds__(NTS, 1)
       const uint32_t par = c & 1;
       const int n = min(C, len - c0);
       const bool last = c + 1 == nch;
-      alive = cw_and(wait_live(&b_ed3, par, vdead) &&    // [D3 | E] done, v landed
-                     (!RAW || wait_live(&vbar, par, vdead)));
+      alive = cw_and(wait_live(&b_ed3, par, vdead));  // [D3 | E] done
       if (!alive) break;
       tc::fence_after_sync();
 
@@ -1129,9 +1031,6 @@ __global__ void __launch_bounds__(NTS, 1)
       const int i0 = 32 * half;
       {
         const int v = row;
-        // element (t, v) of the raw v tile: half v / 64, 128-byte row t, swizzled 16-byte piece
-        const unsigned char *vr = RW + (4 + (v >> 6)) * kRawHalf + (v & 7) * 2;
-        const int vpiece = (v & 63) >> 3;
         // this thread's 32 columns of E and D3, all four loads under one wait
         float e[32], d3[32];
         tc::tmem_ld16x4(lrow + T_E + i0, lrow + T_E + i0 + 16, lrow + T_D3 + i0,
@@ -1144,14 +1043,7 @@ __global__ void __launch_bounds__(NTS, 1)
           for (int j = 0; j < 16; ++j) {
             const int t = t0 + j;
             dd[j] = d3[16 * cb + j] * sGam[t];
-            float bv;  // beta_t v_t[v] (0 for padded tokens)
-            if (RAW) {
-              const uint32_t u = *reinterpret_cast<const unsigned short *>(
-                  vr + t * 128 + ((vpiece ^ (t & 7)) << 4));
-              bv = t < n ? sBeta[t] * __uint_as_float(u << 16) : 0.f;
-            } else {
-              bv = XU[t * XS + v];
-            }
+            const float bv = XU[t * XS + v];  // beta_t v_t[v] (0 for padded tokens)
             f[j] = bv - sBeta[t] * sGam[t] * e[16 * cb + j];
           }
           tc::tmem_st16(lrow + T_F + t0, f);
@@ -1177,11 +1069,7 @@ __global__ void __launch_bounds__(NTS, 1)
       warp_arrive(&g_rdy);  // (this chunk's Ktil^T was fenced when it was built)
 
       if (!last) {
-        cw_sync();  // every warp is past its reads of v (XU), gamma and beta
-        if (RAW && alive) {  // the raw v tile is free: fetch the next chunk's
-          if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RW + 4 * kRawHalf, &vbar);
-          ++n_v;
-        }
+        cw_sync();  // every warp is past its reads of XU, gamma and beta
         stage_next(c0 + C);
         if (alive) warp_arrive(&s_rdy);
       }
@@ -1251,11 +1139,6 @@ __global__ void __launch_bounds__(NTS, 1)
     } else {
       *vdead = 1;
       if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
-      // raw-row loads still in flight land before shared memory is released
-      if (RAW && tid == kCopier) {
-        if (n_r > 0) mbar_wait_bounded(&rbar, (n_r - 1) & 1);
-        if (n_v > 0) mbar_wait_bounded(&vbar, (n_v - 1) & 1);
-      }
     }
   }
   tc::fence_before_sync();
@@ -1911,13 +1794,11 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
         om ? 1 : 0, ck);
     return cudaGetLastError();
   }
-  auto kern = seq_kernel<TI, TO>;
-  constexpr int smem = seq_smem<TI>();
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = seq_kernel<TI, TO>;  // rows staged from global memory
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSeqSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(p.h_v, seq.n_seqs), NTS, smem, s>>>(p, layer, seq, in, static_cast<TO *>(o),
-                                                     scale, off, nc, tiles, maps, raw ? 1 : 0,
-                                                     gb ? 1 : 0, ck);
+  kern<<<dim3(p.h_v, seq.n_seqs), NTS, kSeqSmem, s>>>(p, layer, seq, in, static_cast<TO *>(o),
+                                                         scale, off, nc, tiles, ck);
   return cudaGetLastError();
 }
 
