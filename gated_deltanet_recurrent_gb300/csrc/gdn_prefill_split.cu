@@ -458,6 +458,9 @@ __global__ void __launch_bounds__(NT, 2)
   __shared__ __align__(8) uint64_t lbar;   // tensor-map copies of q, k
   __shared__ uint32_t tmem_slot;
 
+  // the state kernel may start its prologue now (it waits for this grid
+  // before it reads the workspace)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int cidx = blockIdx.x;
   if (cidx >= off[seq.n_seqs]) return;
   int si = 0;  // the sequence holding chunk cidx: the last i with off[i] <= cidx
@@ -1312,6 +1315,8 @@ __global__ void __launch_bounds__(NTS, 1)
       __syncwarp();
     };
     int n_ed3 = 0, n_dd = 0, n_upd = 0, n_t = 1;  // groups issued, tile loads armed
+    // the key-side grid has written the tiles (this launch may start before it ends)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     load_tiles(0);
     bool ok = all_lanes(wait_live(&s_rdy, 0, vdead) && wait_live(&rbar[0], 0, vdead));
     if (ok) {
@@ -1391,13 +1396,19 @@ __global__ void __launch_bounds__(NTS, 1)
     bool alive = true;
     float g_next = 0.f, b_next = 0.f;  // this thread's g, beta of the next chunk (without GB)
 
-    // copier: q, k (g, beta) of chunk c into buffer c % 2
-    auto fetch_qk = [&](int c) {
+    // copier: q, k (g, beta) of chunk c into buffer c % 2, with the chunk's norms
+    // from the key-side kernel (norms = false: the caller copies them later)
+    auto fetch_norms = [&](int c) {
+      if (tid == kCopier)
+        bulk_g2s(NB + (c & 1) * 2 * C, wnorm + (int64_t)c * p.h_k * (2 * C), 2 * C * 4,
+                 &rbar[c & 1]);
+    };
+    auto fetch_qk = [&](int c, bool norms) {
       const int b = c & 1;
       if (tid == kCopier) {
         prefetch_qk_pairs(maps, GB, h, hk, lo + (int64_t)c * C, RQK + b * kQKBuf,
                           RGB + b * 2 * kRawGB, &rbar[b], 2 * C * 4);
-        bulk_g2s(NB + b * 2 * C, wnorm + (int64_t)c * p.h_k * (2 * C), 2 * C * 4, &rbar[b]);
+        if (norms) fetch_norms(c);
       }
       if (b) ++n_r1; else ++n_r0;
     };
@@ -1605,8 +1616,13 @@ __global__ void __launch_bounds__(NTS, 1)
     // state and Ktil^T to the MMA warp
     if (tid == kCopier) prefetch_v(maps, h, lo, RV, &vbar);
     n_v = 1;
-    fetch_qk(0);
-    if (nch > 1) fetch_qk(1);
+    fetch_qk(0, false);
+    if (nch > 1) fetch_qk(1, false);
+    if (tid == kCopier) {  // the norms come from the key-side grid: wait for it first
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      fetch_norms(0);
+      if (nch > 1) fetch_norms(1);
+    }
     if (!GB) load_gb<bf16>(in, p, h, lo, min(C, len), g_next, b_next);
     stage_scalars(0);
     if (!GB && nch > 1) load_gb<bf16>(in, p, h, lo + C, min(C, len - C), g_next, b_next);
@@ -1629,7 +1645,7 @@ __global__ void __launch_bounds__(NTS, 1)
                      wait_live(&vbar, par, vdead));
       if (!alive) break;
       tc::fence_after_sync();
-      if (c + 2 < nch) fetch_qk(c + 2);  // buffer c % 2 is free: [D3 | E] and Ktil^T are done
+      if (c + 2 < nch) fetch_qk(c + 2, true);  // buffer c % 2 is free: [D3 | E], Ktil^T done
 
       const int i0 = 32 * half;
       if (n == C) f_pass(std::true_type(), n, i0, u_d4(c));
@@ -1789,10 +1805,21 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
     auto kern = seq_bf16_kernel<TO>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSeqBf16Smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(p.h_v, seq.n_seqs), NTS, kSeqBf16Smem, s>>>(
-        p, layer, seq, in, static_cast<TO *>(o), scale, off, nc, tiles, maps, gb ? 1 : 0,
-        om ? 1 : 0, ck);
-    return cudaGetLastError();
+    // a programmatic dependent of the key-side kernel: its prologue (state
+    // load, first row copies) overlaps that kernel's tail
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.h_v, seq.n_seqs);
+    cfg.blockDim = dim3(NTS);
+    cfg.dynamicSmemBytes = kSeqBf16Smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, layer, seq, in, static_cast<TO *>(o), scale,
+                              static_cast<const int32_t *>(off), nc,
+                              static_cast<const float *>(tiles), maps, gb ? 1 : 0, om ? 1 : 0, ck);
   }
   auto kern = seq_kernel<TI, TO>;  // rows staged from global memory
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSeqSmem);
