@@ -437,14 +437,19 @@ constexpr int prep_smem() {  // + 1024: the tile is aligned to 1024 bytes inside
 static_assert(2 * (prep_smem<bf16>() + 1024 + 64) <= 228 * 1024, "two bf16 prep CTAs per SM");
 static_assert(prep_smem<float>() <= 227 * 1024, "shared memory");
 
-// One CTA per (chunk, key head, pair of the value heads that read that key
-// head).  Both warpgroups share the staged [Q;K] tile and the Gram product
-// D1 = [Q;K] K^T; warpgroup wg then forms P and A for value head 2 pair + wg
-// of the group and inverts I + A.
+// Persistent: each CTA takes the work items blockIdx.x, blockIdx.x + gridDim.x,
+// ... of the call, item = (chunk, key head, pair of the value heads that read
+// that key head), chunk-major.  Both warpgroups share the staged [Q;K] tile
+// and the Gram product D1 = [Q;K] K^T; warpgroup wg then forms P and A for
+// value head 2 pair + wg of the group and inverts I + A.  Once the Gram MMA
+// has read the tile, the next item's q/k copies (tensor-map rows) and its g,
+// beta loads are issued, so they land while this item's P, A and T are formed.
+// nc: the chunk capacity of the workspace (where the norms start).
 template <typename TI>
 __global__ void __launch_bounds__(NT, 2)
     prep_kernel(PoolView p, SeqIndex seq, QKV in, const int32_t *__restrict__ off,
-                float *__restrict__ work, const __grid_constant__ InMaps maps, int raw_rows) {
+                float *__restrict__ work, int64_t nc, const __grid_constant__ InMaps maps,
+                int raw_rows) {
   constexpr bool B16 = std::is_same<TI, bf16>::value;  // raw bf16 tile, kind::f16
   // 16-byte aligned bf16 rows: the tile arrives by tensor-map copies in the 128-byte
   // swizzle, two K halves [Q;K] x 64 columns (16 KiB each), read by swizzled descriptors
@@ -461,29 +466,62 @@ __global__ void __launch_bounds__(NT, 2)
   // the state kernel may start its prologue now (it waits for this grid
   // before it reads the workspace)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int cidx = blockIdx.x;
-  if (cidx >= off[seq.n_seqs]) return;
-  int si = 0;  // the sequence holding chunk cidx: the last i with off[i] <= cidx
-  for (int b = seq.n_seqs - 1; si < b;) {
-    const int m = (si + b + 1) >> 1;
-    if (off[m] <= cidx) si = m; else b = m - 1;
-  }
-  const int64_t lo = seq.cu_seqlens[si], hi = seq.cu_seqlens[si + 1];
-  const int c0 = (cidx - off[si]) * C;
-  const int64_t rest = hi - lo - c0;
-  const int n = rest < C ? (int)rest : C;
-  const int64_t tok0 = lo + c0;
   const int G = p.h_v / p.h_k, npair = (G + 1) / 2;
-  const int kh = blockIdx.y / npair, pair = blockIdx.y % npair;
+  const int ny = p.h_k * npair;
+  const int64_t items = (int64_t)off[seq.n_seqs] * ny;
+  if ((int64_t)blockIdx.x >= items) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wg = warp >> 2, quad = warp & 3, tt = tid & 127;
-  const bool live = 2 * pair + wg < G;  // this warpgroup has a value head
-  const int h = kh * G + (live ? 2 * pair + wg : 0);
   float *AP = heads + wg * kHeadFloats;
   float *TP = AP + C * AS;
   float *XS_ = TP + C * AS;
   float *sG = XS_ + 1024;
   float *sBeta = sG + C;
+
+  // work item -> chunk, its sequence's token range, key head, pair
+  struct Item {
+    int cidx, n, kh, pair;
+    int64_t tok0;
+  };
+  auto locate = [&](int64_t it) {
+    Item w;
+    w.cidx = (int)(it / ny);
+    const int y = (int)(it % ny);
+    w.kh = y / npair;
+    w.pair = y % npair;
+    int si = 0;  // the sequence holding the chunk: the last i with off[i] <= cidx
+    for (int b = seq.n_seqs - 1; si < b;) {
+      const int m = (si + b + 1) >> 1;
+      if (off[m] <= w.cidx) si = m; else b = m - 1;
+    }
+    const int64_t lo = seq.cu_seqlens[si], hi = seq.cu_seqlens[si + 1];
+    const int c0 = (w.cidx - off[si]) * C;
+    const int64_t rest = hi - lo - c0;
+    w.n = rest < C ? (int)rest : C;
+    w.tok0 = lo + c0;
+    return w;
+  };
+  auto head_of = [&](const Item &w) {
+    const bool lv = 2 * w.pair + wg < G;  // this warpgroup has a value head
+    return w.kh * G + (lv ? 2 * w.pair + wg : 0);
+  };
+  // thread tt < C of each warpgroup: its head's g and beta of token tt (padded 0)
+  auto load_gb1 = [&](const Item &w, float &gt, float &bt) {
+    gt = bt = 0.f;
+    if (tt < w.n && 2 * w.pair + wg < G) {
+      const int h = head_of(w);
+      gt = Elem<TI>::load1(static_cast<const TI *>(in.g) + (w.tok0 + tt) * p.h_v + h);
+      bt = Elem<TI>::load1(static_cast<const TI *>(in.beta) + (w.tok0 + tt) * p.h_v + h);
+    }
+  };
+  auto issue_rows = [&](const Item &w) {  // one thread
+    mbar_arrive_expect_tx(&lbar, 4 * kRawHalf);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      tma3(tile + hf * 2 * kRawHalf, &maps.q, 64 * hf, w.kh, (int)w.tok0, &lbar);
+      tma3(tile + hf * 2 * kRawHalf + kRawHalf, &maps.k, 64 * hf, w.kh, (int)w.tok0, &lbar);
+    }
+  };
 
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 64);
   if (tid == 0) {
@@ -491,208 +529,233 @@ __global__ void __launch_bounds__(NT, 2)
     mbar_init(&lbar, 1);
     mbar_fence_init();
   }
-  if (TMAQK) {
-    __syncthreads();
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&lbar, 4 * kRawHalf);
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        tma3(tile + hf * 2 * kRawHalf, &maps.q, 64 * hf, kh, (int)tok0, &lbar);
-        tma3(tile + hf * 2 * kRawHalf + kRawHalf, &maps.k, 64 * hf, kh, (int)tok0, &lbar);
-      }
-    }
-  }
   for (int e = tt; e < C * C; e += 128) {  // T's strictly-upper 16 x 16 blocks stay zero
     const int r = e / C, c = e % C;
     if ((c >> 4) > (r >> 4)) TP[r * AS + c] = 0.f;
   }
-  if (tt < C) {  // this head's g and beta (padded tokens 0)
-    float gt = 0.f, bt = 0.f;
-    if (live && tt < n) {
-      gt = Elem<TI>::load1(static_cast<const TI *>(in.g) + (tok0 + tt) * p.h_v + h);
-      bt = Elem<TI>::load1(static_cast<const TI *>(in.beta) + (tok0 + tt) * p.h_v + h);
-    }
-    sG[tt] = gt;
-    sBeta[tt] = bt;
-  }
-  const TI *q0 = static_cast<const TI *>(in.q) + tok0 * in.ld_qk + (int64_t)kh * D;
-  const TI *k0 = static_cast<const TI *>(in.k) + tok0 * in.ld_qk + (int64_t)kh * D;
-  bool loaded = true;
-  if (TMAQK) {  // norms of the tensor-map rows, summed in stage_qk_bf16's order
-    loaded = mbar_wait_bounded(&lbar, 0);
-    const int t = stage_token(), part = lane >> 3;
-    float qq = 0.f, kk = 0.f;
-    if (loaded) {
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int c = part + 4 * m;                  // elements 4c .. 4c+3
-        const int col = (4 * c) & 63, hf = (4 * c) >> 6;
-        const int off8 = t * 128 + ((((col >> 3) ^ (t & 7))) << 4) + (col & 7) * 2;
-        const uint2 qv = *reinterpret_cast<const uint2 *>(tile + hf * 2 * kRawHalf + off8);
-        const uint2 kv = *reinterpret_cast<const uint2 *>(tile + hf * 2 * kRawHalf + kRawHalf + off8);
-        const float a0 = __uint_as_float(qv.x << 16), a1 = __uint_as_float(qv.x & 0xffff0000u);
-        const float a2 = __uint_as_float(qv.y << 16), a3 = __uint_as_float(qv.y & 0xffff0000u);
-        const float b0 = __uint_as_float(kv.x << 16), b1 = __uint_as_float(kv.x & 0xffff0000u);
-        const float b2 = __uint_as_float(kv.y << 16), b3 = __uint_as_float(kv.y & 0xffff0000u);
-        qq += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
-        kk += b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
-      }
-    }
-    qq += __shfl_xor_sync(0xffffffffu, qq, 8);
-    qq += __shfl_xor_sync(0xffffffffu, qq, 16);
-    kk += __shfl_xor_sync(0xffffffffu, kk, 8);
-    kk += __shfl_xor_sync(0xffffffffu, kk, 16);
-    if (part == 0) {
-      rq[t] = rsqrtf(qq + kL2Eps);
-      rk[t] = rsqrtf(kk + kL2Eps);
-    }
-  } else if constexpr (B16) {
-    stage_qk_bf16(q0, k0, in.ld_qk, n, tile, rq, rk);
-  } else {
-    // normalised float32 rows; rq = rk = 1 (written through the g / beta slots)
-    stage_rows<TI, false>(q0, k0, nullptr, in.ld_qk, 0, n, 1.f, 1.f,
-                          reinterpret_cast<float *>(tile), nullptr, rq, rk);
-  }
-  __syncthreads();
-  if (TMAQK && pair == 0 && tid < 2 * C) {  // 1/|q_t|, 1/|k_t| for the state kernel
-    float *nb = work + (int64_t)gridDim.x * p.h_v * (2 * TILE) +
-                ((int64_t)cidx * p.h_k + kh) * (2 * C);
-    nb[tid] = tid < C ? rq[tid] : rk[tid - C];
-  }
-  if (quad == 0 && tt < 32) {  // warp 4 wg: cumulative log-decay of this head
-    const float a = sG[2 * lane], b = sG[2 * lane + 1];
-    float incl = a + b;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float up = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += up;
-    }
-    sG[2 * lane] = incl - b;
-    sG[2 * lane + 1] = incl;
-    // cf[i] = e^{G_e - G_i} / |k_i|, e the last token of i's 16-token block (so at
-    // most 1 / |k_i|): the column factor of P and A left of the diagonal blocks
-    const float Ge = __shfl_sync(0xffffffffu, incl, (lane & ~7) | 7);
-    XS_[2 * lane] = rk[2 * lane] * __expf(Ge - (incl - b));
-    XS_[2 * lane + 1] = rk[2 * lane + 1] * __expf(Ge - incl);
-  }
-  tc::fence_async_smem();
+  Item w = locate(blockIdx.x);
+  float g_nx = 0.f, b_nx = 0.f;  // the next item's g, beta (threads tt < C)
+  load_gb1(w, g_nx, b_nx);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tm = tmem_slot;
   const uint32_t lrow = tm + ((uint32_t)(32 * quad) << 16);
+  if (TMAQK && tid == 0) issue_rows(w);
 
-  // D1 = [Q;K] K^T  (M 128, N 64, K 128)
-  if (!__syncthreads_and(loaded)) {  // the q, k copies never landed
-    if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
-    mbar_wait_bounded(&lbar, 0);
-    if (warp == 0) tc::tmem_dealloc(tmem_slot, 64);
-    return;
-  }
-  if (tid == 0) {
-    const uint32_t a_s = smem_addr(tile);
-    constexpr uint32_t KSTEP = 2 * tc::kLBO;
-    if (TMAQK) {  // K halves of 64: 4 steps of 16 (32 bytes) inside each 128-byte row
+  bool ok = true;        // every wait so far completed
+  bool pending = TMAQK;  // a row copy onto lbar is in flight
+  bool mma_out = false;  // a Gram MMA onto bar is in flight
+  uint32_t ph = 0;       // phase of bar and lbar for this item
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x, ph ^= 1u) {
+    const int cidx = w.cidx, n = w.n;
+    const int64_t tok0 = w.tok0;
+    const int kh = w.kh, pair = w.pair;
+    const bool live = 2 * pair + wg < G;
+    const int h = head_of(w);
+    if (tt < C) {
+      sG[tt] = g_nx;
+      sBeta[tt] = b_nx;
+    }
+    const TI *q0 = static_cast<const TI *>(in.q) + tok0 * in.ld_qk + (int64_t)kh * D;
+    const TI *k0 = static_cast<const TI *>(in.k) + tok0 * in.ld_qk + (int64_t)kh * D;
+    bool loaded = true;
+    if (TMAQK) {  // norms of the tensor-map rows, summed in stage_qk_bf16's order
+      loaded = mbar_wait_bounded(&lbar, ph);
+      const int t = stage_token(), part = lane >> 3;
+      float qq = 0.f, kk = 0.f;
+      if (loaded) {
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tc::mma_ss_f16(tm, tc::smem_desc_sw128(a_s + hf * 2 * kRawHalf + 32 * j),
-                         tc::smem_desc_sw128(a_s + hf * 2 * kRawHalf + kRawHalf + 32 * j),
-                         tc::idesc_bf16(128, 64), (hf | j) != 0);
+        for (int m = 0; m < 8; ++m) {
+          const int c = part + 4 * m;                  // elements 4c .. 4c+3
+          const int col = (4 * c) & 63, hf = (4 * c) >> 6;
+          const int off8 = t * 128 + ((((col >> 3) ^ (t & 7))) << 4) + (col & 7) * 2;
+          const uint2 qv = *reinterpret_cast<const uint2 *>(tile + hf * 2 * kRawHalf + off8);
+          const uint2 kv =
+              *reinterpret_cast<const uint2 *>(tile + hf * 2 * kRawHalf + kRawHalf + off8);
+          const float a0 = __uint_as_float(qv.x << 16), a1 = __uint_as_float(qv.x & 0xffff0000u);
+          const float a2 = __uint_as_float(qv.y << 16), a3 = __uint_as_float(qv.y & 0xffff0000u);
+          const float b0 = __uint_as_float(kv.x << 16), b1 = __uint_as_float(kv.x & 0xffff0000u);
+          const float b2 = __uint_as_float(kv.y << 16), b3 = __uint_as_float(kv.y & 0xffff0000u);
+          qq += a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+          kk += b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
+        }
+      }
+      qq += __shfl_xor_sync(0xffffffffu, qq, 8);
+      qq += __shfl_xor_sync(0xffffffffu, qq, 16);
+      kk += __shfl_xor_sync(0xffffffffu, kk, 8);
+      kk += __shfl_xor_sync(0xffffffffu, kk, 16);
+      if (part == 0) {
+        rq[t] = rsqrtf(qq + kL2Eps);
+        rk[t] = rsqrtf(kk + kL2Eps);
+      }
     } else if constexpr (B16) {
-      constexpr uint32_t SBO = tc::sbo_bytes16(D);
-      const uint32_t b_s = a_s + 8 * SBO;
-#pragma unroll
-      for (int j = 0; j < D / 16; ++j)
-        tc::mma_ss_f16(tm, tc::smem_desc(a_s + j * KSTEP, tc::kLBO, SBO),
-                       tc::smem_desc(b_s + j * KSTEP, tc::kLBO, SBO), tc::idesc_bf16(128, 64),
-                       j > 0);
+      stage_qk_bf16(q0, k0, in.ld_qk, n, tile, rq, rk);
     } else {
-      constexpr uint32_t SBO = tc::sbo_bytes(D);
-      const uint32_t b_s = a_s + 8 * SBO;
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j)
-        tc::mma_ss(tm, tc::smem_desc(a_s + j * KSTEP, tc::kLBO, SBO),
-                   tc::smem_desc(b_s + j * KSTEP, tc::kLBO, SBO), tc::idesc_tf32(128, 64), j > 0);
+      // normalised float32 rows; rq = rk = 1 (written through the g / beta slots)
+      stage_rows<TI, false>(q0, k0, nullptr, in.ld_qk, 0, n, 1.f, 1.f,
+                            reinterpret_cast<float *>(tile), nullptr, rq, rk);
     }
-    tc::mma_commit(&bar);
+    if (!__syncthreads_and(loaded)) {  // the q, k copies never landed
+      ok = false;
+      break;
+    }
+    pending = false;
+    if (TMAQK && pair == 0 && tid < 2 * C) {  // 1/|q_t|, 1/|k_t| for the state kernel
+      float *nb = work + nc * p.h_v * (2 * TILE) + ((int64_t)cidx * p.h_k + kh) * (2 * C);
+      nb[tid] = tid < C ? rq[tid] : rk[tid - C];
+    }
+    if (quad == 0 && tt < 32) {  // warp 4 wg: cumulative log-decay of this head
+      const float a = sG[2 * lane], b = sG[2 * lane + 1];
+      float incl = a + b;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float up = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += up;
+      }
+      sG[2 * lane] = incl - b;
+      sG[2 * lane + 1] = incl;
+      // cf[i] = e^{G_e - G_i} / |k_i|, e the last token of i's 16-token block (so at
+      // most 1 / |k_i|): the column factor of P and A left of the diagonal blocks
+      const float Ge = __shfl_sync(0xffffffffu, incl, (lane & ~7) | 7);
+      XS_[2 * lane] = rk[2 * lane] * __expf(Ge - (incl - b));
+      XS_[2 * lane + 1] = rk[2 * lane + 1] * __expf(Ge - incl);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // D1 = [Q;K] K^T  (M 128, N 64, K 128)
+    if (tid == 0) {
+      const uint32_t a_s = smem_addr(tile);
+      constexpr uint32_t KSTEP = 2 * tc::kLBO;
+      if (TMAQK) {  // K halves of 64: 4 steps of 16 (32 bytes) inside each 128-byte row
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tc::mma_ss_f16(tm, tc::smem_desc_sw128(a_s + hf * 2 * kRawHalf + 32 * j),
+                           tc::smem_desc_sw128(a_s + hf * 2 * kRawHalf + kRawHalf + 32 * j),
+                           tc::idesc_bf16(128, 64), (hf | j) != 0);
+      } else if constexpr (B16) {
+        constexpr uint32_t SBO = tc::sbo_bytes16(D);
+        const uint32_t b_s = a_s + 8 * SBO;
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j)
+          tc::mma_ss_f16(tm, tc::smem_desc(a_s + j * KSTEP, tc::kLBO, SBO),
+                         tc::smem_desc(b_s + j * KSTEP, tc::kLBO, SBO), tc::idesc_bf16(128, 64),
+                         j > 0);
+      } else {
+        constexpr uint32_t SBO = tc::sbo_bytes(D);
+        const uint32_t b_s = a_s + 8 * SBO;
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j)
+          tc::mma_ss(tm, tc::smem_desc(a_s + j * KSTEP, tc::kLBO, SBO),
+                     tc::smem_desc(b_s + j * KSTEP, tc::kLBO, SBO), tc::idesc_tf32(128, 64),
+                     j > 0);
+      }
+      tc::mma_commit(&bar);
+    }
+    mma_out = true;
+    const bool alive = __syncthreads_and(mbar_wait_bounded(&bar, ph));
+    tc::fence_after_sync();
+    if (!alive) {
+      ok = false;
+      break;
+    }
+    mma_out = false;
+    // the tile is free again: the next item's rows and scalars travel under this one
+    const int64_t nx = it + gridDim.x;
+    if (nx < items) {
+      w = locate(nx);
+      if (TMAQK) pending = true;
+      if (TMAQK && tid == 0) issue_rows(w);
+      load_gb1(w, g_nx, b_nx);
+    }
+    float *Pg = work + ((int64_t)cidx * p.h_v + h) * (2 * TILE);
+    float *Tg = Pg + TILE;
+    if (live) {
+      // rows 0..63: P[t][i] = e^{G_t - G_i} q~_t.k~_i (i <= t), to the workspace;
+      // rows 64..127: A[t][i] = beta_t e^{G_t - G_i} k~_t.k~_i (i < t), to smem.
+      // Warp w (w % 2 = q2) holds rows t = 32 q2 .. 32 q2 + 31 of one of them.
+      // Columns of the 16-token blocks left of its rows (q2 = 1: i < 32) take
+      // e^{G_t - G_i} = e^{G_t - G_e} e^{G_e - G_i} with e the block's last token
+      // (both factors at most 1, so no overflow at any decay); the warp's own 32
+      // columns take the exact exponential; columns right of them are zero.
+      const int row = 32 * quad + lane;
+      const bool isA = quad >= 2;
+      const int t = isA ? row - 64 : row;
+      const int q2 = quad & 1;
+      const float sc = isA ? sBeta[t] * rk[t] : rq[t];
+      const float gt = sG[t];
+      const float *cf = XS_;
+      auto put = [&](int i, float4 x) {
+        if (isA) *reinterpret_cast<float4 *>(AP + t * AS + i) = x;
+        else *reinterpret_cast<float4 *>(Pg + tc::core_off(t, i, C)) = x;
+      };
+      if (q2 == 1) {
+        const float rf0 = sc * __expf(gt - sG[15]), rf1 = sc * __expf(gt - sG[31]);
+        float v2[32];
+        tc::tmem_ld32(lrow, lrow + 16, v2);
+#pragma unroll
+        for (int j2 = 0; j2 < 32; j2 += 4) {
+          const float rf = j2 < 16 ? rf0 : rf1;
+          const float4 c4 = *reinterpret_cast<const float4 *>(cf + j2);
+          put(j2, make_float4(rf * c4.x * v2[j2], rf * c4.y * v2[j2 + 1], rf * c4.z * v2[j2 + 2],
+                              rf * c4.w * v2[j2 + 3]));
+        }
+      }
+      {
+        const int cb = 32 * q2;
+        const int lim = isA ? t : t + 1;  // columns i < lim are kept
+        float v2[32];
+        tc::tmem_ld32(lrow + cb, lrow + cb + 16, v2);
+#pragma unroll
+        for (int j2 = 0; j2 < 32; j2 += 4) {
+          const int i = cb + j2;
+          const float4 r4 = *reinterpret_cast<const float4 *>(rk + i);
+          const float4 g4 = *reinterpret_cast<const float4 *>(sG + i);
+          float4 x;
+          x.x = i + 0 < lim ? sc * r4.x * __expf(gt - g4.x) * v2[j2 + 0] : 0.f;
+          x.y = i + 1 < lim ? sc * r4.y * __expf(gt - g4.y) * v2[j2 + 1] : 0.f;
+          x.z = i + 2 < lim ? sc * r4.z * __expf(gt - g4.z) * v2[j2 + 2] : 0.f;
+          x.w = i + 3 < lim ? sc * r4.w * __expf(gt - g4.w) * v2[j2 + 3] : 0.f;
+          put(i, x);
+        }
+      }
+      if (q2 == 0 && !isA) {  // P's zero columns 32..63 (A's upper part is never read)
+#pragma unroll
+        for (int j2 = 0; j2 < 32; j2 += 4) put(32 + j2, make_float4(0.f, 0.f, 0.f, 0.f));
+      }
+    }
+    // D1 is read out (the next Gram product overwrites it), and every thread is
+    // past its reads of rq, rk and the tile before the next item rewrites them
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (live) {
+      invert_unit_lower(AP, TP, XS_, tt, 1 + wg);
+#pragma unroll
+      for (int i4 = 0; i4 < C * (C / 4) / 128; ++i4) {  // T tile [t][i] -> workspace
+        const int e = tt + 128 * i4;
+        const int t = e % C, c4 = e / C;
+        *reinterpret_cast<float4 *>(Tg + tc::core_off(t, 4 * c4, C)) =
+            *reinterpret_cast<const float4 *>(TP + t * AS + 4 * c4);
+      }
+    }
   }
-  const bool alive = __syncthreads_and(mbar_wait_bounded(&bar, 0));
-  tc::fence_after_sync();
-  float *Pg = work + ((int64_t)cidx * p.h_v + h) * (2 * TILE);
-  float *Tg = Pg + TILE;
-  if (alive && live) {
-    // rows 0..63: P[t][i] = e^{G_t - G_i} q~_t.k~_i (i <= t), to the workspace;
-    // rows 64..127: A[t][i] = beta_t e^{G_t - G_i} k~_t.k~_i (i < t), to smem.
-    // Warp w (w % 2 = q2) holds rows t = 32 q2 .. 32 q2 + 31 of one of them.
-    // Columns of the 16-token blocks left of its rows (q2 = 1: i < 32) take
-    // e^{G_t - G_i} = e^{G_t - G_e} e^{G_e - G_i} with e the block's last token
-    // (both factors at most 1, so no overflow at any decay); the warp's own 32
-    // columns take the exact exponential; columns right of them are zero.
-    const int row = 32 * quad + lane;
-    const bool isA = quad >= 2;
-    const int t = isA ? row - 64 : row;
-    const int q2 = quad & 1;
-    const float sc = isA ? sBeta[t] * rk[t] : rq[t];
-    const float gt = sG[t];
-    const float *cf = XS_;
-    auto put = [&](int i, float4 x) {
-      if (isA) *reinterpret_cast<float4 *>(AP + t * AS + i) = x;
-      else *reinterpret_cast<float4 *>(Pg + tc::core_off(t, i, C)) = x;
-    };
-    if (q2 == 1) {
-      const float rf0 = sc * __expf(gt - sG[15]), rf1 = sc * __expf(gt - sG[31]);
-      float v2[32];
-      tc::tmem_ld32(lrow, lrow + 16, v2);
-#pragma unroll
-      for (int j2 = 0; j2 < 32; j2 += 4) {
-        const float rf = j2 < 16 ? rf0 : rf1;
-        const float4 c4 = *reinterpret_cast<const float4 *>(cf + j2);
-        put(j2, make_float4(rf * c4.x * v2[j2], rf * c4.y * v2[j2 + 1], rf * c4.z * v2[j2 + 2],
-                            rf * c4.w * v2[j2 + 3]));
-      }
-    }
-    {
-      const int cb = 32 * q2;
-      const int lim = isA ? t : t + 1;  // columns i < lim are kept
-      float v2[32];
-      tc::tmem_ld32(lrow + cb, lrow + cb + 16, v2);
-#pragma unroll
-      for (int j2 = 0; j2 < 32; j2 += 4) {
-        const int i = cb + j2;
-        const float4 r4 = *reinterpret_cast<const float4 *>(rk + i);
-        const float4 g4 = *reinterpret_cast<const float4 *>(sG + i);
-        float4 x;
-        x.x = i + 0 < lim ? sc * r4.x * __expf(gt - g4.x) * v2[j2 + 0] : 0.f;
-        x.y = i + 1 < lim ? sc * r4.y * __expf(gt - g4.y) * v2[j2 + 1] : 0.f;
-        x.z = i + 2 < lim ? sc * r4.z * __expf(gt - g4.z) * v2[j2 + 2] : 0.f;
-        x.w = i + 3 < lim ? sc * r4.w * __expf(gt - g4.w) * v2[j2 + 3] : 0.f;
-        put(i, x);
-      }
-    }
-    if (q2 == 0 && !isA) {  // P's zero columns 32..63 (A's upper part is never read)
-#pragma unroll
-      for (int j2 = 0; j2 < 32; j2 += 4) put(32 + j2, make_float4(0.f, 0.f, 0.f, 0.f));
-    }
-  } else if (!alive) {
+  if (!ok) {
     if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
-    mbar_wait_bounded(&bar, 0);  // a second bounded chance before TMEM is released
+    // a second bounded chance for copies and MMAs in flight before TMEM and
+    // shared memory are released
+    if (pending) mbar_wait_bounded(&lbar, ph);
+    if (mma_out) mbar_wait_bounded(&bar, ph);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tm, 64);
-  if (!alive || !live) return;
-
-  invert_unit_lower(AP, TP, XS_, tt, 1 + wg);
-#pragma unroll
-  for (int it = 0; it < C * (C / 4) / 128; ++it) {  // T tile [t][i] -> workspace
-    const int e = tt + 128 * it;
-    const int t = e % C, c4 = e / C;
-    *reinterpret_cast<float4 *>(Tg + tc::core_off(t, 4 * c4, C)) =
-        *reinterpret_cast<const float4 *>(TP + t * AS + 4 * c4);
-  }
 }
 
 // --------------------------------------------------------------- state side
@@ -1627,15 +1690,12 @@ __global__ void __launch_bounds__(NTS, 1)
     stage_scalars(0);
     if (!GB && nch > 1) load_gb<bf16>(in, p, h, lo + C, min(C, len - C), g_next, b_next);
     alive = cw_and(alive);  // the scan's results are visible
-    if (alive) {
-      split_scale(sGam[C - 1]);
-      build_kt(0);
-      warp_arrive(&g_rdy);
-    }
+    if (alive) split_scale(sGam[C - 1]);
 
-    // Per chunk c: [D3 | E] -> F -> (MMA warp: Delta, state update) while the
-    // next chunk's scalars are staged -> split and scale the new state (the
-    // next [D3 | E] starts) -> outputs and the next Ktil^T under it.
+    // Per chunk c: [D3 | E] -> F -> (MMA warp: Delta) while Ktil^T is built ->
+    // (MMA warp: state update) while the next chunk's scalars are staged ->
+    // split and scale the new state (the next [D3 | E] starts) -> this
+    // chunk's outputs under it.
     for (int c = 0; c < nch && alive; ++c) {
       const int c0 = c * C;
       const uint32_t par = c & 1;
@@ -1645,24 +1705,25 @@ __global__ void __launch_bounds__(NTS, 1)
                      wait_live(&vbar, par, vdead));
       if (!alive) break;
       tc::fence_after_sync();
-      if (c + 2 < nch) fetch_qk(c + 2, true);  // buffer c % 2 is free: [D3 | E], Ktil^T done
 
       const int i0 = 32 * half;
       if (n == C) f_pass(std::true_type(), n, i0, u_d4(c));
       else f_pass(std::false_type(), n, i0, u_d4(c));
       warp_arrive(&f_rdy);
+      build_kt(c);  // the previous update has read the last Ktil^T
+      warp_arrive(&g_rdy);
 
       if (!last) {
-        cw_sync();  // every warp is past its reads of v and of this chunk's scalars
+        cw_sync();  // every warp is past its reads of v, of the raw k and of the scalars
         if (alive) {  // the raw v tile is free: fetch the next chunk's
           if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RV, &vbar);
           ++n_v;
         }
+        if (c + 2 < nch) fetch_qk(c + 2, true);  // buffer c % 2 is free: [D3 | E], Ktil^T done
         stage_scalars(c + 1);
         if (!GB && c + 2 < nch)
           load_gb<bf16>(in, p, h, lo + c0 + 2 * C, min(C, len - c0 - 2 * C), g_next, b_next);
       }
-      if (c > 0) out_chunk(c - 1);  // under this chunk's update: the other D4 buffer
       alive = cw_and(alive && wait_live(&b_upd, par, vdead));  // D4, new state ready
       if (!alive) break;
       tc::fence_after_sync();
@@ -1686,11 +1747,9 @@ __global__ void __launch_bounds__(NTS, 1)
           }
         }
       }
-      if (!last) split_scale(sGam[C - 1]);  // the next [D3 | E] starts here
-
       if (!last) {
-        build_kt(c + 1);
-        warp_arrive(&g_rdy);  // the next state update's operands: scaled S, Ktil^T
+        split_scale(sGam[C - 1]);  // the next [D3 | E] starts here
+        out_chunk(c);              // under it (the next update writes the other D4)
       }
     }
 
@@ -1778,6 +1837,23 @@ bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMap
   return true;
 }
 
+// SMs of the current device (queried once per device)
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 1;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <typename TI, typename TO>
 cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in, void *o,
                      float scale, void *work, cudaStream_t s, const Checkpoints &ck) {
@@ -1798,8 +1874,10 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_bytes);
   if (e != cudaSuccess) return e;
   const int npair = (p.h_v / p.h_k + 1) / 2;
-  prep<<<dim3((unsigned)nc, p.h_k * npair), NT, prep_bytes, s>>>(p, seq, in, off, tiles, maps,
-                                                                  raw ? 1 : 0);
+  // persistent: two CTAs per SM (or one per item when there are fewer)
+  const int64_t items = nc * p.h_k * npair;
+  const int64_t grid = items < 2 * (int64_t)sm_count() ? items : 2 * (int64_t)sm_count();
+  prep<<<(unsigned)grid, NT, prep_bytes, s>>>(p, seq, in, off, tiles, nc, maps, raw ? 1 : 0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (raw) {  // bf16 rows by tensor map: [D3 | E] on kind::f16 over the raw rows
     auto kern = seq_bf16_kernel<TO>;
