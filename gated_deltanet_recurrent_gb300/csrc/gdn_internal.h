@@ -154,7 +154,7 @@ cudaError_t launch_prefill_tc(const PoolView &p, int layer, const SeqIndex &seq,
 
 // Two-launch chunked prefill (dk = dv = 128): key-side tiles of every chunk
 // in parallel into `work`, then the state side sequence by sequence.
-size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v, int h_k);
+size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v);
 cudaError_t launch_prefill_split(const PoolView &p, int layer, const SeqIndex &seq,
                                  const QKV &in, void *o, gdn_dtype o_dtype, float scale,
                                  void *work, cudaStream_t s, const Checkpoints &ck = {});

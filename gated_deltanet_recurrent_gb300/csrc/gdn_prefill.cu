@@ -346,7 +346,7 @@ bool tc_shape(const PoolView &p, const QKV &in) {
 size_t prefill_workspace_bytes(const PoolView &p, const SeqIndex &seq, const QKV &in,
                                size_t limit) {
   if (!tc_shape(p, in)) return 0;
-  const size_t b = prefill_split_workspace_bytes(seq.n_seqs, seq.total_tokens, p.h_v, p.h_k);
+  const size_t b = prefill_split_workspace_bytes(seq.n_seqs, seq.total_tokens, p.h_v);
   return b <= limit ? b : 0;
 }
 

@@ -24,9 +24,9 @@
 // Workspace: (n_seqs + 1) int32 chunk offsets and the sequence order (256-byte
 // aligned), then per (chunk, value head) 32 KiB: the P tile, then the T tile,
 // each 64 x 64 float32 in the K-major core-matrix layout of gdn_tc.cuh; then,
-// when q and k came by tensor map, per (chunk, key head) 1/|q_t| and 1/|k_t|
-// (2 x 64 float32).  Chunks are numbered sequence by sequence; offsets[i] is
-// the first chunk of sequence i.
+// when q and k came by tensor map, per (chunk, value head) the state walk's
+// per-token scalars (5 x 64 float32, below).  Chunks are numbered sequence by
+// sequence; offsets[i] is the first chunk of sequence i.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -44,6 +44,11 @@ constexpr int XS = D + 4;   // plain row stride (floats) of staged values
 constexpr int AS = C + 4;   // plain row stride of A and T
 constexpr int TILE = C * C; // floats of one 64 x 64 tile
 constexpr uint32_t kTileBytes = TILE * 4;
+// The state walk's per-token scalars of one (chunk, value head), written by the
+// key-side kernel when q and k come by tensor map: gamma_t = e^{G_t}, beta_t,
+// gamma_t / |q_t| (scales column t of S Q^T), beta_t gamma_t / |k_t| (column t
+// of S K^T), e^{G_n - G_t} / |k_t| (token t of Ktil); 64 floats each.
+constexpr int kSGam = 0, kSBeta = C, kSQ = 2 * C, kSK = 3 * C, kSKt = 4 * C, kScal = 5 * C;
 
 // offsets, then the state kernels' sequence order (both int32)
 __host__ __device__ inline size_t offsets_bytes(int n_seqs) {
@@ -182,14 +187,12 @@ __device__ __forceinline__ void stage_chunk(const QKV &in, const PoolView &p, in
 
 // Tensor maps of a call's bf16 rows (16-byte aligned): q, k and v are fetched
 // as 64-column halves of [64 tokens][64] bf16 in the 128-byte swizzled layout
-// (8 KiB each, 1024-byte aligned), g and beta as [64 tokens][8 heads] bf16
-// (the 8-head group holding a head).
+// (8 KiB each, 1024-byte aligned).
 struct InMaps {
-  CUtensorMap q, k, v, g, b;   // q, k, v: {128, heads, tokens}; g, b: {h_v, tokens}
-  CUtensorMap o;               // bf16 outputs {128, h_v, tokens}, stores of whole chunks
+  CUtensorMap q, k, v;  // {128, heads, tokens}
+  CUtensorMap o;        // bf16 outputs {128, h_v, tokens}, stores of whole chunks
 };
-constexpr int kRawHalf = C * 64 * 2;            // 8 KiB
-constexpr int kRawGB = C * 8 * 2;               // 1 KiB
+constexpr int kRawHalf = C * 64 * 2;  // 8 KiB
 
 __device__ __forceinline__ void tma3(void *dst, const CUtensorMap *m, int x, int y, int z,
                                      uint64_t *bar) {
@@ -197,14 +200,6 @@ __device__ __forceinline__ void tma3(void *dst, const CUtensorMap *m, int x, int
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tma2(void *dst, const CUtensorMap *m, int x, int y,
-                                     uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -237,23 +232,17 @@ __device__ __forceinline__ void prefetch_v(const InMaps &m, int h, int64_t tok0,
   for (int hf = 0; hf < 2; ++hf) tma3(vdst + hf * kRawHalf, &m.v, 64 * hf, h, (int)tok0, vbar);
 }
 // One thread: the chunk's q and k halves into a [q h0 | k h0 | q h1 | k h1]
-// buffer (each half-pair a 128-row [Q;K] operand block) and, with gb, g and
-// beta to gbt, gbt + kRawGB, all onto bar, which also expects extra_tx bytes
-// of copies the caller issues next.
-__device__ __forceinline__ void prefetch_qk_pairs(const InMaps &m, bool gb, int h, int hk,
-                                                  int64_t tok0, unsigned char *qk,
-                                                  unsigned char *gbt, uint64_t *bar,
+// buffer (each half-pair a 128-row [Q;K] operand block) onto bar, which also
+// expects extra_tx bytes of copies the caller issues next.
+__device__ __forceinline__ void prefetch_qk_pairs(const InMaps &m, int hk, int64_t tok0,
+                                                  unsigned char *qk, uint64_t *bar,
                                                   uint32_t extra_tx) {
-  mbar_arrive_expect_tx(bar, 4 * kRawHalf + (gb ? 2 * kRawGB : 0) + extra_tx);
+  mbar_arrive_expect_tx(bar, 4 * kRawHalf + extra_tx);
   const int z = (int)tok0;
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     tma3(qk + (2 * hf) * kRawHalf, &m.q, 64 * hf, hk, z, bar);
     tma3(qk + (2 * hf + 1) * kRawHalf, &m.k, 64 * hf, hk, z, bar);
-  }
-  if (gb) {
-    tma2(gbt, &m.g, h & ~7, z, bar);
-    tma2(gbt + kRawGB, &m.b, h & ~7, z, bar);
   }
 }
 
@@ -601,10 +590,6 @@ __global__ void __launch_bounds__(NT, 2)
       break;
     }
     pending = false;
-    if (TMAQK && pair == 0 && tid < 2 * C) {  // 1/|q_t|, 1/|k_t| for the state kernel
-      float *nb = work + nc * p.h_v * (2 * TILE) + ((int64_t)cidx * p.h_k + kh) * (2 * C);
-      nb[tid] = tid < C ? rq[tid] : rk[tid - C];
-    }
     if (quad == 0 && tt < 32) {  // warp 4 wg: cumulative log-decay of this head
       const float a = sG[2 * lane], b = sG[2 * lane + 1];
       float incl = a + b;
@@ -615,6 +600,22 @@ __global__ void __launch_bounds__(NT, 2)
       }
       sG[2 * lane] = incl - b;
       sG[2 * lane + 1] = incl;
+      if (TMAQK && live) {  // the state walk's per-token scalars of this (chunk, head)
+        float *sb = work + nc * p.h_v * (2 * TILE) + ((int64_t)cidx * p.h_v + h) * kScal;
+        const float gl = __shfl_sync(0xffffffffu, incl, 31);
+        const float G0 = incl - b, G1 = incl;
+        const float gam0 = expf(G0), gam1 = expf(G1);
+        const float2 be = make_float2(sBeta[2 * lane], sBeta[2 * lane + 1]);
+        const float2 iq = make_float2(rq[2 * lane], rq[2 * lane + 1]);
+        const float2 ik = make_float2(rk[2 * lane], rk[2 * lane + 1]);
+        *reinterpret_cast<float2 *>(sb + kSGam + 2 * lane) = make_float2(gam0, gam1);
+        *reinterpret_cast<float2 *>(sb + kSBeta + 2 * lane) = be;
+        *reinterpret_cast<float2 *>(sb + kSQ + 2 * lane) = make_float2(gam0 * iq.x, gam1 * iq.y);
+        *reinterpret_cast<float2 *>(sb + kSK + 2 * lane) =
+            make_float2(be.x * gam0 * ik.x, be.y * gam1 * ik.y);
+        *reinterpret_cast<float2 *>(sb + kSKt + 2 * lane) =
+            make_float2(expf(gl - G0) * ik.x, expf(gl - G1) * ik.y);
+      }
       // cf[i] = e^{G_e - G_i} / |k_i|, e the last token of i's 16-token block (so at
       // most 1 / |k_i|): the column factor of P and A left of the diagonal blocks
       const float Ge = __shfl_sync(0xffffffffu, incl, (lane & ~7) | 7);
@@ -1238,16 +1239,14 @@ __device__ __forceinline__ uint32_t u_d4(int c) { return (c & 1) ? U_D4B : U_D4A
 constexpr int kQKBuf = 4 * kRawHalf;            // raw [q h0 | k h0 | q h1 | k h1], 32 KiB
 constexpr int B_QK = 0;                         // two q, k buffers (chunk c in buffer c % 2)
 constexpr int B_V = B_QK + 2 * kQKBuf;          // raw v [v h0 | v h1]
-constexpr int B_GB = B_V + 2 * kRawHalf;        // two raw g, beta buffers [g | beta]
-constexpr int B_OS = B_GB + 4 * kRawGB;         // outputs of a chunk, [64 tokens][128]
+constexpr int B_OS = B_V + 2 * kRawHalf;        // outputs of a chunk, [64 tokens][128]
 constexpr int B_PT = B_OS + C * D * 4;          // P tile of even chunks
 constexpr int B_KT = B_PT + TILE * 4;           // Ktil^T tile: [P0; Ktil^T] and
 constexpr int B_PT1 = B_KT + D * C * 4;         // [Ktil^T; P1] are contiguous operands
 constexpr int B_TT = B_PT1 + TILE * 4;          // T tile
-constexpr int B_SC = B_TT + TILE * 4;           // per-token scalars, 8 x 64 floats
-constexpr int B_NB = B_SC + 8 * C * 4;           // two norm buffers [1/|q| | 1/|k|]
-constexpr int kSeqBf16Smem = B_NB + 2 * 2 * C * 4 + 1024;  // + alignment slack
-static_assert(B_V % 1024 == 0 && B_GB % 128 == 0 && B_PT % 16 == 0 && B_KT == B_PT + TILE * 4 &&
+constexpr int B_SB = B_TT + TILE * 4;           // two per-token scalar blocks (chunk c in c % 2)
+constexpr int kSeqBf16Smem = B_SB + 2 * kScal * 4 + 1024;  // + alignment slack
+static_assert(B_V % 1024 == 0 && B_PT % 16 == 0 && B_SB % 16 == 0 && B_KT == B_PT + TILE * 4 &&
                   B_PT1 == B_KT + D * C * 4,
               "tile alignment");
 static_assert(kSeqBf16Smem <= 227 * 1024, "shared memory");
@@ -1257,14 +1256,11 @@ template <typename TO>
 __global__ void __launch_bounds__(NTS, 1)
     seq_bf16_kernel(PoolView p, int layer, SeqIndex seq, QKV in, TO *__restrict__ o, float scale,
                     const int32_t *__restrict__ off, int64_t cap, const float *__restrict__ work,
-                    const __grid_constant__ InMaps maps, int raw_gb, int o_map,
-                    Checkpoints ck) {
+                    const __grid_constant__ InMaps maps, int o_map, Checkpoints ck) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *sm = smem + ((1024u - (smem_addr(smem) & 1023u)) & 1023u);
-  const bool GB = raw_gb != 0;  // g, beta come with the tensor-map copies too
   unsigned char *RQK = sm + B_QK;
   unsigned char *RV = sm + B_V;
-  unsigned char *RGB = sm + B_GB;
   TO *OS = reinterpret_cast<TO *>(sm + B_OS);
   // staged outputs: bf16 as two 64-column halves of [64 tokens][64] in the
   // 128-byte swizzle (the output map's boxes); float32 as plain [64][128] rows
@@ -1275,15 +1271,12 @@ __global__ void __launch_bounds__(NTS, 1)
   float *PT1 = reinterpret_cast<float *>(sm + B_PT1);
   float *KT = reinterpret_cast<float *>(sm + B_KT);
   float *TT = reinterpret_cast<float *>(sm + B_TT);
-  float *sG = reinterpret_cast<float *>(sm + B_SC);  // g, then (scan) nothing further
-  float *sGam = sG + C;    // gamma_t = e^{G_t}
-  float *sBeta = sGam + C;
-  float *sQ = sBeta + 2 * C;  // gamma_t / |q_t|         (scales column t of S Q^T)
-  float *sK = sQ + C;      // beta_t gamma_t / |k_t|     (scales column t of S K^T)
-  float *sKt = sK + C;     // e^{G_n - G_t} / |k_t|      (scales token t of Ktil)
+  // chunk c's per-token scalars (from the key-side kernel), buffer c % 2
+  float *SB = reinterpret_cast<float *>(sm + B_SB);
+  auto scal = [&](int c) -> const float * { return SB + (c & 1) * kScal; };
   __shared__ __align__(8) uint64_t b_ed3, b_dd, b_upd;  // MMA groups done
   __shared__ __align__(8) uint64_t tbar, vbar;           // P / T tiles, raw v landed
-  __shared__ __align__(8) uint64_t rbar[2];              // raw q, k (g, beta) buffers landed
+  __shared__ __align__(8) uint64_t rbar[2];              // raw q, k and scalars landed
   __shared__ __align__(8) uint64_t f_rdy, g_rdy, s_rdy;  // compute warps -> MMA warp
   __shared__ uint32_t tmem_slot;
   __shared__ int dead;  // set by the role that gave up waiting
@@ -1314,9 +1307,8 @@ __global__ void __launch_bounds__(NTS, 1)
   const gdn_dtype sd = p.state_dtype;
   char *Sg = p.state_at(p.state_head_elem(layer, slot, h));  // float32, bf16 or f16 elements
   const float *wsq = work + ((int64_t)off[si] * p.h_v + h) * (2 * TILE);  // chunk 0's tiles
-  // chunk 0's 1/|q_t|, 1/|k_t| (written by the key-side kernel), next chunk 2 C * h_k on
-  const float *wnorm = work + cap * p.h_v * (2 * TILE) + ((int64_t)off[si] * p.h_k + hk) * (2 * C);
-  float *NB = reinterpret_cast<float *>(sm + B_NB);  // two [1/|q| | 1/|k|] buffers
+  // chunk 0's per-token scalars (written by the key-side kernel), next chunk h_v blocks on
+  const float *wscal = work + cap * p.h_v * (2 * TILE) + ((int64_t)off[si] * p.h_v + h) * kScal;
   const int64_t wstep = (int64_t)p.h_v * (2 * TILE);                      // next chunk
 
   if (warp == 0) tc::tmem_alloc(&tmem_slot, SEQ_TMEM);
@@ -1347,6 +1339,27 @@ __global__ void __launch_bounds__(NTS, 1)
     constexpr uint32_t KSTEP = 2 * tc::kLBO;
     const bool leader = lane == 0;
     auto all_lanes = [](bool x) { return __all_sync(0xffffffffu, x) != 0; };
+    // Row copies: v of chunk c onto vbar; q, k of chunk c into buffer c % 2
+    // with the chunk's per-token scalars from the key-side kernel onto rbar[c % 2]
+    // (scalars = false: issued later, once the key-side grid has finished)
+    int n_r0 = 0, n_r1 = 0, n_v = 0;  // copies armed per barrier
+    auto fetch_v = [&](int c) {
+      if (leader) prefetch_v(maps, h, lo + (int64_t)c * C, RV, &vbar);
+      ++n_v;
+    };
+    auto fetch_scal = [&](int c) {
+      if (leader)
+        bulk_g2s(SB + (c & 1) * kScal, wscal + (int64_t)c * p.h_v * kScal, kScal * 4,
+                 &rbar[c & 1]);
+    };
+    auto fetch_qk = [&](int c, bool scalars) {
+      const int b = c & 1;
+      if (leader) {
+        prefetch_qk_pairs(maps, hk, lo + (int64_t)c * C, RQK + b * kQKBuf, &rbar[b], kScal * 4);
+        if (scalars) fetch_scal(c);
+      }
+      if (b) ++n_r1; else ++n_r0;
+    };
     auto load_tiles = [&](int c) {  // P and T tiles of chunk c onto tbar
       if (leader) {
         const float *src = wsq + (int64_t)c * wstep;
@@ -1378,8 +1391,14 @@ __global__ void __launch_bounds__(NTS, 1)
       __syncwarp();
     };
     int n_ed3 = 0, n_dd = 0, n_upd = 0, n_t = 1;  // groups issued, tile loads armed
-    // the key-side grid has written the tiles (this launch may start before it ends)
+    fetch_v(0);
+    fetch_qk(0, false);
+    if (nch > 1) fetch_qk(1, false);
+    // the key-side grid has written the tiles and scalars (this launch may
+    // start before it ends)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    fetch_scal(0);
+    if (nch > 1) fetch_scal(1);
     load_tiles(0);
     bool ok = all_lanes(wait_live(&s_rdy, 0, vdead) && wait_live(&rbar[0], 0, vdead));
     if (ok) {
@@ -1416,6 +1435,10 @@ __global__ void __launch_bounds__(NTS, 1)
       }
       __syncwarp();
       ++n_upd;
+      // under the update: the v tile is free (every warp's F pass is done), and
+      // so is the q, k buffer of chunk c (its [D3 | E], F and Ktil^T are done)
+      if (c + 1 < nch) fetch_v(c + 1);
+      if (c + 2 < nch) fetch_qk(c + 2, true);
       ok = all_lanes(wait_live(&b_upd, par, vdead));
       if (!ok || c + 1 == nch) break;
       load_tiles(c + 1);  // both tiles are free again
@@ -1436,6 +1459,10 @@ __global__ void __launch_bounds__(NTS, 1)
       if (n_dd) mbar_wait_bounded(&b_dd, (n_dd - 1) & 1);
       if (n_upd) mbar_wait_bounded(&b_upd, (n_upd - 1) & 1);
       mbar_wait_bounded(&tbar, (n_t - 1) & 1);
+      // row copies still in flight land before shared memory is released
+      if (n_r0 > 0) mbar_wait_bounded(&rbar[0], (n_r0 - 1) & 1);
+      if (n_r1 > 0) mbar_wait_bounded(&rbar[1], (n_r1 - 1) & 1);
+      if (n_v > 0) mbar_wait_bounded(&vbar, (n_v - 1) & 1);
     }
   } else {
     // ----------------------------------------------------------- compute warps
@@ -1455,66 +1482,10 @@ __global__ void __launch_bounds__(NTS, 1)
       }
       tc::tmem_st_wait();
     }
-    int n_r0 = 0, n_r1 = 0, n_v = 0;  // raw loads armed per barrier
     bool alive = true;
-    float g_next = 0.f, b_next = 0.f;  // this thread's g, beta of the next chunk (without GB)
 
-    // copier: q, k (g, beta) of chunk c into buffer c % 2, with the chunk's norms
-    // from the key-side kernel (norms = false: the caller copies them later)
-    auto fetch_norms = [&](int c) {
-      if (tid == kCopier)
-        bulk_g2s(NB + (c & 1) * 2 * C, wnorm + (int64_t)c * p.h_k * (2 * C), 2 * C * 4,
-                 &rbar[c & 1]);
-    };
-    auto fetch_qk = [&](int c, bool norms) {
-      const int b = c & 1;
-      if (tid == kCopier) {
-        prefetch_qk_pairs(maps, GB, h, hk, lo + (int64_t)c * C, RQK + b * kQKBuf,
-                          RGB + b * 2 * kRawGB, &rbar[b], 2 * C * 4);
-        if (norms) fetch_norms(c);
-      }
-      if (b) ++n_r1; else ++n_r0;
-    };
-    // Per-token scalars of chunk c: g and beta (with the L2 norms of its q and k
-    // rows, which came with them), then (warp 7) the cumulative decays and the
-    // column scales.
-    auto stage_scalars = [&](int c) {
-      const int ns = min(C, len - c * C), b = c & 1;
-      alive = cw_and(alive && wait_live(&rbar[b], (c >> 1) & 1, vdead));
-      const int t = stage_token(), part = lane >> 3;
-      float gt = g_next, bt = b_next;
-      if (GB) {  // this head's column of the [64][8] g and beta tiles (padded tokens 0)
-        const bf16 *g8 = reinterpret_cast<const bf16 *>(RGB + b * 2 * kRawGB);
-        gt = t < ns ? __bfloat162float(g8[t * 8 + (h & 7)]) : 0.f;
-        bt = t < ns ? __bfloat162float(g8[C * 8 + t * 8 + (h & 7)]) : 0.f;
-      }
-      if (part == 0) {
-        sG[t] = gt;
-        sBeta[t] = bt;
-      }
-      cw_sync();
-      if (warp == 7) {  // cumulative log-decay (padded tokens carry g = 0) and the scales
-        const float a = sG[2 * lane], bb = sG[2 * lane + 1];
-        float incl = a + bb;
-#pragma unroll
-        for (int sh = 1; sh < 32; sh <<= 1) {
-          const float up = __shfl_up_sync(0xffffffffu, incl, sh);
-          if (lane >= sh) incl += up;
-        }
-        const float gl = __shfl_sync(0xffffffffu, incl, 31);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int i = 2 * lane + e;
-          const float G = e == 0 ? incl - bb : incl;
-          const float gam = expf(G);
-          sGam[i] = gam;
-          const float *nrm = NB + b * 2 * C;  // 1/|q| then 1/|k|
-          sQ[i] = gam * nrm[i];
-          sK[i] = sBeta[i] * gam * nrm[C + i];
-          sKt[i] = expf(gl - G) * nrm[C + i];
-        }
-      }
-    };
+    // chunk c's copies have landed (every compute thread waits itself)
+    auto rows_landed = [&](int c) { return wait_live(&rbar[c & 1], (c >> 1) & 1, vdead); };
     // S (float32) -> S_bf16 at the F columns, packed two per column (lower k in
     // the low half), for the next [D3 | E], and S <- gn S in place for the next
     // state update (which S_bf16 does not see).  Arrives on s_rdy once all of
@@ -1548,6 +1519,7 @@ __global__ void __launch_bounds__(NTS, 1)
     auto build_kt = [&](int c) {
       const int nn = min(C, len - c * C);
       const unsigned char *kb = RQK + (c & 1) * kQKBuf + kRawHalf;
+      const float *sKt = scal(c) + kSKt;
 #pragma unroll
       for (int it = 0; it < 8; ++it) {
         const int task = it * 8 + warp;
@@ -1573,8 +1545,9 @@ __global__ void __launch_bounds__(NTS, 1)
     // F[v][t] = beta_t v_t[v] - (beta_t gamma_t / |k_t|) (S K^T)[v][t] and the
     // output's state part (gamma_t / |q_t|) (S Q^T)[v][t] into TMEM, this
     // thread's 32 tokens; padded tokens (FULL false) give 0
-    auto f_pass = [&](auto full, int n, int i0, uint32_t d4c) {
+    auto f_pass = [&](auto full, int n, int i0, uint32_t d4c, const float *sc) {
       constexpr bool FULL = decltype(full)::value;
+      const float *sBeta = sc + kSBeta, *sQ = sc + kSQ, *sK = sc + kSK;
       const int v = row;
       const unsigned char *vr = RV + (v >> 6) * kRawHalf + (v & 7) * 2;
       const int vpiece = (v & 63) >> 3;
@@ -1677,25 +1650,12 @@ __global__ void __launch_bounds__(NTS, 1)
 
     // chunk 0 (and 1) on their way; chunk 0's scalars, split state, scaled
     // state and Ktil^T to the MMA warp
-    if (tid == kCopier) prefetch_v(maps, h, lo, RV, &vbar);
-    n_v = 1;
-    fetch_qk(0, false);
-    if (nch > 1) fetch_qk(1, false);
-    if (tid == kCopier) {  // the norms come from the key-side grid: wait for it first
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      fetch_norms(0);
-      if (nch > 1) fetch_norms(1);
-    }
-    if (!GB) load_gb<bf16>(in, p, h, lo, min(C, len), g_next, b_next);
-    stage_scalars(0);
-    if (!GB && nch > 1) load_gb<bf16>(in, p, h, lo + C, min(C, len - C), g_next, b_next);
-    alive = cw_and(alive);  // the scan's results are visible
-    if (alive) split_scale(sGam[C - 1]);
+    alive = cw_and(rows_landed(0));
+    if (alive) split_scale(scal(0)[kSGam + C - 1]);
 
     // Per chunk c: [D3 | E] -> F -> (MMA warp: Delta) while Ktil^T is built ->
-    // (MMA warp: state update) while the next chunk's scalars are staged ->
-    // split and scale the new state (the next [D3 | E] starts) -> this
-    // chunk's outputs under it.
+    // (MMA warp: state update, then the next row copies) -> split and scale the
+    // new state (the next [D3 | E] starts) -> this chunk's outputs under it.
     for (int c = 0; c < nch && alive; ++c) {
       const int c0 = c * C;
       const uint32_t par = c & 1;
@@ -1707,24 +1667,14 @@ __global__ void __launch_bounds__(NTS, 1)
       tc::fence_after_sync();
 
       const int i0 = 32 * half;
-      if (n == C) f_pass(std::true_type(), n, i0, u_d4(c));
-      else f_pass(std::false_type(), n, i0, u_d4(c));
+      if (n == C) f_pass(std::true_type(), n, i0, u_d4(c), scal(c));
+      else f_pass(std::false_type(), n, i0, u_d4(c), scal(c));
       warp_arrive(&f_rdy);
       build_kt(c);  // the previous update has read the last Ktil^T
       warp_arrive(&g_rdy);
 
-      if (!last) {
-        cw_sync();  // every warp is past its reads of v, of the raw k and of the scalars
-        if (alive) {  // the raw v tile is free: fetch the next chunk's
-          if (tid == kCopier) prefetch_v(maps, h, lo + c0 + C, RV, &vbar);
-          ++n_v;
-        }
-        if (c + 2 < nch) fetch_qk(c + 2, true);  // buffer c % 2 is free: [D3 | E], Ktil^T done
-        stage_scalars(c + 1);
-        if (!GB && c + 2 < nch)
-          load_gb<bf16>(in, p, h, lo + c0 + 2 * C, min(C, len - c0 - 2 * C), g_next, b_next);
-      }
-      alive = cw_and(alive && wait_live(&b_upd, par, vdead));  // D4, new state ready
+      // D4 and the new state ready; the next chunk's scalars landed
+      alive = cw_and(alive && wait_live(&b_upd, par, vdead) && (last || rows_landed(c + 1)));
       if (!alive) break;
       tc::fence_after_sync();
       if (ck.every > 0 && c0 + C <= len && (c0 + C) % ck.every == 0) {  // checkpoint: copy S out
@@ -1748,7 +1698,7 @@ __global__ void __launch_bounds__(NTS, 1)
         }
       }
       if (!last) {
-        split_scale(sGam[C - 1]);  // the next [D3 | E] starts here
+        split_scale(scal(c + 1)[kSGam + C - 1]);  // the next [D3 | E] starts here
         out_chunk(c);              // under it (the next update writes the other D4)
       }
     }
@@ -1769,11 +1719,6 @@ __global__ void __launch_bounds__(NTS, 1)
     } else {
       *vdead = 1;
       if (tid == 0) raise_error(p.err, GDN_DEVERR_TIMEOUT);
-      if (tid == kCopier) {  // raw loads still in flight land before shared memory is released
-        if (n_r0 > 0) mbar_wait_bounded(&rbar[0], (n_r0 - 1) & 1);
-        if (n_r1 > 0) mbar_wait_bounded(&rbar[1], (n_r1 - 1) & 1);
-        if (n_v > 0) mbar_wait_bounded(&vbar, (n_v - 1) & 1);
-      }
     }
   }
   tc::fence_before_sync();
@@ -1784,11 +1729,10 @@ __global__ void __launch_bounds__(NTS, 1)
 
 // Tensor maps for the bf16 inputs of a call: q, k {128, h_k, tokens} and v
 // {128, h_v, tokens} with boxes {64, 1, 64} in the 128-byte swizzle (rows and
-// strides 16-byte aligned), and g, beta {h_v, tokens} with boxes {8, 64} when
-// their rows are 16-byte aligned too (gb).  False: stage from global memory.
+// strides 16-byte aligned).  False: stage from global memory.
 // With o_bf16 (a bf16 output tensor [tokens][h_v][128]) also its map, boxes
 // {64, 1, 64} in the 128-byte swizzle, when it starts 16-byte aligned (om).
-bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMaps &m, bool &gb,
+bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMaps &m,
                     const void *o_bf16, bool &om) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
     void *fn = nullptr;
@@ -1801,7 +1745,7 @@ bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMap
     }
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }();
-  gb = om = false;
+  om = false;
   if (encode == nullptr) return false;
   const size_t es = 2;
   auto a16 = [](const void *x) { return (uintptr_t)x % 16 == 0; };
@@ -1820,18 +1764,6 @@ bool encode_in_maps(const PoolView &p, const SeqIndex &seq, const QKV &in, InMap
   if (!map3(&m.q, in.q, p.h_k, in.ld_qk) || !map3(&m.k, in.k, p.h_k, in.ld_qk) ||
       !map3(&m.v, in.v, p.h_v, in.ld_v))
     return false;
-  if (a16(in.g) && a16(in.beta) && ((size_t)p.h_v * es) % 16 == 0) {
-    cuuint64_t dims[2] = {(cuuint64_t)p.h_v, tokens};
-    cuuint64_t strides[1] = {(cuuint64_t)p.h_v * es};
-    cuuint32_t box2[2] = {8, C};
-    auto map2 = [&](CUtensorMap *dst, const void *base) {
-      return encode(dst, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
-                    strides, box2, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-             CUDA_SUCCESS;
-    };
-    gb = map2(&m.g, in.g) && map2(&m.b, in.beta);
-  }
   if (o_bf16 != nullptr && a16(o_bf16))
     om = map3(&m.o, o_bf16, p.h_v, (int64_t)p.h_v * D);
   return true;
@@ -1864,10 +1796,9 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   InMaps maps;
-  bool gb = false;
   bool om = false;
   const bool raw = std::is_same<TI, bf16>::value &&
-                   encode_in_maps(p, seq, in, maps, gb,
+                   encode_in_maps(p, seq, in, maps,
                                   std::is_same<TO, bf16>::value ? o : nullptr, om);
   auto prep = prep_kernel<TI>;
   constexpr int prep_bytes = prep_smem<TI>();
@@ -1897,7 +1828,7 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p, layer, seq, in, static_cast<TO *>(o), scale,
                               static_cast<const int32_t *>(off), nc,
-                              static_cast<const float *>(tiles), maps, gb ? 1 : 0, om ? 1 : 0, ck);
+                              static_cast<const float *>(tiles), maps, om ? 1 : 0, ck);
   }
   auto kern = seq_kernel<TI, TO>;  // rows staged from global memory
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSeqSmem);
@@ -1909,9 +1840,9 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
 
 }  // namespace
 
-size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v, int h_k) {
+size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v) {
   return offsets_bytes(n_seqs) +
-         (size_t)max_chunks(n_seqs, total_tokens) * (h_v * 2 * kTileBytes + h_k * 2 * C * 4);
+         (size_t)max_chunks(n_seqs, total_tokens) * h_v * (2 * kTileBytes + kScal * 4);
 }
 
 cudaError_t launch_prefill_split(const PoolView &p, int layer, const SeqIndex &seq,
