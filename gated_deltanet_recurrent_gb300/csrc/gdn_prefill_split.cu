@@ -50,14 +50,18 @@ constexpr uint32_t kTileBytes = TILE * 4;
 // of S K^T), e^{G_n - G_t} / |k_t| (token t of Ktil); 64 floats each.
 constexpr int kSGam = 0, kSBeta = C, kSQ = 2 * C, kSK = 3 * C, kSKt = 4 * C, kScal = 5 * C;
 
-// offsets, then the state kernels' sequence order (both int32)
-__host__ __device__ inline size_t offsets_bytes(int n_seqs) {
-  return (((size_t)n_seqs + 1) * 4 + (size_t)n_seqs * 4 + 255) & ~(size_t)255;
-}
 // Calls of up to this many sequences walk them longest first.
 constexpr int kOrderMax = 256;
 __host__ __device__ inline int64_t max_chunks(int n_seqs, int total_tokens) {
   return (int64_t)total_tokens / C + n_seqs;  // >= sum over sequences of ceil(len / 64)
+}
+// offsets and the state kernels' sequence order (both int32), then per chunk
+// (up to cap chunks) its first token and token count (int2)
+__host__ __device__ inline size_t chunk_table_offset(int n_seqs) {
+  return ((2 * (size_t)n_seqs + 1) * 4 + 7) & ~(size_t)7;
+}
+__host__ __device__ inline size_t offsets_bytes(int n_seqs, int64_t cap) {
+  return (chunk_table_offset(n_seqs) + (size_t)cap * 8 + 255) & ~(size_t)255;
 }
 
 __device__ __forceinline__ int seq_chunks(const SeqIndex &seq, int i) {
@@ -71,7 +75,8 @@ __device__ __forceinline__ int seq_chunks(const SeqIndex &seq, int i) {
 // workspace's cap chunks; the state kernel rejects them).  Then order[r]
 // (after offsets[n_seqs]) = the sequence with the r-th most chunks, ties by
 // index, so that the state kernels start the longest sequences first
-// (identity order past kOrderMax sequences).
+// (identity order past kOrderMax sequences).  Then table[c] = (first token,
+// tokens) of chunk c < cap, for the key-side kernel.
 __global__ void __launch_bounds__(1024)
     chunk_offsets_kernel(SeqIndex seq, int32_t *off, int64_t cap) {
   __shared__ int64_t part[1024];
@@ -89,9 +94,15 @@ __global__ void __launch_bounds__(1024)
     __syncthreads();
   }
   int64_t run = tid ? part[tid - 1] : 0;
+  int2 *table = reinterpret_cast<int2 *>(reinterpret_cast<char *>(off) + chunk_table_offset(n));
   for (int i = b; i < e; ++i) {
     off[i] = (int32_t)min(run, cap + 1);
-    run += seq_chunks(seq, i);
+    const int nc = seq_chunks(seq, i);
+    const int lo = nc > 0 ? (int)seq.cu_seqlens[i] : 0;
+    const int len = nc > 0 ? (int)seq.cu_seqlens[i + 1] - lo : 0;
+    for (int j = 0; j < nc && run + j < cap; ++j)
+      table[run + j] = make_int2(lo + j * C, min(C, len - j * C));
+    run += nc;
   }
   if (tid == 1023) off[n] = (int32_t)min(part[1023], cap + 1);
   int32_t *order = off + n + 1;
@@ -433,12 +444,13 @@ static_assert(prep_smem<float>() <= 227 * 1024, "shared memory");
 // value head 2 pair + wg of the group and inverts I + A.  Once the Gram MMA
 // has read the tile, the next item's q/k copies (tensor-map rows) and its g,
 // beta loads are issued, so they land while this item's P, A and T are formed.
-// nc: the chunk capacity of the workspace (where the norms start).
+// nc: the chunk capacity of the workspace; table: each chunk's first token
+// and token count.
 template <typename TI>
 __global__ void __launch_bounds__(NT, 2)
     prep_kernel(PoolView p, SeqIndex seq, QKV in, const int32_t *__restrict__ off,
-                float *__restrict__ work, int64_t nc, const __grid_constant__ InMaps maps,
-                int raw_rows) {
+                const int2 *__restrict__ table, float *__restrict__ work, int64_t nc,
+                const __grid_constant__ InMaps maps, int raw_rows) {
   constexpr bool B16 = std::is_same<TI, bf16>::value;  // raw bf16 tile, kind::f16
   // 16-byte aligned bf16 rows: the tile arrives by tensor-map copies in the 128-byte
   // swizzle, two K halves [Q;K] x 64 columns (16 KiB each), read by swizzled descriptors
@@ -457,7 +469,9 @@ __global__ void __launch_bounds__(NT, 2)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int G = p.h_v / p.h_k, npair = (G + 1) / 2;
   const int ny = p.h_k * npair;
-  const int64_t items = (int64_t)off[seq.n_seqs] * ny;
+  // (offsets past the capacity come only from overlapping sequences, which the
+  // state kernel rejects; no chunk beyond it is formed)
+  const int64_t items = min((int64_t)off[seq.n_seqs], nc) * ny;
   if ((int64_t)blockIdx.x >= items) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wg = warp >> 2, quad = warp & 3, tt = tid & 127;
@@ -472,22 +486,14 @@ __global__ void __launch_bounds__(NT, 2)
     int cidx, n, kh, pair;
     int64_t tok0;
   };
-  auto locate = [&](int64_t it) {
+  auto locate = [&](int64_t it, int2 tc) {  // tc = table[it / ny]
     Item w;
     w.cidx = (int)(it / ny);
     const int y = (int)(it % ny);
     w.kh = y / npair;
     w.pair = y % npair;
-    int si = 0;  // the sequence holding the chunk: the last i with off[i] <= cidx
-    for (int b = seq.n_seqs - 1; si < b;) {
-      const int m = (si + b + 1) >> 1;
-      if (off[m] <= w.cidx) si = m; else b = m - 1;
-    }
-    const int64_t lo = seq.cu_seqlens[si], hi = seq.cu_seqlens[si + 1];
-    const int c0 = (w.cidx - off[si]) * C;
-    const int64_t rest = hi - lo - c0;
-    w.n = rest < C ? (int)rest : C;
-    w.tok0 = lo + c0;
+    w.tok0 = tc.x;
+    w.n = tc.y;
     return w;
   };
   auto head_of = [&](const Item &w) {
@@ -522,7 +528,7 @@ __global__ void __launch_bounds__(NT, 2)
     const int r = e / C, c = e % C;
     if ((c >> 4) > (r >> 4)) TP[r * AS + c] = 0.f;
   }
-  Item w = locate(blockIdx.x);
+  Item w = locate(blockIdx.x, table[blockIdx.x / ny]);
   float g_nx = 0.f, b_nx = 0.f;  // the next item's g, beta (threads tt < C)
   load_gb1(w, g_nx, b_nx);
   tc::fence_before_sync();
@@ -538,6 +544,8 @@ __global__ void __launch_bounds__(NT, 2)
   uint32_t ph = 0;       // phase of bar and lbar for this item
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x, ph ^= 1u) {
     const int cidx = w.cidx, n = w.n;
+    const int64_t nx = it + gridDim.x;
+    const int2 tc_nx = nx < items ? table[nx / ny] : make_int2(0, 0);  // used at the prefetch
     const int64_t tok0 = w.tok0;
     const int kh = w.kh, pair = w.pair;
     const bool live = 2 * pair + wg < G;
@@ -600,22 +608,6 @@ __global__ void __launch_bounds__(NT, 2)
       }
       sG[2 * lane] = incl - b;
       sG[2 * lane + 1] = incl;
-      if (TMAQK && live) {  // the state walk's per-token scalars of this (chunk, head)
-        float *sb = work + nc * p.h_v * (2 * TILE) + ((int64_t)cidx * p.h_v + h) * kScal;
-        const float gl = __shfl_sync(0xffffffffu, incl, 31);
-        const float G0 = incl - b, G1 = incl;
-        const float gam0 = expf(G0), gam1 = expf(G1);
-        const float2 be = make_float2(sBeta[2 * lane], sBeta[2 * lane + 1]);
-        const float2 iq = make_float2(rq[2 * lane], rq[2 * lane + 1]);
-        const float2 ik = make_float2(rk[2 * lane], rk[2 * lane + 1]);
-        *reinterpret_cast<float2 *>(sb + kSGam + 2 * lane) = make_float2(gam0, gam1);
-        *reinterpret_cast<float2 *>(sb + kSBeta + 2 * lane) = be;
-        *reinterpret_cast<float2 *>(sb + kSQ + 2 * lane) = make_float2(gam0 * iq.x, gam1 * iq.y);
-        *reinterpret_cast<float2 *>(sb + kSK + 2 * lane) =
-            make_float2(be.x * gam0 * ik.x, be.y * gam1 * ik.y);
-        *reinterpret_cast<float2 *>(sb + kSKt + 2 * lane) =
-            make_float2(expf(gl - G0) * ik.x, expf(gl - G1) * ik.y);
-      }
       // cf[i] = e^{G_e - G_i} / |k_i|, e the last token of i's 16-token block (so at
       // most 1 / |k_i|): the column factor of P and A left of the diagonal blocks
       const float Ge = __shfl_sync(0xffffffffu, incl, (lane & ~7) | 7);
@@ -667,9 +659,8 @@ __global__ void __launch_bounds__(NT, 2)
     }
     mma_out = false;
     // the tile is free again: the next item's rows and scalars travel under this one
-    const int64_t nx = it + gridDim.x;
     if (nx < items) {
-      w = locate(nx);
+      w = locate(nx, tc_nx);
       if (TMAQK) pending = true;
       if (TMAQK && tid == 0) issue_rows(w);
       load_gb1(w, g_nx, b_nx);
@@ -736,6 +727,17 @@ __global__ void __launch_bounds__(NT, 2)
     __syncthreads();
     tc::fence_after_sync();
     if (live) {
+      if (TMAQK && tt >= C) {  // (idle in the inversion's first phase) the state
+        // walk's per-token scalars of this (chunk, head), token i
+        const int i = tt - C;
+        float *sb = work + nc * p.h_v * (2 * TILE) + ((int64_t)cidx * p.h_v + h) * kScal;
+        const float G = sG[i], gam = expf(G), be = sBeta[i], ik = rk[i];
+        sb[kSGam + i] = gam;
+        sb[kSBeta + i] = be;
+        sb[kSQ + i] = gam * rq[i];
+        sb[kSK + i] = be * gam * ik;
+        sb[kSKt + i] = expf(sG[C - 1] - G) * ik;
+      }
       invert_unit_lower(AP, TP, XS_, tt, 1 + wg);
 #pragma unroll
       for (int i4 = 0; i4 < C * (C / 4) / 128; ++i4) {  // T tile [t][i] -> workspace
@@ -1790,8 +1792,11 @@ template <typename TI, typename TO>
 cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QKV &in, void *o,
                      float scale, void *work, cudaStream_t s, const Checkpoints &ck) {
   int32_t *off = static_cast<int32_t *>(work);
-  float *tiles = reinterpret_cast<float *>(static_cast<char *>(work) + offsets_bytes(seq.n_seqs));
   const int64_t nc = max_chunks(seq.n_seqs, seq.total_tokens);
+  const int2 *table =
+      reinterpret_cast<const int2 *>(static_cast<char *>(work) + chunk_table_offset(seq.n_seqs));
+  float *tiles =
+      reinterpret_cast<float *>(static_cast<char *>(work) + offsets_bytes(seq.n_seqs, nc));
   chunk_offsets_kernel<<<1, 1024, 0, s>>>(seq, off, nc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -1808,7 +1813,8 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
   // persistent: two CTAs per SM (or one per item when there are fewer)
   const int64_t items = nc * p.h_k * npair;
   const int64_t grid = items < 2 * (int64_t)sm_count() ? items : 2 * (int64_t)sm_count();
-  prep<<<(unsigned)grid, NT, prep_bytes, s>>>(p, seq, in, off, tiles, nc, maps, raw ? 1 : 0);
+  prep<<<(unsigned)grid, NT, prep_bytes, s>>>(p, seq, in, off, table, tiles, nc, maps,
+                                               raw ? 1 : 0);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (raw) {  // bf16 rows by tensor map: [D3 | E] on kind::f16 over the raw rows
     auto kern = seq_bf16_kernel<TO>;
@@ -1841,8 +1847,8 @@ cudaError_t launch_t(const PoolView &p, int layer, const SeqIndex &seq, const QK
 }  // namespace
 
 size_t prefill_split_workspace_bytes(int n_seqs, int total_tokens, int h_v) {
-  return offsets_bytes(n_seqs) +
-         (size_t)max_chunks(n_seqs, total_tokens) * h_v * (2 * kTileBytes + kScal * 4);
+  const int64_t nc = max_chunks(n_seqs, total_tokens);
+  return offsets_bytes(n_seqs, nc) + (size_t)nc * h_v * (2 * kTileBytes + kScal * 4);
 }
 
 cudaError_t launch_prefill_split(const PoolView &p, int layer, const SeqIndex &seq,
