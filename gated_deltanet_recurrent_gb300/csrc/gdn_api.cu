@@ -486,6 +486,14 @@ gdn_status gdn_decode_step_conv(gdn_pool *p, int32_t layer, const int32_t *slot_
     if (e != cudaSuccess) return cuda_fail(e, "conv + decode launch");
     return ok();
   }
+  // Larger grids: one CTA per (slot, key head) convolves each channel once
+  // while its heads' states stream in, where the shape allows it.
+  if (gdn::decode_conv_group_ok(p->view)) {
+    e = gdn::launch_decode_conv_group(p->view, layer, slot_ids, n, x, ld_x, w, bias, y, ld_y, g,
+                                      beta, dtype, o, o_dtype, scale, s);
+    if (e != cudaSuccess) return cuda_fail(e, "conv + decode launch");
+    return ok();
+  }
   gdn::SeqIndex seq{slot_ids, nullptr, n, n};
   e = gdn::launch_conv_silu(p->view, layer, seq, 1, x, ld_x, w, bias, y, ld_y, nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "conv launch");

@@ -412,6 +412,190 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// ---- one-call decode step, larger grids: one CTA per (slot, key head) ----
+//
+// The CTA convolves every channel its key head's decode reads exactly once:
+// the 2 * 128 q/k channels and the G * dv v channels of the G value heads
+// that share the key head (G = h_v / h_k <= 2), one thread per channel, which
+// also shifts that channel's cache in place (no other CTA reads it, so no
+// ticket is needed).  Meanwhile the G heads' float32 states stream through a
+// ring of kRing 16 KiB tiles (32 rows each; bulk copies issued ahead, one
+// mbarrier per buffer), and each tile is updated row by row in the decode
+// kernel's arithmetic: outputs, y, cache and state are bit-identical to the
+// conv kernel followed by the decode kernel.  dk = 128 (a row is one warp,
+// four columns per lane), dv a multiple of 32, float32 state.
+constexpr int kGroupThreads = 256;
+constexpr int kGroupRows = kBulkBytes / (128 * 4);  // 32 rows per tile
+constexpr int kGroupMaxG = 2;
+constexpr int kRing = 3;
+constexpr int kGroupNch = (2 * 128 + kGroupMaxG * 128 + kGroupThreads - 1) / kGroupThreads;
+constexpr int group_smem_bytes(int dv) {
+  return kRing * kBulkBytes + (2 * 128 + kGroupMaxG * dv) * 4 + 128;
+}
+
+template <typename TI, typename TO, int WM>
+__global__ void __launch_bounds__(kGroupThreads, 4)
+    decode_conv_group_kernel(PoolView p, int layer, const int32_t *__restrict__ slot_ids,
+                             ConvStep cs, TO *__restrict__ o, float scale) {
+  constexpr int DK = 128, R = kGroupRows, RPW = R / (kGroupThreads / 32);  // 4 rows per warp
+  extern __shared__ __align__(128) unsigned char gsm[];
+  float4 *ring = reinterpret_cast<float4 *>(gsm);                  // kRing tiles
+  float *sqk = reinterpret_cast<float *>(gsm + kRing * kBulkBytes);  // q | k conv outputs
+  float *sv = sqk + 2 * DK;                                         // v conv outputs, G heads
+  __shared__ __align__(8) uint64_t full[kRing];
+  __shared__ float s_alpha[kGroupMaxG], s_beta[kGroupMaxG];
+
+  const int hk = blockIdx.x, i = blockIdx.y, tid = threadIdx.x;
+  const int G = p.h_v / p.h_k, dv = p.dv;
+  const int W = WM == 4 ? 4 : p.conv_k;
+  const int nq = p.h_k * DK;
+  const int nch = 2 * DK + G * dv;          // channels this CTA convolves
+  const int tph = dv / R, ntiles = G * tph;  // tiles per head, per CTA
+  const int slot = slot_ids[i];
+  auto channel = [&](int j) {  // the CTA's j-th channel: q, k, then the G heads' v
+    return j < 2 * DK ? (j < DK ? 0 : nq) + hk * DK + j % DK
+                      : 2 * nq + hk * G * dv + (j - 2 * DK);
+  };
+  // slot-independent inputs first
+  const TI *xrow = static_cast<const TI *>(cs.x) + (int64_t)i * cs.ld_x;
+  ConvTap<WM> tap[kGroupNch];
+#pragma unroll
+  for (int e = 0; e < kGroupNch; ++e) {
+    const int j = tid + e * kGroupThreads;
+    if (j < nch) tap_load<WM, TI>(tap[e], xrow, cs.w, cs.bias, channel(j), W);
+  }
+  float graw = 0.f, braw = 0.f;
+  if (tid < G) {
+    const int64_t gb = (int64_t)i * p.h_v + hk * G + tid;
+    graw = Elem<TI>::load1(static_cast<const TI *>(cs.g) + gb);
+    braw = Elem<TI>::load1(static_cast<const TI *>(cs.beta) + gb);
+  }
+  if (slot < 0 || slot >= p.n_slots) {
+    if (hk == 0 && tid == 0) raise_error(p.err, GDN_DEVERR_SLOT);
+    return;
+  }
+  auto tile_src = [&](int t) {  // tile t: rows (t % tph) * R .. of head hk * G + t / tph
+    return p.state_at(p.state_head_elem(layer, slot, hk * G + t / tph) +
+                      (int64_t)(t % tph) * R * DK);
+  };
+  auto issue = [&](int t) {  // one thread
+    uint64_t *b = &full[t % kRing];
+    // test hook: expect 16 bytes the copy never delivers, so the bounded wait
+    // runs out after the copy itself has landed
+    const uint32_t extra =
+        (t == 0 && (p.test_flags & GDN_TEST_DECODE_WAIT_TIMEOUT)) ? 16u : 0u;
+    mbar_arrive_expect_tx(b, kBulkBytes + extra);
+    bulk_g2s(ring + (t % kRing) * (kBulkBytes / 16), tile_src(t), kBulkBytes, b);
+  };
+  if (tid == 0) {
+    for (int b = 0; b < kRing; ++b) mbar_init(&full[b], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int t = 0; t < kRing && t < ntiles; ++t) issue(t);
+
+  TI *cache = static_cast<TI *>(p.conv) +
+              ((int64_t)layer * p.n_slots + slot) * p.conv_ch * (W - 1);
+  TI *yrow = static_cast<TI *>(cs.y) + (int64_t)i * cs.ld_y;
+#pragma unroll
+  for (int e = 0; e < kGroupNch; ++e) {
+    const int j = tid + e * kGroupThreads;
+    if (j < nch) tap_load_cache<WM, TI>(tap[e], cache, channel(j), W);
+  }
+#pragma unroll
+  for (int e = 0; e < kGroupNch; ++e) {
+    const int j = tid + e * kGroupThreads;
+    if (j < nch) {
+      const int c = channel(j);
+      const float yv = tap_conv<WM, TI>(tap[e], W);
+      if (j < 2 * DK) sqk[j] = yv; else sv[j - 2 * DK] = yv;
+      Elem<TI>::store1(yrow + c, yv);
+      // this CTA is the only reader of the channel: shift its cache in place
+      TI *cc = cache + (int64_t)c * (W - 1);
+#pragma unroll
+      for (int m = 0; m < WM - 2; ++m)
+        if (m < W - 2) Elem<TI>::store1(cc + m, tap[e].hist[m + 1]);
+      Elem<TI>::store1(cc + (W - 2), tap[e].x);
+    }
+  }
+  if (tid < G) {
+    s_alpha[tid] = expf(graw);
+    s_beta[tid] = braw;
+  }
+  __syncthreads();  // sqk, sv, s_alpha, s_beta complete
+
+  const int lane = tid & 31, warp = tid >> 5;
+  float4 q4 = reinterpret_cast<const float4 *>(sqk)[lane];
+  float4 k4 = reinterpret_cast<const float4 *>(sqk + DK)[lane];
+  const float kk = group_sum<32>(dot4(k4, k4));
+  const float qq = group_sum<32>(dot4(q4, q4));
+  k4 = scale4(rsqrtf(kk + kL2Eps), k4);
+  q4 = scale4(rsqrtf(qq + kL2Eps), q4);
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int b = t % kRing;
+    if (!__syncthreads_and(mbar_wait_bounded(&full[b], (uint32_t)(t / kRing) & 1u))) {
+      if (tid == 0) {
+        raise_error(p.err, GDN_DEVERR_TIMEOUT);
+        // a second bounded chance for every copy still in flight
+        const int issued = min(t + kRing, ntiles);
+        for (int u = t; u < issued; ++u)
+          mbar_wait_bounded(&full[u % kRing], (uint32_t)(u / kRing) & 1u);
+      }
+      __syncthreads();
+      return;
+    }
+    const int vh = t / tph, r0 = (t % tph) * R;
+    const int h = hk * G + vh;
+    const float alpha = s_alpha[vh], beta = s_beta[vh];
+    const float4 *tile = ring + b * (kBulkBytes / 16);
+    char *S = tile_src(t);
+    TO *op = o + ((int64_t)i * p.h_v + h) * dv + r0;
+    float4 sr[RPW];
+    float acc[RPW];
+#pragma unroll
+    for (int u = 0; u < RPW; ++u) {
+      const int rl = warp * RPW + u;
+      sr[u] = tile[rl * (DK / 4) + lane];
+      acc[u] = dot4(sr[u], k4);
+    }
+#pragma unroll
+    for (int u = 0; u < RPW; ++u) acc[u] = group_sum<32>(acc[u]);
+#pragma unroll
+    for (int u = 0; u < RPW; ++u) {
+      const int rl = warp * RPW + u;
+      const float d = beta * (sv[vh * dv + r0 + rl] - alpha * acc[u]);
+      sr[u] = axpby4(alpha, sr[u], d, k4);
+      acc[u] = dot4(sr[u], q4);
+    }
+#pragma unroll
+    for (int u = 0; u < RPW; ++u) acc[u] = group_sum<32>(acc[u]);
+#pragma unroll
+    for (int u = 0; u < RPW; ++u) {
+      const int rl = warp * RPW + u;
+      state_st4<true>(S, (int64_t)rl * DK + 4 * lane, sr[u], GDN_F32);
+      if (lane == 0) Elem<TO>::store1(op + rl, scale * acc[u]);
+    }
+    __syncthreads();  // every thread is done with buffer b
+    if (tid == 0 && t + kRing < ntiles) issue(t + kRing);
+  }
+}
+
+template <typename TI, typename TO>
+cudaError_t launch_group_t(const PoolView &p, int layer, const int32_t *slot_ids, int n,
+                           const ConvStep &cs, void *o, float scale, cudaStream_t s) {
+  const int bytes = group_smem_bytes(p.dv);
+  const dim3 grid(p.h_k, n);
+  auto kern = p.conv_k == 4 ? decode_conv_group_kernel<TI, TO, 4>
+                            : decode_conv_group_kernel<TI, TO, kMaxConvK>;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kGroupThreads, bytes, s>>>(p, layer, slot_ids, cs, static_cast<TO *>(o), scale);
+  return cudaGetLastError();
+}
+
 template <int DK, typename TI, typename TO>
 struct DecodeConvF {
   static cudaError_t run(const PoolView &p, int layer, const int32_t *slot_ids, int n,
@@ -517,6 +701,26 @@ cudaError_t decode_conv_resident_ctas(const PoolView &p, gdn_dtype dtype, gdn_dt
 int64_t decode_grid_ctas(const PoolView &p, int n) {
   const int R = kBulkBytes / (p.dk * 4);
   return (int64_t)((p.dv + R - 1) / R) * p.h_v * n;
+}
+
+bool decode_conv_group_ok(const PoolView &p) {
+  return p.dk == 128 && p.state_dtype == GDN_F32 && p.h_k > 0 && p.h_v % p.h_k == 0 &&
+         p.h_v / p.h_k <= kGroupMaxG && p.dv % kGroupRows == 0 && p.dv > 0 &&
+         group_smem_bytes(p.dv) <= 227 * 1024 && p.conv_k >= 2 && p.conv_k <= kMaxConvK;
+}
+
+cudaError_t launch_decode_conv_group(const PoolView &p, int layer, const int32_t *slot_ids,
+                                     int n, const void *x, int64_t ld_x, const float *w,
+                                     const float *bias, void *y, int64_t ld_y, const void *g,
+                                     const void *beta, gdn_dtype dtype, void *o,
+                                     gdn_dtype o_dtype, float scale, cudaStream_t s) {
+  if (!decode_conv_group_ok(p)) return cudaErrorInvalidValue;
+  const ConvStep cs{x, ld_x, w, bias, y, ld_y, g, beta};
+  if (dtype == GDN_BF16)
+    return o_dtype == GDN_BF16 ? launch_group_t<bf16, bf16>(p, layer, slot_ids, n, cs, o, scale, s)
+                               : launch_group_t<bf16, float>(p, layer, slot_ids, n, cs, o, scale, s);
+  return o_dtype == GDN_BF16 ? launch_group_t<float, bf16>(p, layer, slot_ids, n, cs, o, scale, s)
+                             : launch_group_t<float, float>(p, layer, slot_ids, n, cs, o, scale, s);
 }
 
 cudaError_t launch_decode_conv(const PoolView &p, int layer, const int32_t *slot_ids, int n,

@@ -116,6 +116,17 @@ cudaError_t launch_decode_conv(const PoolView &p, int layer, const int32_t *slot
                                gdn_dtype dtype, void *o, gdn_dtype o_dtype, float scale,
                                cudaStream_t s);
 
+// The same step with one CTA per (slot, key head): each conv channel once,
+// the key head's value-head states streamed through a ring of bulk tiles; no
+// tickets.  For dk = 128, a float32 state, h_v / h_k <= 2 and dv a multiple
+// of 32 (decode_conv_group_ok); the same results, bit for bit.
+bool decode_conv_group_ok(const PoolView &p);
+cudaError_t launch_decode_conv_group(const PoolView &p, int layer, const int32_t *slot_ids,
+                                     int n, const void *x, int64_t ld_x, const float *w,
+                                     const float *bias, void *y, int64_t ld_y, const void *g,
+                                     const void *beta, gdn_dtype dtype, void *o,
+                                     gdn_dtype o_dtype, float scale, cudaStream_t s);
+
 // Speculative verify of T new drafts per slot.  Normal mode: commit at
 // accept_len[i] (or after all T with commit_all).  Deferred mode (prev.q set):
 // slot i first replays the first prev_accept[i] drafts of the previous round

@@ -434,3 +434,31 @@ def test_prefill_many_sequences_unaligned_outputs(odt):
     assert_maxrel(host(pool.state[0, lid]), ref.S[0, ids], _rel_tol(128), "S")
     rest = np.setdiff1d(np.arange(n + 10), ids)
     assert bool((pool.state[0, torch.from_numpy(rest).long().cuda()] == SENTINEL).all())
+
+
+def test_prefill_two_launch_overlapping_sequences_stay_in_bounds():
+    """cu_seqlens [0, 200, 0, 200] (host checks off): the middle range is
+    reversed and the last overlaps the first, so the sequences claim more
+    64-token chunks (8) than the workspace holds (200 / 64 + 3 = 6).  The
+    key-side kernel forms only the chunks within that capacity, the state
+    kernel rejects the two bad sequences (error word: bad sequence) and leaves
+    their slots alone, and the first sequence still matches the oracle."""
+    rng = np.random.default_rng(46)
+    shape = synth.LayerShape(4, 2, 128, 128, 16, 4)
+    T = 200
+    S0 = synth.random_states(rng, 1, shape)
+    tok = synth.token_inputs(rng, T, shape, "bf16")
+    pool = _pool(shape, 1, 4, host_checks=False)
+    pool.state[0, 0] = dev(S0[0])
+    o = torch.zeros(T, shape.h_v, shape.dv, device="cuda")
+    abi.gdn_prefill_chunked(pool, 0, dev_i32([0, 1, 2]), dev_i32([0, T, 0, T]),
+                            *tok_dev(tok, "bf16"), o)
+    torch.cuda.synchronize()
+    assert abi.gdn_pool_get_error(pool) == abi.DEVERR_SEQ
+    assert bool((pool.state[0, [1, 2, 3]] == SENTINEL).all())
+    ref = O.OraclePool(1, 1, shape.h_v, shape.h_k, shape.dk, shape.dv, 16, 4)
+    ref.S[0, [0]] = S0
+    o_ref = ref.prefill(0, np.array([0], dtype=np.int32), np.array([0, T]), *tok_np(tok))
+    tol = _rel_tol(128)
+    assert_maxrel(host(o), o_ref, tol, "o of the valid sequence")
+    assert_maxrel(host(pool.state[0, 0]), ref.S[0, 0], tol, "S of the valid sequence")
