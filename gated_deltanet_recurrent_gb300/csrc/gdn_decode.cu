@@ -425,12 +425,13 @@ __global__ void __launch_bounds__(kThreads)
 // conv kernel followed by the decode kernel.  dk = 128 (a row is one warp,
 // four columns per lane), dv a multiple of 32, float32 state.
 constexpr int kGroupThreads = 256;
-constexpr int kGroupRows = kBulkBytes / (128 * 4);  // 32 rows per tile
+constexpr int kGroupTile = 16384;                 // bytes of one ring tile
+constexpr int kGroupRows = kGroupTile / (128 * 4);  // 32 rows per tile
 constexpr int kGroupMaxG = 2;
 constexpr int kRing = 3;
 constexpr int kGroupNch = (2 * 128 + kGroupMaxG * 128 + kGroupThreads - 1) / kGroupThreads;
 constexpr int group_smem_bytes(int dv) {
-  return kRing * kBulkBytes + (2 * 128 + kGroupMaxG * dv) * 4 + 128;
+  return kRing * kGroupTile + (2 * 128 + kGroupMaxG * dv) * 4 + 128;
 }
 
 template <typename TI, typename TO, int WM>
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(kGroupThreads, 4)
   constexpr int DK = 128, R = kGroupRows, RPW = R / (kGroupThreads / 32);  // 4 rows per warp
   extern __shared__ __align__(128) unsigned char gsm[];
   float4 *ring = reinterpret_cast<float4 *>(gsm);                  // kRing tiles
-  float *sqk = reinterpret_cast<float *>(gsm + kRing * kBulkBytes);  // q | k conv outputs
+  float *sqk = reinterpret_cast<float *>(gsm + kRing * kGroupTile);  // q | k conv outputs
   float *sv = sqk + 2 * DK;                                         // v conv outputs, G heads
   __shared__ __align__(8) uint64_t full[kRing];
   __shared__ float s_alpha[kGroupMaxG], s_beta[kGroupMaxG];
@@ -484,8 +485,8 @@ __global__ void __launch_bounds__(kGroupThreads, 4)
     // runs out after the copy itself has landed
     const uint32_t extra =
         (t == 0 && (p.test_flags & GDN_TEST_DECODE_WAIT_TIMEOUT)) ? 16u : 0u;
-    mbar_arrive_expect_tx(b, kBulkBytes + extra);
-    bulk_g2s(ring + (t % kRing) * (kBulkBytes / 16), tile_src(t), kBulkBytes, b);
+    mbar_arrive_expect_tx(b, kGroupTile + extra);
+    bulk_g2s(ring + (t % kRing) * (kGroupTile / 16), tile_src(t), kGroupTile, b);
   };
   if (tid == 0) {
     for (int b = 0; b < kRing; ++b) mbar_init(&full[b], 1);
@@ -549,7 +550,7 @@ __global__ void __launch_bounds__(kGroupThreads, 4)
     const int vh = t / tph, r0 = (t % tph) * R;
     const int h = hk * G + vh;
     const float alpha = s_alpha[vh], beta = s_beta[vh];
-    const float4 *tile = ring + b * (kBulkBytes / 16);
+    const float4 *tile = ring + b * (kGroupTile / 16);
     char *S = tile_src(t);
     TO *op = o + ((int64_t)i * p.h_v + h) * dv + r0;
     float4 sr[RPW];
