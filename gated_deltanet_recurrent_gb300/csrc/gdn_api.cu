@@ -6,7 +6,6 @@
 #include <stdio.h>
 
 #include <cmath>
-#include <mutex>
 #include <string>
 #include <vector>
 
@@ -788,23 +787,12 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;  // 64 MiB
 static __device__ __align__(256) unsigned char g_prefill_scratch[kNoAllocScratchBytes];
 
-// The array's device address on `dev` (which must be current), looked up once
-// per device.  In host code the array's name is only a stand-in, never a
-// pointer a kernel may be given.
-cudaError_t noalloc_scratch(int dev, void **out) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static void *addr[kMaxDevices] = {};
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void *p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_prefill_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
-  }
-  *out = addr[dev];
-  return cudaSuccess;
+// The array's device address on the current device, looked up on every call
+// (cheap once the module is loaded, and never stale after a context reset).
+// In host code the array's name is only a stand-in, never a pointer a kernel
+// may be given.
+cudaError_t noalloc_scratch(void **out) {
+  return cudaGetSymbolAddress(out, g_prefill_scratch);
 }
 
 }  // namespace
@@ -838,7 +826,7 @@ gdn_status gdn_prefill_chunked_noalloc(gdn_pool *p, int32_t layer, const int32_t
                 wb, kNoAllocScratchBytes, p->desc.h_v, total_tokens, n_seqs);
   void *work = nullptr;
   if (wb > 0) {
-    const cudaError_t e = noalloc_scratch(p->device, &work);
+    const cudaError_t e = noalloc_scratch(&work);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(prefill scratch)");
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

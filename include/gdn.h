@@ -227,15 +227,18 @@ gdn_status gdn_decode_step(gdn_pool *pool, int32_t layer, const int32_t *slot_id
  * pool's conv_dtype (else GDN_ERR_DTYPE); w, bias as in gdn_conv_silu; o, g,
  * beta, scale as in gdn_decode_step.  Results, y, cache and state are those
  * of the two calls made one after the other, bit for bit.
- * Two forms, chosen by size: while the decode grid (h_v * ceil(dv / rows per
- * CTA) CTAs per slot) fits on the device at once, ONE kernel does it all --
- * each CTA convolves the q/k channels of its key head and the v channels of
- * its state rows itself while its state tile is in flight, and the last of
- * the CTAs sharing a key head (a per-slot ticket in pool memory, no waiting)
- * shifts that head's q/k cache.  Larger calls launch the conv and then the
- * decode as its programmatic dependent launch, which fetches its state tiles
- * (untouched by the conv) before it waits for the conv grid to complete and
- * reads y.  Caller owns every buffer.  An argument or host-check error
+ * Three forms, chosen by size and shape: while the decode grid (h_v *
+ * ceil(dv / rows per CTA) CTAs per slot) fits on the device at once, ONE
+ * kernel does it all -- each CTA convolves the q/k channels of its key head
+ * and the v channels of its state rows itself while its state tile is in
+ * flight, and the last of the CTAs sharing a key head (a per-slot ticket in
+ * pool memory, no waiting) shifts that head's q/k cache.  Larger calls with
+ * dk = 128, a float32 state, h_v / h_k <= 2 and dv a multiple of 32 run ONE
+ * kernel with a CTA per (slot, key head) that convolves each channel once
+ * while the key head's value-head states stream in.  Other larger calls
+ * launch the conv and then the decode as its programmatic dependent launch,
+ * which fetches its state tiles (untouched by the conv) before it waits for
+ * the conv grid to complete and reads y.  Caller owns every buffer.  An argument or host-check error
  * launches nothing; GDN_ERR_CUDA from the second launch of the two-launch
  * form leaves the conv (cache advanced, y written) launched without its
  * decode. */
@@ -373,10 +376,10 @@ gdn_status gdn_spec_verify_deferred(gdn_pool *pool, int32_t layer, const int32_t
  * GPU that loads the library holds until the process exits; it calls no
  * allocator.  A call needing more than 64 MiB -- about 32 KiB per 64-token
  * chunk per value head, counting (tokens / 64 + sequences) chunks -- returns
- * GDN_ERR_SIZE and launches nothing.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) and keeps it for the process:
- * make that first call before any stream capture, and do not call it again on
- * a device after cudaDeviceReset.  Every call shares the one array: calls whose work
+ * GDN_ERR_SIZE and launches nothing.  Each call looks up the array's device
+ * address (cudaGetSymbolAddress, which allocates nothing; the first lookup may
+ * load the library's device code, so make the first call before any stream
+ * capture).  Every call shares the one array: calls whose work
  * overlaps on the GPU (other streams, other threads, other pools of the same
  * device) race on it and must be serialised by the caller. */
 gdn_status gdn_prefill_chunked_noalloc(gdn_pool *pool, int32_t layer, const int32_t *slot_ids,
