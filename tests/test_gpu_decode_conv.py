@@ -1,7 +1,11 @@
 """gdn_decode_step_conv: conv + SiLU and the decode step of one layer in one
-call -- one fused kernel while its grid fits the GPU at once (few slots),
-else the conv launch with the decode as its programmatic dependent launch.
-Both forms are exercised (the decode-step layer with 4 and with 64 slots).
+call -- one fused kernel per (row block, value head, slot) while its grid fits
+the GPU at once (few slots), else one fused kernel per (slot, key head) where
+the shape allows it (dk = 128, float32 state, h_v / h_k <= 2), else the conv
+launch with the decode as its programmatic dependent launch.  The first two
+are exercised here (the decode-step layer with 4 and with 64 slots, and a
+two-head layer with 512 slots, conv width 3, float32 activations); the launch
+pair runs for the other large shapes.
 
 Checked through the C ABI over three consecutive steps:
   * y against the float64 oracle's conv + SiLU (bf16: |got - ref| <= 1e-2 +
@@ -43,6 +47,15 @@ CASES = {
     "small_bf16_strided": dict(shape=synth.LayerShape(4, 2, 64, 64, 512, 4), n_slots=7,
                                n_active=3, dtype="bf16", pad_x=16, pad_y=8, bias=True, layer=0,
                                n_layers=1),
+    # the per-(slot, key head) kernel with one value head per key head, conv
+    # width 3 (its generic-width instantiation), float32 activations, bias
+    "group_f32_w3_g1": dict(shape=synth.LayerShape(2, 2, 128, 128, 768, 3), n_slots=520,
+                            n_active=512, dtype="f32", pad_x=0, pad_y=0, bias=True, layer=1,
+                            n_layers=2),
+    # the decode-step layer at 64 slots with bf16 outputs
+    "gdn_layer_bf16_obf16": dict(shape=synth.GDN_LAYER, n_slots=256, n_active=64, dtype="bf16",
+                                 pad_x=0, pad_y=0, bias=False, layer=0, n_layers=1,
+                                 o_dtype="bf16"),
 }
 
 
@@ -89,7 +102,8 @@ def test_decode_step_conv_matches_oracle_and_two_calls(case):
         X.copy_(dev(x, dt))
         G, B = dev(tok["g"], dt), dev(tok["beta"], dt)
         Y, Y2 = rows(C + c["pad_y"]), rows(C + c["pad_y"])
-        o = torch.empty(n, shape.h_v, shape.dv, device="cuda")
+        odt = torch.bfloat16 if c.get("o_dtype") == "bf16" else torch.float32
+        o = torch.empty(n, shape.h_v, shape.dv, device="cuda", dtype=odt)
         o2 = torch.empty_like(o)
         abi.gdn_decode_step_conv(fused, L, dev_i32(ids), X, W, Y, G, B, o, bias=Bias, scale=scale)
         abi.gdn_conv_silu(split, L, dev_i32(ids), X, W, Y2, bias=Bias)
@@ -117,7 +131,10 @@ def test_decode_step_conv_matches_oracle_and_two_calls(case):
         for i in range(n):
             S_ref[i], o_ref[i] = O.gdn_step(S_ref[i], q[i], k[i], v[i], tok["g"][i],
                                             tok["beta"][i], scale=scale)
-        assert_maxrel(host(o), o_ref, 1e-4, f"{what}: o")
+        if odt == torch.bfloat16:
+            assert_close_bf16(host(o), o_ref, what=f"{what}: o")
+        else:
+            assert_maxrel(host(o), o_ref, 1e-4, f"{what}: o")
         assert_maxrel(host(fused.state[L, lid]), S_ref, 1e-4, f"{what}: S")
 
     mask = np.ones(c["n_slots"], dtype=bool)
