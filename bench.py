@@ -1005,6 +1005,9 @@ def run_gpu(args, rank, world):
         return None
 
     units = b.n * args.steps * world
+    # kernels of one headline step, by the library's own form rule
+    launches_per_step = abi.gdn_decode_step_conv_launches(b.pool, b.n, torch.bfloat16,
+                                                          b.os[0].dtype)
     kernel_avg = t_kernel / args.steps
     achieved = DECODE_KERNEL_BYTES_PER_SLOT * b.n / kernel_avg / 1e9
     line = {
@@ -1034,7 +1037,7 @@ def run_gpu(args, rank, world):
                       "ms_per_step": t_two / args.steps * 1e3,
                       "note": "the same step as gdn_conv_silu then gdn_decode_step, "
                               "an event between them"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "kernel": "decode_bulk_kernel<128, bf16, float, false>",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(),

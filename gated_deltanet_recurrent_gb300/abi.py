@@ -26,7 +26,8 @@ EXPORTED = ("gdn_pool_state_bytes", "gdn_pool_conv_bytes", "gdn_pool_create", "g
             "gdn_pool_copy",
             "gdn_pool_destroy", "gdn_pool_get_error", "gdn_pool_set_test_flags", "gdn_conv_silu",
             "gdn_decode_step",
-            "gdn_decode_step_conv", "gdn_gated_rmsnorm", "gdn_in_proj",
+            "gdn_decode_step_conv", "gdn_decode_step_conv_launches", "gdn_gated_rmsnorm",
+            "gdn_in_proj",
             "gdn_prefill_chunked", "gdn_prefill_recurrent", "gdn_spec_verify",
             "gdn_spec_verify_deferred", "gdn_prefill_chunked_noalloc", "gdn_prefill_chunked_ckpt",
             "gdn_status_string",
@@ -84,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gdn_decode_step": (st, [vp, i32, vp, i32, P(gdn_qkv), vp, st, ctypes.c_float, vp]),
         "gdn_decode_step_conv": (st, [vp, i32, vp, i32, vp, i64, vp, vp, vp, i64, vp, vp, st,
                                       vp, st, ctypes.c_float, vp]),
+        "gdn_decode_step_conv_launches": (st, [vp, i32, st, st, P(i32)]),
         "gdn_gated_rmsnorm": (st, [i64, i32, vp, st, vp, st, vp, ctypes.c_float, vp, st, vp]),
         "gdn_in_proj": (st, [vp, i64, i32, i32, vp, i64, vp, i64, vp, i64, st, vp]),
         "gdn_prefill_chunked": (st, [vp, i32, vp, vp, i32, i32, i32, P(gdn_qkv), vp, st,
@@ -315,6 +317,16 @@ def gdn_decode_step_conv(pool: Pool, layer: int, slot_ids: torch.Tensor, x: torc
         _ptr(bias), _ptr(y), y.stride(0), _ptr(g), _ptr(beta), dts.pop(), _ptr(o), _dt(o), scale,
         _stream(stream)))
     return o
+
+
+def gdn_decode_step_conv_launches(pool: Pool, n: int, dtype: torch.dtype,
+                                  o_dtype: torch.dtype = torch.float32) -> int:
+    """Kernel launches gdn_decode_step_conv makes for n slots (1 or 2; 0 if n = 0)."""
+    codes = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
+    out = ctypes.c_int32(-1)
+    _check(load_library().gdn_decode_step_conv_launches(pool.handle, n, codes[dtype],
+                                                         codes[o_dtype], ctypes.byref(out)))
+    return out.value
 
 
 def gdn_in_proj(pool: Pool, x: torch.Tensor, w: torch.Tensor,

@@ -437,6 +437,53 @@ gdn_status gdn_decode_step(gdn_pool *p, int32_t layer, const int32_t *slot_ids, 
   return ok();
 }
 
+}  // extern "C"
+
+namespace {
+
+// The form gdn_decode_step_conv takes for n slots: one fused kernel per (row
+// block, value head, slot) while that grid is resident at once (small n: one
+// launch and one wave; beyond that its CTAs each recompute their key head's q
+// and k conv), else one fused kernel per (slot, key head) where the shape
+// allows it, else the conv launch followed by the decode as a programmatic
+// dependent launch (the decode fetches its state tiles while the conv runs).
+enum class StepConvForm { kFusedRows, kFusedGroup, kPair };
+
+cudaError_t step_conv_form(const gdn_pool *p, int32_t n, gdn_dtype dtype, gdn_dtype o_dtype,
+                           StepConvForm *form) {
+  int64_t resident = 0;
+  const cudaError_t e =
+      gdn::decode_conv_resident_ctas(p->view, dtype, o_dtype, p->sm_count, &resident);
+  if (e != cudaSuccess) return e;
+  if (gdn::decode_grid_ctas(p->view, n) <= resident) *form = StepConvForm::kFusedRows;
+  else if (gdn::decode_conv_group_ok(p->view)) *form = StepConvForm::kFusedGroup;
+  else *form = StepConvForm::kPair;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_decode_step_conv_launches(gdn_pool *p, int32_t n, gdn_dtype dtype,
+                                         gdn_dtype o_dtype, int32_t *launches) {
+  gdn_status st = check_pool(p, 0);
+  if (st != GDN_OK) return st;
+  if (!launches) return fail(GDN_ERR_ARG, "launches must be non-NULL");
+  if (n < 0 || n > 65535) return fail(GDN_ERR_ARG, "n = %d outside [0, 65535]", n);
+  if (dtype != p->desc.conv_dtype) return fail(GDN_ERR_DTYPE, "dtype differs from the pool's conv_dtype");
+  if (!dtype_ok(o_dtype)) return fail(GDN_ERR_DTYPE, "o dtype must be F32 or BF16");
+  if (n == 0) {
+    *launches = 0;
+    return ok();
+  }
+  StepConvForm form;
+  const cudaError_t e = step_conv_form(p, n, dtype, o_dtype, &form);
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  *launches = form == StepConvForm::kPair ? 2 : 1;
+  return ok();
+}
+
 gdn_status gdn_decode_step_conv(gdn_pool *p, int32_t layer, const int32_t *slot_ids,
                                 int32_t n, const void *x, int64_t ld_x, const float *w,
                                 const float *bias, void *y, int64_t ld_y, const void *g,
@@ -471,23 +518,16 @@ gdn_status gdn_decode_step_conv(gdn_pool *p, int32_t layer, const int32_t *slot_
         (st = check_device_ptr(o, "o")))
       return st;
   }
-  // One fused kernel while its whole grid is resident at once (small n: one
-  // launch and one wave).  Beyond that its CTAs each recompute their key
-  // head's q and k conv, and the conv launch followed by the decode as a
-  // programmatic dependent launch (the decode fetches its state tiles while
-  // the conv runs) is faster.
-  int64_t resident = 0;
-  cudaError_t e = gdn::decode_conv_resident_ctas(p->view, dtype, o_dtype, p->sm_count, &resident);
+  StepConvForm form;
+  cudaError_t e = step_conv_form(p, n, dtype, o_dtype, &form);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
-  if (gdn::decode_grid_ctas(p->view, n) <= resident) {
+  if (form == StepConvForm::kFusedRows) {
     e = gdn::launch_decode_conv(p->view, layer, slot_ids, n, x, ld_x, w, bias, y, ld_y, g, beta,
                                 dtype, o, o_dtype, scale, s);
     if (e != cudaSuccess) return cuda_fail(e, "conv + decode launch");
     return ok();
   }
-  // Larger grids: one CTA per (slot, key head) convolves each channel once
-  // while its heads' states stream in, where the shape allows it.
-  if (gdn::decode_conv_group_ok(p->view)) {
+  if (form == StepConvForm::kFusedGroup) {
     e = gdn::launch_decode_conv_group(p->view, layer, slot_ids, n, x, ld_x, w, bias, y, ld_y, g,
                                       beta, dtype, o, o_dtype, scale, s);
     if (e != cudaSuccess) return cuda_fail(e, "conv + decode launch");

@@ -248,6 +248,17 @@ gdn_status gdn_decode_step_conv(gdn_pool *pool, int32_t layer, const int32_t *sl
                                 const void *beta, gdn_dtype dtype, void *o, gdn_dtype o_dtype,
                                 float scale, gdn_stream stream);
 
+/* The number of kernel launches gdn_decode_step_conv makes for n active slots
+ * on this pool with these dtypes (1: one of the fused forms; 2: the conv and
+ * the decode; 0 for n = 0), chosen by the same rule, without launching
+ * anything (a not-in-the-pages companion of gdn_decode_step_conv, for callers
+ * that count or budget launches, e.g. when sizing a CUDA graph).  *launches:
+ * host int32.  Errors: GDN_ERR_ARG (NULL launches, n outside [0, 65535], the
+ * pool's device not current), GDN_ERR_DTYPE as in gdn_decode_step_conv,
+ * GDN_ERR_CUDA (the occupancy query failed). */
+gdn_status gdn_decode_step_conv_launches(gdn_pool *pool, int32_t n, gdn_dtype dtype,
+                                         gdn_dtype o_dtype, int32_t *launches);
+
 /* Input projection of the layer (baseRT issue #31, "Why this looks
  * tractable": the gdn_in_proj kernel, named there without its formula; the
  * plain reading is the layer's linear projection of the hidden states):

@@ -215,3 +215,23 @@ def test_decode_step_conv_alternating_forms_keep_the_cache_consistent():
         assert torch.equal(one.state, two.state), f"step {step}: state"
         assert torch.equal(one.conv, two.conv), f"step {step}: conv cache"
     assert abi.gdn_pool_get_error(one) == 0
+
+
+def test_decode_step_conv_launch_count_query():
+    """gdn_decode_step_conv_launches reports the form the call takes: one
+    launch for the fused forms (few slots; the decode-step layer at 64 slots),
+    two for the launch pair (a shape the per-key-head kernel does not take,
+    dk = 64, with a grid too large to be resident at once), 0 for no slots;
+    bad arguments are refused."""
+    big = _pool(synth.GDN_LAYER, 1, 8, torch.bfloat16)
+    assert abi.gdn_decode_step_conv_launches(big, 4, torch.bfloat16) == 1
+    assert abi.gdn_decode_step_conv_launches(big, 64, torch.bfloat16, torch.bfloat16) == 1
+    assert abi.gdn_decode_step_conv_launches(big, 0, torch.bfloat16) == 0
+    small = _pool(synth.LayerShape(4, 2, 64, 64, 512, 4), 1, 8, torch.bfloat16)
+    assert abi.gdn_decode_step_conv_launches(small, 8000, torch.bfloat16) == 2
+    with pytest.raises(abi.GDNError) as e:
+        abi.gdn_decode_step_conv_launches(big, -1, torch.bfloat16)
+    assert e.value.name == "GDN_ERR_ARG"
+    with pytest.raises(abi.GDNError) as e:
+        abi.gdn_decode_step_conv_launches(big, 4, torch.float32)
+    assert e.value.name == "GDN_ERR_DTYPE"
