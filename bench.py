@@ -6,9 +6,9 @@ Headline (one JSON line on stdout): decode slot-steps/s for one GDN layer
 (32 value heads sharing 16 key heads, K = V = 128, fp32 state, conv_k = 4
 over 8192 channels, bf16 activations) on a 256-slot pool with 64 active slot
 ids drawn at random.  One step = one gdn_decode_step_conv call: the conv +
-SiLU over the 64 new tokens, then the decode step reading q, k, v straight
-out of the conv output.  L2 is flushed (a 512 MiB write) between timed steps,
-outside the timed events.
+SiLU over the 64 new tokens and the decode step on its q, k, v (at this size
+one fused kernel, a CTA per (slot, key head)).  L2 is flushed (a 512 MiB
+write) between timed steps, outside the timed events.
 
 Also in the line: the same metric end to end through the C ABI with every
 step's inputs copied from pinned host memory and its output copied back inside
@@ -1045,7 +1045,8 @@ def run_gpu(args, rank, world):
                      "algorithmic_bytes_per_launch": DECODE_KERNEL_BYTES_PER_SLOT * b.n,
                      "kernel_us": kernel_avg * 1e6,
                      "timed_on": "the decode launch of the two-call step (events between "
-                                 "the launches; the one-call step overlaps them)"},
+                                 "the launches; the one-call step fuses the conv into its "
+                                 "own kernel)"},
         "clocks": clk,
     }
     if secondary:
