@@ -785,7 +785,7 @@ static_assert(kSeqSmem <= 227 * 1024, "shared memory");
 // stalls issuing a long MMA group holds up no CUDA-core work.
 constexpr int kMmaWarp = 8;
 constexpr int NTS = NT + 32;
-// Compute thread that issues the tensor-map copies of the raw rows (warp 6).
+// Compute thread that issues the tensor-map stores of whole output chunks (warp 6).
 constexpr int kCopier = 192;
 
 // TMEM columns
@@ -1650,8 +1650,8 @@ __global__ void __launch_bounds__(NTS, 1)
       }
     };
 
-    // chunk 0 (and 1) on their way; chunk 0's scalars, split state, scaled
-    // state and Ktil^T to the MMA warp
+    // chunk 0's rows and scalars (fetched by the MMA warp) landed: the split
+    // and scaled state to the MMA warp
     alive = cw_and(rows_landed(0));
     if (alive) split_scale(scal(0)[kSGam + C - 1]);
 
