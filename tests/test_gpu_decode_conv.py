@@ -235,3 +235,48 @@ def test_decode_step_conv_launch_count_query():
     with pytest.raises(abi.GDNError) as e:
         abi.gdn_decode_step_conv_launches(big, 4, torch.float32)
     assert e.value.name == "GDN_ERR_DTYPE"
+
+
+def test_decode_step_conv_bad_slot_skipped_in_both_fused_forms():
+    """Host checks off, one slot id out of range among 4 and among 16 active
+    slots of the decode-step layer (the per-row-block and the per-(slot, key
+    head) fused kernels): the error word reports the bad slot, its entry
+    writes nothing, and every other entry equals the two separate calls on a
+    twin pool, bit for bit."""
+    shape = synth.GDN_LAYER
+    nq = shape.h_k * shape.dk
+    rng = np.random.default_rng(67)
+    for n in (4, 16):
+        pools = []
+        for _ in range(2):
+            p = abi.Pool.for_shape(shape, 1, 32, conv_dtype=torch.bfloat16, host_checks=False)
+            pools.append(p)
+        gen = torch.Generator(device="cuda").manual_seed(7)
+        pools[0].state.normal_(0.0, 0.1, generator=gen)
+        pools[0].conv.copy_(torch.randn(pools[0].conv.shape, device="cuda", generator=gen))
+        pools[1].state.copy_(pools[0].state)
+        pools[1].conv.copy_(pools[0].conv)
+        ids = rng.choice(32, n, replace=False).astype(np.int32)
+        ids[1] = 99  # out of range
+        good = np.array([i for i in range(n) if i != 1])
+        x = dev(synth.conv_input(rng, n, shape.conv_ch, "bf16"), "bf16")
+        w = dev(synth.conv_weights(rng, shape.conv_ch, shape.conv_k))
+        tok = synth.token_inputs(rng, n, shape, "bf16")
+        g, b = dev(tok["g"], "bf16"), dev(tok["beta"], "bf16")
+        y1 = torch.zeros(n, shape.conv_ch, device="cuda", dtype=torch.bfloat16)
+        y2 = torch.zeros_like(y1)
+        o1 = torch.full((n, shape.h_v, shape.dv), 5.0, device="cuda")
+        o2 = torch.full_like(o1, 5.0)
+        abi.gdn_decode_step_conv(pools[0], 0, dev_i32(ids), x, w, y1, g, b, o1)
+        abi.gdn_conv_silu(pools[1], 0, dev_i32(ids), x, w, y2)
+        abi.gdn_decode_step(pools[1], 0, dev_i32(ids), y2[:, :nq].view(n, shape.h_k, shape.dk),
+                            y2[:, nq:2 * nq].view(n, shape.h_k, shape.dk),
+                            y2[:, 2 * nq:].view(n, shape.h_v, shape.dv), g, b, o2)
+        torch.cuda.synchronize()
+        for p in pools:
+            assert abi.gdn_pool_get_error(p) == abi.DEVERR_SLOT, f"n = {n}"
+        gi = torch.from_numpy(good).cuda()
+        assert torch.equal(y1[gi], y2[gi]) and torch.equal(o1[gi], o2[gi]), f"n = {n}"
+        assert bool((o1[1] == 5.0).all()) and bool((y1[1] == 0).all()), f"n = {n}: bad entry"
+        assert torch.equal(pools[0].state, pools[1].state), f"n = {n}: state"
+        assert torch.equal(pools[0].conv, pools[1].conv), f"n = {n}: conv cache"
